@@ -1,0 +1,464 @@
+"""Benchmark: batch-1 decode over a 64-layer q8_0 (or f16) GQA KV cache on GB300.
+
+Workload (default): 64 layers, 40 query heads / 8 KV heads, head_dim 128,
+q8_0 K/V from N(0,1)*0.5, RoPE base 1e6, n_kv = 16384.  One step is one
+decode token through the layer stack: for every layer, quantise-on-append of
+the new K/V row, then split-K decode attention over all n_kv rows.  The step
+is captured once as a CUDA graph of 128 launches and replayed; each replay
+rewrites row n_kv-1 with the same values, so every step does the full work of
+a decode step at n_kv.  The 64 layers read 2.28 GB of distinct KV per step,
+far more than the 129 MB L2, so nothing is served from L2 across steps.
+
+Printed: one JSON line (rank 0).  value = KV GB/s (algorithmic KV bytes of
+the step / device time of the step); roofline = the attention kernel alone
+(bytes per launch / average launch time) against the measured HBM copy
+bandwidth; e2e = the same metric with the step's inputs copied from pinned
+host memory and its outputs copied back inside the timed region; host = the
+host-resident pipeline at 32k (steps/s, H2D GB/s against the measured pinned
+link); cpu_baseline = the CPU oracle on a bounded sample, on the host cores.
+
+--impl reference times the CPU oracle (the only reference this build has) on
+the same workload, a bounded sample per step.
+Multi-GPU: replicas only (one independent cache per rank, no collective on
+the data path); value = bytes of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn KV GB/s (% of HBM peak); host-KV steps/s at 32k (% of PCIe bw)"
+GB = 1e9
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--n-kv", type=int, default=16384)
+    ap.add_argument("--layers", type=int, default=64)
+    ap.add_argument("--type", default="q8_0", choices=["q8_0", "f16"])
+    ap.add_argument("--host-n", type=int, default=32768, help="host-resident context (0 = skip)")
+    ap.add_argument("--host-steps", type=int, default=4)
+    ap.add_argument("--cpu-sample-layers", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- shapes --
+H, HK, D = 40, 8, 128
+
+
+def kv_bytes_per_row(type_: str) -> int:
+    if type_ == "q8_0":
+        return 2 * HK * (D + (D // 32) * 2)  # 2176
+    return 2 * HK * D * 2  # 4096
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j.get("hbm_gbs", 6800.0)), "measured"
+    return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks --
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", "kvc_clocks_%d_%d.csv" % (os.getpid(), index))
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for name, val in zip(names[1:], parts[5:9]):
+                    if val.lower() in ("active", "1"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- CPU oracle --
+def oracle_sample(n_kv: int, n_layers: int, type_: str, seed: int = 0):
+    """Quantised sample layers for the oracle (not timed)."""
+    import oracle
+    from kv_cache_decode_flash_gb300 import synth
+
+    layers = []
+    for l in range(n_layers):
+        k = synth.normal(seed, synth.stream_id("k", l), n_kv * HK * D, 0.5).reshape(n_kv, HK, D)
+        v = synth.normal(seed, synth.stream_id("v", l), n_kv * HK * D, 0.5).reshape(n_kv, HK, D)
+        q = synth.normal(seed, synth.stream_id("q", l), H * D).reshape(H, D)
+        if type_ == "q8_0":
+            kc, ks = oracle.q8_0_quantize(k)
+            vc, vs = oracle.q8_0_quantize(v)
+            layers.append((q, oracle.Q8_0, kc, ks, vc, vs))
+        else:
+            layers.append((q, oracle.F16, oracle.f32_to_f16(k), None, oracle.f32_to_f16(v), None))
+    return layers
+
+
+def time_oracle(layers, n_kv: int, type_: str):
+    """Oracle decode attention over the sample layers, one task per (layer,
+    query head) on all host cores.  Returns (GB/s, seconds, threads)."""
+    import oracle
+
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    scale = float(np.float32(1.0 / np.sqrt(D)))
+
+    def task(args):
+        (q, t, kc, ks, vc, vs), h = args
+        return oracle.attn(q, t, kc, ks, t, vc, vs, scale, heads=(h, h + 1))
+
+    jobs = [(lay, h) for lay in layers for h in range(H)]
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(task, jobs))
+    dt = time.perf_counter() - t0
+    nbytes = len(layers) * n_kv * kv_bytes_per_row(type_)
+    return nbytes / dt / GB, dt, threads
+
+
+# ------------------------------------------------------------ reference --
+def run_reference(args, rank: int):
+    if rank != 0:
+        return
+    n_layers = 1
+    layers = oracle_sample(args.n_kv, n_layers, args.type)
+    for _ in range(max(args.warmup, 0)):
+        time_oracle(layers, args.n_kv, args.type)
+    times, threads = [], 1
+    for _ in range(args.steps):
+        gbs, dt, threads = time_oracle(layers, args.n_kv, args.type)
+        times.append(dt)
+    total = sum(times)
+    nbytes = n_layers * args.n_kv * kv_bytes_per_row(args.type) * args.steps
+    value = nbytes / total / GB
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * total / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(args),
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": "1 of %d layers per step, all %d query heads, n_kv=%d" % (args.layers, H,
+                                                                                                args.n_kv)},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(args):
+    return {"workload": "decode, %d layers, %d/%d heads, head_dim %d, %s KV, n_kv %d, batch 1"
+                        % (args.layers, H, HK, D, args.type, args.n_kv),
+            "layers": args.layers, "n_head": H, "n_head_kv": HK, "head_dim": D, "kv_type": args.type,
+            "n_kv": args.n_kv, "batch": 1, "rope_base": 1e6,
+            "l2": "no flush: each step reads %.2f GB of distinct KV, far above the 129 MB L2"
+                  % (args.layers * args.n_kv * kv_bytes_per_row(args.type) / GB),
+            "parallelism": "replicas"}
+
+
+# --------------------------------------------------------------- our arm --
+def fill_cache(cache, args, dev, torch):
+    from kv_cache_decode_flash_gb300 import synth
+
+    n0 = args.n_kv - 1
+    chunk = 4096
+    for l in range(args.layers):
+        for p0 in range(0, n0, chunk):
+            m = min(chunk, n0 - p0)
+            k = synth.normal_torch(0, synth.stream_id("k", l, p0), m * HK * D, 0.5, dev).view(m, HK, D)
+            v = synth.normal_torch(0, synth.stream_id("v", l, p0), m * HK * D, 0.5, dev).view(m, HK, D)
+            cache.append(l, 0, p0, k, v)
+    torch.cuda.synchronize()
+
+
+def measure_link(torch, dev) -> float:
+    """Pinned host -> device copy bandwidth at a slot-sized transfer (GB/s)."""
+    n = 256 << 20
+    h = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(n, dtype=torch.uint8, device=dev)
+    d.copy_(h, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        d.copy_(h, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    return 5 * n / (e0.elapsed_time(e1) * 1e-3) / GB
+
+
+def host_pipeline(args, dev, torch, kvc):
+    """Host-resident KV at args.host_n: steps/s ordered vs pipelined."""
+    from kv_cache_decode_flash_gb300 import synth
+
+    n = args.host_n
+    L = args.layers
+    t = kvc.KVC_Q8_0 if args.type == "q8_0" else kvc.KVC_F16
+    res = {}
+    link = measure_link(torch, dev)
+    scale = float(1.0 / np.sqrt(D))
+    cache = kvc.KVCache(L, H, HK, D, n + 64, 1, t, t, 1e6, 0, kvc.KVC_HOST_PINNED)
+    try:
+        for l in range(L):
+            for p0 in range(0, n - 1, 8192):
+                m = min(8192, n - 1 - p0)
+                k = synth.normal_torch(0, synth.stream_id("k", l, p0), m * HK * D, 0.5, dev).view(m, HK, D)
+                v = synth.normal_torch(0, synth.stream_id("v", l, p0), m * HK * D, 0.5, dev).view(m, HK, D)
+                cache.append(l, 0, p0, k, v)
+        q = torch.randn(L, 1, H, D, device=dev)
+        kn = torch.randn(L, 1, HK, D, device=dev) * 0.5
+        vn = torch.randn(L, 1, HK, D, device=dev) * 0.5
+        out = torch.empty_like(q)
+        outs = {}
+        pos = n - 1
+        for name, depth, budget in (("ordered", 0, 128 << 20), ("pipelined", 1, 512 << 20),
+                                    ("declined", 1, 128 << 20)):
+            kvc.kvc_pipeline_depth(cache.ctx, depth)
+            kvc.kvc_pipeline_budget(cache.ctx, budget)
+            times = []
+            for step in range(args.host_steps + 1):
+                if step == 1:
+                    torch.cuda.synchronize()
+                    t0 = time.perf_counter()
+                for l in range(L):
+                    cache.append(l, 0, pos, kn[l], vn[l])
+                    cache.attn_decode(l, [0], q[l], out[l], scale)
+                pos += 1
+            torch.cuda.synchronize()
+            dt = (time.perf_counter() - t0) / args.host_steps
+            st = cache.stats()
+            outs[name] = out.clone()
+            # bytes moved host->device per step: every layer's rows (stable prefix) once
+            h2d = L * (pos - 1) * kv_bytes_per_row(args.type)
+            res[name] = {"steps_per_s": round(1.0 / dt, 3), "ms_per_step": round(1000 * dt, 3),
+                         "h2d_gbs": round(h2d / dt / GB, 2), "frac_of_link": round(h2d / dt / GB / link, 3),
+                         "ring_engaged": st["ring_engaged"], "ring_declined": st["ring_declined"],
+                         "ring_mib": round(st["ring_bytes"] / 2**20, 1)}
+        res["n_kv"] = n
+        res["link_gbs"] = round(link, 2)
+        res["link"] = "pinned H2D, 256 MiB copies, measured in this run"
+        res["note"] = "n_kv grows by one row per step (decode); H2D counts every layer's rows once per step"
+    finally:
+        cache.close()
+    return res
+
+
+def run_ours(args, rank: int, world: int):
+    import torch
+
+    from kv_cache_decode_flash_gb300 import kvc
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    t = kvc.KVC_Q8_0 if args.type == "q8_0" else kvc.KVC_F16
+    L, n = args.layers, args.n_kv
+    cache = kvc.KVCache(L, H, HK, D, n + 256, 1, t, t, 1e6, 0, kvc.KVC_DEVICE, local)
+    fill_cache(cache, args, dev, torch)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1)
+    qbuf = torch.randn(L, 1, H, D, device=dev, generator=g)
+    kbuf = torch.randn(L, 1, HK, D, device=dev, generator=g) * 0.5
+    vbuf = torch.randn(L, 1, HK, D, device=dev, generator=g) * 0.5
+    obuf = torch.empty_like(qbuf)
+    scale = float(1.0 / np.sqrt(D))
+
+    s = torch.cuda.Stream(device=dev)
+    # one eager step creates row n-1 in every layer (allocations happen here, not in capture)
+    with torch.cuda.stream(s):
+        for l in range(L):
+            cache.append(l, 0, n - 1, kbuf[l], vbuf[l], stream=s)
+            cache.attn_decode(l, [0], qbuf[l], obuf[l], scale, stream=s)
+    s.synchronize()
+    # the captured step rewrites row n-1: roll the host bookkeeping back by one row
+    # (seq_rm of the last position keeps the device pages; the graph re-appends it)
+    cache.seq_rm(0, n - 1, -1)
+
+    step_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(step_graph, stream=s):
+        for l in range(L):
+            cache.append(l, 0, n - 1, kbuf[l], vbuf[l], stream=torch.cuda.current_stream())
+            cache.attn_decode(l, [0], qbuf[l], obuf[l], scale, stream=torch.cuda.current_stream())
+    attn_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(attn_graph, stream=s):
+        for l in range(L):
+            cache.attn_decode(l, [0], qbuf[l], obuf[l], scale, stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    def timed(fn, steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for _ in range(steps):
+                fn()
+            e1.record(s)
+        torch.cuda.synchronize()
+        barrier()
+        return e0.elapsed_time(e1) * 1e-3
+
+    for _ in range(max(3, args.warmup)):
+        step_graph.replay()
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    clocks.start()
+    t_step = timed(step_graph.replay, args.steps)
+    clk = clocks.stop()
+    for _ in range(3):
+        attn_graph.replay()
+    t_attn = timed(attn_graph.replay, args.steps)
+
+    # end to end through the public API: inputs from pinned host memory, outputs back
+    hq = torch.empty_like(qbuf, device="cpu").pin_memory()
+    hk = torch.empty_like(kbuf, device="cpu").pin_memory()
+    hv = torch.empty_like(vbuf, device="cpu").pin_memory()
+    ho = torch.empty_like(obuf, device="cpu").pin_memory()
+    hq.copy_(qbuf)
+    hk.copy_(kbuf)
+    hv.copy_(vbuf)
+
+    def e2e_step():
+        qbuf.copy_(hq, non_blocking=True)
+        kbuf.copy_(hk, non_blocking=True)
+        vbuf.copy_(hv, non_blocking=True)
+        step_graph.replay()
+        ho.copy_(obuf, non_blocking=True)
+
+    for _ in range(3):
+        with torch.cuda.stream(s):
+            e2e_step()
+    t_e2e = timed(e2e_step, args.steps)
+
+    # max over ranks
+    times = torch.tensor([t_step, t_attn, t_e2e], dtype=torch.float64, device=dev)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    t_step, t_attn, t_e2e = [float(x) for x in times.cpu()]
+
+    row_bytes = kv_bytes_per_row(args.type)
+    step_bytes = L * n * row_bytes
+    value = world * step_bytes * args.steps / t_step / GB
+    attn_launch_s = t_attn / (args.steps * L)
+    achieved = n * row_bytes / attn_launch_s / GB
+    peak, peak_kind = peaks()
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1000 * t_step / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "%s KV, fp32 accumulate" % args.type,
+        "data": "synthetic (splitmix64 + Box-Muller, N(0,1)*0.5 K/V)", "config": config_dict(args),
+        "steps_per_s": round(args.steps / t_step, 2),
+        "hbm_frac": round(value / world / peak, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "attn_kernel (decode attention), %d bytes per launch" % (n * row_bytes),
+                     "peak_kind": "%s (MEASURED_PEAKS.json hbm_gbs, burst copy)" % peak_kind,
+                     "launch_us": round(attn_launch_s * 1e6, 3)},
+        "e2e": {"value": round(world * step_bytes * args.steps / t_e2e / GB, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(hq.numel() * 4 + hk.numel() * 4 + hv.numel() * 4),
+                "d2h_bytes_per_step": int(ho.numel() * 4)},
+        "gpu_launches": 2 * L * args.steps,
+        "clocks": clk,
+    }
+    cache.close()
+    del cache
+    torch.cuda.empty_cache()
+    if rank == 0 and args.host_n > 0:
+        try:
+            out["host"] = host_pipeline(args, dev, torch, kvc)
+        except Exception as e:  # reported, not fatal
+            out["host"] = {"error": str(e)[:300]}
+    if rank == 0 and not args.no_cpu_baseline:
+        layers = oracle_sample(n, args.cpu_sample_layers, args.type)
+        gbs, dt, threads = time_oracle(layers, n, args.type)
+        out["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                               "sample": "%d of %d layers, all %d query heads, n_kv=%d (%.1f s)"
+                                         % (args.cpu_sample_layers, L, H, n, dt)}
+    return out
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        dist.init_process_group(backend)
+    if args.impl == "reference":
+        run_reference(args, rank)
+    else:
+        import __graft_entry__
+
+        __graft_entry__.build()
+        out = run_ours(args, rank, world)
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,269 @@
+/*
+ * kvc.h - decode attention over a quantised grouped-query KV cache on one
+ * GB300 GPU (sm_103a), with the sequence operations a host-RAM cold store is
+ * built from and a host-resident mode that streams each layer's K/V from
+ * pinned host memory through a staging ring.
+ *
+ * Sources (web pages; cited by title and section):
+ *  [F5]   "F5 - Advanced KV Cache Techniques" (opencoti llamafile docs).
+ *  [COLD] "Plan: lossless long context - derived hot/cold sizing (#5) +
+ *          host-RAM KV cold store (#3)" (contenox modeld docs).
+ *  [R4]   "sched: pipeline the delivery of a host-resident KV cache (R4)"
+ *          (llama.cpp pull request).
+ *
+ * Conventions for every call:
+ *  - Every function returns a kvc_status (0 = KVC_OK, negative = error) except
+ *    kvc_destroy, kvc_last_error, kvc_status_str and kvc_params_init.  A bad
+ *    argument never aborts the process; on error the call leaves the cache as
+ *    it was (no partial effect) unless the status is KVC_ECUDA or
+ *    KVC_EINTERNAL, after which the context should be destroyed.
+ *    kvc_last_error(ctx) gives a one-line description of the last error.
+ *  - Ownership: the library owns every KV byte (device pools, pinned host
+ *    store, staging ring, work space).  The caller owns q, out, k, v (device
+ *    pointers, e.g. torch tensors) and all host byte buffers; the library
+ *    never keeps a caller pointer after a call returns.
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *    default stream).  kvc_append and kvc_attn_decode only enqueue work on it
+ *    and return without waiting; calls on one context must be issued from one
+ *    host thread and be ordered on the device (one stream, or events).
+ *    The sequence and state operations are synchronous: they wait for all
+ *    device work already issued in the process, run, and return when their
+ *    effect is complete (kvc_state_get's bytes are valid at return).
+ *  - A context is not thread-safe; distinct contexts are independent.
+ *  - Positions are int32.  Ranges [p0, p1) are half-open; p0 < 0 means 0 and
+ *    p1 < 0 means "no upper bound" (the llama.cpp sequence-op convention).
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct kvc_ctx kvc_ctx;
+
+typedef enum kvc_status {
+    KVC_OK = 0,
+    KVC_EINVAL = -1,     /* bad argument, unsupported geometry or call order */
+    KVC_ENOMEM = -2,     /* device or pinned host allocation failed */
+    KVC_ENOSPC = -3,     /* no free cells / pages left for new rows */
+    KVC_ERANGE = -4,     /* position out of range (e.g. a shift below 0) */
+    KVC_EFORMAT = -5,    /* state bytes malformed or of another geometry */
+    KVC_ECUDA = -6,      /* a CUDA call failed (sticky errors included) */
+    KVC_ETIMEDOUT = -7,  /* a bounded host wait or device wait gave up */
+    KVC_EINTERNAL = -8   /* a kernel reported an inconsistency */
+} kvc_status;
+
+/* Storage type of K and of V.
+ * KVC_Q8_0: blocks of 32 elements stored as 32 int8 codes plus one fp16
+ * scale d; d = max|x| / 127 and code = round-half-away-from-zero(x * (1/d))
+ * in fp32, scale stored as fp16(d) round-to-nearest-even.  The type is named
+ * in [F5] section M6 ("-ctk q8_0") and [R4] section Measurements ("q8_0
+ * K/V"); the pages give no bit layout, so this plainest reading is pinned.
+ * KVC_F16: IEEE binary16, round to nearest even. */
+typedef enum kvc_type { KVC_F16 = 1, KVC_Q8_0 = 8 } kvc_type;
+
+/* Where a context keeps its K/V.
+ * KVC_DEVICE: device HBM, paged, any number of sequences.
+ * KVC_HOST_PINNED: pinned host RAM, one sequence (id 0); each layer's rows
+ * are delivered to the device through a staging ring before attention
+ * ([R4] section What it does).  Only kvc_append and kvc_attn_decode are
+ * available; the sequence and state operations return KVC_EINVAL. */
+typedef enum kvc_residency { KVC_DEVICE = 0, KVC_HOST_PINNED = 1 } kvc_residency;
+
+/* Rotary pairing used by kvc_seq_add.  NEOX pairs (i, i + D/2); NORM pairs
+ * (2i, 2i + 1).  The pages do not say which; NEOX is the default. */
+typedef enum kvc_rope { KVC_ROPE_NEOX = 0, KVC_ROPE_NORM = 1 } kvc_rope;
+
+typedef struct kvc_params {
+    int32_t n_layer;    /* >= 1 */
+    int32_t n_head;     /* query heads H; a multiple of n_head_kv */
+    int32_t n_head_kv;  /* KV heads Hk; query head h reads KV head h / (H/Hk) */
+    int32_t head_dim;   /* D: 64 or 128 */
+    int32_t n_ctx;      /* device: cells per layer shared by all sequences;
+                           host-resident: capacity of the one sequence */
+    int32_t n_seq_max;  /* sequence ids are 0 .. n_seq_max-1 */
+    int32_t type_k;     /* kvc_type */
+    int32_t type_v;     /* kvc_type */
+    float rope_base;    /* theta_i = rope_base^(-2i/D) */
+    int32_t rope_mode;  /* kvc_rope */
+    int32_t residency;  /* kvc_residency */
+    int32_t device;     /* CUDA device ordinal */
+    int32_t page_rows;  /* device residency: cells per page, a multiple of 16
+                           in [16, 4096]; 0 selects 256 */
+} kvc_params;
+
+/* Fill *p with defaults: 1 layer, 8 heads, 2 KV heads, D 64, 512 cells,
+ * 1 sequence, q8_0/q8_0, base 10000, NEOX, device residency, device 0. */
+void kvc_params_init(kvc_params *p);
+
+/* Create a context: validates *p, allocates the K/V store (device pools or
+ * pinned host store), the work space and the per-sequence page tables.
+ * On success *out owns them until kvc_destroy.  Errors: KVC_EINVAL
+ * (geometry), KVC_ENOMEM, KVC_ECUDA. */
+int kvc_create(const kvc_params *p, kvc_ctx **out);
+
+/* Free everything the context owns (waits for its device work).  NULL is a no-op. */
+void kvc_destroy(kvc_ctx *c);
+
+const char *kvc_last_error(const kvc_ctx *c);
+const char *kvc_status_str(int status);
+
+/* Quantise-on-append: write n_tok new rows of layer `layer` for sequence
+ * `seq` at positions pos0 .. pos0+n_tok-1.
+ * k, v: device fp32 [n_tok][n_head_kv][head_dim], contiguous.
+ * The K/V rows of a token are written per layer, as a model produces them
+ * (the cpy_k/cpy_v writes of [F5] section M2 - HeadInfer).  The first layer
+ * to append a position creates the row (allocating cells); the other layers
+ * must then append the same positions in the same order.
+ * Host-resident contexts also write the rows into the staging slot that
+ * holds this layer ([R4] section What it does, item 1: the rows written
+ * this step are the ones outside the stable prefix).
+ * Errors: KVC_EINVAL (ids, n_tok < 1, positions not matching the rows other
+ * layers created), KVC_ENOSPC (no free pages), KVC_ECUDA. */
+int kvc_append(kvc_ctx *c, int layer, int seq, int pos0, int n_tok, const float *k,
+               const float *v, void *stream);
+
+/* Single-token decode attention for n_seq sequences of one layer:
+ *   out[i][h][:] = softmax_j(kq_scale * q[i][h] . K_j) V_j
+ * over every row j the sequence holds for that layer, with K/V read as
+ * stored (q8_0 or f16) and query head h reading KV head h / (H/Hk)
+ * ([F5] sections M2/M3: grouped-query heads stay in whole KV-head groups).
+ * Computed as split-K flash decoding: KV chunks of the same sequence run on
+ * different CTAs and their partial (max, sum, output) triples are merged with
+ * the online-softmax rule ([F5] section M4 - ScoutAttention: merge via
+ * FlashAttention's online-softmax; section F5-opt W4: inter-tile online
+ * softmax).  Accumulation is fp32; the merge order is fixed, so a call is
+ * bitwise repeatable.
+ * seq_ids: HOST int32[n_seq] (distinct ids).  q: device fp32
+ * [n_seq][n_head][head_dim]; out: device fp32, same shape (may not alias q).
+ * A sequence with no rows yields a zero output row.
+ * Host-resident contexts: n_seq must be 1 and seq_ids[0] 0; the layer's rows
+ * are delivered through the staging ring first ([R4] section What it does).
+ * Errors: KVC_EINVAL, KVC_ECUDA. */
+int kvc_attn_decode(kvc_ctx *c, int layer, int n_seq, const int32_t *seq_ids, const float *q,
+                    float *out, float kq_scale, void *stream);
+
+/* Remove the rows of `seq` whose position is in [p0, p1), in every layer
+ * (MemorySeqRemove, [COLD] section llama - KV-byte offload; the context
+ * shift's discard, [F5] section M1).  Rows after the removed ones keep their
+ * order; whole pages are freed, partly used boundary pages are compacted
+ * on the device.  An empty range is a no-op.  Errors: KVC_EINVAL. */
+int kvc_seq_rm(kvc_ctx *c, int seq, int p0, int p1);
+
+/* Copy the rows of `src` whose position is in [p0, p1) to the end of `dst`,
+ * all layers, K and V, positions unchanged (MemorySeqCopy, [COLD] section
+ * llama - KV-byte offload).  The copy is physical: later operations on one
+ * sequence never change the other.  src == dst is a no-op.
+ * Errors: KVC_EINVAL, KVC_ENOSPC. */
+int kvc_seq_cp(kvc_ctx *c, int src, int dst, int p0, int p1);
+
+/* Add `delta` to the position of every row of `seq` whose position is in
+ * [p0, p1) and rotate its stored K by delta positions (MemorySeqAdd, [COLD]
+ * section llama - KV-byte offload; shifted imports rotate RoPE-positioned
+ * keys by the destination/source position delta, [COLD] section OpenVINO -
+ * KV-byte offload).  Each rotary pair (see kvc_rope) turns by the angle
+ * delta * rope_base^(-2i/D), computed in fp64 on the host.  q8_0 K rows are
+ * dequantised, rotated in fp32 and requantised; f16 rows are rotated in fp32
+ * and rounded to f16.  V is untouched.  delta == 0 is a no-op.
+ * Errors: KVC_EINVAL, KVC_ERANGE (a position would leave [0, INT32_MAX]). */
+int kvc_seq_add(kvc_ctx *c, int seq, int p0, int p1, int delta);
+
+/* Export the rows of `seq` with position in [p0, p1) (in row order) as bytes
+ * (StateSeqGetData, [COLD] section llama - KV-byte offload: evicted KV is
+ * parked in host RAM as bytes).  dst: HOST buffer of cap bytes; dst == NULL
+ * only reports the size in *n_written.  Errors: KVC_EINVAL, KVC_ENOSPC when
+ * cap is too small (*n_written then holds the size needed).
+ *
+ * Byte format, version 1, little endian; every section is zero-padded to a
+ * multiple of 16 bytes:
+ *   header, 64 bytes: u32 magic 0x3143564B ("KVC1"), u32 version = 1,
+ *     u32 n_layer, u32 n_head_kv, u32 head_dim, u32 type_k, u32 type_v,
+ *     u32 n_tok, u64 payload_bytes (everything after the positions),
+ *     24 zero bytes;
+ *   positions: int32 pos[n_tok];
+ *   payload: for each layer, the K section then the V section, where a q8_0
+ *     section is codes int8 [n_head_kv][n_tok][head_dim] followed by scales
+ *     u16 (fp16 bits) [n_head_kv][n_tok][head_dim/32], and an f16 section is
+ *     u16 [n_head_kv][n_tok][head_dim]. */
+int kvc_state_get(kvc_ctx *c, int seq, int p0, int p1, void *dst, size_t cap,
+                  size_t *n_written);
+
+/* Import bytes written by kvc_state_get into `seq`, appending the rows at
+ * their stored positions (append mode: StateSeqSetData, [COLD] section
+ * llama - KV-byte offload).  src: HOST buffer of n bytes.  *n_read (may be
+ * NULL) receives the bytes consumed.  The header must match this context's
+ * n_layer, n_head_kv, head_dim, type_k and type_v.
+ * Errors: KVC_EFORMAT (bad magic, version, geometry, length), KVC_ENOSPC. */
+int kvc_state_set(kvc_ctx *c, int seq, const void *src, size_t n, size_t *n_read);
+
+/* Pipeline depth N of the host-resident transport: deliveries are issued N
+ * layers ahead into an (N+2)-slot ring; 0 is the ordered path exactly
+ * (deliver, then attend, in stream order).  Default 1 ([R4] section What it
+ * does: --kv-pipeline-depth).  Changing it releases the ring and clears the
+ * budget latch.  Device-resident contexts accept and ignore it (the
+ * transport is never created).  Errors: KVC_EINVAL (n < 0 or n > 16). */
+int kvc_pipeline_depth(kvc_ctx *c, int n);
+
+/* Device-memory budget of the staging ring, in bytes.  Default 128 MiB
+ * ([R4] section Device memory: --kv-pipeline-budget).  The need,
+ * (N+2) * bytes of one layer's K+V over the current context, is checked
+ * before anything is allocated on every plan; a ring that does not fit is
+ * declined and the decision is latched, the transfer stream and events are
+ * created only when a ring is engaged and released with it, and a declined
+ * context runs the ordered path.  Changing the budget releases the ring and
+ * clears the latch.  Errors: KVC_EINVAL. */
+int kvc_pipeline_budget(kvc_ctx *c, size_t bytes);
+
+/* Number of rows `seq` holds in every layer (after all appends of a step). */
+int kvc_seq_n_tokens(const kvc_ctx *c, int seq, int32_t *n);
+
+/* Positions of the rows of `seq`, in row order.  pos: HOST int32[cap];
+ * *n receives the row count (pos may be NULL to query it). */
+int kvc_seq_positions(const kvc_ctx *c, int seq, int32_t *pos, int32_t cap, int32_t *n);
+
+/* Counters describing the host-resident transport and the caches. */
+typedef struct kvc_stats {
+    int32_t ring_engaged;       /* 1 while a ring is allocated */
+    int32_t ring_declined;      /* 1 once the budget latch tripped */
+    int32_t ring_slots;         /* N+2 when engaged, else 0 */
+    int32_t transfer_stream;    /* 1 while the transfer stream exists */
+    int64_t slot_bytes;         /* bytes of one slot (one layer's K+V) */
+    int64_t ring_bytes;         /* device bytes held by the ring */
+    int64_t ordered_bytes;      /* device bytes of the ordered-path buffer */
+    int64_t deliveries_early;   /* deliveries issued ahead on the transfer stream */
+    int64_t deliveries_ordered; /* deliveries issued in stream order */
+    int64_t bytes_delivered;    /* host-to-device bytes issued */
+    int64_t pages_total;        /* device residency: pages per layer */
+    int64_t pages_free;
+    int64_t device_bytes;       /* all device memory held by the context */
+    int64_t host_pinned_bytes;  /* pinned host memory held by the context */
+} kvc_stats;
+
+int kvc_get_stats(const kvc_ctx *c, kvc_stats *out);
+
+/* Force the split-K chunk length in rows (a multiple of 16) for every later
+ * kvc_attn_decode; 0 restores the automatic choice, which depends only on
+ * the row counts, the geometry and the device's SM count.  Errors: KVC_EINVAL. */
+int kvc_set_chunk_rows(kvc_ctx *c, int rows);
+
+/* Limit, in milliseconds, of every bounded host wait of the synchronous
+ * operations (default 120000).  A wait that runs out returns KVC_ETIMEDOUT. */
+int kvc_set_timeout_ms(kvc_ctx *c, int ms);
+
+/* Host-side fault injection for tests: the next `n` internal allocations
+ * succeed and the ones after fail with KVC_ENOMEM; n < 0 disables it. */
+int kvc_debug_fail_alloc_after(kvc_ctx *c, int n);
+
+/* Read and clear the device error word that kernels set instead of
+ * trapping (a bounded wait that gave up, an index out of range).
+ * *word receives it (0 = none).  Waits for the context's device work. */
+int kvc_check_device_error(kvc_ctx *c, uint32_t *word);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVC_H */

@@ -1,0 +1,955 @@
+// api.cu - the C ABI (include/kvc.h): validation, the cache manager (host
+// metadata of sequences, pages and positions) and the sequence and state
+// operations.  The host-resident transport lives in transport.cu.
+#include "ctx.h"
+
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <chrono>
+#include <climits>
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <thread>
+
+namespace kvc {
+
+// ---------------------------------------------------------------- helpers --
+
+int cuda_fail(Ctx *c, cudaError_t e, const char *what) {
+    return c->fail(KVC_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define KVC_CU(c, call)                                                                                            \
+    do {                                                                                                           \
+        cudaError_t e_ = (call);                                                                                   \
+        if (e_ != cudaSuccess) return cuda_fail((c), e_, #call);                                                   \
+    } while (0)
+
+static bool take_alloc(Ctx *c) {
+    if (c->fail_after < 0) return true;
+    if (c->fail_after == 0) return false;
+    --c->fail_after;
+    return true;
+}
+
+int dev_alloc(Ctx *c, void **p, int64_t bytes, const char *what) {
+    *p = nullptr;
+    if (bytes <= 0) return KVC_OK;
+    if (!take_alloc(c)) return c->fail(KVC_ENOMEM, std::string("injected allocation failure: ") + what);
+    cudaError_t e = cudaMalloc(p, (size_t)bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *p = nullptr;
+        return c->fail(KVC_ENOMEM, std::string("cudaMalloc failed for ") + what + ": " + cudaGetErrorString(e));
+    }
+    c->device_bytes += bytes;
+    return KVC_OK;
+}
+
+void dev_free(Ctx *c, void *p, int64_t bytes) {
+    if (!p) return;
+    cudaFree(p);
+    c->device_bytes -= bytes;
+}
+
+// Wait for the internal stream with a deadline (polling; never an unbounded block).
+int wait_internal(Ctx *c) {
+    KVC_CU(c, cudaEventRecord(c->done, c->st));
+    auto t0 = std::chrono::steady_clock::now();
+    for (;;) {
+        cudaError_t e = cudaEventQuery(c->done);
+        if (e == cudaSuccess) break;
+        if (e != cudaErrorNotReady) return cuda_fail(c, e, "device work of a synchronous operation");
+        auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(std::chrono::steady_clock::now() - t0).count();
+        if (ms > c->timeout_ms) return c->fail(KVC_ETIMEDOUT, "timed out waiting for device work");
+        std::this_thread::sleep_for(std::chrono::microseconds(50));
+    }
+    uint32_t word = 0;
+    KVC_CU(c, cudaMemcpyAsync(&word, c->err_dev, 4, cudaMemcpyDeviceToHost, c->st));
+    KVC_CU(c, cudaStreamSynchronize(c->st));
+    if (word) return c->fail(KVC_EINTERNAL, "a kernel reported device error word " + std::to_string(word));
+    return KVC_OK;
+}
+
+// Synchronous operations first wait for all device work issued so far.
+int enter_sync(Ctx *c) {
+    KVC_CU(c, cudaSetDevice(c->dev));
+    KVC_CU(c, cudaDeviceSynchronize());
+    return KVC_OK;
+}
+
+static int ensure_staging(Ctx *c, int64_t bytes) {
+    if (bytes <= c->staging_bytes) return KVC_OK;
+    dev_free(c, c->staging, c->staging_bytes);
+    c->staging = nullptr;
+    c->staging_bytes = 0;
+    int64_t want = std::max<int64_t>(bytes, 1 << 20);
+    int rc = dev_alloc(c, (void **)&c->staging, want, "staging");
+    if (rc) return rc;
+    c->staging_bytes = want;
+    return KVC_OK;
+}
+
+static int upload_segments(Ctx *c, const std::vector<Segment> &segs) {
+    if (segs.empty()) return KVC_OK;
+    if ((int64_t)segs.size() > c->segs_cap) {
+        dev_free(c, c->segs_dev, c->segs_cap * (int64_t)sizeof(Segment));
+        c->segs_dev = nullptr;
+        c->segs_cap = 0;
+        int64_t cap = std::max<int64_t>((int64_t)segs.size(), 4096);
+        int rc = dev_alloc(c, (void **)&c->segs_dev, cap * (int64_t)sizeof(Segment), "segment list");
+        if (rc) return rc;
+        c->segs_cap = cap;
+    }
+    KVC_CU(c, cudaMemcpyAsync(c->segs_dev, segs.data(), segs.size() * sizeof(Segment), cudaMemcpyHostToDevice,
+                              c->st));
+    KVC_CU(c, launch_copy_segments(c->segs_dev, (int)segs.size(), c->st));
+    return KVC_OK;
+}
+
+// Re-upload the page tables of `s` (synchronous path).
+static int upload_pages(Ctx *c, int s) {
+    Seq &q = c->seqs[s];
+    if (!q.pages.empty())
+        KVC_CU(c, cudaMemcpyAsync(c->pt_dev + (int64_t)s * c->max_pages, q.pages.data(), q.pages.size() * 4,
+                                  cudaMemcpyHostToDevice, c->st));
+    q.dev_pages = (int32_t)q.pages.size();
+    return KVC_OK;
+}
+
+// Physical row index of (page, kv head, cell) in a layer pool.
+static inline int64_t prow(const Ctx *c, int32_t page, int g, int32_t cell) {
+    return ((int64_t)page * c->Hk + g) * c->P + cell;
+}
+
+static inline void phys(const Ctx *c, const Seq &q, int64_t r, int32_t &page, int32_t &cell) {
+    const int64_t lr = r + q.off;
+    page = q.pages[(size_t)(lr / c->P)];
+    cell = (int32_t)(lr % c->P);
+}
+
+// Pages needed to hold rows [0, n) of a sequence with offset off.
+static inline int32_t pages_for(const Ctx *c, int32_t off, int64_t n) {
+    return n <= 0 ? 0 : (int32_t)((off + n + c->P - 1) / c->P);
+}
+
+// Grow sequence `s` by `add` rows (pages only; positions and counts are the
+// caller's).  Returns the indices of the new pages in q.pages via `first_new`.
+static int grow_pages(Ctx *c, Seq &q, int64_t add, size_t *first_new) {
+    *first_new = q.pages.size();
+    const int32_t need = pages_for(c, q.off, (int64_t)q.n + add);
+    if (need > c->max_pages) return c->fail(KVC_ENOSPC, "sequence would exceed the page table");
+    const int32_t extra = need - (int32_t)q.pages.size();
+    if (extra > (int32_t)c->free_pages.size()) return c->fail(KVC_ENOSPC, "no free pages");
+    for (int32_t i = 0; i < extra; ++i) {
+        q.pages.push_back(c->free_pages.back());
+        c->free_pages.pop_back();
+    }
+    return KVC_OK;
+}
+
+static void release_tail_pages(Ctx *c, Seq &q) {
+    const int32_t need = pages_for(c, q.off, q.n);
+    while ((int32_t)q.pages.size() > need) {
+        c->free_pages.push_back(q.pages.back());
+        q.pages.pop_back();
+    }
+    if (q.n == 0) q.off = 0;
+    q.dev_pages = std::min<int32_t>(q.dev_pages, (int32_t)q.pages.size());
+}
+
+// Byte segments copying logical rows [a, a+len) of sequence qa to logical rows
+// [b, b+len) of qb (same layer pools), all layers, K and V.
+static void add_row_copies(const Ctx *c, const Seq &qa, int64_t a, const Seq &qb, int64_t b, int64_t len,
+                           std::vector<Segment> &out) {
+    int64_t done = 0;
+    while (done < len) {
+        int32_t pa, ca, pb, cb;
+        phys(c, qa, a + done, pa, ca);
+        phys(c, qb, b + done, pb, cb);
+        int64_t run = std::min<int64_t>(len - done, std::min<int64_t>(c->P - ca, c->P - cb));
+        for (int l = 0; l < c->L; ++l) {
+            for (int g = 0; g < c->Hk; ++g) {
+                const int64_t ra = prow(c, pa, g, ca) + (int64_t)l * c->pool_rows;
+                const int64_t rb = prow(c, pb, g, cb) + (int64_t)l * c->pool_rows;
+                out.push_back({c->kdata + ra * c->krow, c->kdata + rb * c->krow, run * c->krow});
+                out.push_back({c->vdata + ra * c->vrow, c->vdata + rb * c->vrow, run * c->vrow});
+                if (c->ksb) out.push_back({c->kscales + ra * c->ksb, c->kscales + rb * c->ksb, run * c->ksb});
+                if (c->vsb) out.push_back({c->vscales + ra * c->vsb, c->vscales + rb * c->vsb, run * c->vsb});
+            }
+        }
+        done += run;
+    }
+}
+
+static inline int64_t pad16(int64_t x) { return (x + 15) / 16 * 16; }
+
+// State format sizes (see include/kvc.h).
+static int64_t section_bytes(const Ctx *c, int type, int64_t n) {
+    if (type == KVC_Q8_0) return pad16((int64_t)c->Hk * n * c->D) + pad16((int64_t)c->Hk * n * (c->D / QK) * 2);
+    return pad16((int64_t)c->Hk * n * c->D * 2);
+}
+static int64_t payload_bytes(const Ctx *c, int64_t n) {
+    return (int64_t)c->L * (section_bytes(c, c->tk, n) + section_bytes(c, c->tv, n));
+}
+static int64_t state_bytes(const Ctx *c, int64_t n) { return 64 + pad16(4 * n) + payload_bytes(c, n); }
+
+// Segments between the pools and a packed payload laid out as in the state
+// format, for the rows idx[] of sequence q.  to_payload selects direction.
+static void add_payload_copies(const Ctx *c, const Seq &q, const std::vector<int64_t> &idx, uint8_t *payload,
+                               bool to_payload, std::vector<Segment> &out) {
+    const int64_t n = (int64_t)idx.size();
+    int64_t off = 0;
+    // runs of consecutive logical rows that stay inside one page
+    std::vector<std::pair<int64_t, int64_t>> runs; // (selection index, length)
+    for (int64_t i = 0; i < n;) {
+        int64_t j = i + 1;
+        int32_t p0, c0;
+        phys(c, q, idx[i], p0, c0);
+        while (j < n && idx[j] == idx[j - 1] + 1 && c0 + (j - i) < c->P) ++j;
+        runs.push_back({i, j - i});
+        i = j;
+    }
+    for (int l = 0; l < c->L; ++l) {
+        for (int t = 0; t < 2; ++t) {
+            const int type = t == 0 ? c->tk : c->tv;
+            uint8_t *data = t == 0 ? c->kdata : c->vdata;
+            uint8_t *scales = t == 0 ? c->kscales : c->vscales;
+            const int rowb = t == 0 ? c->krow : c->vrow;
+            const int sb = t == 0 ? c->ksb : c->vsb;
+            const int64_t data_off = off;
+            const int64_t scale_off = off + pad16((int64_t)c->Hk * n * rowb);
+            for (auto &rn : runs) {
+                int32_t pg, cl;
+                phys(c, q, idx[rn.first], pg, cl);
+                for (int g = 0; g < c->Hk; ++g) {
+                    const int64_t R = prow(c, pg, g, cl) + (int64_t)l * c->pool_rows;
+                    uint8_t *pd = payload + data_off + ((int64_t)g * n + rn.first) * rowb;
+                    uint8_t *cd = data + R * rowb;
+                    if (to_payload)
+                        out.push_back({cd, pd, rn.second * rowb});
+                    else
+                        out.push_back({pd, cd, rn.second * rowb});
+                    if (type == KVC_Q8_0) {
+                        uint8_t *ps = payload + scale_off + ((int64_t)g * n + rn.first) * sb;
+                        uint8_t *cs = scales + R * sb;
+                        if (to_payload)
+                            out.push_back({cs, ps, rn.second * sb});
+                        else
+                            out.push_back({ps, cs, rn.second * sb});
+                    }
+                }
+            }
+            off += section_bytes(c, type, n);
+        }
+    }
+}
+
+static void select_rows(const Seq &q, int64_t p0, int64_t p1, std::vector<int64_t> &idx) {
+    idx.clear();
+    for (int64_t r = 0; r < q.n; ++r)
+        if (q.pos[(size_t)r] >= p0 && q.pos[(size_t)r] < p1) idx.push_back(r);
+}
+
+static void norm_range(int p0, int p1, int64_t &a, int64_t &b) {
+    a = p0 < 0 ? 0 : p0;
+    b = p1 < 0 ? (int64_t)INT32_MAX + 1 : p1;
+}
+
+} // namespace kvc
+
+using namespace kvc;
+
+// -------------------------------------------------------------- transport --
+namespace kvc {
+int transport_attn(Ctx *c, int layer, const float *q, float *out, float kq_scale, cudaStream_t st);
+int transport_append(Ctx *c, int layer, int n_tok, const float *k, const float *v, cudaStream_t st);
+void transport_release(Ctx *c);
+int launch_attention(Ctx *c, const LayerView &lv, const CUtensorMap *tmk, const CUtensorMap *tmv, int P,
+                     int64_t scale_limit, int n_seq, const AttnSeq *seqs_in, const float *q, float *out,
+                     float kq_scale, cudaStream_t st);
+} // namespace kvc
+
+// ------------------------------------------------------------------ ABI ----
+
+extern "C" {
+
+void kvc_params_init(kvc_params *p) {
+    if (!p) return;
+    std::memset(p, 0, sizeof(*p));
+    p->n_layer = 1;
+    p->n_head = 8;
+    p->n_head_kv = 2;
+    p->head_dim = 64;
+    p->n_ctx = 512;
+    p->n_seq_max = 1;
+    p->type_k = KVC_Q8_0;
+    p->type_v = KVC_Q8_0;
+    p->rope_base = 10000.0f;
+    p->rope_mode = KVC_ROPE_NEOX;
+    p->residency = KVC_DEVICE;
+    p->device = 0;
+    p->page_rows = 0;
+}
+
+const char *kvc_status_str(int s) {
+    switch (s) {
+    case KVC_OK: return "ok";
+    case KVC_EINVAL: return "invalid argument";
+    case KVC_ENOMEM: return "out of memory";
+    case KVC_ENOSPC: return "no space";
+    case KVC_ERANGE: return "out of range";
+    case KVC_EFORMAT: return "bad state format";
+    case KVC_ECUDA: return "CUDA error";
+    case KVC_ETIMEDOUT: return "timed out";
+    case KVC_EINTERNAL: return "internal error";
+    default: return "unknown status";
+    }
+}
+
+const char *kvc_last_error(const kvc_ctx *c) {
+    if (!c) return "null context";
+    return reinterpret_cast<const Ctx *>(c)->err.c_str();
+}
+
+void kvc_destroy(kvc_ctx *cc) {
+    if (!cc) return;
+    Ctx *c = reinterpret_cast<Ctx *>(cc);
+    cudaSetDevice(c->dev);
+    cudaDeviceSynchronize();
+    transport_release(c);
+    if (c->tr.ordered.kdata) {
+        cudaFree(c->tr.ordered.kdata);
+        cudaFree(c->tr.ordered.vdata);
+        cudaFree(c->tr.ordered.kscales);
+        cudaFree(c->tr.ordered.vscales);
+    }
+    cudaFree(c->kdata);
+    cudaFree(c->vdata);
+    cudaFree(c->kscales);
+    cudaFree(c->vscales);
+    cudaFree(c->pt_dev);
+    cudaFree(c->part);
+    cudaFree(c->tickets);
+    cudaFree(c->err_dev);
+    cudaFree(c->staging);
+    cudaFree(c->segs_dev);
+    cudaFree(c->rows_dev);
+    cudaFree(c->zero_pt);
+    if (c->hk) cudaFreeHost(c->hk);
+    if (c->hv) cudaFreeHost(c->hv);
+    if (c->hks) cudaFreeHost(c->hks);
+    if (c->hvs) cudaFreeHost(c->hvs);
+    for (auto ev : c->app_ev)
+        if (ev) cudaEventDestroy(ev);
+    if (c->st) cudaStreamDestroy(c->st);
+    if (c->done) cudaEventDestroy(c->done);
+    delete c;
+}
+
+int kvc_create(const kvc_params *p, kvc_ctx **out) {
+    if (!p || !out) return KVC_EINVAL;
+    *out = nullptr;
+    Ctx *c = new (std::nothrow) Ctx();
+    if (!c) return KVC_ENOMEM;
+    c->prm = *p;
+    auto bad = [&](const char *m) {
+        c->err = m;
+        delete c;
+        return KVC_EINVAL;
+    };
+    if (p->n_layer < 1 || p->n_head < 1 || p->n_head_kv < 1 || p->n_head % p->n_head_kv) return bad("bad head counts");
+    if (p->head_dim != 64 && p->head_dim != 128) return bad("head_dim must be 64 or 128");
+    if (p->n_head / p->n_head_kv > MAX_GROUP) return bad("more than 8 query heads per KV head");
+    if (p->n_ctx < 1 || p->n_seq_max < 1) return bad("n_ctx and n_seq_max must be positive");
+    if ((p->type_k != KVC_Q8_0 && p->type_k != KVC_F16) || (p->type_v != KVC_Q8_0 && p->type_v != KVC_F16))
+        return bad("type must be KVC_Q8_0 or KVC_F16");
+    if (p->type_k != p->type_v) return bad("K and V must have the same type");
+    if (p->rope_mode != KVC_ROPE_NEOX && p->rope_mode != KVC_ROPE_NORM) return bad("bad rope_mode");
+    if (!(p->rope_base > 1.0f) || !std::isfinite(p->rope_base)) return bad("rope_base must be > 1");
+    if (p->residency != KVC_DEVICE && p->residency != KVC_HOST_PINNED) return bad("bad residency");
+    int page_rows = p->page_rows ? p->page_rows : 256;
+    if (page_rows < 16 || page_rows > 4096 || page_rows % 16) return bad("page_rows must be a multiple of 16 in [16, 4096]");
+    if (p->residency == KVC_HOST_PINNED && p->n_seq_max != 1) return bad("host-resident contexts hold one sequence");
+
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || p->device < 0 || p->device >= ndev) {
+        cudaGetLastError();
+        c->err = "no such CUDA device";
+        delete c;
+        return KVC_ECUDA;
+    }
+    c->dev = p->device;
+    cudaSetDevice(c->dev);
+    cudaDeviceGetAttribute(&c->sms, cudaDevAttrMultiProcessorCount, c->dev);
+    c->H = p->n_head;
+    c->Hk = p->n_head_kv;
+    c->D = p->head_dim;
+    c->r = c->H / c->Hk;
+    c->L = p->n_layer;
+    c->tk = p->type_k;
+    c->tv = p->type_v;
+    c->krow = c->tk == KVC_Q8_0 ? c->D : 2 * c->D;
+    c->vrow = c->tv == KVC_Q8_0 ? c->D : 2 * c->D;
+    c->ksb = c->tk == KVC_Q8_0 ? (c->D / QK) * 2 : 0;
+    c->vsb = c->tv == KVC_Q8_0 ? (c->D / QK) * 2 : 0;
+    c->host = p->residency == KVC_HOST_PINNED;
+
+    auto fail = [&](int rc) {
+        kvc_destroy(reinterpret_cast<kvc_ctx *>(c));
+        return rc;
+    };
+    int rc;
+    if (cudaStreamCreateWithFlags(&c->st, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c->done, cudaEventDisableTiming) != cudaSuccess) {
+        c->err = "stream/event creation failed";
+        return fail(KVC_ECUDA);
+    }
+    if ((rc = dev_alloc(c, (void **)&c->err_dev, 4, "error word"))) return fail(rc);
+    cudaMemset(c->err_dev, 0, 4);
+    if ((rc = dev_alloc(c, (void **)&c->tickets, (int64_t)MAX_SEQ_PER_LAUNCH * c->Hk * 4, "tickets")))
+        return fail(rc);
+    cudaMemset(c->tickets, 0, (size_t)MAX_SEQ_PER_LAUNCH * c->Hk * 4);
+
+    if (!c->host) {
+        c->P = page_rows;
+        c->n_pages = (int32_t)((p->n_ctx + c->P - 1) / c->P) + p->n_seq_max;
+        c->max_pages = c->n_pages;
+        c->pool_rows = (int64_t)c->n_pages * c->Hk * c->P;
+        c->kdata_bytes = (int64_t)c->L * c->pool_rows * c->krow + 64;
+        c->vdata_bytes = (int64_t)c->L * c->pool_rows * c->vrow + 64;
+        c->kscale_bytes = c->ksb ? (int64_t)c->L * c->pool_rows * c->ksb + 64 : 0;
+        c->vscale_bytes = c->vsb ? (int64_t)c->L * c->pool_rows * c->vsb + 64 : 0;
+        if ((rc = dev_alloc(c, (void **)&c->kdata, c->kdata_bytes, "K pool"))) return fail(rc);
+        if ((rc = dev_alloc(c, (void **)&c->vdata, c->vdata_bytes, "V pool"))) return fail(rc);
+        if ((rc = dev_alloc(c, (void **)&c->kscales, c->kscale_bytes, "K scales"))) return fail(rc);
+        if ((rc = dev_alloc(c, (void **)&c->vscales, c->vscale_bytes, "V scales"))) return fail(rc);
+        // zeroed so that rows never written read as finite zeros
+        cudaMemsetAsync(c->kdata, 0, c->kdata_bytes, c->st);
+        cudaMemsetAsync(c->vdata, 0, c->vdata_bytes, c->st);
+        if (c->kscales) cudaMemsetAsync(c->kscales, 0, c->kscale_bytes, c->st);
+        if (c->vscales) cudaMemsetAsync(c->vscales, 0, c->vscale_bytes, c->st);
+        if ((rc = dev_alloc(c, (void **)&c->pt_dev, (int64_t)p->n_seq_max * c->max_pages * 4, "page tables")))
+            return fail(rc);
+        cudaMemsetAsync(c->pt_dev, 0, (size_t)p->n_seq_max * c->max_pages * 4, c->st);
+        c->free_pages.reserve(c->n_pages);
+        for (int32_t i = c->n_pages - 1; i >= 0; --i) c->free_pages.push_back(i);
+        c->tmk.resize(c->L);
+        c->tmv.resize(c->L);
+        const int64_t rows_all = (int64_t)c->L * c->pool_rows;
+        if (rows_all > INT32_MAX) {
+            c->err = "pool too large for 32-bit TMA row coordinates";
+            return fail(KVC_EINVAL);
+        }
+        for (int l = 0; l < c->L; ++l) {
+            std::string why;
+            if (!encode_rows_map(&c->tmk[l], c->kdata + (int64_t)l * c->pool_rows * c->krow, c->pool_rows, c->krow,
+                                 c->tk, true, &why) ||
+                !encode_rows_map(&c->tmv[l], c->vdata + (int64_t)l * c->pool_rows * c->vrow, c->pool_rows, c->vrow,
+                                 c->tv, false, &why)) {
+                c->err = why;
+                return fail(KVC_ECUDA);
+            }
+        }
+        // partials for chunks of at least 64 rows; grown on demand for smaller forced chunks
+        const int64_t chunks = (int64_t)p->n_ctx / 64 + 2 * (int64_t)p->n_seq_max + c->sms;
+        c->part_floats = chunks * c->Hk * (int64_t)attn_partial_floats(c->r, c->D);
+        if ((rc = dev_alloc(c, (void **)&c->part, c->part_floats * 4, "partials"))) return fail(rc);
+    } else {
+        c->P = p->n_ctx;
+        const int64_t rows = (int64_t)c->L * c->Hk * p->n_ctx;
+        const int64_t bk = rows * c->krow + 64, bv = rows * c->vrow + 64;
+        const int64_t bks = c->ksb ? rows * c->ksb + 64 : 0, bvs = c->vsb ? rows * c->vsb + 64 : 0;
+        auto halloc = [&](uint8_t **h, uint8_t **d, int64_t b) -> int {
+            if (!b) return KVC_OK;
+            if (!take_alloc(c)) return c->fail(KVC_ENOMEM, "injected allocation failure: host store");
+            if (cudaHostAlloc((void **)h, (size_t)b, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
+                cudaGetLastError();
+                *h = nullptr;
+                return c->fail(KVC_ENOMEM, "cudaHostAlloc failed for the host store");
+            }
+            std::memset(*h, 0, (size_t)b);
+            if (cudaHostGetDevicePointer((void **)d, *h, 0) != cudaSuccess)
+                return c->fail(KVC_ECUDA, "cudaHostGetDevicePointer failed");
+            c->host_bytes += b;
+            return KVC_OK;
+        };
+        if ((rc = halloc(&c->hk, &c->hk_d, bk)) || (rc = halloc(&c->hv, &c->hv_d, bv)) ||
+            (rc = halloc(&c->hks, &c->hks_d, bks)) || (rc = halloc(&c->hvs, &c->hvs_d, bvs)))
+            return fail(rc);
+        if ((rc = dev_alloc(c, (void **)&c->zero_pt, 4, "slot page table"))) return fail(rc);
+        c->app_ev.assign((size_t)c->L, nullptr);
+        for (auto &ev : c->app_ev)
+            if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
+                c->err = "event creation failed";
+                return fail(KVC_ECUDA);
+            }
+        cudaMemsetAsync(c->zero_pt, 0, 4, c->st);
+        const int64_t chunks = (int64_t)p->n_ctx / 64 + 2 + c->sms;
+        c->part_floats = chunks * c->Hk * (int64_t)attn_partial_floats(c->r, c->D);
+        if ((rc = dev_alloc(c, (void **)&c->part, c->part_floats * 4, "partials"))) return fail(rc);
+    }
+    c->seqs.resize(p->n_seq_max);
+    for (auto &q : c->seqs) q.lfill.assign(c->L, 0);
+    if (cudaStreamSynchronize(c->st) != cudaSuccess) {
+        c->err = "initialisation failed";
+        return fail(KVC_ECUDA);
+    }
+    *out = reinterpret_cast<kvc_ctx *>(c);
+    return KVC_OK;
+}
+
+int kvc_append(kvc_ctx *cc, int layer, int seq, int pos0, int n_tok, const float *k, const float *v,
+               void *stream) {
+    if (!cc) return KVC_EINVAL;
+    Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (layer < 0 || layer >= c->L) return c->fail(KVC_EINVAL, "layer out of range");
+    if (seq < 0 || seq >= (int)c->seqs.size()) return c->fail(KVC_EINVAL, "sequence id out of range");
+    if (n_tok < 1 || !k || !v) return c->fail(KVC_EINVAL, "n_tok must be >= 1 and k, v non-null");
+    if (pos0 < 0 || (int64_t)pos0 + n_tok - 1 > INT32_MAX) return c->fail(KVC_ERANGE, "positions out of range");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    KVC_CU(c, cudaSetDevice(c->dev));
+    Seq &q = c->seqs[seq];
+    const int32_t fill = q.lfill[layer];
+    const bool creates = fill == q.n;
+    if (!creates) {
+        if ((int64_t)fill + n_tok > q.n) return c->fail(KVC_EINVAL, "append runs past the rows other layers created");
+        for (int i = 0; i < n_tok; ++i)
+            if (q.pos[(size_t)fill + i] != pos0 + i)
+                return c->fail(KVC_EINVAL, "append positions differ from the rows other layers created");
+    }
+    if (c->host) {
+        if (creates && (int64_t)q.n + n_tok > c->P) return c->fail(KVC_ENOSPC, "host store is full");
+        int rc = transport_append(c, layer, n_tok, k, v, st);
+        if (rc) return rc;
+    } else {
+        if (creates) {
+            size_t first_new;
+            int rc = grow_pages(c, q, n_tok, &first_new);
+            if (rc) return rc;
+            // new page-table entries travel as kernel arguments (no host copy)
+            std::vector<int32_t> idx, val;
+            for (size_t i = (size_t)q.dev_pages; i < q.pages.size(); ++i) {
+                idx.push_back((int32_t)((int64_t)seq * c->max_pages + (int64_t)i));
+                val.push_back(q.pages[i]);
+            }
+            if (!idx.empty()) {
+                cudaError_t e = launch_pt_update(c->pt_dev, (int)idx.size(), idx.data(), val.data(), st);
+                if (e != cudaSuccess) return cuda_fail(c, e, "page table update");
+                q.dev_pages = (int32_t)q.pages.size();
+            }
+        }
+        AppendDst d;
+        const int64_t lo = (int64_t)layer * c->pool_rows;
+        d.lv.k.data = c->kdata + lo * c->krow;
+        d.lv.k.scales = c->ksb ? reinterpret_cast<uint16_t *>(c->kscales + lo * c->ksb) : nullptr;
+        d.lv.v.data = c->vdata + lo * c->vrow;
+        d.lv.v.scales = c->vsb ? reinterpret_cast<uint16_t *>(c->vscales + lo * c->vsb) : nullptr;
+        d.pt = c->pt_dev + (int64_t)seq * c->max_pages;
+        d.off = q.off;
+        d.row0 = fill;
+        d.P = c->P;
+        cudaError_t e = launch_append(c->tk, c->tv, c->Hk, c->D, n_tok, k, v, &d, 1, st);
+        if (e != cudaSuccess) return cuda_fail(c, e, "append kernel");
+    }
+    if (creates) {
+        for (int i = 0; i < n_tok; ++i) q.pos.push_back(pos0 + i);
+        q.n += n_tok;
+    }
+    q.lfill[layer] += n_tok;
+    return KVC_OK;
+}
+
+int kvc_attn_decode(kvc_ctx *cc, int layer, int n_seq, const int32_t *seq_ids, const float *q, float *out,
+                    float kq_scale, void *stream) {
+    if (!cc) return KVC_EINVAL;
+    Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (layer < 0 || layer >= c->L) return c->fail(KVC_EINVAL, "layer out of range");
+    if (n_seq < 1 || !seq_ids || !q || !out) return c->fail(KVC_EINVAL, "n_seq >= 1 and non-null pointers required");
+    if (!std::isfinite(kq_scale)) return c->fail(KVC_EINVAL, "kq_scale must be finite");
+    if (q == out) return c->fail(KVC_EINVAL, "out may not alias q");
+    std::vector<char> seen(c->seqs.size(), 0);
+    for (int i = 0; i < n_seq; ++i) {
+        if (seq_ids[i] < 0 || seq_ids[i] >= (int)c->seqs.size()) return c->fail(KVC_EINVAL, "sequence id out of range");
+        if (seen[(size_t)seq_ids[i]]) return c->fail(KVC_EINVAL, "duplicate sequence id");
+        seen[(size_t)seq_ids[i]] = 1;
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    KVC_CU(c, cudaSetDevice(c->dev));
+    if (c->host) {
+        if (n_seq != 1 || seq_ids[0] != 0) return c->fail(KVC_EINVAL, "host-resident contexts attend sequence 0 only");
+        return transport_attn(c, layer, q, out, kq_scale, st);
+    }
+    std::vector<AttnSeq> seqs((size_t)n_seq);
+    for (int i = 0; i < n_seq; ++i) {
+        const Seq &s = c->seqs[(size_t)seq_ids[i]];
+        AttnSeq &a = seqs[(size_t)i];
+        a.page_table = c->pt_dev + (int64_t)seq_ids[i] * c->max_pages;
+        a.off = s.off;
+        a.n_rows = s.lfill[layer];
+        a.out_row = i;
+    }
+    LayerView lv;
+    const int64_t lo = (int64_t)layer * c->pool_rows;
+    lv.k.data = c->kdata + lo * c->krow;
+    lv.k.scales = c->ksb ? reinterpret_cast<uint16_t *>(c->kscales + lo * c->ksb) : nullptr;
+    lv.v.data = c->vdata + lo * c->vrow;
+    lv.v.scales = c->vsb ? reinterpret_cast<uint16_t *>(c->vscales + lo * c->vsb) : nullptr;
+    const int64_t scale_limit = c->ksb ? c->kscale_bytes - lo * c->ksb : 0;
+    return launch_attention(c, lv, &c->tmk[(size_t)layer], &c->tmv[(size_t)layer], c->P, scale_limit, n_seq,
+                            seqs.data(), q, out, kq_scale, st);
+}
+
+int kvc_seq_rm(kvc_ctx *cc, int seq, int p0, int p1) {
+    if (!cc) return KVC_EINVAL;
+    Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (c->host) return c->fail(KVC_EINVAL, "sequence operations need a device-resident context");
+    if (seq < 0 || seq >= (int)c->seqs.size()) return c->fail(KVC_EINVAL, "sequence id out of range");
+    Seq &q = c->seqs[(size_t)seq];
+    if (!q.synced()) return c->fail(KVC_EINVAL, "layers are not in sync (a step's appends are incomplete)");
+    int64_t a, b;
+    norm_range(p0, p1, a, b);
+    std::vector<int64_t> rm;
+    select_rows(q, a, b, rm);
+    if (rm.empty()) return KVC_OK;
+    int rc = enter_sync(c);
+    if (rc) return rc;
+    const int64_t k = (int64_t)rm.size();
+    const bool prefix = rm.front() == 0 && rm.back() == k - 1;
+    const bool suffix = rm.front() == q.n - k && rm.back() == q.n - 1;
+    if (k == q.n) {
+        q.n = 0;
+        q.pos.clear();
+        release_tail_pages(c, q);
+    } else if (prefix) {
+        q.off += (int32_t)k;
+        q.n -= (int32_t)k;
+        q.pos.erase(q.pos.begin(), q.pos.begin() + k);
+        int32_t drop = q.off / c->P;
+        for (int32_t i = 0; i < drop; ++i) c->free_pages.push_back(q.pages[(size_t)i]);
+        q.pages.erase(q.pages.begin(), q.pages.begin() + drop);
+        q.off -= drop * c->P;
+        q.dev_pages = 0;
+    } else if (suffix) {
+        q.n -= (int32_t)k;
+        q.pos.resize((size_t)q.n);
+        release_tail_pages(c, q);
+    } else {
+        // compact: kept rows from the first removed row on go through staging
+        const int64_t i0 = rm.front();
+        std::vector<int64_t> keep;
+        size_t j = 0;
+        for (int64_t r = i0; r < q.n; ++r) {
+            if (j < rm.size() && rm[j] == r) {
+                ++j;
+                continue;
+            }
+            keep.push_back(r);
+        }
+        const int64_t nk = (int64_t)keep.size();
+        const int64_t per_row = (int64_t)c->L * c->Hk * (c->krow + c->vrow + c->ksb + c->vsb);
+        if ((rc = ensure_staging(c, nk * per_row + 64))) return rc;
+        // pack the kept rows, then unpack them at logical rows i0 .. i0+nk-1
+        std::vector<Segment> segs;
+        add_payload_copies(c, q, keep, c->staging, true, segs);
+        if ((rc = upload_segments(c, segs))) return rc;
+        if ((rc = wait_internal(c))) return rc;
+        std::vector<int64_t> dst((size_t)nk);
+        for (int64_t i = 0; i < nk; ++i) dst[(size_t)i] = i0 + i;
+        segs.clear();
+        add_payload_copies(c, q, dst, c->staging, false, segs);
+        if ((rc = upload_segments(c, segs))) return rc;
+        if ((rc = wait_internal(c))) return rc;
+        std::vector<int32_t> np;
+        np.reserve((size_t)(q.n - k));
+        for (int64_t r = 0; r < i0; ++r) np.push_back(q.pos[(size_t)r]);
+        for (int64_t r : keep) np.push_back(q.pos[(size_t)r]);
+        q.pos.swap(np);
+        q.n -= (int32_t)k;
+        release_tail_pages(c, q);
+    }
+    for (auto &f : q.lfill) f = q.n;
+    if ((rc = upload_pages(c, seq))) return rc;
+    return wait_internal(c);
+}
+
+int kvc_seq_cp(kvc_ctx *cc, int src, int dst, int p0, int p1) {
+    if (!cc) return KVC_EINVAL;
+    Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (c->host) return c->fail(KVC_EINVAL, "sequence operations need a device-resident context");
+    if (src < 0 || src >= (int)c->seqs.size() || dst < 0 || dst >= (int)c->seqs.size())
+        return c->fail(KVC_EINVAL, "sequence id out of range");
+    if (src == dst) return KVC_OK;
+    Seq &a = c->seqs[(size_t)src];
+    Seq &b = c->seqs[(size_t)dst];
+    if (!a.synced() || !b.synced()) return c->fail(KVC_EINVAL, "layers are not in sync");
+    int64_t lo, hi;
+    norm_range(p0, p1, lo, hi);
+    std::vector<int64_t> sel;
+    select_rows(a, lo, hi, sel);
+    if (sel.empty()) return KVC_OK;
+    int rc = enter_sync(c);
+    if (rc) return rc;
+    size_t first_new;
+    if ((rc = grow_pages(c, b, (int64_t)sel.size(), &first_new))) return rc;
+    const int64_t base = b.n;
+    b.n += (int32_t)sel.size();
+    for (int64_t r : sel) b.pos.push_back(a.pos[(size_t)r]);
+    for (auto &f : b.lfill) f = b.n;
+    std::vector<Segment> segs;
+    for (size_t i = 0; i < sel.size();) {
+        size_t j = i + 1;
+        while (j < sel.size() && sel[j] == sel[j - 1] + 1) ++j;
+        add_row_copies(c, a, sel[i], b, base + (int64_t)i, (int64_t)(j - i), segs);
+        i = j;
+    }
+    if ((rc = upload_pages(c, dst))) return rc;
+    if ((rc = upload_segments(c, segs))) return rc;
+    return wait_internal(c);
+}
+
+int kvc_seq_add(kvc_ctx *cc, int seq, int p0, int p1, int delta) {
+    if (!cc) return KVC_EINVAL;
+    Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (c->host) return c->fail(KVC_EINVAL, "sequence operations need a device-resident context");
+    if (seq < 0 || seq >= (int)c->seqs.size()) return c->fail(KVC_EINVAL, "sequence id out of range");
+    Seq &q = c->seqs[(size_t)seq];
+    if (!q.synced()) return c->fail(KVC_EINVAL, "layers are not in sync");
+    int64_t a, b;
+    norm_range(p0, p1, a, b);
+    std::vector<int64_t> sel;
+    select_rows(q, a, b, sel);
+    if (sel.empty() || delta == 0) return KVC_OK;
+    for (int64_t r : sel) {
+        const int64_t np = (int64_t)q.pos[(size_t)r] + delta;
+        if (np < 0 || np > INT32_MAX) return c->fail(KVC_ERANGE, "shifted position out of range");
+    }
+    int rc = enter_sync(c);
+    if (rc) return rc;
+    // head-rows of layer 0 to rotate; the kernel repeats them for every layer
+    const int64_t n_rows = (int64_t)sel.size() * c->Hk;
+    if (n_rows > c->rows_cap) {
+        dev_free(c, c->rows_dev, c->rows_cap * 8);
+        c->rows_dev = nullptr;
+        c->rows_cap = 0;
+        if ((rc = dev_alloc(c, (void **)&c->rows_dev, n_rows * 8, "row list"))) return rc;
+        c->rows_cap = n_rows;
+    }
+    std::vector<int64_t> rows;
+    rows.reserve((size_t)n_rows);
+    for (int64_t r : sel) {
+        int32_t pg, cl;
+        phys(c, q, r, pg, cl);
+        for (int g = 0; g < c->Hk; ++g) rows.push_back(prow(c, pg, g, cl));
+    }
+    KVC_CU(c, cudaMemcpyAsync(c->rows_dev, rows.data(), rows.size() * 8, cudaMemcpyHostToDevice, c->st));
+    // cos/sin of delta * theta_i in fp64, theta_i = base^(-2i/D)
+    float2 cs[64];
+    for (int i = 0; i < c->D / 2; ++i) {
+        const double theta = std::pow((double)c->prm.rope_base, -2.0 * i / (double)c->D);
+        const double phi = (double)delta * theta;
+        cs[i] = make_float2((float)std::cos(phi), (float)std::sin(phi));
+    }
+    cudaError_t e = launch_rope_shift(c->tk, c->D, c->prm.rope_mode, c->kdata,
+                                      reinterpret_cast<uint16_t *>(c->kscales), c->pool_rows, c->L, c->rows_dev,
+                                      n_rows, cs, c->st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "rope shift kernel");
+    if ((rc = wait_internal(c))) return rc;
+    for (int64_t r : sel) q.pos[(size_t)r] += delta;
+    return KVC_OK;
+}
+
+int kvc_state_get(kvc_ctx *cc, int seq, int p0, int p1, void *dst, size_t cap, size_t *n_written) {
+    if (!cc) return KVC_EINVAL;
+    Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (c->host) return c->fail(KVC_EINVAL, "state operations need a device-resident context");
+    if (seq < 0 || seq >= (int)c->seqs.size() || !n_written) return c->fail(KVC_EINVAL, "bad sequence id or n_written");
+    Seq &q = c->seqs[(size_t)seq];
+    if (!q.synced()) return c->fail(KVC_EINVAL, "layers are not in sync");
+    int64_t a, b;
+    norm_range(p0, p1, a, b);
+    std::vector<int64_t> sel;
+    select_rows(q, a, b, sel);
+    const int64_t n = (int64_t)sel.size();
+    const int64_t size = state_bytes(c, n);
+    *n_written = (size_t)size;
+    if (!dst) return KVC_OK;
+    if ((int64_t)cap < size) return c->fail(KVC_ENOSPC, "destination buffer too small");
+    int rc = enter_sync(c);
+    if (rc) return rc;
+    uint8_t *out = reinterpret_cast<uint8_t *>(dst);
+    std::memset(out, 0, (size_t)(64 + pad16(4 * n)));
+    uint32_t hdr[8] = {0x3143564Bu, 1u, (uint32_t)c->L, (uint32_t)c->Hk, (uint32_t)c->D,
+                       (uint32_t)c->tk, (uint32_t)c->tv, (uint32_t)n};
+    std::memcpy(out, hdr, sizeof(hdr));
+    const uint64_t pl = (uint64_t)payload_bytes(c, n);
+    std::memcpy(out + 32, &pl, 8);
+    for (int64_t i = 0; i < n; ++i) std::memcpy(out + 64 + 4 * i, &q.pos[(size_t)sel[(size_t)i]], 4);
+    if (n > 0) {
+        if ((rc = ensure_staging(c, (int64_t)pl))) return rc;
+        KVC_CU(c, cudaMemsetAsync(c->staging, 0, (size_t)pl, c->st)); // padding bytes are zero
+        std::vector<Segment> segs;
+        add_payload_copies(c, q, sel, c->staging, true, segs);
+        if ((rc = upload_segments(c, segs))) return rc;
+        KVC_CU(c, cudaMemcpyAsync(out + 64 + pad16(4 * n), c->staging, (size_t)pl, cudaMemcpyDeviceToHost, c->st));
+        if ((rc = wait_internal(c))) return rc;
+    }
+    return KVC_OK;
+}
+
+int kvc_state_set(kvc_ctx *cc, int seq, const void *src, size_t nbytes, size_t *n_read) {
+    if (!cc) return KVC_EINVAL;
+    Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (c->host) return c->fail(KVC_EINVAL, "state operations need a device-resident context");
+    if (seq < 0 || seq >= (int)c->seqs.size() || !src) return c->fail(KVC_EINVAL, "bad sequence id or source");
+    Seq &q = c->seqs[(size_t)seq];
+    if (!q.synced()) return c->fail(KVC_EINVAL, "layers are not in sync");
+    const uint8_t *in = reinterpret_cast<const uint8_t *>(src);
+    if (nbytes < 64) return c->fail(KVC_EFORMAT, "state shorter than its header");
+    uint32_t hdr[8];
+    uint64_t pl;
+    std::memcpy(hdr, in, sizeof(hdr));
+    std::memcpy(&pl, in + 32, 8);
+    if (hdr[0] != 0x3143564Bu || hdr[1] != 1u) return c->fail(KVC_EFORMAT, "bad magic or version");
+    if (hdr[2] != (uint32_t)c->L || hdr[3] != (uint32_t)c->Hk || hdr[4] != (uint32_t)c->D ||
+        hdr[5] != (uint32_t)c->tk || hdr[6] != (uint32_t)c->tv)
+        return c->fail(KVC_EFORMAT, "state geometry or types differ from this context");
+    const int64_t n = (int64_t)hdr[7];
+    if (n > INT32_MAX) return c->fail(KVC_EFORMAT, "bad token count");
+    if (pl != (uint64_t)payload_bytes(c, n)) return c->fail(KVC_EFORMAT, "payload size does not match the header");
+    const int64_t size = state_bytes(c, n);
+    if ((int64_t)nbytes < size) return c->fail(KVC_EFORMAT, "state truncated");
+    std::vector<int32_t> pos((size_t)n);
+    for (int64_t i = 0; i < n; ++i) {
+        std::memcpy(&pos[(size_t)i], in + 64 + 4 * i, 4);
+        if (pos[(size_t)i] < 0) return c->fail(KVC_EFORMAT, "negative position in state");
+    }
+    if (n_read) *n_read = (size_t)size;
+    if (n == 0) return KVC_OK;
+    int rc = enter_sync(c);
+    if (rc) return rc;
+    size_t first_new;
+    if ((rc = grow_pages(c, q, n, &first_new))) return rc;
+    if ((rc = ensure_staging(c, (int64_t)pl))) {
+        release_tail_pages(c, q);
+        return rc;
+    }
+    KVC_CU(c, cudaMemcpyAsync(c->staging, in + 64 + pad16(4 * n), (size_t)pl, cudaMemcpyHostToDevice, c->st));
+    const int64_t base = q.n;
+    q.n += (int32_t)n;
+    q.pos.insert(q.pos.end(), pos.begin(), pos.end());
+    for (auto &f : q.lfill) f = q.n;
+    std::vector<int64_t> idx((size_t)n);
+    for (int64_t i = 0; i < n; ++i) idx[(size_t)i] = base + i;
+    std::vector<Segment> segs;
+    add_payload_copies(c, q, idx, c->staging, false, segs);
+    if ((rc = upload_pages(c, seq))) return rc;
+    if ((rc = upload_segments(c, segs))) return rc;
+    return wait_internal(c);
+}
+
+int kvc_pipeline_depth(kvc_ctx *cc, int n) {
+    if (!cc) return KVC_EINVAL;
+    Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (n < 0 || n > 16) return c->fail(KVC_EINVAL, "depth must be in [0, 16]");
+    if (c->host) {
+        cudaSetDevice(c->dev);
+        cudaDeviceSynchronize();
+        transport_release(c);
+        c->tr.latched = false;
+    }
+    c->tr.depth = n;
+    return KVC_OK;
+}
+
+int kvc_pipeline_budget(kvc_ctx *cc, size_t bytes) {
+    if (!cc) return KVC_EINVAL;
+    Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (bytes > ((size_t)1 << 50)) return c->fail(KVC_EINVAL, "budget too large");
+    if (c->host) {
+        cudaSetDevice(c->dev);
+        cudaDeviceSynchronize();
+        transport_release(c);
+        c->tr.latched = false;
+    }
+    c->tr.budget = (int64_t)bytes;
+    return KVC_OK;
+}
+
+int kvc_seq_n_tokens(const kvc_ctx *cc, int seq, int32_t *n) {
+    if (!cc || !n) return KVC_EINVAL;
+    const Ctx *c = reinterpret_cast<const Ctx *>(cc);
+    if (seq < 0 || seq >= (int)c->seqs.size()) return KVC_EINVAL;
+    *n = c->seqs[(size_t)seq].n;
+    return KVC_OK;
+}
+
+int kvc_seq_positions(const kvc_ctx *cc, int seq, int32_t *pos, int32_t cap, int32_t *n) {
+    if (!cc || !n) return KVC_EINVAL;
+    const Ctx *c = reinterpret_cast<const Ctx *>(cc);
+    if (seq < 0 || seq >= (int)c->seqs.size()) return KVC_EINVAL;
+    const Seq &q = c->seqs[(size_t)seq];
+    *n = q.n;
+    if (pos) {
+        if (cap < q.n) return KVC_ENOSPC;
+        std::memcpy(pos, q.pos.data(), (size_t)q.n * 4);
+    }
+    return KVC_OK;
+}
+
+int kvc_get_stats(const kvc_ctx *cc, kvc_stats *o) {
+    if (!cc || !o) return KVC_EINVAL;
+    const Ctx *c = reinterpret_cast<const Ctx *>(cc);
+    std::memset(o, 0, sizeof(*o));
+    o->ring_engaged = c->tr.ring.empty() ? 0 : 1;
+    o->ring_declined = c->tr.latched ? 1 : 0;
+    o->ring_slots = (int32_t)c->tr.ring.size();
+    o->transfer_stream = c->tr.xfer ? 1 : 0;
+    o->slot_bytes = c->tr.ring.empty() ? c->tr.ordered.bytes : c->tr.ring[0].bytes;
+    for (auto &s : c->tr.ring) o->ring_bytes += s.bytes;
+    o->ordered_bytes = c->tr.ordered.bytes;
+    o->deliveries_early = c->tr.early;
+    o->deliveries_ordered = c->tr.in_order;
+    o->bytes_delivered = c->tr.bytes;
+    o->pages_total = c->n_pages;
+    o->pages_free = (int64_t)c->free_pages.size();
+    o->device_bytes = c->device_bytes;
+    o->host_pinned_bytes = c->host_bytes;
+    return KVC_OK;
+}
+
+int kvc_set_chunk_rows(kvc_ctx *cc, int rows) {
+    if (!cc) return KVC_EINVAL;
+    Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (rows < 0 || rows % 16) return c->fail(KVC_EINVAL, "chunk rows must be a non-negative multiple of 16");
+    c->chunk_override = rows;
+    return KVC_OK;
+}
+
+int kvc_set_timeout_ms(kvc_ctx *cc, int ms) {
+    if (!cc) return KVC_EINVAL;
+    Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (ms < 1) return c->fail(KVC_EINVAL, "timeout must be positive");
+    c->timeout_ms = ms;
+    return KVC_OK;
+}
+
+int kvc_debug_fail_alloc_after(kvc_ctx *cc, int n) {
+    if (!cc) return KVC_EINVAL;
+    reinterpret_cast<Ctx *>(cc)->fail_after = n < 0 ? -1 : n;
+    return KVC_OK;
+}
+
+int kvc_check_device_error(kvc_ctx *cc, uint32_t *word) {
+    if (!cc || !word) return KVC_EINVAL;
+    Ctx *c = reinterpret_cast<Ctx *>(cc);
+    KVC_CU(c, cudaSetDevice(c->dev));
+    KVC_CU(c, cudaDeviceSynchronize());
+    KVC_CU(c, cudaMemcpy(word, c->err_dev, 4, cudaMemcpyDeviceToHost));
+    KVC_CU(c, cudaMemset(c->err_dev, 0, 4));
+    return KVC_OK;
+}
+
+} // extern "C"

@@ -1,0 +1,114 @@
+// ctx.h - the context behind the C ABI: cache manager state (host metadata),
+// device pools and the host-resident transport.  Not part of the ABI.
+#pragma once
+
+#include "kvc_internal.h"
+
+#include <string>
+#include <vector>
+
+namespace kvc {
+
+// Logical rows of a sequence are contiguous: logical row r lives in page
+// pages[(off + r) / P] at cell (off + r) % P.  pos[r] is its position.
+// lfill[l] rows of layer l have been written; a step's appends create rows
+// on the first layer and fill the others, so every sequence operation
+// requires lfill[l] == n for all layers.
+struct Seq {
+    std::vector<int32_t> pages;
+    int32_t off = 0;
+    int32_t n = 0;
+    std::vector<int32_t> pos;
+    std::vector<int32_t> lfill;
+    int32_t dev_pages = 0; // leading entries of `pages` known to match the device table
+    bool synced() const {
+        for (int32_t f : lfill)
+            if (f != n) return false;
+        return true;
+    }
+};
+
+// One staging slot of the host-resident transport: one layer's K+V over the
+// context, laid out [Hk][cap][row].
+struct Slot {
+    void *kdata = nullptr, *vdata = nullptr;
+    uint16_t *kscales = nullptr, *vscales = nullptr;
+    int32_t cap = 0;
+    int64_t bytes = 0;
+    int64_t scale_bytes = 0; // bytes of each scale buffer
+    CUtensorMap tmk, tmv;
+    cudaEvent_t ready = nullptr, release = nullptr;
+    int32_t layer = -1; // layer held (-1 none)
+    int32_t rows = 0;   // rows of that layer present
+    bool consumed_once = false;
+};
+
+struct Transport {
+    int depth = 1;
+    int64_t budget = 128ll << 20;
+    bool latched = false;
+    std::vector<Slot> ring; // engaged ring (depth + 2 slots) or empty
+    Slot ordered;           // ordered-path buffer
+    cudaStream_t xfer = nullptr;
+    int64_t cursor = 0;     // deliveries issued into the ring
+    int64_t early = 0, in_order = 0, bytes = 0;
+};
+
+struct Ctx {
+    kvc_params prm;
+    std::string err;
+    int dev = 0;
+    int sms = 0;
+    int H = 0, Hk = 0, D = 0, r = 0, L = 0, P = 0;
+    int tk = 0, tv = 0;
+    int krow = 0, vrow = 0, ksb = 0, vsb = 0; // data row bytes, scale row bytes (0 for f16)
+    bool host = false;
+
+    // device residency
+    int32_t n_pages = 0;
+    int64_t pool_rows = 0; // rows per layer = n_pages * Hk * P
+    std::vector<int32_t> free_pages;
+    uint8_t *kdata = nullptr, *vdata = nullptr;
+    uint8_t *kscales = nullptr, *vscales = nullptr;
+    int64_t kdata_bytes = 0, vdata_bytes = 0, kscale_bytes = 0, vscale_bytes = 0;
+    std::vector<CUtensorMap> tmk, tmv; // per layer
+    int32_t *pt_dev = nullptr;         // [n_seq_max][max_pages]
+    int32_t max_pages = 0;
+    std::vector<Seq> seqs;
+
+    // host residency: pinned store [L][Hk][n_ctx][row], mapped
+    uint8_t *hk = nullptr, *hv = nullptr, *hks = nullptr, *hvs = nullptr;
+    uint8_t *hk_d = nullptr, *hv_d = nullptr, *hks_d = nullptr, *hvs_d = nullptr; // device aliases
+    int64_t host_bytes = 0;
+    Transport tr;
+    std::vector<cudaEvent_t> app_ev; // per layer: recorded after each append (orders early deliveries)
+    int32_t *zero_pt = nullptr;      // device page table {0} used for slots
+
+    // attention work space
+    float *part = nullptr;
+    int64_t part_floats = 0;
+    int32_t *tickets = nullptr;
+    uint32_t *err_dev = nullptr;
+    int chunk_override = 0;
+
+    // staging for sequence / state operations
+    uint8_t *staging = nullptr;
+    int64_t staging_bytes = 0;
+    Segment *segs_dev = nullptr;
+    int64_t segs_cap = 0;
+    int64_t *rows_dev = nullptr;
+    int64_t rows_cap = 0;
+    cudaStream_t st = nullptr; // internal stream of the synchronous operations
+    cudaEvent_t done = nullptr;
+
+    int timeout_ms = 120000;
+    int fail_after = -1;
+    int64_t device_bytes = 0;
+
+    int fail(int code, const std::string &msg) {
+        err = msg;
+        return code;
+    }
+};
+
+} // namespace kvc

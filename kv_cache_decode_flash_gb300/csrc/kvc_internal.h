@@ -1,0 +1,109 @@
+// kvc_internal.h - shared declarations of the CUDA library (not part of the ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/kvc.h"
+
+namespace kvc {
+
+constexpr int QK = 32;                 // elements per q8_0 block
+constexpr int MAX_SEQ_PER_LAUNCH = 64; // sequences carried in one attention launch
+constexpr int MAX_GROUP = 8;           // query heads per KV head supported by the attention kernel
+constexpr int ATTN_WARPS = 8;          // warps per attention CTA
+constexpr int ATTN_TILE = 16 * ATTN_WARPS; // rows per pipeline stage (16 rows per warp)
+constexpr int TMA_BOX_ROWS = 16;       // rows per TMA box
+
+// Device error word bits (kernels set them instead of trapping).
+constexpr uint32_t ERR_WAIT_TIMEOUT = 1u << 0;
+constexpr uint32_t ERR_BAD_INDEX = 1u << 1;
+constexpr uint32_t ERR_BAD_CONFIG = 1u << 2;
+
+// Addressing of one layer's K or V store.  Row index of (page, kv head g,
+// cell) is (page * Hk + g) * P + cell; data rows are `row_bytes` long,
+// q8_0 scale rows are `scale_bytes` long (fp16 per 32 elements).
+struct TensorView {
+    void *data;        // int8 codes (q8_0) or fp16 halves (f16)
+    uint16_t *scales;  // q8_0 only, else nullptr
+};
+
+struct LayerView {
+    TensorView k, v;
+};
+
+// Per-sequence description in an attention launch.
+struct AttnSeq {
+    const int32_t *page_table; // device, logical page -> physical page
+    int32_t off;               // offset of logical row 0 in the first page
+    int32_t n_rows;            // rows to attend over
+    int32_t chunk0;            // first global chunk index of this sequence
+    int32_t n_chunks;          // chunks of this sequence (>= 1)
+    int32_t out_row;           // index of this sequence in q / out
+    int32_t ticket;            // index of this sequence's ticket row
+};
+
+struct AttnParams {
+    int32_t H, Hk, D, r, P;
+    int32_t chunk_rows;
+    int32_t n_seq;
+    int32_t total_chunks;
+    float kq_scale_log2; // kq_scale * log2(e)
+    const float *q;
+    float *out;
+    const uint16_t *ks; // K scales of this layer (q8_0), else nullptr
+    const uint16_t *vs; // V scales of this layer (q8_0), else nullptr
+    float *part;        // split-K partials
+    int32_t *tickets;   // [MAX_SEQ_PER_LAUNCH * Hk] arrival counters, self-resetting
+    uint32_t *err;      // device error word
+    int64_t scale_limit_bytes; // bytes readable from ks / vs (bounds of the bulk copies)
+    AttnSeq seq[MAX_SEQ_PER_LAUNCH];
+};
+
+// Launch the decode attention kernel for one layer.
+cudaError_t launch_attn(int type, const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv,
+                        cudaStream_t st);
+int attn_ctas_per_sm(int type, int D, int r);
+size_t attn_partial_floats(int r, int D); // floats per (chunk, kv head) partial
+
+// Quantise-on-append.  Destination of token t: logical row row0 + t of a
+// sequence with page table pt and first-page offset off (pt == nullptr:
+// single page 0, cell = row0 + t).
+struct AppendDst {
+    LayerView lv;
+    const int32_t *pt;
+    int32_t off;
+    int32_t row0;
+    int32_t P;
+};
+cudaError_t launch_append(int type_k, int type_v, int Hk, int D, int n_tok, const float *k, const float *v,
+                          const AppendDst *dst, int n_dst, cudaStream_t st);
+
+// Write page-table entries: pt[idx[i]] = val[i], up to 32 per launch.
+cudaError_t launch_pt_update(int32_t *pt, int n, const int32_t *idx, const int32_t *val, cudaStream_t st);
+
+// Copy a list of byte segments (device list of {src, dst, bytes}).
+struct Segment {
+    const uint8_t *src;
+    uint8_t *dst;
+    int64_t bytes;
+};
+cudaError_t launch_copy_segments(const Segment *segs_dev, int n, cudaStream_t st);
+
+// RoPE shift of stored K rows.  rows_dev: device list of physical row
+// indices (page * Hk + g) * P + cell of every head-row to rotate in one layer
+// (applied to every layer: layer_stride_rows apart).  cs: device float2
+// [D/2] (cos, sin) of delta * theta_i.
+cudaError_t launch_rope_shift(int type_k, int D, int mode, void *kdata, uint16_t *kscales, int64_t layer_rows,
+                              int n_layer, const int64_t *rows_dev, int64_t n_rows, const float2 *cs,
+                              cudaStream_t st);
+
+// Encode a 2D tiled tensor map (rows x row_bytes) for the attention kernel.
+bool encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int row_bytes, int type, bool swizzle,
+                     std::string *why);
+
+} // namespace kvc

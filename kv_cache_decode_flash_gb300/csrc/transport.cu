@@ -1,0 +1,357 @@
+// transport.cu - split-K launch planning and the host-resident transport.
+//
+// Host-resident KV ("sched: pipeline the delivery of a host-resident KV
+// cache (R4)", section What it does) keeps each layer's K/V in pinned host
+// memory.  Before a layer's attention its rows reach the device through a
+// staging ring of N+2 slots that lives outside any allocator, each slot
+// holding one layer's K+V over the context, with a ready/release event pair:
+//  1. stable prefix: a delivery carries the rows the layer holds when it is
+//     issued; rows written later in the step (the token being appended) are
+//     written into the slot by the append itself, so no delivery ever has to
+//     wait for them (item 1);
+//  2. the ring: delivery of layer l+N is issued right after the attention of
+//     layer l is enqueued, on a transfer stream of its own, into the slot
+//     whose previous reader was N+2 deliveries back; the transfer stream
+//     waits for that reader's release event and records the slot's ready
+//     event, which the attention waits for (items 2 and 3: two slots of
+//     margin, deliveries issued after enqueue, recycling ordered stream to
+//     stream, never through the host);
+//  3. depth N (0 = ordered path exactly) and the budget: (N+2) slots must fit
+//     the budget, checked before anything is allocated on every plan, a
+//     declined ring is latched, and the transfer stream is created with the
+//     ring and released with it (section Device memory).
+// The ordered path delivers a layer in stream order on the caller's stream
+// into one buffer, then attends.  Both paths attend over the same rows with
+// the same chunking, so their outputs are byte-identical.
+#include "ctx.h"
+
+#include <algorithm>
+#include <cstring>
+
+namespace kvc {
+
+int cuda_fail(Ctx *c, cudaError_t e, const char *what);
+int dev_alloc(Ctx *c, void **p, int64_t bytes, const char *what);
+void dev_free(Ctx *c, void *p, int64_t bytes);
+
+#define KVC_CU(c, call)                                                                                            \
+    do {                                                                                                           \
+        cudaError_t e_ = (call);                                                                                   \
+        if (e_ != cudaSuccess) return cuda_fail((c), e_, #call);                                                   \
+    } while (0)
+
+// ------------------------------------------------------ split-K planning ----
+
+// Rows per chunk: enough chunks that every SM gets work in whole waves, no
+// chunk longer than 2048 rows (bounded merge fan-in and tail), at least 64
+// rows (partials stay a small fraction of the bytes read).  Depends only on
+// the row counts, the geometry and the SM count.
+static int auto_chunk_rows(const Ctx *c, int64_t total_rows) {
+    const int64_t slots = (int64_t)c->sms * attn_ctas_per_sm(c->tk, c->D, c->r);
+    const int64_t work = std::max<int64_t>(total_rows * c->Hk, 1);
+    const int64_t cmax = 2048;
+    const int64_t waves = std::max<int64_t>(1, (work + slots * cmax - 1) / (slots * cmax));
+    int64_t C = (work + waves * slots - 1) / (waves * slots);
+    C = (C + 15) / 16 * 16;
+    return (int)std::min<int64_t>(cmax, std::max<int64_t>(64, C));
+}
+
+int launch_attention(Ctx *c, const LayerView &lv, const CUtensorMap *tmk, const CUtensorMap *tmv, int P,
+                     int64_t scale_limit, int n_seq, const AttnSeq *seqs_in, const float *q, float *out,
+                     float kq_scale, cudaStream_t st) {
+    int64_t total = 0;
+    for (int i = 0; i < n_seq; ++i) total += seqs_in[i].n_rows;
+    const int C = c->chunk_override ? c->chunk_override : auto_chunk_rows(c, total);
+    const int64_t pf = (int64_t)attn_partial_floats(c->r, c->D);
+    for (int base = 0; base < n_seq; base += MAX_SEQ_PER_LAUNCH) {
+        const int cnt = std::min(MAX_SEQ_PER_LAUNCH, n_seq - base);
+        AttnParams p;
+        std::memset(&p, 0, sizeof(p));
+        p.H = c->H;
+        p.Hk = c->Hk;
+        p.D = c->D;
+        p.r = c->r;
+        p.P = P;
+        p.chunk_rows = C;
+        p.n_seq = cnt;
+        p.kq_scale_log2 = (float)((double)kq_scale * 1.4426950408889634);
+        p.q = q;
+        p.out = out;
+        p.ks = lv.k.scales;
+        p.vs = lv.v.scales;
+        p.tickets = c->tickets;
+        p.err = c->err_dev;
+        p.scale_limit_bytes = scale_limit;
+        int32_t chunks = 0;
+        for (int i = 0; i < cnt; ++i) {
+            AttnSeq a = seqs_in[base + i];
+            a.chunk0 = chunks;
+            a.n_chunks = std::max(1, (a.n_rows + C - 1) / C);
+            a.ticket = i;
+            p.seq[i] = a;
+            chunks += a.n_chunks;
+        }
+        p.total_chunks = chunks;
+        const int64_t need = (int64_t)chunks * c->Hk * pf;
+        if (need > c->part_floats) {
+            // grows only for forced chunk sizes or unusual batches (not inside graph capture)
+            KVC_CU(c, cudaStreamSynchronize(st));
+            dev_free(c, c->part, c->part_floats * 4);
+            c->part = nullptr;
+            c->part_floats = 0;
+            int rc = dev_alloc(c, (void **)&c->part, need * 4, "partials");
+            if (rc) return rc;
+            c->part_floats = need;
+        }
+        p.part = c->part;
+        cudaError_t e = launch_attn(c->tk, p, tmk, tmv, st);
+        if (e != cudaSuccess) return cuda_fail(c, e, "attention kernel");
+    }
+    return KVC_OK;
+}
+
+// ------------------------------------------------------- host transport ----
+
+static int64_t slot_bytes_for(const Ctx *c, int64_t cap) {
+    return (int64_t)c->Hk * cap * (c->krow + c->vrow + c->ksb + c->vsb) + 4 * 64;
+}
+
+// Capacity of a slot for a context of n rows: n rounded up to 1024 rows,
+// within the host store's capacity.
+static int32_t cap_for(const Ctx *c, int64_t n) {
+    int64_t cap = (std::max<int64_t>(n, 1) + 1023) / 1024 * 1024;
+    return (int32_t)std::min<int64_t>(cap, c->P);
+}
+
+static void free_slot(Ctx *c, Slot &s) {
+    if (s.kdata) dev_free(c, s.kdata, 0);
+    if (s.vdata) dev_free(c, s.vdata, 0);
+    if (s.kscales) dev_free(c, s.kscales, 0);
+    if (s.vscales) dev_free(c, s.vscales, 0);
+    c->device_bytes -= s.bytes;
+    if (s.ready) cudaEventDestroy(s.ready);
+    if (s.release) cudaEventDestroy(s.release);
+    s = Slot();
+}
+
+static int alloc_slot(Ctx *c, Slot &s, int32_t cap) {
+    s = Slot();
+    const int64_t rows = (int64_t)c->Hk * cap;
+    int rc;
+    const int64_t before = c->device_bytes;
+    if ((rc = dev_alloc(c, &s.kdata, rows * c->krow + 64, "slot K"))) return rc;
+    if ((rc = dev_alloc(c, &s.vdata, rows * c->vrow + 64, "slot V"))) return rc;
+    if (c->ksb && (rc = dev_alloc(c, (void **)&s.kscales, rows * c->ksb + 64, "slot K scales"))) return rc;
+    if (c->vsb && (rc = dev_alloc(c, (void **)&s.vscales, rows * c->vsb + 64, "slot V scales"))) return rc;
+    // device_bytes is adjusted by free_slot with s.bytes
+    s.bytes = c->device_bytes - before;
+    c->device_bytes = before + s.bytes;
+    s.scale_bytes = c->ksb ? rows * c->ksb + 64 : 0;
+    s.cap = cap;
+    KVC_CU(c, cudaMemset(s.kdata, 0, (size_t)(rows * c->krow + 64)));
+    KVC_CU(c, cudaMemset(s.vdata, 0, (size_t)(rows * c->vrow + 64)));
+    if (s.kscales) KVC_CU(c, cudaMemset(s.kscales, 0, (size_t)(rows * c->ksb + 64)));
+    if (s.vscales) KVC_CU(c, cudaMemset(s.vscales, 0, (size_t)(rows * c->vsb + 64)));
+    std::string why;
+    if (!encode_rows_map(&s.tmk, s.kdata, rows, c->krow, c->tk, true, &why) ||
+        !encode_rows_map(&s.tmv, s.vdata, rows, c->vrow, c->tv, false, &why))
+        return c->fail(KVC_ECUDA, why);
+    KVC_CU(c, cudaEventCreateWithFlags(&s.ready, cudaEventDisableTiming));
+    KVC_CU(c, cudaEventCreateWithFlags(&s.release, cudaEventDisableTiming));
+    return KVC_OK;
+}
+
+void transport_release(Ctx *c) {
+    for (auto &s : c->tr.ring) free_slot(c, s);
+    c->tr.ring.clear();
+    if (c->tr.xfer) {
+        cudaStreamDestroy(c->tr.xfer);
+        c->tr.xfer = nullptr;
+    }
+    c->tr.cursor = 0;
+}
+
+static void dev_free_slot_memory(Ctx *c, Slot &s) {
+    // free_slot without touching the bookkeeping of device_bytes twice
+    free_slot(c, s);
+}
+
+// Decide ordered vs pipelined for a context of n rows; allocate or grow the
+// ring when it fits the budget.  Returns true when the ring is engaged.
+static int plan(Ctx *c, int64_t n, cudaStream_t st, bool *engaged) {
+    *engaged = false;
+    Transport &t = c->tr;
+    if (t.depth == 0 || t.latched) return KVC_OK;
+    const int32_t cap = cap_for(c, n);
+    const int64_t need = (int64_t)(t.depth + 2) * slot_bytes_for(c, cap);
+    if (need > t.budget) {
+        // declined before anything is allocated, and latched: the context only grows
+        if (!t.ring.empty()) {
+            KVC_CU(c, cudaStreamSynchronize(st));
+            if (t.xfer) KVC_CU(c, cudaStreamSynchronize(t.xfer));
+            transport_release(c);
+        }
+        t.latched = true;
+        return KVC_OK;
+    }
+    if (t.ring.empty() || t.ring[0].cap < n) {
+        if (!t.ring.empty()) {
+            KVC_CU(c, cudaStreamSynchronize(st));
+            if (t.xfer) KVC_CU(c, cudaStreamSynchronize(t.xfer));
+            transport_release(c);
+        }
+        t.ring.resize((size_t)(t.depth + 2));
+        for (auto &s : t.ring) {
+            int rc = alloc_slot(c, s, cap);
+            if (rc) {
+                transport_release(c);
+                return rc;
+            }
+        }
+        KVC_CU(c, cudaStreamCreateWithFlags(&t.xfer, cudaStreamNonBlocking));
+        t.cursor = 0;
+    }
+    *engaged = true;
+    return KVC_OK;
+}
+
+// Issue H2D copies of rows [0, rows) of `layer` from the host store into slot s.
+static int deliver(Ctx *c, Slot &s, int layer, int32_t rows, cudaStream_t x) {
+    const int64_t hcap = c->P;
+    struct Part {
+        uint8_t *host;
+        void *dev;
+        int rowb;
+    } parts[4] = {{c->hk, s.kdata, c->krow}, {c->hv, s.vdata, c->vrow}, {c->hks, s.kscales, c->ksb},
+                  {c->hvs, s.vscales, c->vsb}};
+    for (auto &pt : parts) {
+        if (!pt.rowb || rows == 0) continue;
+        const uint8_t *src = pt.host + (int64_t)layer * c->Hk * hcap * pt.rowb;
+        KVC_CU(c, cudaMemcpy2DAsync(pt.dev, (size_t)s.cap * pt.rowb, src, (size_t)hcap * pt.rowb,
+                                    (size_t)rows * pt.rowb, (size_t)c->Hk, cudaMemcpyHostToDevice, x));
+        c->tr.bytes += (int64_t)rows * pt.rowb * c->Hk;
+    }
+    s.layer = layer;
+    s.rows = rows;
+    return KVC_OK;
+}
+
+static Slot *find_slot(Ctx *c, int layer, int32_t rows) {
+    for (auto &s : c->tr.ring)
+        if (s.layer == layer && s.rows == rows) return &s;
+    return nullptr;
+}
+
+// Early delivery into the next ring slot on the transfer stream.
+static int deliver_early(Ctx *c, int layer) {
+    Transport &t = c->tr;
+    const int32_t rows = c->seqs[0].lfill[(size_t)layer];
+    if (rows == 0 || find_slot(c, layer, rows)) return KVC_OK;
+    if (rows > t.ring[0].cap) return KVC_OK; // the next plan grows the ring
+    Slot &s = t.ring[(size_t)(t.cursor % (int64_t)t.ring.size())];
+    ++t.cursor;
+    if (s.consumed_once) KVC_CU(c, cudaStreamWaitEvent(t.xfer, s.release, 0));
+    // the host rows being delivered were written by append kernels on the compute stream
+    KVC_CU(c, cudaStreamWaitEvent(t.xfer, c->app_ev[(size_t)layer], 0));
+    int rc = deliver(c, s, layer, rows, t.xfer);
+    if (rc) return rc;
+    KVC_CU(c, cudaEventRecord(s.ready, t.xfer));
+    ++t.early;
+    return KVC_OK;
+}
+
+static void slot_layer_view(const Slot &s, LayerView &lv) {
+    lv.k.data = s.kdata;
+    lv.k.scales = reinterpret_cast<uint16_t *>(s.kscales);
+    lv.v.data = s.vdata;
+    lv.v.scales = reinterpret_cast<uint16_t *>(s.vscales);
+}
+
+int transport_append(Ctx *c, int layer, int n_tok, const float *k, const float *v, cudaStream_t st) {
+    Seq &q = c->seqs[0];
+    const int32_t fill = q.lfill[(size_t)layer];
+    AppendDst d[2];
+    int nd = 1;
+    const int64_t lo = (int64_t)layer * c->Hk * c->P;
+    d[0].lv.k.data = c->hk_d + lo * c->krow;
+    d[0].lv.k.scales = c->ksb ? reinterpret_cast<uint16_t *>(c->hks_d + lo * c->ksb) : nullptr;
+    d[0].lv.v.data = c->hv_d + lo * c->vrow;
+    d[0].lv.v.scales = c->vsb ? reinterpret_cast<uint16_t *>(c->hvs_d + lo * c->vsb) : nullptr;
+    d[0].pt = nullptr;
+    d[0].off = 0;
+    d[0].row0 = fill;
+    d[0].P = c->P;
+    // rows written this step also go straight into the slot holding the
+    // layer's stable prefix, after that delivery has landed
+    Slot *s = find_slot(c, layer, fill);
+    if (s && fill + n_tok <= s->cap) {
+        KVC_CU(c, cudaStreamWaitEvent(st, s->ready, 0));
+        slot_layer_view(*s, d[1].lv);
+        d[1].pt = nullptr;
+        d[1].off = 0;
+        d[1].row0 = fill;
+        d[1].P = s->cap;
+        nd = 2;
+    }
+    cudaError_t e = launch_append(c->tk, c->tv, c->Hk, c->D, n_tok, k, v, d, nd, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "append kernel");
+    KVC_CU(c, cudaEventRecord(c->app_ev[(size_t)layer], st));
+    if (nd == 2) s->rows = fill + n_tok;
+    return KVC_OK;
+}
+
+int transport_attn(Ctx *c, int layer, const float *q, float *out, float kq_scale, cudaStream_t st) {
+    Seq &sq = c->seqs[0];
+    const int32_t rows = sq.lfill[(size_t)layer];
+    bool engaged = false;
+    int rc = plan(c, sq.n, st, &engaged);
+    if (rc) return rc;
+    Slot *s = nullptr;
+    if (engaged) {
+        s = find_slot(c, layer, rows);
+        if (!s) {
+            // not delivered ahead: deliver now, in stream order, into the next slot
+            Transport &t = c->tr;
+            s = &t.ring[(size_t)(t.cursor % (int64_t)t.ring.size())];
+            ++t.cursor;
+            if (s->consumed_once) KVC_CU(c, cudaStreamWaitEvent(st, s->release, 0));
+            if ((rc = deliver(c, *s, layer, rows, st))) return rc;
+            KVC_CU(c, cudaEventRecord(s->ready, st));
+            ++t.in_order;
+        }
+        KVC_CU(c, cudaStreamWaitEvent(st, s->ready, 0));
+    } else {
+        Slot &o = c->tr.ordered;
+        if (o.cap < rows || !o.kdata) {
+            if (o.kdata) {
+                KVC_CU(c, cudaStreamSynchronize(st));
+                dev_free_slot_memory(c, o);
+            }
+            if ((rc = alloc_slot(c, o, cap_for(c, std::max<int64_t>(rows, sq.n))))) return rc;
+        }
+        if ((rc = deliver(c, o, layer, rows, st))) return rc;
+        ++c->tr.in_order;
+        s = &o;
+    }
+    LayerView lv;
+    slot_layer_view(*s, lv);
+    AttnSeq a;
+    std::memset(&a, 0, sizeof(a));
+    a.page_table = c->zero_pt;
+    a.off = 0;
+    a.n_rows = rows;
+    a.out_row = 0;
+    rc = launch_attention(c, lv, &s->tmk, &s->tmv, s->cap, s->scale_bytes, 1, &a, q, out, kq_scale, st);
+    if (rc) return rc;
+    if (engaged) {
+        KVC_CU(c, cudaEventRecord(s->release, st));
+        s->consumed_once = true;
+        // look-ahead: the next N layers (wrapping into the next step)
+        for (int k = 1; k <= c->tr.depth; ++k) {
+            if ((rc = deliver_early(c, (layer + k) % c->L))) return rc;
+        }
+    }
+    return KVC_OK;
+}
+
+} // namespace kvc

@@ -1,0 +1,370 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bit-exact: q8_0 codes and scales after append, seq_cp / seq_rm results and
+state export/import (compared as state bytes).  Tolerance: attention outputs
+max abs 1e-3 and relative L2 1e-4 (fp32 accumulation); f16 K after a RoPE
+shift max abs 2e-3; requantised q8_0 K after a shift codes within +-1 and
+scales within 1 fp16 ulp.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from twin import Twin, kv_inputs, q_inputs, assert_attn_close, attn_errors
+
+pytestmark = pytest.mark.gpu
+
+Q8, F16 = oracle.Q8_0, oracle.F16
+
+
+def _state_compare(tw, seq, exact=True):
+    g = tw.gpu.state_get(seq, -1, -1)
+    o = tw.ref.state_get(seq, -1, -1)
+    assert len(g) == len(o)
+    if exact:
+        assert g == o
+    return g, o
+
+
+@pytest.mark.parametrize("type_", [Q8, F16])
+@pytest.mark.parametrize("D", [64, 128])
+def test_append_bit_exact(type_, D):
+    tw = Twin(2, 8, 2, D, 700, type_=type_, page_rows=64)
+    try:
+        # several appends per layer, crossing page boundaries, then a decode-style step
+        for l in range(2):
+            k, v = kv_inputs(1, l, 300, 2, D)
+            tw.append(l, 0, 0, k, v)
+        for l in range(2):
+            k, v = kv_inputs(2, l, 77, 2, D, pos0=300)
+            tw.append(l, 0, 300, k, v)
+        for l in range(2):
+            k, v = kv_inputs(3, l, 1, 2, D, pos0=377)
+            tw.append(l, 0, 377, k, v)
+        _state_compare(tw, 0)
+    finally:
+        tw.close()
+
+
+def test_c1_tiny_config():
+    """1 layer, 8/2 heads, D 64, 512 tokens of q8_0 from N(0,1), scale 1/8,
+    decode at 512; then remove [0, 128) and slide [128, 512) by -128 (RoPE
+    base 1e4); decode at 384."""
+    tw = Twin(1, 8, 2, 64, 512, type_=Q8)
+    try:
+        tw.fill(0, 512, seed=0)
+        _state_compare(tw, 0)
+        q = q_inputs(0, 0, 1, 8, 64)
+        got, want = tw.attn(0, [0], q, 0.125)
+        assert_attn_close(got, want, "decode at 512")
+        tw.gpu.seq_rm(0, 0, 128)
+        tw.ref.seq_rm(0, 0, 128)
+        _state_compare(tw, 0)
+        tw.gpu.seq_add(0, 128, 512, -128)
+        tw.ref.seq_add(0, 128, 512, -128)
+        assert np.array_equal(tw.gpu.positions(0), np.arange(384))
+        _check_shifted_q8(tw, 0)
+        q2 = q_inputs(0, 0, 1, 8, 64, extra=1)
+        got, want = tw.attn(0, [0], q2, 0.125)
+        assert_attn_close(got, want, "decode at 384 after the shift")
+    finally:
+        tw.close()
+
+
+def _check_shifted_q8(tw, seq):
+    g = tw.ref.parse_state(tw.gpu.state_get(seq, -1, -1))
+    pos_g, Kg, Vg = g
+    pos_o = tw.ref.positions(seq)
+    assert np.array_equal(pos_g, pos_o)
+    for l in range(tw.L):
+        Ko, Vo = tw.ref.seqs[seq].K[l], tw.ref.seqs[seq].V[l]
+        assert np.array_equal(Vg[l].a, Vo.a) and np.array_equal(Vg[l].s, Vo.s)  # V untouched, exact
+        dc = np.abs(Kg[l].a.astype(int) - Ko.a.astype(int))
+        assert dc.max() <= 1, "requantised K codes differ by %d" % dc.max()
+        ds = np.abs(Kg[l].s.astype(int) - Ko.s.astype(int))
+        assert ds.max() <= 1, "requantised K scales differ by %d ulp" % ds.max()
+
+
+@pytest.mark.parametrize("type_", [Q8, F16])
+def test_attn_chunk_sizes_and_repeatability(type_):
+    n = 1000
+    tw = Twin(1, 40, 8, 128, 1024, type_=type_)
+    try:
+        tw.fill(0, n, seed=4, sigma=0.5)
+        q = q_inputs(4, 0, 1, 40, 128)
+        scale = float(np.float32(1 / np.sqrt(128)))
+        want = None
+        for C in (32, 64, 128, 256, 1008, 0):
+            tw.kvc.kvc_set_chunk_rows(tw.gpu.ctx, C)
+            got, want = tw.attn(0, [0], q, scale)
+            assert_attn_close(got, want, "chunk %d" % C)
+            again, _ = tw.attn(0, [0], q, scale)
+            assert np.array_equal(got, again), "not bitwise repeatable at chunk %d" % C
+    finally:
+        tw.close()
+
+
+@pytest.mark.parametrize("type_", [Q8, F16])
+@pytest.mark.parametrize("r", [4, 5, 8, 3])
+def test_attn_group_sizes(type_, r):
+    Hk = 2
+    tw = Twin(1, r * Hk, Hk, 128, 600, type_=type_)
+    try:
+        tw.fill(0, 555, seed=5)
+        q = q_inputs(5, 0, 1, r * Hk, 128)
+        got, want = tw.attn(0, [0], q, 0.088)
+        assert_attn_close(got, want, "r=%d" % r)
+    finally:
+        tw.close()
+
+
+@pytest.mark.parametrize("type_", [Q8, F16])
+def test_ragged_batch(type_):
+    lens = [0, 1, 15, 16, 17, 255, 256, 257, 1000, 2100]
+    tw = Twin(1, 32, 8, 128, sum(lens) + 64, n_seq_max=len(lens), type_=type_, page_rows=128)
+    try:
+        for s, n in enumerate(lens):
+            if n:
+                tw.fill(s, n, seed=6)
+        q = q_inputs(6, 0, len(lens), 32, 128)
+        got, want = tw.attn(0, list(range(len(lens))), q, 0.0884)
+        assert_attn_close(got, want, "ragged batch")
+        assert np.all(got[0] == 0)  # empty sequence -> zero output
+        # a permuted subset addresses q/out rows by call order
+        ids = [9, 3, 0, 7]
+        got2, want2 = tw.attn(0, ids, q[: len(ids)], 0.0884)
+        assert_attn_close(got2, want2, "subset")
+    finally:
+        tw.close()
+
+
+def test_many_sequences_multiple_launches():
+    # more than 64 sequences in one call are split into several launches
+    n_seq = 70
+    tw = Twin(1, 8, 2, 64, 70 * 40 + 70 * 16, n_seq_max=n_seq, type_=Q8, page_rows=16)
+    try:
+        for s in range(n_seq):
+            tw.fill(s, 5 + (s * 7) % 33, seed=7)
+        q = q_inputs(7, 0, n_seq, 8, 64)
+        got, want = tw.attn(0, list(range(n_seq)), q, 0.125)
+        assert_attn_close(got, want, "70 sequences")
+    finally:
+        tw.close()
+
+
+@pytest.mark.parametrize("type_", [Q8, F16])
+def test_seq_ops_bit_exact(type_):
+    tw = Twin(2, 8, 2, 64, 2048, n_seq_max=4, type_=type_, page_rows=32)
+    try:
+        tw.fill(0, 500, seed=8)
+        tw.fill(1, 100, seed=9, pos0=1000)
+        for op in [("cp", 0, 2, 40, 300), ("rm", 0, 100, 150), ("rm", 0, 0, 37), ("rm", 0, 450, -1),
+                   ("cp", 1, 0, -1, -1), ("rm", 2, 0, 10), ("cp", 2, 3, -1, -1), ("rm", 0, -1, -1),
+                   ("cp", 3, 0, 100, 200)]:
+            if op[0] == "cp":
+                tw.gpu.seq_cp(*op[1:])
+                tw.ref.seq_cp(*op[1:])
+            else:
+                tw.gpu.seq_rm(*op[1:])
+                tw.ref.seq_rm(*op[1:])
+            for s in range(4):
+                assert np.array_equal(tw.gpu.positions(s), tw.ref.positions(s)), op
+                _state_compare(tw, s)
+        # attention over compacted and copied sequences still matches
+        q = q_inputs(8, 1, 2, 8, 64)
+        got, want = tw.attn(1, [0, 3], q, 0.125)
+        assert_attn_close(got, want, "after seq ops")
+    finally:
+        tw.close()
+
+
+@pytest.mark.parametrize("type_", [Q8, F16])
+def test_state_roundtrip(type_):
+    tw = Twin(3, 8, 2, 128, 4096, n_seq_max=3, type_=type_, page_rows=64)
+    try:
+        tw.fill(0, 777, seed=10)
+        blob = tw.gpu.state_get(0, 100, 600)
+        assert blob == tw.ref.state_get(0, 100, 600)
+        tw.gpu.state_set(1, blob)
+        tw.ref.state_set(1, blob)
+        assert tw.gpu.state_get(1, -1, -1) == blob
+        # import again into a non-empty sequence (append mode)
+        tw.gpu.state_set(1, blob)
+        tw.ref.state_set(1, blob)
+        _state_compare(tw, 1)
+        with pytest.raises(tw.kvc.KvcError):
+            bad = bytearray(blob)
+            bad[16] ^= 1  # head_dim
+            tw.gpu.state_set(2, bytes(bad))
+        with pytest.raises(tw.kvc.KvcError):
+            tw.gpu.state_set(2, blob[:-16])
+        assert tw.gpu.n_tokens(2) == 0
+    finally:
+        tw.close()
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_seq_add_q8_0(mode):
+    tw = Twin(2, 8, 2, 128, 2048, type_=Q8, rope_base=1e6, rope_mode=mode)
+    try:
+        tw.fill(0, 1500, seed=11, sigma=0.5)
+        tw.gpu.seq_add(0, 200, 1200, -150)
+        tw.ref.seq_add(0, 200, 1200, -150)
+        _check_shifted_q8(tw, 0)
+        tw.gpu.seq_add(0, -1, -1, 0)  # delta 0 is a no-op
+        with pytest.raises(tw.kvc.KvcError):
+            tw.gpu.seq_add(0, 0, 100, -1)  # would go negative
+    finally:
+        tw.close()
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_seq_add_f16(mode):
+    tw = Twin(2, 8, 2, 64, 1024, type_=F16, rope_base=1e4, rope_mode=mode)
+    try:
+        tw.fill(0, 900, seed=12)
+        tw.gpu.seq_add(0, 100, 800, 131072)
+        tw.ref.seq_add(0, 100, 800, 131072)
+        pos_g, Kg, Vg = tw.ref.parse_state(tw.gpu.state_get(0, -1, -1))
+        assert np.array_equal(pos_g, tw.ref.positions(0))
+        for l in range(2):
+            a = oracle.f16_to_f64(Kg[l].a)
+            b = oracle.f16_to_f64(tw.ref.seqs[0].K[l].a)
+            assert np.abs(a - b).max() <= 2e-3
+            assert np.array_equal(Vg[l].a, tw.ref.seqs[0].V[l].a)
+    finally:
+        tw.close()
+
+
+def test_cold_store_cycle_small():
+    """Evict the oldest block through a scratch sequence and re-admit it at
+    the tail, as the cold store does, then decode."""
+    tw = Twin(2, 8, 2, 128, 4096, n_seq_max=2, type_=Q8, rope_base=1e6, page_rows=64)
+    try:
+        n, blk = 1024, 256
+        tw.fill(0, n, seed=13, sigma=0.5)
+        for side in (tw.gpu, tw.ref):
+            side.seq_cp(0, 1, 0, blk)
+        blob = tw.gpu.state_get(1, -1, -1)
+        assert blob == tw.ref.state_get(1, -1, -1)
+        for side in (tw.gpu, tw.ref):
+            side.seq_rm(1, -1, -1)
+            side.seq_rm(0, 0, blk)
+            side.seq_add(0, blk, n, -blk)
+        _check_shifted_q8(tw, 0)
+        # admit: import into scratch, shift to the tail, copy into sequence 0
+        for side in (tw.gpu, tw.ref):
+            side.state_set(1, blob)
+            side.seq_add(1, -1, -1, n - blk)
+            side.seq_cp(1, 0, -1, -1)
+            side.seq_rm(1, -1, -1)
+        assert np.array_equal(tw.gpu.positions(0), tw.ref.positions(0))
+        _check_shifted_q8(tw, 0)
+    finally:
+        tw.close()
+
+
+def _host_run(depth, budget, L=8, H=40, Hk=8, D=128, n=2000, steps=3):
+    import torch
+
+    from kv_cache_decode_flash_gb300 import kvc
+
+    cache = kvc.KVCache(L, H, Hk, D, 4096, 1, Q8, Q8, 1e6, 0, kvc.KVC_HOST_PINNED)
+    kvc.kvc_pipeline_depth(cache.ctx, depth)
+    kvc.kvc_pipeline_budget(cache.ctx, budget)
+    dev = torch.device("cuda:0")
+    res = []
+    try:
+        for step in range(steps):
+            m = n if step == 0 else 1
+            pos0 = 0 if step == 0 else n + step - 1
+            for l in range(L):
+                k, v = kv_inputs(14, l, m, Hk, D, pos0=pos0, sigma=0.5)
+                cache.append(l, 0, pos0, torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev))
+                q = torch.from_numpy(q_inputs(14, l, 1, H, D, extra=step)).to(dev)
+                out = torch.empty_like(q)
+                cache.attn_decode(l, [0], q, out, float(1 / np.sqrt(D)))
+                res.append(out.cpu().numpy())
+        return np.stack(res), cache.stats()
+    finally:
+        cache.close()
+
+
+def test_host_resident_ordered_and_pipelined_byte_identical():
+    """Depth 0 (ordered), pipelined rings of depth 1 and 4, and a ring the
+    budget declines all produce the same bytes.  Eight layers, so even the
+    depth-4 ring (6 slots) cannot hold the whole stack."""
+    base, st0 = _host_run(0, 128 << 20)
+    assert st0["ring_engaged"] == 0 and st0["transfer_stream"] == 0 and st0["ring_declined"] == 0
+    for depth, budget, engaged in ((1, 512 << 20, True), (4, 512 << 20, True), (1, 1 << 10, False)):
+        out, st = _host_run(depth, budget)
+        assert np.array_equal(out, base), (depth, budget)
+        if engaged:
+            assert st["ring_engaged"] == 1 and st["transfer_stream"] == 1 and st["deliveries_early"] > 0
+            assert st["ring_slots"] == depth + 2
+        else:
+            assert st["ring_engaged"] == 0 and st["ring_declined"] == 1 and st["transfer_stream"] == 0
+            assert st["ring_bytes"] == 0
+
+
+def test_host_resident_pipelined_vs_oracle():
+    import torch
+
+    from kv_cache_decode_flash_gb300 import kvc
+
+    L, H, Hk, D, n = 3, 40, 8, 128, 1500
+    cache = kvc.KVCache(L, H, Hk, D, 2048, 1, Q8, Q8, 1e6, 0, kvc.KVC_HOST_PINNED)
+    kvc.kvc_pipeline_budget(cache.ctx, 512 << 20)
+    ref = oracle.OracleCache(L, H, Hk, D, Q8, Q8, 1e6, 0)
+    dev = torch.device("cuda:0")
+    try:
+        for l in range(L):
+            k, v = kv_inputs(15, l, n, Hk, D, sigma=0.5)
+            cache.append(l, 0, 0, torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev))
+            ref.append(l, 0, 0, k, v)
+        for step in range(2):
+            for l in range(L):
+                k, v = kv_inputs(16, l, 1, Hk, D, pos0=n + step, sigma=0.5)
+                cache.append(l, 0, n + step, torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev))
+                ref.append(l, 0, n + step, k, v)
+                q = q_inputs(16, l, 1, H, D, extra=step)
+                qd = torch.from_numpy(q).to(dev)
+                out = torch.empty_like(qd)
+                cache.attn_decode(l, [0], qd, out, float(1 / np.sqrt(D)))
+                torch.cuda.synchronize()
+                want = ref.attn(l, [0], q, float(np.float32(1 / np.sqrt(D))))
+                assert_attn_close(out.cpu().numpy().astype(np.float64), want, "host layer %d" % l)
+        assert cache.stats()["ring_engaged"] == 1
+    finally:
+        cache.close()
+
+
+def test_invalid_arguments_are_rejected():
+    from kv_cache_decode_flash_gb300 import kvc
+
+    tw = Twin(1, 8, 2, 64, 256, n_seq_max=2, type_=Q8)
+    try:
+        ctx = tw.gpu.ctx
+        L = kvc.load()
+        assert L.kvc_append(ctx, 5, 0, 0, 1, 1, 1, None) == kvc.KVC_EINVAL  # layer
+        assert L.kvc_append(ctx, 0, 9, 0, 1, 1, 1, None) == kvc.KVC_EINVAL  # seq
+        assert L.kvc_append(ctx, 0, 0, -5, 1, 1, 1, None) == kvc.KVC_ERANGE
+        assert L.kvc_seq_rm(ctx, 7, 0, 1) == kvc.KVC_EINVAL
+        assert L.kvc_set_chunk_rows(ctx, 17) == kvc.KVC_EINVAL
+        assert L.kvc_pipeline_depth(ctx, 99) == kvc.KVC_EINVAL
+    finally:
+        tw.close()
+
+
+def test_enospc_leaves_cache_unchanged():
+    tw = Twin(1, 8, 2, 64, 64, n_seq_max=1, type_=Q8, page_rows=16)
+    try:
+        tw.fill(0, 60, seed=18)
+        before = tw.gpu.state_get(0, -1, -1)
+        k, v = kv_inputs(19, 0, 200, 2, 64)
+        with pytest.raises(tw.kvc.KvcError) as e:
+            tw.gpu.append(0, 0, 60, *[tw.torch.from_numpy(a).to(tw.dev) for a in (k, v)])
+        assert e.value.status == tw.kvc.KVC_ENOSPC
+        assert tw.gpu.state_get(0, -1, -1) == before
+    finally:
+        tw.close()
