@@ -114,7 +114,7 @@ const char *kvc_status_str(int status);
 
 /* Quantise-on-append: write n_tok new rows of layer `layer` for sequence
  * `seq` at positions pos0 .. pos0+n_tok-1.
- * k, v: device fp32 [n_tok][n_head_kv][head_dim], contiguous.
+ * k, v: device fp32 [n_tok][n_head_kv][head_dim], contiguous, 16-byte aligned.
  * The K/V rows of a token are written per layer, as a model produces them
  * (the cpy_k/cpy_v writes of [F5] section M2 - HeadInfer).  The first layer
  * to append a position creates the row (allocating cells); the other layers
@@ -139,7 +139,8 @@ int kvc_append(kvc_ctx *c, int layer, int seq, int pos0, int n_tok, const float 
  * softmax).  Accumulation is fp32; the merge order is fixed, so a call is
  * bitwise repeatable.
  * seq_ids: HOST int32[n_seq] (distinct ids).  q: device fp32
- * [n_seq][n_head][head_dim]; out: device fp32, same shape (may not alias q).
+ * [n_seq][n_head][head_dim]; out: device fp32, same shape (may not alias q);
+ * both 16-byte aligned.
  * A sequence with no rows yields a zero output row.
  * Host-resident contexts: n_seq must be 1 and seq_ids[0] 0; the layer's rows
  * are delivered through the staging ring first ([R4] section What it does).

@@ -77,6 +77,7 @@ int wait_internal(Ctx *c) {
 int enter_sync(Ctx *c) {
     KVC_CU(c, cudaSetDevice(c->dev));
     KVC_CU(c, cudaDeviceSynchronize());
+    c->clear_recent();
     return KVC_OK;
 }
 
@@ -396,6 +397,7 @@ int kvc_create(const kvc_params *p, kvc_ctx **out) {
     c->ksb = c->tk == KVC_Q8_0 ? (c->D / QK) * 2 : 0;
     c->vsb = c->tv == KVC_Q8_0 ? (c->D / QK) * 2 : 0;
     c->host = p->residency == KVC_HOST_PINNED;
+    c->occ = attn_ctas_per_sm(c->tk, c->D, c->r);
 
     auto fail = [&](int rc) {
         kvc_destroy(reinterpret_cast<kvc_ctx *>(c));
@@ -493,6 +495,7 @@ int kvc_create(const kvc_params *p, kvc_ctx **out) {
     }
     c->seqs.resize(p->n_seq_max);
     for (auto &q : c->seqs) q.lfill.assign(c->L, 0);
+    c->recent.assign(p->n_seq_max, std::vector<int32_t>(c->L, 0));
     if (cudaStreamSynchronize(c->st) != cudaSuccess) {
         c->err = "initialisation failed";
         return fail(KVC_ECUDA);
@@ -508,6 +511,7 @@ int kvc_append(kvc_ctx *cc, int layer, int seq, int pos0, int n_tok, const float
     if (layer < 0 || layer >= c->L) return c->fail(KVC_EINVAL, "layer out of range");
     if (seq < 0 || seq >= (int)c->seqs.size()) return c->fail(KVC_EINVAL, "sequence id out of range");
     if (n_tok < 1 || !k || !v) return c->fail(KVC_EINVAL, "n_tok must be >= 1 and k, v non-null");
+    if (((uintptr_t)k | (uintptr_t)v) & 15) return c->fail(KVC_EINVAL, "k and v must be 16-byte aligned");
     if (pos0 < 0 || (int64_t)pos0 + n_tok - 1 > INT32_MAX) return c->fail(KVC_ERANGE, "positions out of range");
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     KVC_CU(c, cudaSetDevice(c->dev));
@@ -559,6 +563,7 @@ int kvc_append(kvc_ctx *cc, int layer, int seq, int pos0, int n_tok, const float
         q.n += n_tok;
     }
     q.lfill[layer] += n_tok;
+    c->recent[(size_t)seq][(size_t)layer] += n_tok;
     return KVC_OK;
 }
 
@@ -570,6 +575,7 @@ int kvc_attn_decode(kvc_ctx *cc, int layer, int n_seq, const int32_t *seq_ids, c
     if (n_seq < 1 || !seq_ids || !q || !out) return c->fail(KVC_EINVAL, "n_seq >= 1 and non-null pointers required");
     if (!std::isfinite(kq_scale)) return c->fail(KVC_EINVAL, "kq_scale must be finite");
     if (q == out) return c->fail(KVC_EINVAL, "out may not alias q");
+    if (((uintptr_t)q | (uintptr_t)out) & 15) return c->fail(KVC_EINVAL, "q and out must be 16-byte aligned");
     std::vector<char> seen(c->seqs.size(), 0);
     for (int i = 0; i < n_seq; ++i) {
         if (seq_ids[i] < 0 || seq_ids[i] >= (int)c->seqs.size()) return c->fail(KVC_EINVAL, "sequence id out of range");
@@ -590,6 +596,7 @@ int kvc_attn_decode(kvc_ctx *cc, int layer, int n_seq, const int32_t *seq_ids, c
         a.off = s.off;
         a.n_rows = s.lfill[layer];
         a.out_row = i;
+        a.stable_rows = std::max(0, a.n_rows - c->recent[(size_t)seq_ids[i]][(size_t)layer]);
     }
     LayerView lv;
     const int64_t lo = (int64_t)layer * c->pool_rows;
@@ -598,8 +605,10 @@ int kvc_attn_decode(kvc_ctx *cc, int layer, int n_seq, const int32_t *seq_ids, c
     lv.v.data = c->vdata + lo * c->vrow;
     lv.v.scales = c->vsb ? reinterpret_cast<uint16_t *>(c->vscales + lo * c->vsb) : nullptr;
     const int64_t scale_limit = c->ksb ? c->kscale_bytes - lo * c->ksb : 0;
-    return launch_attention(c, lv, &c->tmk[(size_t)layer], &c->tmv[(size_t)layer], c->P, scale_limit, n_seq,
-                            seqs.data(), q, out, kq_scale, st);
+    int rc = launch_attention(c, lv, &c->tmk[(size_t)layer], &c->tmv[(size_t)layer], c->P, scale_limit, n_seq,
+                              seqs.data(), q, out, kq_scale, st);
+    if (rc == KVC_OK) c->clear_recent(); // kernels after this one start only once it has waited
+    return rc;
 }
 
 int kvc_seq_rm(kvc_ctx *cc, int seq, int p0, int p1) {

@@ -4,6 +4,7 @@
 
 #include "kvc_internal.h"
 
+#include <algorithm>
 #include <string>
 #include <vector>
 
@@ -59,6 +60,7 @@ struct Ctx {
     std::string err;
     int dev = 0;
     int sms = 0;
+    int occ = 1; // attention CTAs resident per SM (from the occupancy calculator)
     int H = 0, Hk = 0, D = 0, r = 0, L = 0, P = 0;
     int tk = 0, tv = 0;
     int krow = 0, vrow = 0, ksb = 0, vsb = 0; // data row bytes, scale row bytes (0 for f16)
@@ -75,6 +77,13 @@ struct Ctx {
     int32_t *pt_dev = nullptr;         // [n_seq_max][max_pages]
     int32_t max_pages = 0;
     std::vector<Seq> seqs;
+    // rows appended per (sequence, layer) since the last fence (an attention
+    // launch or a synchronous operation); an attention launched with a
+    // programmatic dependency may read every other row before it waits
+    std::vector<std::vector<int32_t>> recent;
+    void clear_recent() {
+        for (auto &v : recent) std::fill(v.begin(), v.end(), 0);
+    }
 
     // host residency: pinned store [L][Hk][n_ctx][row], mapped
     uint8_t *hk = nullptr, *hv = nullptr, *hks = nullptr, *hvs = nullptr;

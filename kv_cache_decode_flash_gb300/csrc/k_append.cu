@@ -95,6 +95,11 @@ struct AppendArgs {
 template <int D>
 __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AppendArgs a) {
     constexpr int EPL = RowShape<D>::EPL;
+    // Let the next kernel (typically this layer's attention) be scheduled now:
+    // it only reads rows below the ones written here before its own wait.
+    // Inputs may come from the preceding kernel, so wait before reading them.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     if (w >= (int64_t)a.n_tok * a.Hk) return;
@@ -135,14 +140,18 @@ cudaError_t launch_append(int type_k, int type_v, int Hk, int D, int n_tok, cons
     a.v = v;
     for (int i = 0; i < n_dst && i < 2; ++i) a.dst[i] = dst[i];
     const int64_t warps = (int64_t)n_tok * Hk;
-    const unsigned grid = (unsigned)((warps + 7) / 8);
-    if (D == 128)
-        append_kernel<128><<<grid, 256, 0, st>>>(a);
-    else if (D == 64)
-        append_kernel<64><<<grid, 256, 0, st>>>(a);
-    else
-        return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((warps + 7) / 8));
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (D == 128) return cudaLaunchKernelEx(&cfg, append_kernel<128>, a);
+    if (D == 64) return cudaLaunchKernelEx(&cfg, append_kernel<64>, a);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_pt_update(int32_t *pt, int n, const int32_t *idx, const int32_t *val, cudaStream_t st) {

@@ -31,8 +31,6 @@
 namespace kvc {
 namespace {
 
-constexpr int W = ATTN_WARPS;
-constexpr int T = ATTN_TILE;
 constexpr uint32_t WAIT_LIMIT = 1u << 24;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -145,10 +143,40 @@ __device__ __forceinline__ void mul2(float2 &acc, const float2 a) {
     acc = *reinterpret_cast<float2 *>(&cr);
 }
 
-// Static shape of one kernel instance.
+
+// Four int8 codes -> four fp32 values (two float2), exact (see codes_to_f32x8).
+__device__ __forceinline__ void codes_to_f32x4(uint32_t w, float2 (&v)[2]) {
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t mag = 0x4B000000u;
+    uint32_t f[4];
+    asm("prmt.b32 %0, %1, %2, 0x7650;" : "=r"(f[0]) : "r"(u), "r"(mag));
+    asm("prmt.b32 %0, %1, %2, 0x7651;" : "=r"(f[1]) : "r"(u), "r"(mag));
+    asm("prmt.b32 %0, %1, %2, 0x7652;" : "=r"(f[2]) : "r"(u), "r"(mag));
+    asm("prmt.b32 %0, %1, %2, 0x7653;" : "=r"(f[3]) : "r"(u), "r"(mag));
+    const float b = 8388736.0f; // 2^23 + 128
+    const float2 bb = make_float2(b, b);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        float2 x = make_float2(__uint_as_float(f[2 * i]), __uint_as_float(f[2 * i + 1]));
+        unsigned long long xr = *reinterpret_cast<unsigned long long *>(&x);
+        unsigned long long br = *reinterpret_cast<const unsigned long long *>(&bb);
+        asm("sub.rn.f32x2 %0, %0, %1;" : "+l"(xr) : "l"(br));
+        v[i] = *reinterpret_cast<float2 *>(&xr);
+    }
+}
+
+// Programmatic dependent launch: wait for the preceding kernel's results /
+// let the next kernel be scheduled.  No-ops without a programmatic edge.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Static shape of one kernel instance.  W warps per CTA, each owning 16 rows
+// of every tile; stages sized so two CTAs fit on an SM.
 template <int TYPE, int D, int R>
 struct Shape {
     static constexpr bool Q8 = TYPE == KVC_Q8_0;
+    static constexpr int W = Q8 ? 8 : 4;              // warps per CTA
+    static constexpr int T = 16 * W;                  // rows per tile
     static constexpr int NB = D / 32;                 // q8_0 blocks per row
     static constexpr int KROW = Q8 ? D : 2 * D;       // bytes per K row
     static constexpr int VROW = KROW;                 // bytes per V row
@@ -156,17 +184,22 @@ struct Shape {
     static constexpr int KSUB = Q8 ? 1 : (D == 128 ? 2 : 1); // f16 K sub-tiles of 64 halves
     static constexpr int SCALE_BUF = Q8 ? ((T * SB + 32 + 127) / 128) * 128 : 0;
     static constexpr int KBYTES = T * KROW, VBYTES = T * VROW;
-    static constexpr int STAGE = ((KBYTES + VBYTES + 2 * SCALE_BUF + 1023) / 1024) * 1024; // keeps every stage 1024-byte aligned (swizzle atoms)
-    static constexpr int STAGES = (STAGE >= 64 * 1024) ? 3 : 4;
+    static constexpr int STAGE = ((KBYTES + VBYTES + 2 * SCALE_BUF + 1023) / 1024) * 1024; // 1024-aligned stages
     static constexpr int KSTEPS = D / 16;
     static constexpr int NBX = Q8 ? NB : 1;           // probability blocks per row
     static constexpr int RP = 4 * ((R + 1) / 2);      // floats per (row, block) in the exchange
     static constexpr int PROW = NBX * RP + 4;         // floats per row in the exchange
     static constexpr int PBUF = 16 * PROW;            // floats per warp
-    static constexpr int LPR = D / 8;                 // PV lanes per row (8 dims per lane)
+    // as many stages (2..4) as fit in 110 KiB with the exchange buffers: two CTAs per SM
+    static constexpr int FIT = (110 * 1024 - W * PBUF * 4 - 2048) / STAGE;
+    static constexpr int STAGES = FIT < 2 ? 2 : (FIT > 4 ? 4 : FIT);
+    static constexpr int LPR = D / 4;                 // PV lanes per row (4 dims per lane)
     static constexpr int RPS = 32 / LPR;              // PV rows per step
-    static constexpr int PF = R * (D + 2);            // floats of one partial
+    static constexpr int OOFF = ((2 * R + 3) / 4) * 4;  // partial: m[R], l[R], pad, then o[R][D] 16-byte aligned
+    static constexpr int PF = OOFF + R * D;            // floats of one partial
     static constexpr int SMEM = STAGES * STAGE + W * PBUF * 4 + W * 16 * 4 + 2 * STAGES * 8 + 64 + 1024;
+    static constexpr int MINB = Q8 ? 2 : 4;           // CTAs per SM the register budget targets
+    static constexpr int MERGE_CAP = (STAGES * STAGE) / (8 * R); // chunks the grid merge can stage
 };
 
 // Byte offset of 16-byte chunk `c` of row `row` in a TMA-swizzled K tile.
@@ -184,10 +217,11 @@ struct TileInfo {
 };
 
 template <int TYPE, int D, int R>
-__global__ void __launch_bounds__(W * 32, 1)
+__global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::MINB)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmk,
                 const __grid_constant__ CUtensorMap tmv) {
     using S = Shape<TYPE, D, R>;
+    constexpr int W = S::W, T = S::T, NT = W * 32;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *stages = smem;
@@ -197,12 +231,13 @@ __global__ void __launch_bounds__(W * 32, 1)
     uint64_t *empty = full + S::STAGES;
     TileInfo *tinfo = reinterpret_cast<TileInfo *>(empty + S::STAGES);
     __shared__ int s_flag;
+    __shared__ float s_M[R], s_L[R];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = blockIdx.y;
     const int chunk = blockIdx.x;
 
-    // ---- which sequence / chunk --------------------------------------------
+    // ---- which sequence / chunk (parameters only: safe before the wait) ----
     int si = 0;
     for (int i = 1; i < p.n_seq; ++i)
         if (chunk >= p.seq[i].chunk0) si = i;
@@ -212,20 +247,10 @@ __global__ void __launch_bounds__(W * 32, 1)
     const int row_begin = lc * p.chunk_rows;
     const int row_end = min(sq.n_rows, row_begin + p.chunk_rows);
 
-    // tile enumeration (identical for producer and consumers)
-    auto tile_at = [&](int r0, int &page, int &cell, int &n) {
-        const int lr = sq.off + r0;
-        page = sq.page_table[lr / p.P];
-        cell = lr % p.P;
-        n = min(min(T, row_end - r0), p.P - cell);
-    };
+    // tiles never cross a page: their sizes follow from (off, rows, P) alone
+    auto tile_rows = [&](int r0) { return min(min(T, row_end - r0), p.P - (sq.off + r0) % p.P); };
     int n_tiles = 0;
-    for (int r0 = row_begin; r0 < row_end;) {
-        int pg, cl, n;
-        tile_at(r0, pg, cl, n);
-        r0 += n;
-        ++n_tiles;
-    }
+    for (int r0 = row_begin; r0 < row_end; r0 += tile_rows(r0)) ++n_tiles;
 
     if (tid == 0) {
         for (int s = 0; s < S::STAGES; ++s) {
@@ -240,8 +265,10 @@ __global__ void __launch_bounds__(W * 32, 1)
     int prod_r0 = row_begin, prod_k = 0;
     auto issue = [&](int k) {
         const int s = k % S::STAGES;
-        int page, cell, n;
-        tile_at(prod_r0, page, cell, n);
+        const int n = tile_rows(prod_r0);
+        const int lr = sq.off + prod_r0;
+        const int page = sq.page_table[lr / p.P];
+        const int cell = lr % p.P;
         prod_r0 += n;
         const int64_t R0 = ((int64_t)page * p.Hk + g) * p.P + cell;
         uint8_t *st = stages + s * S::STAGE;
@@ -284,6 +311,14 @@ __global__ void __launch_bounds__(W * 32, 1)
             }
         }
     };
+    // Tiles made only of rows no in-flight kernel writes (the stable prefix)
+    // are requested before waiting for the preceding kernel.
+    if (tid == 0) {
+        while (prod_k < n_tiles && prod_k < S::STAGES && prod_r0 + tile_rows(prod_r0) <= sq.stable_rows)
+            issue(prod_k++);
+    }
+    pdl_wait();
+    pdl_trigger();
     if (tid == 0) {
         for (; prod_k < n_tiles && prod_k < S::STAGES; ++prod_k) issue(prod_k);
     }
@@ -338,24 +373,20 @@ __global__ void __launch_bounds__(W * 32, 1)
 
     // ---- per-warp online-softmax state -------------------------------------
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f; // heads 2t, 2t+1
-    float2 o[R][4];
+    float2 o[R][2];
 #pragma unroll
     for (int h = 0; h < R; ++h)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) o[h][j] = make_float2(0.f, 0.f);
+        for (int j = 0; j < 2; ++j) o[h][j] = make_float2(0.f, 0.f);
     float *pbuf = pbuf_all + warp * S::PBUF;
     float *abuf = abuf_all + warp * 16;
     const int rbase = warp * 16;
-    const int pv_ro = lane / S::LPR, pv_d0 = 8 * (lane % S::LPR);
+    const int pv_ro = lane / S::LPR, pv_d0 = 4 * (lane % S::LPR);
     const int pv_b = S::Q8 ? pv_d0 / 32 : 0;
 
-    bool ok = true;
     for (int k = 0; k < n_tiles; ++k) {
         const int s = k % S::STAGES;
-        if (!mbar_wait(&full[s], (k / S::STAGES) & 1, p.err)) {
-            ok = false;
-            break;
-        }
+        if (!mbar_wait(&full[s], (k / S::STAGES) & 1, p.err)) break;
         const uint8_t *st = stages + s * S::STAGE;
         const int n = tinfo[s].n;
         const int rows_w = min(max(n - rbase, 0), 16);
@@ -458,8 +489,8 @@ __global__ void __launch_bounds__(W * 32, 1)
                 }
             }
             if (gq == 0) {
-                if (2 * tq < 16) abuf[2 * tq] = al0;
-                if (2 * tq + 1 < 16) abuf[2 * tq + 1] = al1;
+                abuf[2 * tq] = al0;
+                abuf[2 * tq + 1] = al1;
             }
             __syncwarp();
             // ---------------- rescale and PV on the CUDA cores ----------------
@@ -475,48 +506,41 @@ __global__ void __launch_bounds__(W * 32, 1)
 #pragma unroll
                 for (int h = 0; h < R; ++h)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) mul2(o[h][j], al[h]);
+                    for (int j = 0; j < 2; ++j) mul2(o[h][j], al[h]);
             }
             const uint8_t *vt = st + S::KBYTES;
+#pragma unroll 4
             for (int r0 = 0; r0 < rows_w; r0 += S::RPS) {
                 const int row = r0 + pv_ro;
-                float2 vv[4];
+                float2 vv[2];
                 if constexpr (S::Q8) {
-                    const uint2 w2 = *reinterpret_cast<const uint2 *>(vt + (rbase + row) * S::VROW + pv_d0);
-                    codes_to_f32x8(w2.x, w2.y, vv);
+                    const uint32_t w = *reinterpret_cast<const uint32_t *>(vt + (rbase + row) * S::VROW + pv_d0);
+                    codes_to_f32x4(w, vv);
                 } else {
-                    const uint4 w4 = *reinterpret_cast<const uint4 *>(vt + (rbase + row) * S::VROW + 2 * pv_d0);
-                    const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        __half2 hh = *reinterpret_cast<const __half2 *>(&wv[j]);
-                        vv[j] = __half22float2(hh);
-                    }
+                    const uint2 w2 = *reinterpret_cast<const uint2 *>(vt + (rbase + row) * S::VROW + 2 * pv_d0);
+                    vv[0] = __half22float2(*reinterpret_cast<const __half2 *>(&w2.x));
+                    vv[1] = __half22float2(*reinterpret_cast<const __half2 *>(&w2.y));
                 }
                 const float *pp = pbuf + row * S::PROW + pv_b * S::RP;
 #pragma unroll
                 for (int hp = 0; hp < (R + 1) / 2; ++hp) {
                     const float4 q4 = *reinterpret_cast<const float4 *>(pp + 4 * hp);
                     const float2 pa = make_float2(q4.x, q4.y), pb = make_float2(q4.z, q4.w);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) fma2(o[2 * hp][j], pa, vv[j]);
+                    fma2(o[2 * hp][0], pa, vv[0]);
+                    fma2(o[2 * hp][1], pa, vv[1]);
                     if (2 * hp + 1 < R) {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) fma2(o[2 * hp + 1][j], pb, vv[j]);
+                        fma2(o[2 * hp + 1][0], pb, vv[0]);
+                        fma2(o[2 * hp + 1][1], pb, vv[1]);
                     }
                 }
             }
-            __syncwarp();
         }
         // release the stage; thread 0 refills it once every warp is done
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
         if (tid == 0 && prod_k < n_tiles) {
             const int ps = prod_k % S::STAGES;
-            if (mbar_wait(&empty[ps], ((prod_k / S::STAGES) - 1) & 1, p.err))
-                issue(prod_k);
-            else
-                ok = false;
+            if (mbar_wait(&empty[ps], ((prod_k / S::STAGES) - 1) & 1, p.err)) issue(prod_k);
             ++prod_k;
         }
     }
@@ -527,7 +551,6 @@ __global__ void __launch_bounds__(W * 32, 1)
             mbar_wait(&full[s], (k / S::STAGES) & 1, p.err);
         }
     }
-    (void)ok;
     __syncthreads();
 
     // ---- reduce the row-parallel lanes of each warp ----------------------------
@@ -536,14 +559,14 @@ __global__ void __launch_bounds__(W * 32, 1)
 #pragma unroll
         for (int h = 0; h < R; ++h)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 2; ++j) {
                 o[h][j].x += __shfl_xor_sync(0xffffffffu, o[h][j].x, m);
                 o[h][j].y += __shfl_xor_sync(0xffffffffu, o[h][j].y, m);
             }
     // ---- CTA merge of the warps (stages are free now) -------------------------
-    float *wm = reinterpret_cast<float *>(stages);      // [W][R]
-    float *wl = wm + W * R;                              // [W][R]
-    float *wo = wl + W * R;                              // [W][R][D]
+    float *wm = reinterpret_cast<float *>(stages); // [W][R]
+    float *wl = wm + W * R;                         // [W][R]
+    float *wo = wl + W * R;                         // [W][R][D]
     if (gq == 0) {
         if (2 * tq < R) {
             wm[warp * R + 2 * tq] = m0;
@@ -556,17 +579,17 @@ __global__ void __launch_bounds__(W * 32, 1)
     }
     if (lane < S::LPR) {
 #pragma unroll
-        for (int h = 0; h < R; ++h)
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                *reinterpret_cast<float2 *>(wo + (warp * R + h) * D + pv_d0 + 2 * j) = o[h][j];
+        for (int h = 0; h < R; ++h) {
+            float4 v4 = make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
+            *reinterpret_cast<float4 *>(wo + (warp * R + h) * D + pv_d0) = v4;
+        }
     }
     __syncthreads();
 
     const int n_chunks = sq.n_chunks;
     float *part = p.part + ((int64_t)chunk * p.Hk + g) * S::PF;
     float *outp = p.out + ((int64_t)sq.out_row * p.H + (int64_t)g * r_act) * D;
-    for (int idx = tid; idx < r_act * D; idx += W * 32) {
+    for (int idx = tid; idx < r_act * D; idx += NT) {
         const int h = idx / D, i = idx % D;
         float M = -INFINITY;
 #pragma unroll
@@ -585,7 +608,7 @@ __global__ void __launch_bounds__(W * 32, 1)
                 part[h] = M;
                 part[R + h] = L;
             }
-            part[2 * R + h * D + i] = O;
+            part[S::OOFF + h * D + i] = O;
         }
     }
     if (n_chunks == 1) return;
@@ -604,19 +627,57 @@ __global__ void __launch_bounds__(W * 32, 1)
     __threadfence();
     const float *part0 = p.part + ((int64_t)sq.chunk0 * p.Hk + g) * S::PF;
     const int64_t cstride = (int64_t)p.Hk * S::PF;
-    for (int idx = tid; idx < r_act * D; idx += W * 32) {
-        const int h = idx / D, i = idx % D;
+    float *cm = wm;                         // [n_chunks][R] maxima, then weights
+    float *cl = wm + n_chunks * R;          // [n_chunks][R] sums
+    // (the host keeps n_chunks <= MERGE_CAP)
+    for (int idx = tid; idx < n_chunks * R; idx += NT) {
+        const int c = idx / R, h = idx % R;
+        cm[idx] = __ldcg(part0 + c * cstride + h);
+        cl[idx] = __ldcg(part0 + c * cstride + R + h);
+    }
+    __syncthreads();
+    if (tid < r_act) {
         float M = -INFINITY;
-        for (int c = 0; c < n_chunks; ++c) M = fmaxf(M, __ldcg(part0 + c * cstride + h));
-        float L = 0.f, O = 0.f;
-        for (int c = 0; c < n_chunks; ++c) {
-            const float *pc = part0 + c * cstride;
-            const float mc = __ldcg(pc + h);
-            const float f = (M == -INFINITY) ? 0.f : exp2f(mc - M);
-            L += __ldcg(pc + R + h) * f;
-            O += __ldcg(pc + 2 * R + h * D + i) * f;
+        for (int c = 0; c < n_chunks; ++c) M = fmaxf(M, cm[c * R + tid]);
+        float L = 0.f;
+        for (int c = 0; c < n_chunks; ++c) L += (M == -INFINITY) ? 0.f : cl[c * R + tid] * exp2f(cm[c * R + tid] - M);
+        s_M[tid] = M;
+        s_L[tid] = L;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < n_chunks * R; idx += NT) {
+        const int h = idx % R;
+        cm[idx] = (h < r_act && s_M[h] != -INFINITY) ? exp2f(cm[idx] - s_M[h]) : 0.f;
+    }
+    __syncthreads();
+    // every thread owns 4 consecutive outputs; chunks are read 16 at a time
+    // with independent loads so the L2 round trips overlap
+    const int ncol = r_act * (D / 4);
+    for (int col = tid; col < ncol; col += NT) {
+        const int h = col / (D / 4), i4 = col % (D / 4);
+        const float *src = part0 + S::OOFF + h * D + 4 * i4;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c0 = 0; c0 < n_chunks; c0 += 16) {
+            float4 v[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+                v[u] = (c0 + u < n_chunks) ? __ldcg(reinterpret_cast<const float4 *>(src + (c0 + u) * cstride))
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const float w = (c0 + u < n_chunks) ? cm[(c0 + u) * R + h] : 0.f;
+                O.x += w * v[u].x;
+                O.y += w * v[u].y;
+                O.z += w * v[u].z;
+                O.w += w * v[u].w;
+            }
         }
-        outp[h * D + i] = (L > 0.f) ? O / L : 0.f;
+        const float L = s_L[h];
+        float *dst = outp + h * D + 4 * i4;
+        dst[0] = (L > 0.f) ? O.x / L : 0.f;
+        dst[1] = (L > 0.f) ? O.y / L : 0.f;
+        dst[2] = (L > 0.f) ? O.z / L : 0.f;
+        dst[3] = (L > 0.f) ? O.w / L : 0.f;
     }
 }
 
@@ -630,9 +691,17 @@ cudaError_t launch_t(const AttnParams &p, const CUtensorMap *tmk, const CUtensor
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    dim3 grid(p.total_chunks, p.Hk);
-    attn_kernel<TYPE, D, R><<<grid, W * 32, S::SMEM, st>>>(p, *tmk, *tmv);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.total_chunks, p.Hk);
+    cfg.blockDim = dim3(S::W * 32);
+    cfg.dynamicSmemBytes = S::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_kernel<TYPE, D, R>, p, *tmk, *tmv);
 }
 
 template <int TYPE, int D>
@@ -643,14 +712,49 @@ cudaError_t launch_d(const AttnParams &p, const CUtensorMap *tmk, const CUtensor
     return cudaErrorInvalidValue;
 }
 
+template <int TYPE, int D, int R>
+int occupancy() {
+    using S = Shape<TYPE, D, R>;
+    int n = 0;
+    cudaFuncSetAttribute(attn_kernel<TYPE, D, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<TYPE, D, R>, S::W * 32, S::SMEM) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return 1;
+    }
+    return n > 0 ? n : 1;
+}
+
+template <int TYPE, int D>
+int occupancy_d(int r) {
+    if (r <= 4) return occupancy<TYPE, D, 4>();
+    if (r == 5) return occupancy<TYPE, D, 5>();
+    return occupancy<TYPE, D, 8>();
+}
+
+template <int TYPE, int D>
+int merge_cap_d(int r) {
+    if (r <= 4) return Shape<TYPE, D, 4>::MERGE_CAP;
+    if (r == 5) return Shape<TYPE, D, 5>::MERGE_CAP;
+    return Shape<TYPE, D, 8>::MERGE_CAP;
+}
+
 } // namespace
 
 size_t attn_partial_floats(int r, int D) {
     const int R = r <= 4 ? 4 : (r == 5 ? 5 : 8);
-    return (size_t)R * (D + 2);
+    return (size_t)(((2 * R + 3) / 4) * 4 + R * D);
 }
 
-int attn_ctas_per_sm(int type, int D, int r) { return 1; }
+int attn_ctas_per_sm(int type, int D, int r) {
+    if (type == KVC_Q8_0) return D == 128 ? occupancy_d<KVC_Q8_0, 128>(r) : occupancy_d<KVC_Q8_0, 64>(r);
+    return D == 128 ? occupancy_d<KVC_F16, 128>(r) : occupancy_d<KVC_F16, 64>(r);
+}
+
+int attn_merge_cap(int type, int D, int r) {
+    if (type == KVC_Q8_0) return D == 128 ? merge_cap_d<KVC_Q8_0, 128>(r) : merge_cap_d<KVC_Q8_0, 64>(r);
+    return D == 128 ? merge_cap_d<KVC_F16, 128>(r) : merge_cap_d<KVC_F16, 64>(r);
+}
 
 cudaError_t launch_attn(int type, const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv,
                         cudaStream_t st) {

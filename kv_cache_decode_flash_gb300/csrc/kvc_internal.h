@@ -15,8 +15,6 @@ namespace kvc {
 constexpr int QK = 32;                 // elements per q8_0 block
 constexpr int MAX_SEQ_PER_LAUNCH = 64; // sequences carried in one attention launch
 constexpr int MAX_GROUP = 8;           // query heads per KV head supported by the attention kernel
-constexpr int ATTN_WARPS = 8;          // warps per attention CTA
-constexpr int ATTN_TILE = 16 * ATTN_WARPS; // rows per pipeline stage (16 rows per warp)
 constexpr int TMA_BOX_ROWS = 16;       // rows per TMA box
 
 // Device error word bits (kernels set them instead of trapping).
@@ -45,6 +43,8 @@ struct AttnSeq {
     int32_t n_chunks;          // chunks of this sequence (>= 1)
     int32_t out_row;           // index of this sequence in q / out
     int32_t ticket;            // index of this sequence's ticket row
+    int32_t stable_rows;       // leading rows no possibly in-flight kernel writes (readable before
+                               // the programmatic-dependency wait)
 };
 
 struct AttnParams {
@@ -68,6 +68,7 @@ struct AttnParams {
 cudaError_t launch_attn(int type, const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv,
                         cudaStream_t st);
 int attn_ctas_per_sm(int type, int D, int r);
+int attn_merge_cap(int type, int D, int r); // most chunks per (sequence, kv head) one merge can take
 size_t attn_partial_floats(int r, int D); // floats per (chunk, kv head) partial
 
 // Quantise-on-append.  Destination of token t: logical row row0 + t of a

@@ -47,7 +47,7 @@ void dev_free(Ctx *c, void *p, int64_t bytes);
 // rows (partials stay a small fraction of the bytes read).  Depends only on
 // the row counts, the geometry and the SM count.
 static int auto_chunk_rows(const Ctx *c, int64_t total_rows) {
-    const int64_t slots = (int64_t)c->sms * attn_ctas_per_sm(c->tk, c->D, c->r);
+    const int64_t slots = (int64_t)c->sms * c->occ;
     const int64_t work = std::max<int64_t>(total_rows * c->Hk, 1);
     const int64_t cmax = 2048;
     const int64_t waves = std::max<int64_t>(1, (work + slots * cmax - 1) / (slots * cmax));
@@ -61,7 +61,13 @@ int launch_attention(Ctx *c, const LayerView &lv, const CUtensorMap *tmk, const 
                      float kq_scale, cudaStream_t st) {
     int64_t total = 0;
     for (int i = 0; i < n_seq; ++i) total += seqs_in[i].n_rows;
-    const int C = c->chunk_override ? c->chunk_override : auto_chunk_rows(c, total);
+    int C = c->chunk_override ? c->chunk_override : auto_chunk_rows(c, total);
+    // one merge stages at most `cap` partials per (sequence, kv head)
+    const int cap = attn_merge_cap(c->tk, c->D, c->r);
+    for (int i = 0; i < n_seq; ++i) {
+        const int need = (seqs_in[i].n_rows + cap - 1) / cap;
+        if (need > C) C = (need + 15) / 16 * 16;
+    }
     const int64_t pf = (int64_t)attn_partial_floats(c->r, c->D);
     for (int base = 0; base < n_seq; base += MAX_SEQ_PER_LAUNCH) {
         const int cnt = std::min(MAX_SEQ_PER_LAUNCH, n_seq - base);
@@ -341,8 +347,10 @@ int transport_attn(Ctx *c, int layer, const float *q, float *out, float kq_scale
     a.off = 0;
     a.n_rows = rows;
     a.out_row = 0;
+    a.stable_rows = std::max(0, rows - c->recent[0][(size_t)layer]);
     rc = launch_attention(c, lv, &s->tmk, &s->tmv, s->cap, s->scale_bytes, 1, &a, q, out, kq_scale, st);
     if (rc) return rc;
+    c->clear_recent();
     if (engaged) {
         KVC_CU(c, cudaEventRecord(s->release, st));
         s->consumed_once = true;

@@ -346,9 +346,10 @@ def test_invalid_arguments_are_rejected():
     try:
         ctx = tw.gpu.ctx
         L = kvc.load()
-        assert L.kvc_append(ctx, 5, 0, 0, 1, 1, 1, None) == kvc.KVC_EINVAL  # layer
-        assert L.kvc_append(ctx, 0, 9, 0, 1, 1, 1, None) == kvc.KVC_EINVAL  # seq
-        assert L.kvc_append(ctx, 0, 0, -5, 1, 1, 1, None) == kvc.KVC_ERANGE
+        assert L.kvc_append(ctx, 5, 0, 0, 1, 256, 256, None) == kvc.KVC_EINVAL  # layer
+        assert L.kvc_append(ctx, 0, 9, 0, 1, 256, 256, None) == kvc.KVC_EINVAL  # seq
+        assert L.kvc_append(ctx, 0, 0, -5, 1, 256, 256, None) == kvc.KVC_ERANGE
+        assert L.kvc_append(ctx, 0, 0, 0, 1, 260, 256, None) == kvc.KVC_EINVAL  # misaligned k
         assert L.kvc_seq_rm(ctx, 7, 0, 1) == kvc.KVC_EINVAL
         assert L.kvc_set_chunk_rows(ctx, 17) == kvc.KVC_EINVAL
         assert L.kvc_pipeline_depth(ctx, 99) == kvc.KVC_EINVAL
