@@ -264,6 +264,37 @@ int kvc_debug_fail_alloc_after(kvc_ctx *c, int n);
  * *word receives it (0 = none).  Waits for the context's device work. */
 int kvc_check_device_error(kvc_ctx *c, uint32_t *word);
 
+/* Decode attention over caller-owned K/V that allocates no memory.
+ * The pages have no counterpart for this call; it exists for callers that
+ * cannot let a library call cudaMalloc: serving runtimes that reserve all
+ * device memory up front and hand it out from their own arena (an
+ * allocation behind their back breaks their accounting or simply fails),
+ * and latency-critical paths that cannot afford an allocation's implicit
+ * device synchronisation.  It computes the same thing as kvc_attn_decode
+ * for one sequence of one layer, with the same kernel, without a context:
+ *   out[h][:] = softmax_j(kq_scale * q[h] . K_j) V_j,  j < n_kv.
+ * type: KVC_Q8_0 or KVC_F16.  K and V are the caller's device buffers, laid
+ * out head-major like one layer of the state export format:
+ *   q8_0: k, v = int8 codes [n_head_kv][n_kv][head_dim], ks, vs = fp16 scale
+ *         bits [n_head_kv][n_kv][head_dim/32]; f16: k, v = fp16 halves
+ *         [n_head_kv][n_kv][head_dim], ks = vs = NULL.
+ * q, out: device fp32 [n_head][head_dim].  Every pointer 16-byte aligned;
+ * scale buffers readable up to the next multiple of 16 bytes.
+ * Work space (split-K partials, arrival tickets, error word) lives in one
+ * fixed 8 MiB device array inside the library, which every GPU that loads
+ * the library holds until the process exits.  The first call on a device
+ * looks up that array's device address (set-up, no allocation), so make it
+ * before recording work you cannot interrupt.  All calls share the array and
+ * it keeps the previous call's contents: the call clears what must start at
+ * zero in stream order, and calls whose kernels overlap on the GPU (other
+ * streams, other threads) race on it, so order them.
+ * Errors: KVC_EINVAL (types, shapes, null or misaligned pointers),
+ * KVC_ERANGE (n_kv so large that the partials do not fit the 8 MiB work
+ * space; plain kvc_attn_decode has no such limit), KVC_ECUDA. */
+int kvc_attn_decode_static(int type, int n_head, int n_head_kv, int head_dim, int n_kv, const void *k,
+                           const uint16_t *ks, const void *v, const uint16_t *vs, const float *q,
+                           float *out, float kq_scale, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
