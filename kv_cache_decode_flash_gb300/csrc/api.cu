@@ -438,8 +438,8 @@ int kvc_create(const kvc_params *p, kvc_ctx **out) {
         cudaMemsetAsync(c->pt_dev, 0, (size_t)p->n_seq_max * c->max_pages * 4, c->st);
         c->free_pages.reserve(c->n_pages);
         for (int32_t i = c->n_pages - 1; i >= 0; --i) c->free_pages.push_back(i);
-        c->tmk.resize(c->L);
-        c->tmv.resize(c->L);
+        c->tmk.resize(2 * (size_t)c->L);
+        c->tmv.resize(2 * (size_t)c->L);
         const int64_t rows_all = (int64_t)c->L * c->pool_rows;
         if (rows_all > INT32_MAX) {
             c->err = "pool too large for 32-bit TMA row coordinates";
@@ -447,12 +447,15 @@ int kvc_create(const kvc_params *p, kvc_ctx **out) {
         }
         for (int l = 0; l < c->L; ++l) {
             std::string why;
-            if (!encode_rows_map(&c->tmk[l], c->kdata + (int64_t)l * c->pool_rows * c->krow, c->pool_rows, c->krow,
-                                 c->tk, true, &why) ||
-                !encode_rows_map(&c->tmv[l], c->vdata + (int64_t)l * c->pool_rows * c->vrow, c->pool_rows, c->vrow,
-                                 c->tv, false, &why)) {
-                c->err = why;
-                return fail(KVC_ECUDA);
+            for (int b = 0; b < 2; ++b) {
+                const int box = b ? (int)std::min<int64_t>(TMA_BIG_ROWS, c->pool_rows) : TMA_BOX_ROWS;
+                if (!encode_rows_map(&c->tmk[2 * l + b], c->kdata + (int64_t)l * c->pool_rows * c->krow, c->pool_rows,
+                                     c->krow, c->tk, true, &why, box) ||
+                    !encode_rows_map(&c->tmv[2 * l + b], c->vdata + (int64_t)l * c->pool_rows * c->vrow, c->pool_rows,
+                                     c->vrow, c->tv, true, &why, box)) {
+                    c->err = why;
+                    return fail(KVC_ECUDA);
+                }
             }
         }
         // partials for chunks of at least 64 rows; grown on demand for smaller forced chunks
@@ -605,7 +608,7 @@ int kvc_attn_decode(kvc_ctx *cc, int layer, int n_seq, const int32_t *seq_ids, c
     lv.v.data = c->vdata + lo * c->vrow;
     lv.v.scales = c->vsb ? reinterpret_cast<uint16_t *>(c->vscales + lo * c->vsb) : nullptr;
     const int64_t scale_limit = c->ksb ? c->kscale_bytes - lo * c->ksb : 0;
-    int rc = launch_attention(c, lv, &c->tmk[(size_t)layer], &c->tmv[(size_t)layer], c->P, scale_limit, n_seq,
+    int rc = launch_attention(c, lv, &c->tmk[2 * (size_t)layer], &c->tmv[2 * (size_t)layer], c->P, scale_limit, n_seq,
                               seqs.data(), q, out, kq_scale, st);
     if (rc == KVC_OK) c->clear_recent(); // kernels after this one start only once it has waited
     return rc;

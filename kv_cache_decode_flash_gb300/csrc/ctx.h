@@ -37,7 +37,7 @@ struct Slot {
     int32_t cap = 0;
     int64_t bytes = 0;
     int64_t scale_bytes = 0; // bytes of each scale buffer
-    CUtensorMap tmk, tmv;
+    CUtensorMap tmk[2], tmv[2]; // 16-row and 128-row boxes
     cudaEvent_t ready = nullptr, release = nullptr;
     int32_t layer = -1; // layer held (-1 none)
     int32_t rows = 0;   // rows of that layer present
@@ -73,7 +73,7 @@ struct Ctx {
     uint8_t *kdata = nullptr, *vdata = nullptr;
     uint8_t *kscales = nullptr, *vscales = nullptr;
     int64_t kdata_bytes = 0, vdata_bytes = 0, kscale_bytes = 0, vscale_bytes = 0;
-    std::vector<CUtensorMap> tmk, tmv; // per layer
+    std::vector<CUtensorMap> tmk, tmv; // per layer: [2l] 16-row boxes, [2l+1] 128-row boxes
     int32_t *pt_dev = nullptr;         // [n_seq_max][max_pages]
     int32_t max_pages = 0;
     std::vector<Seq> seqs;

@@ -101,68 +101,47 @@ __device__ __forceinline__ void codes_to_half2(uint32_t w, uint32_t &h01, uint32
     asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(h23) : "r"(bias));
 }
 
-// Eight int8 codes (two words) -> eight fp32 values, as four float2.
-// Each byte goes into the low mantissa byte of 2^23 (0x4B0000xx = 2^23 + u);
-// subtracting 2^23 + 128 gives the signed code exactly.
-__device__ __forceinline__ void codes_to_f32x8(uint32_t w0, uint32_t w1, float2 (&v)[4]) {
-    const uint32_t u0 = w0 ^ 0x80808080u, u1 = w1 ^ 0x80808080u;
-    const uint32_t mag = 0x4B000000u;
-    uint32_t f[8];
-    asm("prmt.b32 %0, %1, %2, 0x7650;" : "=r"(f[0]) : "r"(u0), "r"(mag));
-    asm("prmt.b32 %0, %1, %2, 0x7651;" : "=r"(f[1]) : "r"(u0), "r"(mag));
-    asm("prmt.b32 %0, %1, %2, 0x7652;" : "=r"(f[2]) : "r"(u0), "r"(mag));
-    asm("prmt.b32 %0, %1, %2, 0x7653;" : "=r"(f[3]) : "r"(u0), "r"(mag));
-    asm("prmt.b32 %0, %1, %2, 0x7650;" : "=r"(f[4]) : "r"(u1), "r"(mag));
-    asm("prmt.b32 %0, %1, %2, 0x7651;" : "=r"(f[5]) : "r"(u1), "r"(mag));
-    asm("prmt.b32 %0, %1, %2, 0x7652;" : "=r"(f[6]) : "r"(u1), "r"(mag));
-    asm("prmt.b32 %0, %1, %2, 0x7653;" : "=r"(f[7]) : "r"(u1), "r"(mag));
-    const float b = 8388736.0f; // 2^23 + 128
-    const float2 bb = make_float2(b, b);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float2 x = make_float2(__uint_as_float(f[2 * i]), __uint_as_float(f[2 * i + 1]));
-        unsigned long long xr = *reinterpret_cast<unsigned long long *>(&x);
-        unsigned long long br = *reinterpret_cast<const unsigned long long *>(&bb);
-        asm("sub.rn.f32x2 %0, %0, %1;" : "+l"(xr) : "l"(br));
-        v[i] = *reinterpret_cast<float2 *>(&xr);
-    }
+
+
+
+
+
+
+__device__ __forceinline__ void ldsm_x4(const void *p, uint32_t &a, uint32_t &b, uint32_t &c, uint32_t &d) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                 : "r"(smem_u32(p)));
 }
-
-__device__ __forceinline__ void fma2(float2 &acc, const float2 a, const float2 b) {
-    unsigned long long ar = *reinterpret_cast<const unsigned long long *>(&a);
-    unsigned long long br = *reinterpret_cast<const unsigned long long *>(&b);
-    unsigned long long cr = *reinterpret_cast<unsigned long long *>(&acc);
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(cr) : "l"(ar), "l"(br));
-    acc = *reinterpret_cast<float2 *>(&cr);
+__device__ __forceinline__ void ldsm_x4_trans(const void *p, uint32_t &a, uint32_t &b, uint32_t &c, uint32_t &d) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                 : "r"(smem_u32(p)));
 }
-
-__device__ __forceinline__ void mul2(float2 &acc, const float2 a) {
-    unsigned long long ar = *reinterpret_cast<const unsigned long long *>(&a);
-    unsigned long long cr = *reinterpret_cast<unsigned long long *>(&acc);
-    asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(cr) : "l"(ar));
-    acc = *reinterpret_cast<float2 *>(&cr);
+// 2^x (approximate, relative error ~2^-22; +0 for -inf)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
-
-
-// Four int8 codes -> four fp32 values (two float2), exact (see codes_to_f32x8).
-__device__ __forceinline__ void codes_to_f32x4(uint32_t w, float2 (&v)[2]) {
+// Split two fp32 values into fp16 hi + lo pairs: hi keeps the top 11
+// significant bits (exactly representable), lo = x - hi rounded to fp16.
+__device__ __forceinline__ void split_pack(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const float h0 = __uint_as_float(__float_as_uint(x0) & 0xFFFFE000u);
+    const float h1 = __uint_as_float(__float_as_uint(x1) & 0xFFFFE000u);
+    const __half2 hh = __floats2half2_rn(h0, h1), ll = __floats2half2_rn(x0 - h0, x1 - h1);
+    hi = *reinterpret_cast<const uint32_t *>(&hh);
+    lo = *reinterpret_cast<const uint32_t *>(&ll);
+}
+// A transposed V word holds codes (row 2t, dim 2g), (row 2t, dim 2g+1),
+// (row 2t+1, dim 2g), (row 2t+1, dim 2g+1); return the exact half2 of the
+// even dim (rows 2t, 2t+1) and of the odd dim.
+__device__ __forceinline__ void vcodes_to_half2(uint32_t w, uint32_t &ev, uint32_t &od) {
     const uint32_t u = w ^ 0x80808080u;
-    const uint32_t mag = 0x4B000000u;
-    uint32_t f[4];
-    asm("prmt.b32 %0, %1, %2, 0x7650;" : "=r"(f[0]) : "r"(u), "r"(mag));
-    asm("prmt.b32 %0, %1, %2, 0x7651;" : "=r"(f[1]) : "r"(u), "r"(mag));
-    asm("prmt.b32 %0, %1, %2, 0x7652;" : "=r"(f[2]) : "r"(u), "r"(mag));
-    asm("prmt.b32 %0, %1, %2, 0x7653;" : "=r"(f[3]) : "r"(u), "r"(mag));
-    const float b = 8388736.0f; // 2^23 + 128
-    const float2 bb = make_float2(b, b);
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        float2 x = make_float2(__uint_as_float(f[2 * i]), __uint_as_float(f[2 * i + 1]));
-        unsigned long long xr = *reinterpret_cast<unsigned long long *>(&x);
-        unsigned long long br = *reinterpret_cast<const unsigned long long *>(&bb);
-        asm("sub.rn.f32x2 %0, %0, %1;" : "+l"(xr) : "l"(br));
-        v[i] = *reinterpret_cast<float2 *>(&xr);
-    }
+    asm("prmt.b32 %0, %1, %2, 0x5240;" : "=r"(ev) : "r"(u), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x5341;" : "=r"(od) : "r"(u), "r"(0x64646464u));
+    const uint32_t bias = 0x64806480u; // half2(1152, 1152)
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(ev) : "r"(bias));
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(od) : "r"(bias));
 }
 
 // Programmatic dependent launch: wait for the preceding kernel's results /
@@ -175,7 +154,7 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 template <int TYPE, int D, int R>
 struct Shape {
     static constexpr bool Q8 = TYPE == KVC_Q8_0;
-    static constexpr int W = Q8 ? 8 : 4;              // warps per CTA
+    static constexpr int W = Q8 ? 16 : 8;             // warps per CTA (one CTA per SM)
     static constexpr int T = 16 * W;                  // rows per tile
     static constexpr int NB = D / 32;                 // q8_0 blocks per row
     static constexpr int KROW = Q8 ? D : 2 * D;       // bytes per K row
@@ -186,20 +165,20 @@ struct Shape {
     static constexpr int KBYTES = T * KROW, VBYTES = T * VROW;
     static constexpr int STAGE = ((KBYTES + VBYTES + 2 * SCALE_BUF + 1023) / 1024) * 1024; // 1024-aligned stages
     static constexpr int KSTEPS = D / 16;
-    static constexpr int NBX = Q8 ? NB : 1;           // probability blocks per row
-    static constexpr int RP = 4 * ((R + 1) / 2);      // floats per (row, block) in the exchange
-    static constexpr int PROW = NBX * RP + 4;         // floats per row in the exchange
-    static constexpr int PBUF = 16 * PROW;            // floats per warp
-    // as many stages (2..4) as fit in 110 KiB with the exchange buffers: two CTAs per SM
-    static constexpr int FIT = (110 * 1024 - W * PBUF * 4 - 2048) / STAGE;
+    static constexpr int NBX = Q8 ? NB : 1;           // scale blocks per row (1 for f16)
+    static constexpr int PSTR = 24;                   // floats per head slot in the exchange (16 rows + pad)
+    static constexpr int PBUF = 8 * PSTR;             // floats per warp: p[8 head slots][rows]
+    static constexpr int MAXT = 512;                  // tiles per chunk (host keeps chunks within it)
+    // as many stages (2..4) as fit next to the exchange buffers in one SM's shared memory
+    static constexpr int FIT = (232448 - 4096 - W * PBUF * 4 - 1024 - MAXT * 8 - 256) / STAGE;
     static constexpr int STAGES = FIT < 2 ? 2 : (FIT > 4 ? 4 : FIT);
-    static constexpr int LPR = D / 4;                 // PV lanes per row (4 dims per lane)
-    static constexpr int RPS = 32 / LPR;              // PV rows per step
     static constexpr int OOFF = ((2 * R + 3) / 4) * 4;  // partial: m[R], l[R], pad, then o[R][D] 16-byte aligned
     static constexpr int PF = OOFF + R * D;            // floats of one partial
-    static constexpr int SMEM = STAGES * STAGE + W * PBUF * 4 + W * 16 * 4 + 2 * STAGES * 8 + 64 + 1024;
-    static constexpr int MINB = Q8 ? 2 : 4;           // CTAs per SM the register budget targets
-    static constexpr int MERGE_CAP = (STAGES * STAGE) / (8 * R); // chunks the grid merge can stage
+    static constexpr int SMEM = STAGES * STAGE + W * PBUF * 4 + 2 * STAGES * 8 + STAGES * 4 + 64 + MAXT * 8 + 1024;
+    static constexpr int MINB = 1;                    // one CTA per SM (registers capped at 128 by W)
+    static constexpr int MERGE_CAP = (STAGES * STAGE) / (4 * (PF + R)); // chunks the grid merge can stage
+    static constexpr int BIG = 128;                    // rows of a large TMA box (small boxes are 16 rows)
+    static constexpr int NMT = D / 16;                 // PV m-tiles of 16 dims
 };
 
 // Byte offset of 16-byte chunk `c` of row `row` in a TMA-swizzled K tile.
@@ -219,19 +198,23 @@ struct TileInfo {
 template <int TYPE, int D, int R>
 __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::MINB)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmk,
-                const __grid_constant__ CUtensorMap tmv) {
+                const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmkb,
+                const __grid_constant__ CUtensorMap tmvb) {
     using S = Shape<TYPE, D, R>;
     constexpr int W = S::W, T = S::T, NT = W * 32;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *stages = smem;
     float *pbuf_all = reinterpret_cast<float *>(smem + S::STAGES * S::STAGE);
-    float *abuf_all = pbuf_all + W * S::PBUF;
-    uint64_t *full = reinterpret_cast<uint64_t *>(abuf_all + W * 16);
+    uint64_t *full = reinterpret_cast<uint64_t *>(pbuf_all + W * S::PBUF);
     uint64_t *empty = full + S::STAGES;
     TileInfo *tinfo = reinterpret_cast<TileInfo *>(empty + S::STAGES);
+    int *s_cnt = reinterpret_cast<int *>(tinfo + S::STAGES); // warps done with each stage
+    int *s_tstart = s_cnt + S::STAGES;                        // first row of every tile
+    int *s_tpage = s_tstart + S::MAXT;                        // its physical page
     __shared__ int s_flag;
     __shared__ float s_M[R], s_L[R];
+    __shared__ float s_ww[W * 8]; // per-warp merge weights [warp][head]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = blockIdx.y;
@@ -249,31 +232,37 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
 
     // tiles never cross a page: their sizes follow from (off, rows, P) alone
     auto tile_rows = [&](int r0) { return min(min(T, row_end - r0), p.P - (sq.off + r0) % p.P); };
-    int n_tiles = 0;
-    for (int r0 = row_begin; r0 < row_end; r0 += tile_rows(r0)) ++n_tiles;
-
     if (tid == 0) {
+        int nt = 0;
+        for (int r0 = row_begin; r0 < row_end && nt < S::MAXT; r0 += tile_rows(r0)) s_tstart[nt++] = r0;
+        s_flag = nt;
         for (int s = 0; s < S::STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], W);
+            s_cnt[s] = 0;
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    const int n_tiles = s_flag;
+    if (warp == 0)
+        for (int k = lane; k < n_tiles; k += 32) s_tpage[k] = sq.page_table[(sq.off + s_tstart[k]) / p.P];
+    __syncthreads();
 
-    // ---- producer (thread 0) -----------------------------------------------
-    int prod_r0 = row_begin, prod_k = 0;
+    // ---- tile loads: the first stages by thread 0, every later one by the last
+    // warp to finish with the stage it reuses ----------------------------------
     auto issue = [&](int k) {
         const int s = k % S::STAGES;
-        const int n = tile_rows(prod_r0);
-        const int lr = sq.off + prod_r0;
-        const int page = sq.page_table[lr / p.P];
-        const int cell = lr % p.P;
-        prod_r0 += n;
+        const int r0 = s_tstart[k];
+        const int n = tile_rows(r0);
+        const int page = s_tpage[k];
+        const int cell = (sq.off + r0) % p.P;
         const int64_t R0 = ((int64_t)page * p.Hk + g) * p.P + cell;
         uint8_t *st = stages + s * S::STAGE;
-        const int nb = (n + TMA_BOX_ROWS - 1) / TMA_BOX_ROWS;
-        unsigned bytes = (unsigned)(nb * TMA_BOX_ROWS * (S::KROW + S::VROW));
+        // large boxes first, then 16-row boxes for the rest of the tile
+        const int nbig = n / S::BIG;
+        const int nsmall = (n - nbig * S::BIG + TMA_BOX_ROWS - 1) / TMA_BOX_ROWS;
+        unsigned bytes = (unsigned)((nbig * S::BIG + nsmall * TMA_BOX_ROWS) * (S::KROW + S::VROW));
         int delta = 0;
         unsigned sbytes = 0;
         int64_t saligned = 0;
@@ -292,16 +281,22 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
         tinfo[s].n = n;
         tinfo[s].delta = delta;
         mbar_expect_tx(&full[s], bytes);
-        for (int b = 0; b < nb; ++b) {
-            const int y = (int)(R0 + b * TMA_BOX_ROWS);
-            if constexpr (S::Q8 || S::KSUB == 1) {
-                tma_load_2d(st + b * TMA_BOX_ROWS * (S::Q8 ? S::KROW : 128), &tmk, 0, y, &full[s]);
+        auto box = [&](const CUtensorMap *mk, const CUtensorMap *mv, int ro) {
+            const int y = (int)(R0 + ro);
+            if constexpr (S::KSUB == 1) {
+                // rows of at most 128 bytes: one swizzled box per tensor
+                tma_load_2d(st + ro * S::KROW, mk, 0, y, &full[s]);
+                tma_load_2d(st + S::KBYTES + ro * S::VROW, mv, 0, y, &full[s]);
             } else {
-                tma_load_2d(st + b * TMA_BOX_ROWS * 128, &tmk, 0, y, &full[s]);
-                tma_load_2d(st + T * 128 + b * TMA_BOX_ROWS * 128, &tmk, 64, y, &full[s]);
+                // 256-byte f16 rows: two 128-byte sub-tiles per tensor
+                tma_load_2d(st + ro * 128, mk, 0, y, &full[s]);
+                tma_load_2d(st + T * 128 + ro * 128, mk, 64, y, &full[s]);
+                tma_load_2d(st + S::KBYTES + ro * 128, mv, 0, y, &full[s]);
+                tma_load_2d(st + S::KBYTES + T * 128 + ro * 128, mv, 64, y, &full[s]);
             }
-            tma_load_2d(st + S::KBYTES + b * TMA_BOX_ROWS * S::VROW, &tmv, 0, y, &full[s]);
-        }
+        };
+        for (int b = 0; b < nbig; ++b) box(&tmkb, &tmvb, b * S::BIG);
+        for (int b = 0; b < nsmall; ++b) box(&tmk, &tmv, nbig * S::BIG + b * TMA_BOX_ROWS);
         if constexpr (S::Q8) {
             if (sbytes) {
                 bulk_load(st + S::KBYTES + S::VBYTES, reinterpret_cast<const uint8_t *>(p.ks) + saligned, sbytes,
@@ -313,8 +308,9 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
     };
     // Tiles made only of rows no in-flight kernel writes (the stable prefix)
     // are requested before waiting for the preceding kernel.
+    int prod_k = 0; // thread 0: tiles issued before the loop
     if (tid == 0) {
-        while (prod_k < n_tiles && prod_k < S::STAGES && prod_r0 + tile_rows(prod_r0) <= sq.stable_rows)
+        while (prod_k < n_tiles && prod_k < S::STAGES && s_tstart[prod_k] + tile_rows(s_tstart[prod_k]) <= sq.stable_rows)
             issue(prod_k++);
     }
     pdl_wait();
@@ -371,70 +367,68 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
     const float hs0 = ldexpf(1.0f, -e0), hs1 = ldexpf(1.0f, -e1);
     const bool hv0 = 2 * tq < r_act, hv1 = 2 * tq + 1 < r_act;
 
-    // ---- per-warp online-softmax state -------------------------------------
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f; // heads 2t, 2t+1
-    float2 o[R][2];
+    // ---- per-warp state -------------------------------------------------------
+    // softmax state of heads 2t, 2t+1; PV accumulators O^T[dims][heads] as
+    // m16n8 fragments (rows = dims, columns = heads 2t, 2t+1)
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    constexpr int NMT = D / 16;
+    float acc[NMT][4];
 #pragma unroll
-    for (int h = 0; h < R; ++h)
+    for (int mt = 0; mt < NMT; ++mt)
 #pragma unroll
-        for (int j = 0; j < 2; ++j) o[h][j] = make_float2(0.f, 0.f);
-    float *pbuf = pbuf_all + warp * S::PBUF;
-    float *abuf = abuf_all + warp * 16;
+        for (int j = 0; j < 4; ++j) acc[mt][j] = 0.f;
+    int sexp = 0;        // P' range exponent S of this warp (valid once have_s)
+    bool have_s = false;
+    float *pw = pbuf_all + warp * S::PBUF; // p[head slot][row], head stride PSTR
     const int rbase = warp * 16;
-    const int pv_ro = lane / S::LPR, pv_d0 = 4 * (lane % S::LPR);
-    const int pv_b = S::Q8 ? pv_d0 / 32 : 0;
 
     for (int k = 0; k < n_tiles; ++k) {
         const int s = k % S::STAGES;
         if (!mbar_wait(&full[s], (k / S::STAGES) & 1, p.err)) break;
         const uint8_t *st = stages + s * S::STAGE;
+        const uint8_t *vt = st + S::KBYTES;
         const int n = tinfo[s].n;
         const int rows_w = min(max(n - rbase, 0), 16);
         if (rows_w > 0) {
             // ---------------- QK on the tensor cores ----------------
             float sc[4] = {0.f, 0.f, 0.f, 0.f}; // (row g, 2t) (row g, 2t+1) (row g+8, 2t) (row g+8, 2t+1)
             const int ra = rbase + gq, rb = ra + 8;
+            // ldmatrix lane roles: rows 0-7 / 8-15 of the warp's slab, first / second 16-byte chunk
+            const int lm_row = rbase + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int lm_hi = lane >> 4;
             if constexpr (S::Q8) {
                 const uint16_t *ksc = reinterpret_cast<const uint16_t *>(st + S::KBYTES + S::VBYTES) +
                                       tinfo[s].delta * S::NB;
 #pragma unroll
                 for (int b = 0; b < S::NB; ++b) {
-                    float ch[4] = {0.f, 0.f, 0.f, 0.f}, cl[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int s2 = 0; s2 < 2; ++s2) {
-                        const int ks = 2 * b + s2;
-                        const uint32_t wa = *reinterpret_cast<const uint32_t *>(st + swz<S::KROW>(ra, ks) + 4 * tq);
-                        const uint32_t wb = *reinterpret_cast<const uint32_t *>(st + swz<S::KROW>(rb, ks) + 4 * tq);
-                        uint32_t a0, a1, a2, a3;
-                        codes_to_half2(wa, a0, a2);
-                        codes_to_half2(wb, a1, a3);
-                        mma16816(ch, a0, a1, a2, a3, bh[ks][0], bh[ks][1]);
-                        mma16816(cl, a0, a1, a2, a3, bl[ks][0], bl[ks][1]);
-                    }
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4(st + swz<S::KROW>(lm_row, 2 * b + lm_hi), r0, r1, r2, r3);
+                    float c[4] = {0.f, 0.f, 0.f, 0.f};
+                    uint32_t a0, a1, a2, a3;
+                    codes_to_half2(r0, a0, a2);
+                    codes_to_half2(r1, a1, a3);
+                    mma16816(c, a0, a1, a2, a3, bh[2 * b][0], bh[2 * b][1]);
+                    mma16816(c, a0, a1, a2, a3, bl[2 * b][0], bl[2 * b][1]);
+                    codes_to_half2(r2, a0, a2);
+                    codes_to_half2(r3, a1, a3);
+                    mma16816(c, a0, a1, a2, a3, bh[2 * b + 1][0], bh[2 * b + 1][1]);
+                    mma16816(c, a0, a1, a2, a3, bl[2 * b + 1][0], bl[2 * b + 1][1]);
                     const float da = __half2float(__ushort_as_half(ksc[ra * S::NB + b]));
                     const float db = __half2float(__ushort_as_half(ksc[rb * S::NB + b]));
-                    sc[0] = fmaf(da, ch[0] + cl[0], sc[0]);
-                    sc[1] = fmaf(da, ch[1] + cl[1], sc[1]);
-                    sc[2] = fmaf(db, ch[2] + cl[2], sc[2]);
-                    sc[3] = fmaf(db, ch[3] + cl[3], sc[3]);
+                    sc[0] = fmaf(da, c[0], sc[0]);
+                    sc[1] = fmaf(da, c[1], sc[1]);
+                    sc[2] = fmaf(db, c[2], sc[2]);
+                    sc[3] = fmaf(db, c[3], sc[3]);
                 }
             } else {
-                float ch[4] = {0.f, 0.f, 0.f, 0.f}, cl[4] = {0.f, 0.f, 0.f, 0.f};
                 const int lrow = rbase + (lane & 15);
 #pragma unroll
                 for (int ks = 0; ks < S::KSTEPS; ++ks) {
-                    const int sub = ks / 4;
-                    const int c = 2 * (ks % 4) + (lane >> 4);
-                    const uint32_t addr = smem_u32(st + sub * T * 128 + swz<128>(lrow, c));
                     uint32_t a0, a1, a2, a3;
-                    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                                 : "r"(addr));
-                    mma16816(ch, a0, a1, a2, a3, bh[ks][0], bh[ks][1]);
-                    mma16816(cl, a0, a1, a2, a3, bl[ks][0], bl[ks][1]);
+                    ldsm_x4(st + (ks / 4) * T * 128 + swz<128>(lrow, 2 * (ks % 4) + (lane >> 4)), a0, a1, a2, a3);
+                    mma16816(sc, a0, a1, a2, a3, bh[ks][0], bh[ks][1]);
+                    mma16816(sc, a0, a1, a2, a3, bl[ks][0], bl[ks][1]);
                 }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) sc[j] = ch[j] + cl[j];
             }
             // log2-domain scores; rows beyond the tile are -inf
             float s2v[4];
@@ -449,14 +443,13 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
                 t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, m));
                 t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, m));
             }
-            const float mn0 = fmaxf(m0, t0), mn1 = fmaxf(m1, t1);
-            const float al0 = (mn0 == -INFINITY) ? 1.f : exp2f(m0 - mn0);
-            const float al1 = (mn1 == -INFINITY) ? 1.f : exp2f(m1 - mn1);
+            const float mn0 = fmaxf(m0, t0), mn1 = fmaxf(m1, t1); // finite: the slab has a live row
+            const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
             float pr[4];
-            pr[0] = (hv0 && s2v[0] != -INFINITY) ? exp2f(s2v[0] - mn0) : 0.f;
-            pr[1] = (hv1 && s2v[1] != -INFINITY) ? exp2f(s2v[1] - mn1) : 0.f;
-            pr[2] = (hv0 && s2v[2] != -INFINITY) ? exp2f(s2v[2] - mn0) : 0.f;
-            pr[3] = (hv1 && s2v[3] != -INFINITY) ? exp2f(s2v[3] - mn1) : 0.f;
+            pr[0] = hv0 ? ex2(s2v[0] - mn0) : 0.f;
+            pr[1] = hv1 ? ex2(s2v[1] - mn1) : 0.f;
+            pr[2] = hv0 ? ex2(s2v[2] - mn0) : 0.f;
+            pr[3] = hv1 ? ex2(s2v[3] - mn1) : 0.f;
             float rs0 = pr[0] + pr[2], rs1 = pr[1] + pr[3];
 #pragma unroll
             for (int m = 4; m < 32; m <<= 1) {
@@ -467,210 +460,269 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
             l1 = l1 * al1 + rs1;
             m0 = mn0;
             m1 = mn1;
-            // ---------------- exchange: p * d_v per block, duplicated in pairs ----
-            if (4 * tq < S::RP) {
-                const uint16_t *vsc =
-                    S::Q8 ? reinterpret_cast<const uint16_t *>(st + S::KBYTES + S::VBYTES + S::SCALE_BUF) +
-                                tinfo[s].delta * S::NB
-                          : nullptr;
+            // probabilities to [head][row] for the PV B operand
+            pw[(2 * tq) * S::PSTR + gq] = pr[0];
+            pw[(2 * tq + 1) * S::PSTR + gq] = pr[1];
+            pw[(2 * tq) * S::PSTR + gq + 8] = pr[2];
+            pw[(2 * tq + 1) * S::PSTR + gq + 8] = pr[3];
+            // ---------------- V scales of the rows this lane feeds (2t, 2t+1, 2t+8, 2t+9) -------
+            const int rr[4] = {2 * tq, 2 * tq + 1, 2 * tq + 8, 2 * tq + 9};
+            float dv[4][S::NBX];
+            int s_tile = 14; // f16: P' = p <= 1
+            if constexpr (S::Q8) {
+                const uint16_t *vsc = reinterpret_cast<const uint16_t *>(st + S::KBYTES + S::VBYTES + S::SCALE_BUF) +
+                                      tinfo[s].delta * S::NB;
+                float dmax = 0.f;
 #pragma unroll
-                for (int hr = 0; hr < 2; ++hr) {
-                    const int row = gq + 8 * hr; // row within the warp's 16
-                    const float pa = pr[2 * hr], pb = pr[2 * hr + 1];
-                    const bool live = row < rows_w;
+                for (int i = 0; i < 4; ++i) {
+                    const bool live = rr[i] < rows_w;
 #pragma unroll
-                    for (int b = 0; b < S::NBX; ++b) {
-                        float dv = 1.f;
-                        if constexpr (S::Q8) dv = live ? __half2float(__ushort_as_half(vsc[(rbase + row) * S::NB + b])) : 0.f;
-                        const float xa = live ? pa * dv : 0.f, xb = live ? pb * dv : 0.f;
-                        *reinterpret_cast<float4 *>(pbuf + row * S::PROW + b * S::RP + 4 * tq) =
-                            make_float4(xa, xa, xb, xb);
+                    for (int b = 0; b < S::NB; ++b) {
+                        const float d = __half2float(__ushort_as_half(vsc[(rbase + rr[i]) * S::NB + b]));
+                        dv[i][b] = live ? d : 0.f;
+                        dmax = fmaxf(dmax, dv[i][b]);
                     }
                 }
+                dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, 1));
+                dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, 2));
+                // 2^S * max(p * d) < 2^15: hi and lo of P' stay in fp16 range
+                s_tile = (dmax > 0.f) ? 14 - ilogbf(dmax) : (have_s ? sexp : 0);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) dv[i][0] = (rr[i] < rows_w) ? 1.f : 0.f;
             }
-            if (gq == 0) {
-                abuf[2 * tq] = al0;
-                abuf[2 * tq + 1] = al1;
+            const int s_new = have_s ? min(sexp, s_tile) : s_tile;
+            // rescale the accumulators: softmax max moved (alpha) and/or S decreased
+            const float sf = have_s ? ldexpf(1.f, s_new - sexp) : 1.f;
+            const float f0 = al0 * sf, f1 = al1 * sf;
+            if (__any_sync(0xffffffffu, f0 != 1.f || f1 != 1.f)) {
+#pragma unroll
+                for (int mt = 0; mt < NMT; ++mt) {
+                    acc[mt][0] *= f0;
+                    acc[mt][1] *= f1;
+                    acc[mt][2] *= f0;
+                    acc[mt][3] *= f1;
+                }
             }
+            sexp = s_new;
+            have_s = true;
             __syncwarp();
-            // ---------------- rescale and PV on the CUDA cores ----------------
-            float2 al[R];
-            bool any = false;
-#pragma unroll
-            for (int h = 0; h < R; ++h) {
-                const float a = abuf[h];
-                al[h] = make_float2(a, a);
-                any |= (a != 1.f);
+            // ---------------- PV on the tensor cores: O^T += V^T (P' hi + lo)^T --------------
+            const float ps = ldexpf(1.f, s_new);
+            float pv[4];
+            {
+                const float2 pa = *reinterpret_cast<const float2 *>(pw + gq * S::PSTR + 2 * tq);
+                const float2 pb = *reinterpret_cast<const float2 *>(pw + gq * S::PSTR + 2 * tq + 8);
+                pv[0] = pa.x * ps;
+                pv[1] = pa.y * ps;
+                pv[2] = pb.x * ps;
+                pv[3] = pb.y * ps;
             }
-            if (any) {
 #pragma unroll
-                for (int h = 0; h < R; ++h)
+            for (int b = 0; b < S::NBX; ++b) {
+                float x[4];
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) mul2(o[h][j], al[h]);
-            }
-            const uint8_t *vt = st + S::KBYTES;
-#pragma unroll 4
-            for (int r0 = 0; r0 < rows_w; r0 += S::RPS) {
-                const int row = r0 + pv_ro;
-                float2 vv[2];
+                for (int i = 0; i < 4; ++i) x[i] = pv[i] * dv[i][b];
+                uint32_t b0h, b1h, b0l, b1l;
+                split_pack(x[0], x[1], b0h, b0l);
+                split_pack(x[2], x[3], b1h, b1l);
                 if constexpr (S::Q8) {
-                    const uint32_t w = *reinterpret_cast<const uint32_t *>(vt + (rbase + row) * S::VROW + pv_d0);
-                    codes_to_f32x4(w, vv);
+                    uint32_t v0, v1, v2, v3;
+                    ldsm_x4_trans(vt + swz<S::VROW>(lm_row, 2 * b + lm_hi), v0, v1, v2, v3);
+                    // v0: rows 0-7 / bytes 0-15, v1: rows 8-15 / bytes 0-15,
+                    // v2: rows 0-7 / bytes 16-31, v3: rows 8-15 / bytes 16-31 of block b
+                    uint32_t e0, e1, e2, e3, o0, o1, o2, o3;
+                    vcodes_to_half2(v0, e0, o0);
+                    vcodes_to_half2(v2, e1, o1);
+                    vcodes_to_half2(v1, e2, o2);
+                    vcodes_to_half2(v3, e3, o3);
+                    mma16816(acc[2 * b], e0, e1, e2, e3, b0h, b1h);
+                    mma16816(acc[2 * b], e0, e1, e2, e3, b0l, b1l);
+                    mma16816(acc[2 * b + 1], o0, o1, o2, o3, b0h, b1h);
+                    mma16816(acc[2 * b + 1], o0, o1, o2, o3, b0l, b1l);
                 } else {
-                    const uint2 w2 = *reinterpret_cast<const uint2 *>(vt + (rbase + row) * S::VROW + 2 * pv_d0);
-                    vv[0] = __half22float2(*reinterpret_cast<const __half2 *>(&w2.x));
-                    vv[1] = __half22float2(*reinterpret_cast<const __half2 *>(&w2.y));
-                }
-                const float *pp = pbuf + row * S::PROW + pv_b * S::RP;
+                    // f16: the single "block" spans all D dims, NMT m-tiles of 16 dims
+                    const int lv_row = rbase + (lane & 7) + (lane >> 4) * 8;
+                    const int lv_c = (lane >> 3) & 1;
 #pragma unroll
-                for (int hp = 0; hp < (R + 1) / 2; ++hp) {
-                    const float4 q4 = *reinterpret_cast<const float4 *>(pp + 4 * hp);
-                    const float2 pa = make_float2(q4.x, q4.y), pb = make_float2(q4.z, q4.w);
-                    fma2(o[2 * hp][0], pa, vv[0]);
-                    fma2(o[2 * hp][1], pa, vv[1]);
-                    if (2 * hp + 1 < R) {
-                        fma2(o[2 * hp + 1][0], pb, vv[0]);
-                        fma2(o[2 * hp + 1][1], pb, vv[1]);
+                    for (int mt = 0; mt < NMT; ++mt) {
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4_trans(vt + (mt / 4) * T * 128 + swz<128>(lv_row, 2 * (mt % 4) + lv_c), a0, a1, a2,
+                                      a3);
+                        mma16816(acc[mt], a0, a1, a2, a3, b0h, b1h);
+                        mma16816(acc[mt], a0, a1, a2, a3, b0l, b1l);
                     }
                 }
             }
         }
-        // release the stage; thread 0 refills it once every warp is done
+        // release the stage; the last warp done with it loads tile k + STAGES into it
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        if (tid == 0 && prod_k < n_tiles) {
-            const int ps = prod_k % S::STAGES;
-            if (mbar_wait(&empty[ps], ((prod_k / S::STAGES) - 1) & 1, p.err)) issue(prod_k);
-            ++prod_k;
-        }
-    }
-    // drain: make sure no copy is still landing in shared memory before reuse
-    if (tid == 0) {
-        for (int k = max(0, prod_k - S::STAGES); k < prod_k; ++k) {
-            const int s = k % S::STAGES;
-            mbar_wait(&full[s], (k / S::STAGES) & 1, p.err);
+        if (lane == 0) {
+            mbar_arrive(&empty[s]); // release: this warp's reads of the stage are complete
+            if (atomicAdd(&s_cnt[s], 1) == W - 1) {
+                s_cnt[s] = 0;
+                const int kn = k + S::STAGES;
+                if (kn < n_tiles && mbar_wait(&empty[s], (k / S::STAGES) & 1, p.err)) issue(kn);
+            }
         }
     }
     __syncthreads();
 
-    // ---- reduce the row-parallel lanes of each warp ----------------------------
-#pragma unroll
-    for (int m = S::LPR; m < 32; m <<= 1)
-#pragma unroll
-        for (int h = 0; h < R; ++h)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                o[h][j].x += __shfl_xor_sync(0xffffffffu, o[h][j].x, m);
-                o[h][j].y += __shfl_xor_sync(0xffffffffu, o[h][j].y, m);
-            }
     // ---- CTA merge of the warps (stages are free now) -------------------------
-    float *wm = reinterpret_cast<float *>(stages); // [W][R]
-    float *wl = wm + W * R;                         // [W][R]
-    float *wo = wl + W * R;                         // [W][R][D]
-    if (gq == 0) {
-        if (2 * tq < R) {
-            wm[warp * R + 2 * tq] = m0;
-            wl[warp * R + 2 * tq] = l0;
-        }
-        if (2 * tq + 1 < R) {
-            wm[warp * R + 2 * tq + 1] = m1;
-            wl[warp * R + 2 * tq + 1] = l1;
-        }
-    }
-    if (lane < S::LPR) {
+    // Each warp stores its fragments as they sit in registers (lane-major,
+    // conflict free), its softmax state and its P' range exponent.
+    constexpr int FRAG = S::NMT * 32;                           // float4 fragments per warp
+    float4 *wf = reinterpret_cast<float4 *>(stages);           // [W][NMT][32]
+    float *wm = reinterpret_cast<float *>(wf + W * FRAG);      // [W][8]
+    float *wl = wm + W * 8;                                     // [W][8]
+    float *wus = wl + W * 8;                                    // [W]
 #pragma unroll
-        for (int h = 0; h < R; ++h) {
-            float4 v4 = make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
-            *reinterpret_cast<float4 *>(wo + (warp * R + h) * D + pv_d0) = v4;
-        }
+    for (int mt = 0; mt < S::NMT; ++mt)
+        wf[(warp * S::NMT + mt) * 32 + lane] = make_float4(acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3]);
+    if (gq == 0) {
+        wm[warp * 8 + 2 * tq] = m0;
+        wm[warp * 8 + 2 * tq + 1] = m1;
+        wl[warp * 8 + 2 * tq] = l0;
+        wl[warp * 8 + 2 * tq + 1] = l1;
     }
+    if (lane == 0) wus[warp] = have_s ? ldexpf(1.f, -sexp) : 0.f;
     __syncthreads();
 
     const int n_chunks = sq.n_chunks;
     float *part = p.part + ((int64_t)chunk * p.Hk + g) * S::PF;
     float *outp = p.out + ((int64_t)sq.out_row * p.H + (int64_t)g * r_act) * D;
-    for (int idx = tid; idx < r_act * D; idx += NT) {
-        const int h = idx / D, i = idx % D;
-        float M = -INFINITY;
+    // per-head weights of the warps (softmax rescale; the P' scale only weighs O):
+    // one warp per head, one lane per warp of the CTA
+    for (int h = warp; h < r_act; h += W) {
+        const float mw = (lane < W) ? wm[lane * 8 + h] : -INFINITY;
+        float M = mw;
 #pragma unroll
-        for (int w = 0; w < W; ++w) M = fmaxf(M, wm[w * R + h]);
-        float L = 0.f, O = 0.f;
+        for (int m = 16; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
+        const float f = (lane < W && M != -INFINITY) ? ex2(mw - M) : 0.f;
+        if (lane < W) s_ww[lane * 8 + h] = f * wus[lane];
+        float L = (lane < W) ? wl[lane * 8 + h] * f : 0.f;
 #pragma unroll
-        for (int w = 0; w < W; ++w) {
-            const float f = (M == -INFINITY) ? 0.f : exp2f(wm[w * R + h] - M);
-            L += wl[w * R + h] * f;
-            O += wo[(w * R + h) * D + i] * f;
-        }
-        if (n_chunks == 1) {
-            outp[h * D + i] = (L > 0.f) ? O / L : 0.f;
-        } else {
-            if (i == 0) {
+        for (int m = 16; m > 0; m >>= 1) L += __shfl_xor_sync(0xffffffffu, L, m);
+        if (lane == 0) {
+            s_M[h] = M;
+            s_L[h] = L;
+            if (n_chunks > 1) {
                 part[h] = M;
                 part[R + h] = L;
             }
-            part[S::OOFF + h * D + i] = O;
+        }
+    }
+    __syncthreads();
+    // fragment (mt, ln): heads 2t, 2t+1 of lane ln, dims of rows g and g+8
+    for (int it = tid; it < FRAG; it += NT) {
+        const int mt = it / 32, ln = it % 32, fg = ln >> 2, ft = ln & 3;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            const float4 v = wf[(w * S::NMT + mt) * 32 + ln];
+            const float f0 = s_ww[w * 8 + 2 * ft], f1 = s_ww[w * 8 + 2 * ft + 1];
+            O.x += f0 * v.x;
+            O.y += f1 * v.y;
+            O.z += f0 * v.z;
+            O.w += f1 * v.w;
+        }
+        int dA, dB;
+        if constexpr (S::Q8) {
+            dA = 32 * (mt / 2) + 2 * fg + (mt % 2);
+            dB = dA + 16;
+        } else {
+            dA = 16 * mt + fg;
+            dB = dA + 8;
+        }
+        const int h0 = 2 * ft, h1 = 2 * ft + 1;
+        if (n_chunks == 1) {
+            if (h0 < r_act) {
+                const float L = s_L[h0];
+                outp[h0 * D + dA] = (L > 0.f) ? O.x / L : 0.f;
+                outp[h0 * D + dB] = (L > 0.f) ? O.z / L : 0.f;
+            }
+            if (h1 < r_act) {
+                const float L = s_L[h1];
+                outp[h1 * D + dA] = (L > 0.f) ? O.y / L : 0.f;
+                outp[h1 * D + dB] = (L > 0.f) ? O.w / L : 0.f;
+            }
+        } else {
+            if (h0 < R) {
+                part[S::OOFF + h0 * D + dA] = O.x;
+                part[S::OOFF + h0 * D + dB] = O.z;
+            }
+            if (h1 < R) {
+                part[S::OOFF + h1 * D + dA] = O.y;
+                part[S::OOFF + h1 * D + dB] = O.w;
+            }
         }
     }
     if (n_chunks == 1) return;
 
     // ---- split-K merge by the last CTA of this (sequence, kv head) ------------
-    __threadfence();
     __syncthreads();
     if (tid == 0) {
+        // release: this CTA's partial (cumulative over the barrier above) is
+        // visible before the ticket; the last arrival acquires all of them
         int *ticket = p.tickets + sq.ticket * p.Hk + g;
-        const int prev = atomicAdd(ticket, 1);
+        int prev;
+        asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(prev) : "l"(ticket) : "memory");
         s_flag = (prev == n_chunks - 1);
         if (s_flag) *ticket = 0; // ready for the next launch
     }
     __syncthreads();
     if (!s_flag) return;
-    __threadfence();
     const float *part0 = p.part + ((int64_t)sq.chunk0 * p.Hk + g) * S::PF;
     const int64_t cstride = (int64_t)p.Hk * S::PF;
-    float *cm = wm;                         // [n_chunks][R] maxima, then weights
-    float *cl = wm + n_chunks * R;          // [n_chunks][R] sums
+    // one round of independent loads stages every partial in shared memory
     // (the host keeps n_chunks <= MERGE_CAP)
-    for (int idx = tid; idx < n_chunks * R; idx += NT) {
-        const int c = idx / R, h = idx % R;
-        cm[idx] = __ldcg(part0 + c * cstride + h);
-        cl[idx] = __ldcg(part0 + c * cstride + R + h);
+    constexpr int Q4 = S::PF / 4; // float4 per partial
+    float4 *stg = reinterpret_cast<float4 *>(stages);
+    const int items = n_chunks * Q4;
+    for (int base = 0; base < items; base += 8 * NT) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int it = base + u * NT + tid;
+            v[u] = (it < items) ? __ldcg(reinterpret_cast<const float4 *>(part0 + (it / Q4) * cstride) + it % Q4)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int it = base + u * NT + tid;
+            if (it < items) stg[it] = v[u];
+        }
     }
     __syncthreads();
-    if (tid < r_act) {
+    const float *sp = reinterpret_cast<const float *>(stg);
+    float *cw = reinterpret_cast<float *>(stg + items); // [n_chunks][R] weights
+    for (int h = warp; h < r_act; h += W) {
         float M = -INFINITY;
-        for (int c = 0; c < n_chunks; ++c) M = fmaxf(M, cm[c * R + tid]);
+        for (int c = lane; c < n_chunks; c += 32) M = fmaxf(M, sp[c * S::PF + h]);
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
         float L = 0.f;
-        for (int c = 0; c < n_chunks; ++c) L += (M == -INFINITY) ? 0.f : cl[c * R + tid] * exp2f(cm[c * R + tid] - M);
-        s_M[tid] = M;
-        s_L[tid] = L;
+        for (int c = lane; c < n_chunks; c += 32) {
+            const float f = (M == -INFINITY) ? 0.f : ex2(sp[c * S::PF + h] - M);
+            cw[c * R + h] = f;
+            L += f * sp[c * S::PF + R + h];
+        }
+        // fixed-order tree: the same bits on every call
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) L += __shfl_xor_sync(0xffffffffu, L, m);
+        if (lane == 0) s_L[h] = L;
     }
     __syncthreads();
-    for (int idx = tid; idx < n_chunks * R; idx += NT) {
-        const int h = idx % R;
-        cm[idx] = (h < r_act && s_M[h] != -INFINITY) ? exp2f(cm[idx] - s_M[h]) : 0.f;
-    }
-    __syncthreads();
-    // every thread owns 4 consecutive outputs; chunks are read 16 at a time
-    // with independent loads so the L2 round trips overlap
-    const int ncol = r_act * (D / 4);
-    for (int col = tid; col < ncol; col += NT) {
+    for (int col = tid; col < r_act * (D / 4); col += NT) {
         const int h = col / (D / 4), i4 = col % (D / 4);
-        const float *src = part0 + S::OOFF + h * D + 4 * i4;
         float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c0 = 0; c0 < n_chunks; c0 += 16) {
-            float4 v[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u)
-                v[u] = (c0 + u < n_chunks) ? __ldcg(reinterpret_cast<const float4 *>(src + (c0 + u) * cstride))
-                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const float w = (c0 + u < n_chunks) ? cm[(c0 + u) * R + h] : 0.f;
-                O.x += w * v[u].x;
-                O.y += w * v[u].y;
-                O.z += w * v[u].z;
-                O.w += w * v[u].w;
-            }
+        for (int c = 0; c < n_chunks; ++c) {
+            const float w = cw[c * R + h];
+            const float4 v = *reinterpret_cast<const float4 *>(sp + c * S::PF + S::OOFF + h * D + 4 * i4);
+            O.x += w * v.x;
+            O.y += w * v.y;
+            O.z += w * v.z;
+            O.w += w * v.w;
         }
         const float L = s_L[h];
         float *dst = outp + h * D + 4 * i4;
@@ -683,6 +735,7 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
 
 template <int TYPE, int D, int R>
 cudaError_t launch_t(const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv, cudaStream_t st) {
+    // tmk / tmv point at {16-row map, 128-row map} pairs
     using S = Shape<TYPE, D, R>;
     static bool configured = false;
     if (!configured) {
@@ -701,7 +754,7 @@ cudaError_t launch_t(const AttnParams &p, const CUtensorMap *tmk, const CUtensor
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_kernel<TYPE, D, R>, p, *tmk, *tmv);
+    return cudaLaunchKernelEx(&cfg, attn_kernel<TYPE, D, R>, p, tmk[0], tmv[0], tmk[1], tmv[1]);
 }
 
 template <int TYPE, int D>
@@ -769,7 +822,7 @@ cudaError_t launch_attn(int type, const AttnParams &p, const CUtensorMap *tmk, c
 }
 
 bool encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int row_bytes, int type, bool swizzle,
-                     std::string *why) {
+                     std::string *why, int box_rows) {
     using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -792,7 +845,7 @@ bool encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int row_byt
     cuuint64_t gstride[1] = {(cuuint64_t)row_bytes};
     // swizzled K: inner box of 128 bytes (or the whole 64-byte row); plain V: the whole row
     cuuint32_t inner = swizzle ? (cuuint32_t)((row_bytes >= 128 ? 128 : row_bytes) / esize) : (cuuint32_t)elems;
-    cuuint32_t box[2] = {inner, (cuuint32_t)TMA_BOX_ROWS};
+    cuuint32_t box[2] = {inner, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE;
     if (swizzle) sw = (inner * esize == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;

@@ -80,19 +80,23 @@ extern "C" int kvc_attn_decode_static(int type, int n_head, int n_head_kv, int h
     C = std::min<int64_t>(2048, std::max<int64_t>(64, (C + 15) / 16 * 16));
     const int cap = attn_merge_cap(type, head_dim, r);
     if ((n_kv + cap - 1) / cap > C) C = ((n_kv + cap - 1) / cap + 15) / 16 * 16;
+    C = std::min<int64_t>(C, 8000); // a chunk spans at most 512 tiles
     const int n_chunks = std::max<int>(1, (int)((n_kv + C - 1) / C));
     const size_t part_bytes = (size_t)n_chunks * n_head_kv * attn_partial_floats(r, head_dim) * sizeof(float);
     if (part_bytes > STATIC_SCRATCH_BYTES - HEADER_BYTES) return KVC_ERANGE; // beyond the fixed work space
 
     const int row_bytes = type == KVC_Q8_0 ? head_dim : 2 * head_dim;
     const int64_t rows = (int64_t)n_head_kv * std::max(n_kv, 1);
-    CUtensorMap tmk, tmv;
+    CUtensorMap tmk[2], tmv[2]; // 16-row and 128-row boxes
     // an empty sequence still needs valid maps; they are never used
     const void *kb = n_kv > 0 ? k : (const void *)(base + HEADER_BYTES);
     const void *vb = n_kv > 0 ? v : (const void *)(base + HEADER_BYTES);
-    if (!encode_rows_map(&tmk, kb, rows, row_bytes, type, true, nullptr) ||
-        !encode_rows_map(&tmv, vb, rows, row_bytes, type, false, nullptr))
-        return KVC_ECUDA;
+    for (int b = 0; b < 2; ++b) {
+        const int box = b ? (int)std::min<int64_t>(TMA_BIG_ROWS, rows) : TMA_BOX_ROWS;
+        if (!encode_rows_map(&tmk[b], kb, rows, row_bytes, type, true, nullptr, box) ||
+            !encode_rows_map(&tmv[b], vb, rows, row_bytes, type, true, nullptr, box))
+            return KVC_ECUDA;
+    }
 
     // tickets, the error word and the one-entry page table (page 0) must start
     // at zero; the array keeps the previous call's contents, so clear them in
@@ -130,5 +134,5 @@ extern "C" int kvc_attn_decode_static(int type, int n_head, int n_head_kv, int h
     a.out_row = 0;
     a.ticket = 0;
     a.stable_rows = 0; // caller buffers: nothing is read before the dependency wait
-    return launch_attn(type, p, &tmk, &tmv, st) == cudaSuccess ? KVC_OK : KVC_ECUDA;
+    return launch_attn(type, p, tmk, tmv, st) == cudaSuccess ? KVC_OK : KVC_ECUDA;
 }

@@ -8,14 +8,15 @@
 #include <string>
 #include <vector>
 
-#include "../../include/kvc.h"
+#include "kvc.h" // include/ is on the include path
 
 namespace kvc {
 
 constexpr int QK = 32;                 // elements per q8_0 block
 constexpr int MAX_SEQ_PER_LAUNCH = 64; // sequences carried in one attention launch
 constexpr int MAX_GROUP = 8;           // query heads per KV head supported by the attention kernel
-constexpr int TMA_BOX_ROWS = 16;       // rows per TMA box
+constexpr int TMA_BOX_ROWS = 16;       // rows per small TMA box
+constexpr int TMA_BIG_ROWS = 128;      // rows per large TMA box
 
 // Device error word bits (kernels set them instead of trapping).
 constexpr uint32_t ERR_WAIT_TIMEOUT = 1u << 0;
@@ -64,7 +65,9 @@ struct AttnParams {
     AttnSeq seq[MAX_SEQ_PER_LAUNCH];
 };
 
-// Launch the decode attention kernel for one layer.
+// Launch the decode attention kernel for one layer.  tmk / tmv each point at
+// a pair of maps over the same rows: boxes of TMA_BOX_ROWS rows, then of
+// TMA_BIG_ROWS rows.
 cudaError_t launch_attn(int type, const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv,
                         cudaStream_t st);
 int attn_ctas_per_sm(int type, int D, int r);
@@ -105,6 +108,6 @@ cudaError_t launch_rope_shift(int type_k, int D, int mode, void *kdata, uint16_t
 
 // Encode a 2D tiled tensor map (rows x row_bytes) for the attention kernel.
 bool encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int row_bytes, int type, bool swizzle,
-                     std::string *why);
+                     std::string *why, int box_rows = TMA_BOX_ROWS);
 
 } // namespace kvc

@@ -68,6 +68,8 @@ int launch_attention(Ctx *c, const LayerView &lv, const CUtensorMap *tmk, const 
         const int need = (seqs_in[i].n_rows + cap - 1) / cap;
         if (need > C) C = (need + 15) / 16 * 16;
     }
+    // a chunk spans at most 512 tiles of at least 16 rows
+    C = std::min(C, 8000);
     const int64_t pf = (int64_t)attn_partial_floats(c->r, c->D);
     for (int base = 0; base < n_seq; base += MAX_SEQ_PER_LAUNCH) {
         const int cnt = std::min(MAX_SEQ_PER_LAUNCH, n_seq - base);
@@ -159,9 +161,12 @@ static int alloc_slot(Ctx *c, Slot &s, int32_t cap) {
     if (s.kscales) KVC_CU(c, cudaMemset(s.kscales, 0, (size_t)(rows * c->ksb + 64)));
     if (s.vscales) KVC_CU(c, cudaMemset(s.vscales, 0, (size_t)(rows * c->vsb + 64)));
     std::string why;
-    if (!encode_rows_map(&s.tmk, s.kdata, rows, c->krow, c->tk, true, &why) ||
-        !encode_rows_map(&s.tmv, s.vdata, rows, c->vrow, c->tv, false, &why))
-        return c->fail(KVC_ECUDA, why);
+    for (int b = 0; b < 2; ++b) {
+        const int box = b ? (int)std::min<int64_t>(TMA_BIG_ROWS, rows) : TMA_BOX_ROWS;
+        if (!encode_rows_map(&s.tmk[b], s.kdata, rows, c->krow, c->tk, true, &why, box) ||
+            !encode_rows_map(&s.tmv[b], s.vdata, rows, c->vrow, c->tv, true, &why, box))
+            return c->fail(KVC_ECUDA, why);
+    }
     KVC_CU(c, cudaEventCreateWithFlags(&s.ready, cudaEventDisableTiming));
     KVC_CU(c, cudaEventCreateWithFlags(&s.release, cudaEventDisableTiming));
     return KVC_OK;
@@ -348,7 +353,7 @@ int transport_attn(Ctx *c, int layer, const float *q, float *out, float kq_scale
     a.n_rows = rows;
     a.out_row = 0;
     a.stable_rows = std::max(0, rows - c->recent[0][(size_t)layer]);
-    rc = launch_attention(c, lv, &s->tmk, &s->tmv, s->cap, s->scale_bytes, 1, &a, q, out, kq_scale, st);
+    rc = launch_attention(c, lv, s->tmk, s->tmv, s->cap, s->scale_bytes, 1, &a, q, out, kq_scale, st);
     if (rc) return rc;
     c->clear_recent();
     if (engaged) {
