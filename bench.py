@@ -54,7 +54,13 @@ def parse():
     ap.add_argument("--host-n", type=int, default=32768, help="host-resident context (0 = skip)")
     ap.add_argument("--host-steps", type=int, default=4)
     ap.add_argument("--cpu-sample-layers", type=int, default=4)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="repeat the oracle sample for at least this long")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the variant, ragged and churn measurements")
+    ap.add_argument("--churn-cycles", type=int, default=64)
+    ap.add_argument("--host-matrix", action="store_true",
+                    help="host-resident decline matrix: n_kv 32k/64k/128k x depth 0/1/4 x budget 128/512 MiB")
+    ap.add_argument("--churn-n", type=int, default=131072)
     return ap.parse_args()
 
 
@@ -124,6 +130,27 @@ class Clocks:
         os.unlink(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def attn_traffic(type_: str, n_kv: int):
+    """DRAM read + write bytes of one attention launch, from the committed ncu
+    summary of the q8_0 n_kv 16384 launch; None for other workloads or once
+    the kernel source no longer matches the hash the summary was taken on."""
+    import hashlib
+    import re
+
+    if type_ != "q8_0" or n_kv != 16384:
+        return None
+    try:
+        text = open(os.path.join(ROOT, "profiles", "attn_kernel_q8_0_16k.md")).read()
+        src = open(os.path.join(ROOT, "kv_cache_decode_flash_gb300", "csrc", "k_attn.cu"), "rb").read()
+    except OSError:
+        return None
+    h = re.search(r"kernel_sha256: ([0-9a-f]+)", text)
+    t = re.search(r"`traffic_bytes_per_launch`[^|]*\|\s*(\d+)", text)
+    if not h or not t or not hashlib.sha256(src).hexdigest().startswith(h.group(1)):
+        return None
+    return int(t.group(1))
 
 
 # ------------------------------------------------------------- CPU oracle --
@@ -236,15 +263,24 @@ def measure_link(torch, dev) -> float:
     return 5 * n / (e0.elapsed_time(e1) * 1e-3) / GB
 
 
-def host_pipeline(args, dev, torch, kvc):
-    """Host-resident KV at args.host_n: steps/s ordered vs pipelined."""
+HOST_CELLS = (("ordered", 0, 128 << 20), ("pipelined", 1, 512 << 20), ("pipelined_depth4", 4, 1 << 30),
+              ("declined", 1, 128 << 20))
+MATRIX_CELLS = (("N0", 0, 128 << 20), ("N1_128MiB", 1, 128 << 20), ("N1_512MiB", 1, 512 << 20),
+                ("N4_128MiB", 4, 128 << 20), ("N4_512MiB", 4, 512 << 20))
+
+
+def host_pipeline(args, dev, torch, kvc, n=None, cells=HOST_CELLS, link=None):
+    """Host-resident KV at n (default args.host_n): steps/s and H2D GB/s for
+    each (name, depth, budget) cell, run one after another on one cache (the
+    context grows by host_steps + 1 rows per cell).  Ordered/pipelined byte
+    identity is a parity test, not measured here."""
     from kv_cache_decode_flash_gb300 import synth
 
-    n = args.host_n
+    n = n or args.host_n
     L = args.layers
     t = kvc.KVC_Q8_0 if args.type == "q8_0" else kvc.KVC_F16
     res = {}
-    link = measure_link(torch, dev)
+    link = link or measure_link(torch, dev)
     scale = float(1.0 / np.sqrt(D))
     cache = kvc.KVCache(L, H, HK, D, n + 64, 1, t, t, 1e6, 0, kvc.KVC_HOST_PINNED)
     try:
@@ -258,10 +294,8 @@ def host_pipeline(args, dev, torch, kvc):
         kn = torch.randn(L, 1, HK, D, device=dev) * 0.5
         vn = torch.randn(L, 1, HK, D, device=dev) * 0.5
         out = torch.empty_like(q)
-        outs = {}
         pos = n - 1
-        for name, depth, budget in (("ordered", 0, 128 << 20), ("pipelined", 1, 512 << 20),
-                                    ("declined", 1, 128 << 20)):
+        for name, depth, budget in cells:
             kvc.kvc_pipeline_depth(cache.ctx, depth)
             kvc.kvc_pipeline_budget(cache.ctx, budget)
             times = []
@@ -276,7 +310,6 @@ def host_pipeline(args, dev, torch, kvc):
             torch.cuda.synchronize()
             dt = (time.perf_counter() - t0) / args.host_steps
             st = cache.stats()
-            outs[name] = out.clone()
             # bytes moved host->device per step: every layer's rows (stable prefix) once
             h2d = L * (pos - 1) * kv_bytes_per_row(args.type)
             res[name] = {"steps_per_s": round(1.0 / dt, 3), "ms_per_step": round(1000 * dt, 3),
@@ -290,6 +323,149 @@ def host_pipeline(args, dev, torch, kvc):
     finally:
         cache.close()
     return res
+
+
+# ------------------------------------------------------- further rows --
+def attn_only_gbs(kvc, torch, dev, type_: str, n: int, reps: int = 50):
+    """KV GB/s of back-to-back attention launches, one per layer, over enough
+    distinct layers that one pass reads at least 512 MB (no L2 reuse)."""
+    from kv_cache_decode_flash_gb300 import synth
+
+    layers = max(8, -(-(512 << 20) // (n * kv_bytes_per_row(type_))))
+
+    t = kvc.KVC_Q8_0 if type_ == "q8_0" else kvc.KVC_F16
+    cache = kvc.KVCache(layers, H, HK, D, n + 64, 1, t, t, 1e6)
+    try:
+        for l in range(layers):
+            for p0 in range(0, n, 8192):
+                m = min(8192, n - p0)
+                k = synth.normal_torch(0, synth.stream_id("k", l, p0), m * HK * D, 0.5, dev).view(m, HK, D)
+                cache.append(l, 0, p0, k, k)
+        q = torch.randn(layers, 1, H, D, device=dev)
+        o = torch.empty_like(q)
+        s = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(s):
+            for l in range(layers):
+                cache.attn_decode(l, [0], q[l], o[l], 0.088, stream=s)
+        s.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=s):
+            for l in range(layers):
+                cache.attn_decode(l, [0], q[l], o[l], 0.088, stream=torch.cuda.current_stream())
+        for _ in range(3):
+            gr.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            gr.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        dt = e0.elapsed_time(e1) * 1e-3 / (reps * layers)
+        return {"n_kv": n, "kv_type": type_, "layers": layers, "launch_us": round(dt * 1e6, 3),
+                "gbs": round(n * kv_bytes_per_row(type_) / dt / GB, 1)}
+    finally:
+        cache.close()
+
+
+def ragged(kvc, torch, dev, type_: str, reps: int = 20):
+    """32 sequences, lengths uniform in [1024, 32768] (seed 0), 32/8 heads,
+    D 128, one layer; one attention call over the whole batch."""
+    from kv_cache_decode_flash_gb300 import synth
+
+    Hq = 32
+    lens = synth.randint(0, synth.stream_id("len"), 32, 1024, 32768).tolist()
+    t = kvc.KVC_Q8_0 if type_ == "q8_0" else kvc.KVC_F16
+    cache = kvc.KVCache(1, Hq, HK, D, sum(lens) + 32 * 256, 32, t, t, 1e6)
+    try:
+        for sidx, n in enumerate(lens):
+            for p0 in range(0, n, 8192):
+                m = min(8192, n - p0)
+                k = synth.normal_torch(0, synth.stream_id("k", 0, sidx * 4096 + p0 // 8192), m * HK * D, 1.0, dev).view(m, HK, D)
+                v = synth.normal_torch(0, synth.stream_id("v", 0, sidx * 4096 + p0 // 8192), m * HK * D, 1.0, dev).view(m, HK, D)
+                cache.append(0, sidx, p0, k, v)
+        q = torch.randn(32, Hq, D, device=dev)
+        o = torch.empty_like(q)
+        ids = list(range(32))
+        for _ in range(3):
+            cache.attn_decode(0, ids, q, o, 0.088)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            cache.attn_decode(0, ids, q, o, 0.088)
+        e1.record()
+        torch.cuda.synchronize()
+        dt = e0.elapsed_time(e1) * 1e-3 / reps
+        rows = sum(lens)
+        return {"kv_type": type_, "sequences": 32, "rows": rows, "ms_per_call": round(dt * 1e3, 4),
+                "gbs": round(rows * kv_bytes_per_row(type_) / dt / GB, 1)}
+    finally:
+        cache.close()
+
+
+def churn(kvc, torch, dev, n: int, cycles: int, layers: int):
+    """Cold-store churn on a q8_0 cache of n tokens: evict the oldest 8192
+    rows (copy to a scratch sequence, export, drop, remove, slide) and
+    re-admit them at the tail (import, shift, copy in), then one decode step
+    over the layer stack.  Per-op GB/s; every op is synchronous."""
+    from kv_cache_decode_flash_gb300 import synth
+
+    blk = 8192
+    row_all = layers * kv_bytes_per_row("q8_0")          # one row, all layers, K+V
+    krow_all = layers * HK * (D + (D // 32) * 2)         # K only (what a shift rewrites)
+    cache = kvc.KVCache(layers, H, HK, D, n + 2 * blk + 512, 2, kvc.KVC_Q8_0, kvc.KVC_Q8_0, 1e6)
+    try:
+        for l in range(layers):
+            for p0 in range(0, n, 8192):
+                m = min(8192, n - p0)
+                k = synth.normal_torch(0, synth.stream_id("k", l, p0), m * HK * D, 0.5, dev).view(m, HK, D)
+                v = synth.normal_torch(0, synth.stream_id("v", l, p0), m * HK * D, 0.5, dev).view(m, HK, D)
+                cache.append(l, 0, p0, k, v)
+        torch.cuda.synchronize()
+        size = kvc.kvc_state_size(cache.ctx, 0, 0, blk)
+        host = torch.empty(size, dtype=torch.uint8, pin_memory=True)
+        again = torch.empty(size, dtype=torch.uint8, pin_memory=True)
+        q = torch.randn(layers, 1, H, D, device=dev)
+        o = torch.empty_like(q)
+        acc = {k: 0.0 for k in ("seq_cp", "state_get", "seq_rm", "slide", "state_set", "shift", "copy_in", "decode")}
+
+        def timed(name, fn):
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            acc[name] += time.perf_counter() - t0
+
+        ok = exact = True
+        for c in range(cycles):
+            timed("seq_cp", lambda: cache.seq_cp(0, 1, 0, blk))
+            timed("state_get", lambda: cache.state_get(1, -1, -1, host))
+            cache.seq_rm(1, -1, -1)
+            timed("seq_rm", lambda: cache.seq_rm(0, 0, blk))
+            timed("slide", lambda: cache.seq_add(0, blk, n, -blk))
+            timed("state_set", lambda: cache.state_set(1, host))
+            if c in (0, cycles - 1):  # export -> import -> export is byte-exact
+                cache.state_get(1, -1, -1, again)
+                exact = exact and bool(torch.equal(host, again))
+            timed("shift", lambda: cache.seq_add(1, -1, -1, n - blk))
+            timed("copy_in", lambda: cache.seq_cp(1, 0, -1, -1))
+            cache.seq_rm(1, -1, -1)
+            timed("decode", lambda: [cache.attn_decode(l, [0], q[l], o[l], 0.088) for l in range(layers)])
+            pos = cache.positions(0)
+            ok = ok and bool((np.sort(pos) == np.arange(n)).all())
+        byts = {"seq_cp": 2 * blk * row_all, "state_get": size, "seq_rm": 0, "slide": 2 * (n - blk) * krow_all,
+                "state_set": size, "shift": 2 * blk * krow_all, "copy_in": 2 * blk * row_all,
+                "decode": n * row_all}
+        ops = {}
+        for k2, v2 in acc.items():
+            per = v2 / cycles
+            ops[k2] = {"ms": round(per * 1e3, 3), "gbs": round(byts[k2] / per / GB, 1) if byts[k2] else None}
+        return {"n_kv": n, "block": blk, "cycles": cycles, "layers": layers, "positions_ok": ok,
+                "state_round_trip_exact": exact,
+                "bytes": "seq_cp/copy_in/slide/shift: read+write; state_get/set: bytes exported; decode: KV read",
+                "ops": ops}
+    finally:
+        cache.close()
 
 
 def run_ours(args, rank: int, world: int):
@@ -407,10 +583,12 @@ def run_ours(args, rank: int, world: int):
         "steps_per_s": round(args.steps / t_step, 2),
         "hbm_frac": round(value / world / peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4), "traffic": attn_traffic(args.type, n),
                      "kernel": "attn_kernel (decode attention), %d bytes per launch" % (n * row_bytes),
                      "peak_kind": "%s (MEASURED_PEAKS.json hbm_gbs, burst copy)" % peak_kind,
-                     "launch_us": round(attn_launch_s * 1e6, 3)},
+                     "launch_us": round(attn_launch_s * 1e6, 3),
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, "
+                                       "profiles/attn_kernel_q8_0_16k.md (null when the kernel changed)"},
         "e2e": {"value": round(world * step_bytes * args.steps / t_e2e / GB, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(hq.numel() * 4 + hk.numel() * 4 + hv.numel() * 4),
                 "d2h_bytes_per_step": int(ho.numel() * 4)},
@@ -425,12 +603,41 @@ def run_ours(args, rank: int, world: int):
             out["host"] = host_pipeline(args, dev, torch, kvc)
         except Exception as e:  # reported, not fatal
             out["host"] = {"error": str(e)[:300]}
+    if rank == 0 and args.host_matrix:
+        link = measure_link(torch, dev)
+        mat = {}
+        for hn in (32768, 65536, 131072):
+            try:
+                mat[str(hn)] = host_pipeline(args, dev, torch, kvc, hn, MATRIX_CELLS, link)
+            except Exception as e:  # reported, not fatal
+                mat[str(hn)] = {"error": str(e)[:300]}
+            torch.cuda.empty_cache()
+        out["host_matrix"] = mat
+    if rank == 0 and not args.no_extra:
+        ex = {}
+        for name, fn in (("q8_0_4k", lambda: attn_only_gbs(kvc, torch, dev, "q8_0", 4096)),
+                         ("f16_16k", lambda: attn_only_gbs(kvc, torch, dev, "f16", 16384)),
+                         ("f16_4k", lambda: attn_only_gbs(kvc, torch, dev, "f16", 4096)),
+                         ("ragged_q8_0", lambda: ragged(kvc, torch, dev, "q8_0")),
+                         ("ragged_f16", lambda: ragged(kvc, torch, dev, "f16")),
+                         ("churn", lambda: churn(kvc, torch, dev, args.churn_n, args.churn_cycles, args.layers))):
+            try:
+                ex[name] = fn()
+            except Exception as e:  # reported, not fatal
+                ex[name] = {"error": str(e)[:300]}
+            torch.cuda.empty_cache()
+        out["rows"] = ex
     if rank == 0 and not args.no_cpu_baseline:
         layers = oracle_sample(n, args.cpu_sample_layers, args.type)
-        gbs, dt, threads = time_oracle(layers, n, args.type)
+        passes, dt, threads = 0, 0.0, 1
+        while passes == 0 or dt < args.cpu_seconds:
+            _, d1, threads = time_oracle(layers, n, args.type)
+            dt += d1
+            passes += 1
+        gbs = passes * len(layers) * n * kv_bytes_per_row(args.type) / dt / GB
         out["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-                               "sample": "%d of %d layers, all %d query heads, n_kv=%d (%.1f s)"
-                                         % (args.cpu_sample_layers, L, H, n, dt)}
+                               "sample": "%d of %d layers x %d passes, all %d query heads, n_kv=%d (%.1f s)"
+                                         % (args.cpu_sample_layers, L, passes, H, n, dt)}
     return out
 
 
