@@ -93,20 +93,26 @@ static int ensure_staging(Ctx *c, int64_t bytes) {
     return KVC_OK;
 }
 
-static int upload_segments(Ctx *c, const std::vector<Segment> &segs) {
-    if (segs.empty()) return KVC_OK;
-    if ((int64_t)segs.size() > c->segs_cap) {
-        dev_free(c, c->segs_dev, c->segs_cap * (int64_t)sizeof(Segment));
-        c->segs_dev = nullptr;
-        c->segs_cap = 0;
-        int64_t cap = std::max<int64_t>((int64_t)segs.size(), 4096);
-        int rc = dev_alloc(c, (void **)&c->segs_dev, cap * (int64_t)sizeof(Segment), "segment list");
+// Upload a run list to the device.
+static int upload_runs(Ctx *c, const std::vector<RowRun> &runs) {
+    if (runs.empty()) return KVC_OK;
+    if ((int64_t)runs.size() > c->runs_cap) {
+        dev_free(c, c->runs_dev, c->runs_cap * (int64_t)sizeof(RowRun));
+        c->runs_dev = nullptr;
+        c->runs_cap = 0;
+        int64_t cap = std::max<int64_t>((int64_t)runs.size(), 1024);
+        int rc = dev_alloc(c, (void **)&c->runs_dev, cap * (int64_t)sizeof(RowRun), "run list");
         if (rc) return rc;
-        c->segs_cap = cap;
+        c->runs_cap = cap;
     }
-    KVC_CU(c, cudaMemcpyAsync(c->segs_dev, segs.data(), segs.size() * sizeof(Segment), cudaMemcpyHostToDevice,
-                              c->st));
-    KVC_CU(c, launch_copy_segments(c->segs_dev, (int)segs.size(), c->st));
+    KVC_CU(c, cudaMemcpyAsync(c->runs_dev, runs.data(), runs.size() * sizeof(RowRun), cudaMemcpyHostToDevice, c->st));
+    return KVC_OK;
+}
+
+static int ensure_copy_stream(Ctx *c) {
+    if (c->st_copy) return KVC_OK;
+    KVC_CU(c, cudaStreamCreateWithFlags(&c->st_copy, cudaStreamNonBlocking));
+    for (auto &ev : c->st_ev) KVC_CU(c, cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
     return KVC_OK;
 }
 
@@ -161,26 +167,33 @@ static void release_tail_pages(Ctx *c, Seq &q) {
     q.dev_pages = std::min<int32_t>(q.dev_pages, (int32_t)q.pages.size());
 }
 
-// Byte segments copying logical rows [a, a+len) of sequence qa to logical rows
-// [b, b+len) of qb (same layer pools), all layers, K and V.
+// Pool copy arguments of this context (no payload).
+static RunCopyArgs pool_args(const Ctx *c) {
+    RunCopyArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.base[0] = c->kdata;
+    a.base[1] = c->vdata;
+    a.base[2] = c->ksb ? c->kscales : nullptr;
+    a.base[3] = c->vsb ? c->vscales : nullptr;
+    a.rowb[0] = c->krow;
+    a.rowb[1] = c->vrow;
+    a.rowb[2] = c->ksb;
+    a.rowb[3] = c->vsb;
+    a.pool_rows = c->pool_rows;
+    return a;
+}
+
+// Runs copying logical rows [a, a+len) of sequence qa to logical rows
+// [b, b+len) of qb (every layer and tensor: see RowRun).
 static void add_row_copies(const Ctx *c, const Seq &qa, int64_t a, const Seq &qb, int64_t b, int64_t len,
-                           std::vector<Segment> &out) {
+                           std::vector<RowRun> &out) {
     int64_t done = 0;
     while (done < len) {
         int32_t pa, ca, pb, cb;
         phys(c, qa, a + done, pa, ca);
         phys(c, qb, b + done, pb, cb);
         int64_t run = std::min<int64_t>(len - done, std::min<int64_t>(c->P - ca, c->P - cb));
-        for (int l = 0; l < c->L; ++l) {
-            for (int g = 0; g < c->Hk; ++g) {
-                const int64_t ra = prow(c, pa, g, ca) + (int64_t)l * c->pool_rows;
-                const int64_t rb = prow(c, pb, g, cb) + (int64_t)l * c->pool_rows;
-                out.push_back({c->kdata + ra * c->krow, c->kdata + rb * c->krow, run * c->krow});
-                out.push_back({c->vdata + ra * c->vrow, c->vdata + rb * c->vrow, run * c->vrow});
-                if (c->ksb) out.push_back({c->kscales + ra * c->ksb, c->kscales + rb * c->ksb, run * c->ksb});
-                if (c->vsb) out.push_back({c->vscales + ra * c->vsb, c->vscales + rb * c->vsb, run * c->vsb});
-            }
-        }
+        for (int g = 0; g < c->Hk; ++g) out.push_back(RowRun{prow(c, pa, g, ca), prow(c, pb, g, cb), (int32_t)run, 0});
         done += run;
     }
 }
@@ -197,55 +210,56 @@ static int64_t payload_bytes(const Ctx *c, int64_t n) {
 }
 static int64_t state_bytes(const Ctx *c, int64_t n) { return 64 + pad16(4 * n) + payload_bytes(c, n); }
 
-// Segments between the pools and a packed payload laid out as in the state
-// format, for the rows idx[] of sequence q.  to_payload selects direction.
-static void add_payload_copies(const Ctx *c, const Seq &q, const std::vector<int64_t> &idx, uint8_t *payload,
-                               bool to_payload, std::vector<Segment> &out) {
+// Runs between the pools and a packed payload laid out as in the state
+// format, for the rows idx[] of sequence q (row i of the selection is payload
+// row g * N + i of head g, N = idx.size()).
+static void add_payload_copies(const Ctx *c, const Seq &q, const std::vector<int64_t> &idx,
+                               std::vector<RowRun> &out) {
     const int64_t n = (int64_t)idx.size();
-    int64_t off = 0;
-    // runs of consecutive logical rows that stay inside one page
-    std::vector<std::pair<int64_t, int64_t>> runs; // (selection index, length)
     for (int64_t i = 0; i < n;) {
+        int32_t pg, cl;
+        phys(c, q, idx[(size_t)i], pg, cl);
         int64_t j = i + 1;
-        int32_t p0, c0;
-        phys(c, q, idx[i], p0, c0);
-        while (j < n && idx[j] == idx[j - 1] + 1 && c0 + (j - i) < c->P) ++j;
-        runs.push_back({i, j - i});
+        while (j < n && idx[(size_t)j] == idx[(size_t)j - 1] + 1 && cl + (j - i) < c->P) ++j;
+        for (int g = 0; g < c->Hk; ++g)
+            out.push_back(RowRun{prow(c, pg, g, cl), (int64_t)g * n + i, (int32_t)(j - i), 0});
         i = j;
     }
-    for (int l = 0; l < c->L; ++l) {
+}
+
+// Copy arguments between the pools and a payload of n rows per head.
+static RunCopyArgs payload_args(const Ctx *c, int64_t n, uint8_t *payload, bool to_payload) {
+    RunCopyArgs a = pool_args(c);
+    a.payload = payload;
+    a.to_payload = to_payload ? 1 : 0;
+    const int64_t ks = section_bytes(c, c->tk, n);
+    a.layer_bytes = ks + section_bytes(c, c->tv, n);
+    a.toff[0] = 0;
+    a.toff[2] = pad16((int64_t)c->Hk * n * c->krow);
+    a.toff[1] = ks;
+    a.toff[3] = ks + pad16((int64_t)c->Hk * n * c->vrow);
+    return a;
+}
+
+// Layer groups of the chunked state copies: group i is layers
+// [L i / k, L (i + 1) / k), k = min(L, STATE_CHUNKS).
+static inline int state_chunks(const Ctx *c) { return std::min(c->L, Ctx::STATE_CHUNKS); }
+static inline int chunk_layer(const Ctx *c, int i) { return (int)((int64_t)c->L * i / state_chunks(c)); }
+
+// Zero the padding bytes of every section of a host payload.
+static void zero_payload_pads(const Ctx *c, uint8_t *payload, int64_t n) {
+    int64_t off = 0;
+    for (int l = 0; l < c->L; ++l)
         for (int t = 0; t < 2; ++t) {
             const int type = t == 0 ? c->tk : c->tv;
-            uint8_t *data = t == 0 ? c->kdata : c->vdata;
-            uint8_t *scales = t == 0 ? c->kscales : c->vscales;
-            const int rowb = t == 0 ? c->krow : c->vrow;
-            const int sb = t == 0 ? c->ksb : c->vsb;
-            const int64_t data_off = off;
-            const int64_t scale_off = off + pad16((int64_t)c->Hk * n * rowb);
-            for (auto &rn : runs) {
-                int32_t pg, cl;
-                phys(c, q, idx[rn.first], pg, cl);
-                for (int g = 0; g < c->Hk; ++g) {
-                    const int64_t R = prow(c, pg, g, cl) + (int64_t)l * c->pool_rows;
-                    uint8_t *pd = payload + data_off + ((int64_t)g * n + rn.first) * rowb;
-                    uint8_t *cd = data + R * rowb;
-                    if (to_payload)
-                        out.push_back({cd, pd, rn.second * rowb});
-                    else
-                        out.push_back({pd, cd, rn.second * rowb});
-                    if (type == KVC_Q8_0) {
-                        uint8_t *ps = payload + scale_off + ((int64_t)g * n + rn.first) * sb;
-                        uint8_t *cs = scales + R * sb;
-                        if (to_payload)
-                            out.push_back({cs, ps, rn.second * sb});
-                        else
-                            out.push_back({ps, cs, rn.second * sb});
-                    }
-                }
+            const int64_t db = (int64_t)c->Hk * n * (t == 0 ? c->krow : c->vrow);
+            std::memset(payload + off + db, 0, (size_t)(pad16(db) - db));
+            if (type == KVC_Q8_0) {
+                const int64_t sb = (int64_t)c->Hk * n * (t == 0 ? c->ksb : c->vsb);
+                std::memset(payload + off + pad16(db) + sb, 0, (size_t)(pad16(sb) - sb));
             }
             off += section_bytes(c, type, n);
         }
-    }
 }
 
 static void select_rows(const Seq &q, int64_t p0, int64_t p1, std::vector<int64_t> &idx) {
@@ -336,8 +350,8 @@ void kvc_destroy(kvc_ctx *cc) {
     cudaFree(c->tickets);
     cudaFree(c->err_dev);
     cudaFree(c->staging);
-    cudaFree(c->segs_dev);
-    cudaFree(c->rows_dev);
+    cudaFree(c->runs_dev);
+    cudaFree(c->spans_dev);
     cudaFree(c->zero_pt);
     if (c->hk) cudaFreeHost(c->hk);
     if (c->hv) cudaFreeHost(c->hv);
@@ -347,6 +361,9 @@ void kvc_destroy(kvc_ctx *cc) {
         if (ev) cudaEventDestroy(ev);
     if (c->st) cudaStreamDestroy(c->st);
     if (c->done) cudaEventDestroy(c->done);
+    if (c->st_copy) cudaStreamDestroy(c->st_copy);
+    for (auto ev : c->st_ev)
+        if (ev) cudaEventDestroy(ev);
     delete c;
 }
 
@@ -661,18 +678,21 @@ int kvc_seq_rm(kvc_ctx *cc, int seq, int p0, int p1) {
             keep.push_back(r);
         }
         const int64_t nk = (int64_t)keep.size();
-        const int64_t per_row = (int64_t)c->L * c->Hk * (c->krow + c->vrow + c->ksb + c->vsb);
-        if ((rc = ensure_staging(c, nk * per_row + 64))) return rc;
+        if ((rc = ensure_staging(c, payload_bytes(c, nk)))) return rc;
         // pack the kept rows, then unpack them at logical rows i0 .. i0+nk-1
-        std::vector<Segment> segs;
-        add_payload_copies(c, q, keep, c->staging, true, segs);
-        if ((rc = upload_segments(c, segs))) return rc;
+        std::vector<RowRun> runs;
+        add_payload_copies(c, q, keep, runs);
+        if ((rc = upload_runs(c, runs))) return rc;
+        KVC_CU(c, launch_copy_runs(payload_args(c, nk, c->staging, true), c->runs_dev, (int64_t)runs.size(), c->L,
+                                   c->st));
         if ((rc = wait_internal(c))) return rc;
         std::vector<int64_t> dst((size_t)nk);
         for (int64_t i = 0; i < nk; ++i) dst[(size_t)i] = i0 + i;
-        segs.clear();
-        add_payload_copies(c, q, dst, c->staging, false, segs);
-        if ((rc = upload_segments(c, segs))) return rc;
+        runs.clear();
+        add_payload_copies(c, q, dst, runs);
+        if ((rc = upload_runs(c, runs))) return rc;
+        KVC_CU(c, launch_copy_runs(payload_args(c, nk, c->staging, false), c->runs_dev, (int64_t)runs.size(), c->L,
+                                   c->st));
         if ((rc = wait_internal(c))) return rc;
         std::vector<int32_t> np;
         np.reserve((size_t)(q.n - k));
@@ -710,15 +730,16 @@ int kvc_seq_cp(kvc_ctx *cc, int src, int dst, int p0, int p1) {
     b.n += (int32_t)sel.size();
     for (int64_t r : sel) b.pos.push_back(a.pos[(size_t)r]);
     for (auto &f : b.lfill) f = b.n;
-    std::vector<Segment> segs;
+    std::vector<RowRun> runs;
     for (size_t i = 0; i < sel.size();) {
         size_t j = i + 1;
         while (j < sel.size() && sel[j] == sel[j - 1] + 1) ++j;
-        add_row_copies(c, a, sel[i], b, base + (int64_t)i, (int64_t)(j - i), segs);
+        add_row_copies(c, a, sel[i], b, base + (int64_t)i, (int64_t)(j - i), runs);
         i = j;
     }
     if ((rc = upload_pages(c, dst))) return rc;
-    if ((rc = upload_segments(c, segs))) return rc;
+    if ((rc = upload_runs(c, runs))) return rc;
+    KVC_CU(c, launch_copy_runs(pool_args(c), c->runs_dev, (int64_t)runs.size(), c->L, c->st));
     return wait_internal(c);
 }
 
@@ -740,23 +761,30 @@ int kvc_seq_add(kvc_ctx *cc, int seq, int p0, int p1, int delta) {
     }
     int rc = enter_sync(c);
     if (rc) return rc;
-    // head-rows of layer 0 to rotate; the kernel repeats them for every layer
-    const int64_t n_rows = (int64_t)sel.size() * c->Hk;
-    if (n_rows > c->rows_cap) {
-        dev_free(c, c->rows_dev, c->rows_cap * 8);
-        c->rows_dev = nullptr;
-        c->rows_cap = 0;
-        if ((rc = dev_alloc(c, (void **)&c->rows_dev, n_rows * 8, "row list"))) return rc;
-        c->rows_cap = n_rows;
-    }
-    std::vector<int64_t> rows;
-    rows.reserve((size_t)n_rows);
-    for (int64_t r : sel) {
+    // runs of consecutive cells inside one page, one span per KV head (layer 0;
+    // the kernel repeats them for every layer), at most ROPE_SPAN_MAX rows each
+    std::vector<RopeSpan> spans;
+    for (size_t i = 0; i < sel.size();) {
         int32_t pg, cl;
-        phys(c, q, r, pg, cl);
-        for (int g = 0; g < c->Hk; ++g) rows.push_back(prow(c, pg, g, cl));
+        phys(c, q, sel[i], pg, cl);
+        size_t j = i + 1;
+        while (j < sel.size() && sel[j] == sel[j - 1] + 1 && (int64_t)(j - i) < ROPE_SPAN_MAX &&
+               cl + (int64_t)(j - i) < c->P)
+            ++j;
+        for (int g = 0; g < c->Hk; ++g) spans.push_back(RopeSpan{prow(c, pg, g, cl), (int32_t)(j - i), 0});
+        i = j;
     }
-    KVC_CU(c, cudaMemcpyAsync(c->rows_dev, rows.data(), rows.size() * 8, cudaMemcpyHostToDevice, c->st));
+    const int64_t n_spans = (int64_t)spans.size();
+    if (n_spans > c->spans_cap) {
+        dev_free(c, c->spans_dev, c->spans_cap * (int64_t)sizeof(RopeSpan));
+        c->spans_dev = nullptr;
+        c->spans_cap = 0;
+        if ((rc = dev_alloc(c, (void **)&c->spans_dev, n_spans * (int64_t)sizeof(RopeSpan), "span list")))
+            return rc;
+        c->spans_cap = n_spans;
+    }
+    KVC_CU(c, cudaMemcpyAsync(c->spans_dev, spans.data(), spans.size() * sizeof(RopeSpan), cudaMemcpyHostToDevice,
+                              c->st));
     // cos/sin of delta * theta_i in fp64, theta_i = base^(-2i/D)
     float2 cs[64];
     for (int i = 0; i < c->D / 2; ++i) {
@@ -765,8 +793,8 @@ int kvc_seq_add(kvc_ctx *cc, int seq, int p0, int p1, int delta) {
         cs[i] = make_float2((float)std::cos(phi), (float)std::sin(phi));
     }
     cudaError_t e = launch_rope_shift(c->tk, c->D, c->prm.rope_mode, c->kdata,
-                                      reinterpret_cast<uint16_t *>(c->kscales), c->pool_rows, c->L, c->rows_dev,
-                                      n_rows, cs, c->st);
+                                      reinterpret_cast<uint16_t *>(c->kscales), c->pool_rows, c->L, c->spans_dev,
+                                      n_spans, cs, c->st);
     if (e != cudaSuccess) return cuda_fail(c, e, "rope shift kernel");
     if ((rc = wait_internal(c))) return rc;
     for (int64_t r : sel) q.pos[(size_t)r] += delta;
@@ -801,12 +829,30 @@ int kvc_state_get(kvc_ctx *cc, int seq, int p0, int p1, void *dst, size_t cap, s
     for (int64_t i = 0; i < n; ++i) std::memcpy(out + 64 + 4 * i, &q.pos[(size_t)sel[(size_t)i]], 4);
     if (n > 0) {
         if ((rc = ensure_staging(c, (int64_t)pl))) return rc;
-        KVC_CU(c, cudaMemsetAsync(c->staging, 0, (size_t)pl, c->st)); // padding bytes are zero
-        std::vector<Segment> segs;
-        add_payload_copies(c, q, sel, c->staging, true, segs);
-        if ((rc = upload_segments(c, segs))) return rc;
-        KVC_CU(c, cudaMemcpyAsync(out + 64 + pad16(4 * n), c->staging, (size_t)pl, cudaMemcpyDeviceToHost, c->st));
+        if ((rc = ensure_copy_stream(c))) return rc;
+        std::vector<RowRun> runs;
+        add_payload_copies(c, q, sel, runs);
+        if ((rc = upload_runs(c, runs))) return rc;
+        const RunCopyArgs ca = payload_args(c, n, c->staging, true);
+        // pack a layer group on st, then copy it to the host on st_copy while
+        // the next group is packed
+        uint8_t *hp = out + 64 + pad16(4 * n);
+        const int64_t per_layer = section_bytes(c, c->tk, n) + section_bytes(c, c->tv, n);
+        const int k = state_chunks(c);
+        for (int i = 0; i < k; ++i) {
+            const int l0 = chunk_layer(c, i), l1 = chunk_layer(c, i + 1);
+            RunCopyArgs cl = ca;
+            cl.l0 = l0;
+            KVC_CU(c, launch_copy_runs(cl, c->runs_dev, (int64_t)runs.size(), l1 - l0, c->st));
+            KVC_CU(c, cudaEventRecord(c->st_ev[i], c->st));
+            KVC_CU(c, cudaStreamWaitEvent(c->st_copy, c->st_ev[i], 0));
+            KVC_CU(c, cudaMemcpyAsync(hp + l0 * per_layer, c->staging + l0 * per_layer, (size_t)((l1 - l0) * per_layer),
+                                      cudaMemcpyDeviceToHost, c->st_copy));
+        }
+        KVC_CU(c, cudaEventRecord(c->st_ev[Ctx::STATE_CHUNKS], c->st_copy));
+        KVC_CU(c, cudaStreamWaitEvent(c->st, c->st_ev[Ctx::STATE_CHUNKS], 0));
         if ((rc = wait_internal(c))) return rc;
+        zero_payload_pads(c, hp, n); // the staging buffer's padding bytes are not written
     }
     return KVC_OK;
 }
@@ -848,17 +894,33 @@ int kvc_state_set(kvc_ctx *cc, int seq, const void *src, size_t nbytes, size_t *
         release_tail_pages(c, q);
         return rc;
     }
-    KVC_CU(c, cudaMemcpyAsync(c->staging, in + 64 + pad16(4 * n), (size_t)pl, cudaMemcpyHostToDevice, c->st));
     const int64_t base = q.n;
     q.n += (int32_t)n;
     q.pos.insert(q.pos.end(), pos.begin(), pos.end());
     for (auto &f : q.lfill) f = q.n;
     std::vector<int64_t> idx((size_t)n);
     for (int64_t i = 0; i < n; ++i) idx[(size_t)i] = base + i;
-    std::vector<Segment> segs;
-    add_payload_copies(c, q, idx, c->staging, false, segs);
+    std::vector<RowRun> runs;
+    add_payload_copies(c, q, idx, runs);
     if ((rc = upload_pages(c, seq))) return rc;
-    if ((rc = upload_segments(c, segs))) return rc;
+    if ((rc = upload_runs(c, runs))) return rc;
+    const RunCopyArgs ca = payload_args(c, n, c->staging, false);
+    if ((rc = ensure_copy_stream(c))) return rc;
+    // copy a layer group to the device on st_copy, unpack it on st while the
+    // next group is copied (the staging buffer is idle: enter_sync waited)
+    const uint8_t *hp = in + 64 + pad16(4 * n);
+    const int64_t per_layer = section_bytes(c, c->tk, n) + section_bytes(c, c->tv, n);
+    const int k = state_chunks(c);
+    for (int i = 0; i < k; ++i) {
+        const int l0 = chunk_layer(c, i), l1 = chunk_layer(c, i + 1);
+        RunCopyArgs cl = ca;
+        cl.l0 = l0;
+        KVC_CU(c, cudaMemcpyAsync(c->staging + l0 * per_layer, hp + l0 * per_layer, (size_t)((l1 - l0) * per_layer),
+                                  cudaMemcpyHostToDevice, c->st_copy));
+        KVC_CU(c, cudaEventRecord(c->st_ev[i], c->st_copy));
+        KVC_CU(c, cudaStreamWaitEvent(c->st, c->st_ev[i], 0));
+        KVC_CU(c, launch_copy_runs(cl, c->runs_dev, (int64_t)runs.size(), l1 - l0, c->st));
+    }
     return wait_internal(c);
 }
 

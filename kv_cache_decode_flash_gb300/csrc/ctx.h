@@ -103,12 +103,17 @@ struct Ctx {
     // staging for sequence / state operations
     uint8_t *staging = nullptr;
     int64_t staging_bytes = 0;
-    Segment *segs_dev = nullptr;
-    int64_t segs_cap = 0;
-    int64_t *rows_dev = nullptr;
-    int64_t rows_cap = 0;
+    RowRun *runs_dev = nullptr;
+    int64_t runs_cap = 0;
+    RopeSpan *spans_dev = nullptr;
+    int64_t spans_cap = 0;
     cudaStream_t st = nullptr; // internal stream of the synchronous operations
     cudaEvent_t done = nullptr;
+    // state export/import: host copies of layer groups on their own stream,
+    // overlapped with the pack/unpack kernels on st (created on first use)
+    static constexpr int STATE_CHUNKS = 8;
+    cudaStream_t st_copy = nullptr;
+    cudaEvent_t st_ev[STATE_CHUNKS + 1] = {};
 
     int timeout_ms = 120000;
     int fail_after = -1;

@@ -90,20 +90,43 @@ cudaError_t launch_append(int type_k, int type_v, int Hk, int D, int n_tok, cons
 // Write page-table entries: pt[idx[i]] = val[i], up to 32 per launch.
 cudaError_t launch_pt_update(int32_t *pt, int n, const int32_t *idx, const int32_t *val, cudaStream_t st);
 
-// Copy a list of byte segments (device list of {src, dst, bytes}).
-struct Segment {
-    const uint8_t *src;
-    uint8_t *dst;
-    int64_t bytes;
+// Range copies of the sequence operations.  A run is n consecutive physical
+// rows of one KV head starting at pool row `row0` (layer 0); `other` is the
+// first row on the other side: a pool row (pool to pool) or the row index
+// g * N + i of the packed state layout (N rows exported, g the KV head).
+// Every run is applied to layers [l0, l0 + n_layers) and to each present
+// tensor (K codes, V codes, K scales, V scales).
+struct RowRun {
+    int64_t row0;
+    int64_t other;
+    int32_t n;
+    int32_t pad;
 };
-cudaError_t launch_copy_segments(const Segment *segs_dev, int n, cudaStream_t st);
+struct RunCopyArgs {
+    uint8_t *base[4];    // K codes, V codes, K scales, V scales (null: absent)
+    int32_t rowb[4];     // bytes per row of each
+    int64_t pool_rows;   // rows of one layer pool
+    uint8_t *payload;    // null: pool to pool (row0 -> other)
+    int64_t layer_bytes; // payload bytes of one layer
+    int64_t toff[4];     // offset of each tensor inside a payload layer
+    int32_t to_payload;  // payload copies: 1 pool -> payload, 0 payload -> pool
+    int32_t l0;          // first layer
+};
+cudaError_t launch_copy_runs(const RunCopyArgs &a, const RowRun *runs_dev, int64_t n_runs, int n_layers,
+                             cudaStream_t st);
 
-// RoPE shift of stored K rows.  rows_dev: device list of physical row
-// indices (page * Hk + g) * P + cell of every head-row to rotate in one layer
-// (applied to every layer: layer_stride_rows apart).  cs: device float2
-// [D/2] (cos, sin) of delta * theta_i.
+// RoPE shift of stored K rows.  A span is `n` consecutive physical rows
+// starting at row0 = (page * Hk + g) * P + cell of the layer-0 pool; every
+// span is applied to each of the n_layer layers (layer_rows apart).  cs:
+// (cos, sin) of delta * theta_i for i < D/2, copied into the launch.
+struct RopeSpan {
+    int64_t row0;
+    int32_t n;
+    int32_t pad;
+};
+constexpr int ROPE_SPAN_MAX = 512; // rows of one span (one CTA)
 cudaError_t launch_rope_shift(int type_k, int D, int mode, void *kdata, uint16_t *kscales, int64_t layer_rows,
-                              int n_layer, const int64_t *rows_dev, int64_t n_rows, const float2 *cs,
+                              int n_layer, const RopeSpan *spans_dev, int64_t n_spans, const float2 *cs,
                               cudaStream_t st);
 
 // Encode a 2D tiled tensor map (rows x row_bytes) for the attention kernel.

@@ -178,9 +178,10 @@ def test_seq_ops_bit_exact(type_):
         tw.close()
 
 
-@pytest.mark.parametrize("type_", [Q8, F16])
-def test_state_roundtrip(type_):
-    tw = Twin(3, 8, 2, 128, 4096, n_seq_max=3, type_=type_, page_rows=64)
+# 10 layers: the export/import copies run in 8 uneven layer groups
+@pytest.mark.parametrize("type_,n_layer", [(Q8, 3), (F16, 3), (Q8, 10), (F16, 10)])
+def test_state_roundtrip(type_, n_layer):
+    tw = Twin(n_layer, 8, 2, 128, 4096, n_seq_max=3, type_=type_, page_rows=64)
     try:
         tw.fill(0, 777, seed=10)
         blob = tw.gpu.state_get(0, 100, 600)
@@ -203,9 +204,11 @@ def test_state_roundtrip(type_):
         tw.close()
 
 
-@pytest.mark.parametrize("mode", [0, 1])
-def test_seq_add_q8_0(mode):
-    tw = Twin(2, 8, 2, 128, 2048, type_=Q8, rope_base=1e6, rope_mode=mode)
+# page_rows 2048 puts the shifted range in one page run longer than a shift
+# kernel span (512 rows), so spans are split inside a page
+@pytest.mark.parametrize("mode,D,page_rows", [(0, 128, 0), (1, 128, 0), (0, 64, 2048), (1, 64, 2048)])
+def test_seq_add_q8_0(mode, D, page_rows):
+    tw = Twin(2, 8, 2, D, 2048, type_=Q8, rope_base=1e6, rope_mode=mode, page_rows=page_rows)
     try:
         tw.fill(0, 1500, seed=11, sigma=0.5)
         tw.gpu.seq_add(0, 200, 1200, -150)
@@ -218,9 +221,9 @@ def test_seq_add_q8_0(mode):
         tw.close()
 
 
-@pytest.mark.parametrize("mode", [0, 1])
-def test_seq_add_f16(mode):
-    tw = Twin(2, 8, 2, 64, 1024, type_=F16, rope_base=1e4, rope_mode=mode)
+@pytest.mark.parametrize("mode,D,page_rows", [(0, 64, 0), (1, 64, 0), (0, 128, 1024), (1, 128, 1024)])
+def test_seq_add_f16(mode, D, page_rows):
+    tw = Twin(2, 8, 2, D, 1024, type_=F16, rope_base=1e4, rope_mode=mode, page_rows=page_rows)
     try:
         tw.fill(0, 900, seed=12)
         tw.gpu.seq_add(0, 100, 800, 131072)
