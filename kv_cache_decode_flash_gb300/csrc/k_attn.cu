@@ -144,6 +144,26 @@ __device__ __forceinline__ void vcodes_to_half2(uint32_t w, uint32_t &ev, uint32
     asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(od) : "r"(bias));
 }
 
+// The NB fp16 scales of one row (NB = 2 or 4), one 4- or 8-byte load.
+template <int NB>
+__device__ __forceinline__ void load_scales(const uint8_t *p, uint32_t (&w)[NB / 2]) {
+    if constexpr (NB == 4) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(p);
+        w[0] = v.x;
+        w[1] = v.y;
+    } else {
+        w[0] = *reinterpret_cast<const uint32_t *>(p);
+    }
+}
+template <int N>
+__device__ __forceinline__ float half_at(const uint32_t (&w)[N], int b) {
+    return __half2float(__ushort_as_half((uint16_t)(w[b >> 1] >> (16 * (b & 1)))));
+}
+
+// Slack of the lazily raised softmax maximum (log2 units): probabilities stay
+// below 2^RESCALE_SLACK between raises.
+constexpr int RESCALE_SLACK = 8;
+
 // Programmatic dependent launch: wait for the preceding kernel's results /
 // let the next kernel be scheduled.  No-ops without a programmatic edge.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -397,8 +417,11 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
             const int lm_row = rbase + (lane & 7) + ((lane >> 3) & 1) * 8;
             const int lm_hi = lane >> 4;
             if constexpr (S::Q8) {
-                const uint16_t *ksc = reinterpret_cast<const uint16_t *>(st + S::KBYTES + S::VBYTES) +
-                                      tinfo[s].delta * S::NB;
+                // K scales of rows ra, rb: NB halves each, one 8- (or 4-) byte load per row
+                const uint8_t *ksb = st + S::KBYTES + S::VBYTES + (tinfo[s].delta + rbase) * S::SB;
+                uint32_t kw[2][S::NB / 2];
+                load_scales<S::NB>(ksb + gq * S::SB, kw[0]);
+                load_scales<S::NB>(ksb + (gq + 8) * S::SB, kw[1]);
 #pragma unroll
                 for (int b = 0; b < S::NB; ++b) {
                     uint32_t r0, r1, r2, r3;
@@ -413,8 +436,7 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
                     codes_to_half2(r3, a1, a3);
                     mma16816(c, a0, a1, a2, a3, bh[2 * b + 1][0], bh[2 * b + 1][1]);
                     mma16816(c, a0, a1, a2, a3, bl[2 * b + 1][0], bl[2 * b + 1][1]);
-                    const float da = __half2float(__ushort_as_half(ksc[ra * S::NB + b]));
-                    const float db = __half2float(__ushort_as_half(ksc[rb * S::NB + b]));
+                    const float da = half_at(kw[0], b), db = half_at(kw[1], b);
                     sc[0] = fmaf(da, c[0], sc[0]);
                     sc[1] = fmaf(da, c[1], sc[1]);
                     sc[2] = fmaf(db, c[2], sc[2]);
@@ -437,29 +459,27 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
             s2v[2] = (gq + 8 < rows_w) ? sc[2] * hs0 : -INFINITY;
             s2v[3] = (gq + 8 < rows_w) ? sc[3] * hs1 : -INFINITY;
             // ---------------- online softmax (per warp) ----------------
+            // The running maxima m0, m1 (warp-uniform) are only raised when a
+            // score exceeds them by more than RESCALE_SLACK (log2 units), so
+            // most tiles need no cross-lane reduction; probabilities are then
+            // at most 2^RESCALE_SLACK, which the P' range exponent allows for.
             float t0 = fmaxf(s2v[0], s2v[2]), t1 = fmaxf(s2v[1], s2v[3]);
+            const bool raise = __any_sync(0xffffffffu, t0 > m0 + RESCALE_SLACK || t1 > m1 + RESCALE_SLACK);
+            float mn0 = m0, mn1 = m1;
+            if (raise) {
 #pragma unroll
-            for (int m = 4; m < 32; m <<= 1) {
-                t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, m));
-                t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, m));
+                for (int m = 4; m < 32; m <<= 1) {
+                    t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, m));
+                    t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, m));
+                }
+                mn0 = fmaxf(m0, t0); // finite: the slab has a live row
+                mn1 = fmaxf(m1, t1);
             }
-            const float mn0 = fmaxf(m0, t0), mn1 = fmaxf(m1, t1); // finite: the slab has a live row
-            const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
             float pr[4];
             pr[0] = hv0 ? ex2(s2v[0] - mn0) : 0.f;
             pr[1] = hv1 ? ex2(s2v[1] - mn1) : 0.f;
             pr[2] = hv0 ? ex2(s2v[2] - mn0) : 0.f;
             pr[3] = hv1 ? ex2(s2v[3] - mn1) : 0.f;
-            float rs0 = pr[0] + pr[2], rs1 = pr[1] + pr[3];
-#pragma unroll
-            for (int m = 4; m < 32; m <<= 1) {
-                rs0 += __shfl_xor_sync(0xffffffffu, rs0, m);
-                rs1 += __shfl_xor_sync(0xffffffffu, rs1, m);
-            }
-            l0 = l0 * al0 + rs0;
-            l1 = l1 * al1 + rs1;
-            m0 = mn0;
-            m1 = mn1;
             // probabilities to [head][row] for the PV B operand
             pw[(2 * tq) * S::PSTR + gq] = pr[0];
             pw[(2 * tq + 1) * S::PSTR + gq] = pr[1];
@@ -467,35 +487,33 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
             pw[(2 * tq + 1) * S::PSTR + gq + 8] = pr[3];
             // ---------------- V scales of the rows this lane feeds (2t, 2t+1, 2t+8, 2t+9) -------
             const int rr[4] = {2 * tq, 2 * tq + 1, 2 * tq + 8, 2 * tq + 9};
-            float dv[4][S::NBX];
-            int s_tile = 14; // f16: P' = p <= 1
+            uint32_t vw[4][S::NBX / 2 > 0 ? S::NBX / 2 : 1];
+            int s_tile = 14 - RESCALE_SLACK; // f16: P' = p <= 2^RESCALE_SLACK
             if constexpr (S::Q8) {
-                const uint16_t *vsc = reinterpret_cast<const uint16_t *>(st + S::KBYTES + S::VBYTES + S::SCALE_BUF) +
-                                      tinfo[s].delta * S::NB;
-                float dmax = 0.f;
+                const uint8_t *vsb = st + S::KBYTES + S::VBYTES + S::SCALE_BUF + (tinfo[s].delta + rbase) * S::SB;
+                uint32_t wm = 0;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const bool live = rr[i] < rows_w;
+                    load_scales<S::NB>(vsb + rr[i] * S::SB, vw[i]);
+                    // rows past the tile may hold stale bytes: their scales count as 0
 #pragma unroll
-                    for (int b = 0; b < S::NB; ++b) {
-                        const float d = __half2float(__ushort_as_half(vsc[(rbase + rr[i]) * S::NB + b]));
-                        dv[i][b] = live ? d : 0.f;
-                        dmax = fmaxf(dmax, dv[i][b]);
+                    for (int h = 0; h < S::NB / 2; ++h) {
+                        vw[i][h] = (rr[i] < rows_w) ? vw[i][h] : 0u;
+                        wm = __vmaxu2(wm, vw[i][h]); // non-negative fp16: integer order
                     }
                 }
-                dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, 1));
-                dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, 2));
-                // 2^S * max(p * d) < 2^15: hi and lo of P' stay in fp16 range
-                s_tile = (dmax > 0.f) ? 14 - ilogbf(dmax) : (have_s ? sexp : 0);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) dv[i][0] = (rr[i] < rows_w) ? 1.f : 0.f;
+                wm = __vmaxu2(wm, __shfl_xor_sync(0xffffffffu, wm, 1));
+                wm = __vmaxu2(wm, __shfl_xor_sync(0xffffffffu, wm, 2));
+                const float dmax = __half2float(__ushort_as_half((uint16_t)max(wm & 0xffffu, wm >> 16)));
+                // 2^S * max(p * d) < 2^15 with p <= 2^RESCALE_SLACK: hi and lo of P' stay in fp16 range
+                s_tile = (dmax > 0.f) ? 14 - RESCALE_SLACK - ilogbf(dmax) : (have_s ? sexp : 0);
             }
             const int s_new = have_s ? min(sexp, s_tile) : s_tile;
-            // rescale the accumulators: softmax max moved (alpha) and/or S decreased
-            const float sf = have_s ? ldexpf(1.f, s_new - sexp) : 1.f;
-            const float f0 = al0 * sf, f1 = al1 * sf;
-            if (__any_sync(0xffffffffu, f0 != 1.f || f1 != 1.f)) {
+            // rescale the accumulators: the softmax maxima moved and/or S decreased
+            if (raise || s_new != sexp || !have_s) {
+                const float sf = have_s ? ldexpf(1.f, s_new - sexp) : 1.f;
+                const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1); // 0 while m is -inf
+                const float f0 = al0 * sf, f1 = al1 * sf;
 #pragma unroll
                 for (int mt = 0; mt < NMT; ++mt) {
                     acc[mt][0] *= f0;
@@ -503,12 +521,19 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
                     acc[mt][2] *= f0;
                     acc[mt][3] *= f1;
                 }
+                l0 *= f0;
+                l1 *= f1;
+                m0 = mn0;
+                m1 = mn1;
             }
+            // per-lane partial row sums, in the same 2^S domain as the accumulators
+            const float ps = ldexpf(1.f, s_new);
+            l0 = fmaf(pr[0] + pr[2], ps, l0);
+            l1 = fmaf(pr[1] + pr[3], ps, l1);
             sexp = s_new;
             have_s = true;
             __syncwarp();
             // ---------------- PV on the tensor cores: O^T += V^T (P' hi + lo)^T --------------
-            const float ps = ldexpf(1.f, s_new);
             float pv[4];
             {
                 const float2 pa = *reinterpret_cast<const float2 *>(pw + gq * S::PSTR + 2 * tq);
@@ -522,7 +547,12 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
             for (int b = 0; b < S::NBX; ++b) {
                 float x[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) x[i] = pv[i] * dv[i][b];
+                for (int i = 0; i < 4; ++i) {
+                    if constexpr (S::Q8)
+                        x[i] = pv[i] * half_at(vw[i], b);
+                    else
+                        x[i] = pv[i]; // rows past the tile have p = 0
+                }
                 uint32_t b0h, b1h, b0l, b1l;
                 split_pack(x[0], x[1], b0h, b0l);
                 split_pack(x[2], x[3], b1h, b1l);
@@ -579,6 +609,12 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
 #pragma unroll
     for (int mt = 0; mt < S::NMT; ++mt)
         wf[(warp * S::NMT + mt) * 32 + lane] = make_float4(acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3]);
+    // row sums: lanes gq = 0..7 hold different rows of the same heads
+#pragma unroll
+    for (int m = 4; m < 32; m <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, m);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, m);
+    }
     if (gq == 0) {
         wm[warp * 8 + 2 * tq] = m0;
         wm[warp * 8 + 2 * tq + 1] = m1;
@@ -598,8 +634,9 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
         float M = mw;
 #pragma unroll
         for (int m = 16; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
-        const float f = (lane < W && M != -INFINITY) ? ex2(mw - M) : 0.f;
-        if (lane < W) s_ww[lane * 8 + h] = f * wus[lane];
+        // O and l of a warp are both in its 2^S domain: one weight for both
+        const float f = (lane < W && M != -INFINITY) ? ex2(mw - M) * wus[lane] : 0.f;
+        if (lane < W) s_ww[lane * 8 + h] = f;
         float L = (lane < W) ? wl[lane * 8 + h] * f : 0.f;
 #pragma unroll
         for (int m = 16; m > 0; m >>= 1) L += __shfl_xor_sync(0xffffffffu, L, m);
