@@ -169,13 +169,17 @@ constexpr int RESCALE_SLACK = 8;
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// Static shape of one kernel instance.  W warps per CTA, each owning 16 rows
-// of every tile; stages sized so two CTAs fit on an SM.
+// Static shape of one kernel instance.  W compute warps in groups of GW;
+// group j takes tiles j, j + G, j + 2G, ... and each of its warps owns 16
+// rows of a tile.  One more warp issues the tile loads.
 template <int TYPE, int D, int R>
 struct Shape {
     static constexpr bool Q8 = TYPE == KVC_Q8_0;
-    static constexpr int W = Q8 ? 16 : 8;             // warps per CTA (one CTA per SM)
-    static constexpr int T = 16 * W;                  // rows per tile
+    static constexpr int W = Q8 ? 16 : 8;             // compute warps per CTA (one CTA per SM)
+    static constexpr int GW = 8;                      // warps per group
+    static constexpr int G = W / GW;                  // groups
+    static constexpr int NTHREADS = (W + 1) * 32;     // compute warps + the load warp
+    static constexpr int T = 16 * GW;                 // rows per tile
     static constexpr int NB = D / 32;                 // q8_0 blocks per row
     static constexpr int KROW = Q8 ? D : 2 * D;       // bytes per K row
     static constexpr int VROW = KROW;                 // bytes per V row
@@ -189,13 +193,14 @@ struct Shape {
     static constexpr int PSTR = 24;                   // floats per head slot in the exchange (16 rows + pad)
     static constexpr int PBUF = 8 * PSTR;             // floats per warp: p[8 head slots][rows]
     static constexpr int MAXT = 512;                  // tiles per chunk (host keeps chunks within it)
-    // as many stages (2..4) as fit next to the exchange buffers in one SM's shared memory
-    static constexpr int FIT = (232448 - 4096 - W * PBUF * 4 - 1024 - MAXT * 8 - 256) / STAGE;
-    static constexpr int STAGES = FIT < 2 ? 2 : (FIT > 4 ? 4 : FIT);
+    // as many stages (2..8) as fit next to the exchange buffers in one SM's shared memory
+    static constexpr int QF_BYTES = KSTEPS * 32 * 16 + 64; // q fragments (one copy for all warps) + head scales
+    static constexpr int FIT = (232448 - 4096 - W * PBUF * 4 - 1024 - MAXT * 8 - 256 - QF_BYTES) / STAGE;
+    static constexpr int STAGES = FIT < 2 ? 2 : (FIT > 8 ? 8 : FIT);
     static constexpr int OOFF = ((2 * R + 3) / 4) * 4;  // partial: m[R], l[R], pad, then o[R][D] 16-byte aligned
     static constexpr int PF = OOFF + R * D;            // floats of one partial
-    static constexpr int SMEM = STAGES * STAGE + W * PBUF * 4 + 2 * STAGES * 8 + STAGES * 4 + 64 + MAXT * 8 + 1024;
-    static constexpr int MINB = 1;                    // one CTA per SM (registers capped at 128 by W)
+    static constexpr int SMEM =
+        STAGES * STAGE + W * PBUF * 4 + 2 * STAGES * 8 + STAGES * 8 + 64 + MAXT * 8 + QF_BYTES + 1024;
     static constexpr int MERGE_CAP = (STAGES * STAGE) / (4 * (PF + R)); // chunks the grid merge can stage
     static constexpr int BIG = 128;                    // rows of a large TMA box (small boxes are 16 rows)
     static constexpr int NMT = D / 16;                 // PV m-tiles of 16 dims
@@ -216,12 +221,12 @@ struct TileInfo {
 };
 
 template <int TYPE, int D, int R>
-__global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::MINB)
+__global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmk,
                 const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmkb,
                 const __grid_constant__ CUtensorMap tmvb) {
     using S = Shape<TYPE, D, R>;
-    constexpr int W = S::W, T = S::T, NT = W * 32;
+    constexpr int W = S::W, T = S::T, NT = S::NTHREADS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *stages = smem;
@@ -229,9 +234,11 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
     uint64_t *full = reinterpret_cast<uint64_t *>(pbuf_all + W * S::PBUF);
     uint64_t *empty = full + S::STAGES;
     TileInfo *tinfo = reinterpret_cast<TileInfo *>(empty + S::STAGES);
-    int *s_cnt = reinterpret_cast<int *>(tinfo + S::STAGES); // warps done with each stage
-    int *s_tstart = s_cnt + S::STAGES;                        // first row of every tile
+    int *s_tstart = reinterpret_cast<int *>(tinfo + S::STAGES); // first row of every tile
     int *s_tpage = s_tstart + S::MAXT;                        // its physical page
+    // q fragments of every k-step, lane-major: {hi b0, hi b1, lo b0, lo b1}
+    uint4 *qfs = reinterpret_cast<uint4 *>(((uintptr_t)(s_tpage + S::MAXT) + 15) & ~(uintptr_t)15);
+    float *shs = reinterpret_cast<float *>(qfs + S::KSTEPS * 32); // 2^-e of each head slot
     __shared__ int s_flag;
     __shared__ float s_M[R], s_L[R];
     __shared__ float s_ww[W * 8]; // per-warp merge weights [warp][head]
@@ -258,8 +265,7 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
         s_flag = nt;
         for (int s = 0; s < S::STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], W);
-            s_cnt[s] = 0;
+            mbar_init(&empty[s], S::GW); // the group of warps that reads the stage
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -269,8 +275,7 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
         for (int k = lane; k < n_tiles; k += 32) s_tpage[k] = sq.page_table[(sq.off + s_tstart[k]) / p.P];
     __syncthreads();
 
-    // ---- tile loads: the first stages by thread 0, every later one by the last
-    // warp to finish with the stage it reuses ----------------------------------
+    // ---- tile loads, all issued by lane 0 of the load warp (warp W) -----------
     auto issue = [&](int k) {
         const int s = k % S::STAGES;
         const int r0 = s_tstart[k];
@@ -328,81 +333,97 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
     };
     // Tiles made only of rows no in-flight kernel writes (the stable prefix)
     // are requested before waiting for the preceding kernel.
-    int prod_k = 0; // thread 0: tiles issued before the loop
-    if (tid == 0) {
+    const bool loader = warp == W && lane == 0;
+    int prod_k = 0; // tiles issued before the wait
+    if (loader) {
         while (prod_k < n_tiles && prod_k < S::STAGES && s_tstart[prod_k] + tile_rows(s_tstart[prod_k]) <= sq.stable_rows)
             issue(prod_k++);
     }
     pdl_wait();
     pdl_trigger();
-    if (tid == 0) {
+    if (loader) {
         for (; prod_k < n_tiles && prod_k < S::STAGES; ++prod_k) issue(prod_k);
     }
 
-    // ---- query fragments (B operand of QK), hi + lo fp16 -------------------
-    const int gq = lane >> 2, tq = lane & 3;
-    const int hslot = gq; // head slot this lane feeds into the MMA B operand
-    const bool hvalid = hslot < r_act;
-    const float *qrow = p.q + ((int64_t)sq.out_row * p.H + (int64_t)g * r_act + (hvalid ? hslot : 0)) * D;
-    float qv[S::KSTEPS][4];
-    float amax = 0.0f;
-#pragma unroll
-    for (int ks = 0; ks < S::KSTEPS; ++ks) {
-        int d0, d1;
-        if constexpr (S::Q8) {
-            d0 = 16 * ks + 4 * tq;
-            d1 = d0 + 2;
-        } else {
-            d0 = 16 * ks + 2 * tq;
-            d1 = d0 + 8;
-        }
-        float2 x0 = hvalid ? *reinterpret_cast<const float2 *>(qrow + d0) : make_float2(0.f, 0.f);
-        float2 x1 = hvalid ? *reinterpret_cast<const float2 *>(qrow + d1) : make_float2(0.f, 0.f);
-        qv[ks][0] = x0.x * p.kq_scale_log2;
-        qv[ks][1] = x0.y * p.kq_scale_log2;
-        qv[ks][2] = x1.x * p.kq_scale_log2;
-        qv[ks][3] = x1.y * p.kq_scale_log2;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fabsf(qv[ks][j]));
-    }
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    // power-of-two scaling that puts max|q| in [2^13, 2^14): hi and lo stay normal fp16
-    const int e_q = (amax > 0.0f) ? 13 - ilogbf(amax) : 0;
-    uint32_t bh[S::KSTEPS][2], bl[S::KSTEPS][2];
-#pragma unroll
-    for (int ks = 0; ks < S::KSTEPS; ++ks) {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const float x0 = ldexpf(qv[ks][2 * j], e_q), x1 = ldexpf(qv[ks][2 * j + 1], e_q);
-            const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-            const __half l0 = __float2half_rn(x0 - __half2float(h0)), l1 = __float2half_rn(x1 - __half2float(h1));
-            bh[ks][j] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
-            bl[ks][j] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
-        }
-    }
-    // 2^-e for the two heads (2t, 2t+1) whose scores this lane accumulates
-    const int e0 = __shfl_sync(0xffffffffu, e_q, (2 * tq) * 4);
-    const int e1 = __shfl_sync(0xffffffffu, e_q, (2 * tq + 1) * 4);
-    const float hs0 = ldexpf(1.0f, -e0), hs1 = ldexpf(1.0f, -e1);
-    const bool hv0 = 2 * tq < r_act, hv1 = 2 * tq + 1 < r_act;
-
-    // ---- per-warp state -------------------------------------------------------
-    // softmax state of heads 2t, 2t+1; PV accumulators O^T[dims][heads] as
-    // m16n8 fragments (rows = dims, columns = heads 2t, 2t+1)
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    // per-warp results of the compute warps (read by the CTA merge)
     constexpr int NMT = D / 16;
     float acc[NMT][4];
 #pragma unroll
     for (int mt = 0; mt < NMT; ++mt)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[mt][j] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     int sexp = 0;        // P' range exponent S of this warp (valid once have_s)
     bool have_s = false;
-    float *pw = pbuf_all + warp * S::PBUF; // p[head slot][row], head stride PSTR
-    const int rbase = warp * 16;
+    const int gq = lane >> 2, tq = lane & 3;
+    // ---- query fragments (B operand of QK), hi + lo fp16, built once by warp 0
+    if (warp == 0) {
+        const bool hq = gq < r_act; // head slot this lane feeds into the MMA B operand
+        const float *qrow = p.q + ((int64_t)sq.out_row * p.H + (int64_t)g * r_act + (hq ? gq : 0)) * D;
+        float qv[S::KSTEPS][4];
+        float amax = 0.0f;
+#pragma unroll
+        for (int ks = 0; ks < S::KSTEPS; ++ks) {
+            int d0, d1;
+            if constexpr (S::Q8) {
+                d0 = 16 * ks + 4 * tq;
+                d1 = d0 + 2;
+            } else {
+                d0 = 16 * ks + 2 * tq;
+                d1 = d0 + 8;
+            }
+            float2 x0 = hq ? *reinterpret_cast<const float2 *>(qrow + d0) : make_float2(0.f, 0.f);
+            float2 x1 = hq ? *reinterpret_cast<const float2 *>(qrow + d1) : make_float2(0.f, 0.f);
+            qv[ks][0] = x0.x * p.kq_scale_log2;
+            qv[ks][1] = x0.y * p.kq_scale_log2;
+            qv[ks][2] = x1.x * p.kq_scale_log2;
+            qv[ks][3] = x1.y * p.kq_scale_log2;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fabsf(qv[ks][j]));
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        // power-of-two scaling that puts max|q| in [2^13, 2^14): hi and lo stay normal fp16
+        const int e_q = (amax > 0.0f) ? 13 - ilogbf(amax) : 0;
+#pragma unroll
+        for (int ks = 0; ks < S::KSTEPS; ++ks) {
+            uint32_t bh[2], bl[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float x0 = ldexpf(qv[ks][2 * j], e_q), x1 = ldexpf(qv[ks][2 * j + 1], e_q);
+                const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+                const __half l0 = __float2half_rn(x0 - __half2float(h0)), l1 = __float2half_rn(x1 - __half2float(h1));
+                bh[j] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+                bl[j] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+            }
+            qfs[ks * 32 + lane] = make_uint4(bh[0], bh[1], bl[0], bl[1]);
+        }
+        if (tq == 0) shs[gq] = ldexpf(1.0f, -e_q);
+    }
+    __syncthreads();
 
-    for (int k = 0; k < n_tiles; ++k) {
+    if (warp == W) {
+        // the load warp: refill each stage as soon as its group has released it
+        if (lane == 0) {
+            for (int k = S::STAGES; k < n_tiles; ++k) {
+                const int s = k % S::STAGES;
+                if (!mbar_wait(&empty[s], ((k / S::STAGES) - 1) & 1, p.err)) break;
+                issue(k);
+            }
+        }
+    } else {
+
+    // 2^-e for the two heads (2t, 2t+1) whose scores this lane accumulates
+    const float hs0 = shs[2 * tq], hs1 = shs[2 * tq + 1];
+    const bool hv0 = 2 * tq < r_act, hv1 = 2 * tq + 1 < r_act;
+
+    // ---- per-warp state -------------------------------------------------------
+    // softmax state of heads 2t, 2t+1; PV accumulators O^T[dims][heads] as
+    // m16n8 fragments (rows = dims, columns = heads 2t, 2t+1)
+    float *pw = pbuf_all + warp * S::PBUF; // p[head slot][row], head stride PSTR
+    const int rbase = (warp % S::GW) * 16;  // this warp's rows in a tile of its group
+
+    for (int k = warp / S::GW; k < n_tiles; k += S::G) {
         const int s = k % S::STAGES;
         if (!mbar_wait(&full[s], (k / S::STAGES) & 1, p.err)) break;
         const uint8_t *st = stages + s * S::STAGE;
@@ -430,12 +451,13 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
                     uint32_t a0, a1, a2, a3;
                     codes_to_half2(r0, a0, a2);
                     codes_to_half2(r1, a1, a3);
-                    mma16816(c, a0, a1, a2, a3, bh[2 * b][0], bh[2 * b][1]);
-                    mma16816(c, a0, a1, a2, a3, bl[2 * b][0], bl[2 * b][1]);
+                    const uint4 qa = qfs[(2 * b) * 32 + lane], qb = qfs[(2 * b + 1) * 32 + lane];
+                    mma16816(c, a0, a1, a2, a3, qa.x, qa.y);
+                    mma16816(c, a0, a1, a2, a3, qa.z, qa.w);
                     codes_to_half2(r2, a0, a2);
                     codes_to_half2(r3, a1, a3);
-                    mma16816(c, a0, a1, a2, a3, bh[2 * b + 1][0], bh[2 * b + 1][1]);
-                    mma16816(c, a0, a1, a2, a3, bl[2 * b + 1][0], bl[2 * b + 1][1]);
+                    mma16816(c, a0, a1, a2, a3, qb.x, qb.y);
+                    mma16816(c, a0, a1, a2, a3, qb.z, qb.w);
                     const float da = half_at(kw[0], b), db = half_at(kw[1], b);
                     sc[0] = fmaf(da, c[0], sc[0]);
                     sc[1] = fmaf(da, c[1], sc[1]);
@@ -448,8 +470,9 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
                 for (int ks = 0; ks < S::KSTEPS; ++ks) {
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4(st + (ks / 4) * T * 128 + swz<128>(lrow, 2 * (ks % 4) + (lane >> 4)), a0, a1, a2, a3);
-                    mma16816(sc, a0, a1, a2, a3, bh[ks][0], bh[ks][1]);
-                    mma16816(sc, a0, a1, a2, a3, bl[ks][0], bl[ks][1]);
+                    const uint4 qk = qfs[ks * 32 + lane];
+                    mma16816(sc, a0, a1, a2, a3, qk.x, qk.y);
+                    mma16816(sc, a0, a1, a2, a3, qk.z, qk.w);
                 }
             }
             // log2-domain scores; rows beyond the tile are -inf
@@ -587,15 +610,9 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
         }
         // release the stage; the last warp done with it loads tile k + STAGES into it
         __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(&empty[s]); // release: this warp's reads of the stage are complete
-            if (atomicAdd(&s_cnt[s], 1) == W - 1) {
-                s_cnt[s] = 0;
-                const int kn = k + S::STAGES;
-                if (kn < n_tiles && mbar_wait(&empty[s], (k / S::STAGES) & 1, p.err)) issue(kn);
-            }
-        }
+        if (lane == 0) mbar_arrive(&empty[s]); // release: this warp's reads of the stage are complete
     }
+    } // compute warps
     __syncthreads();
 
     // ---- CTA merge of the warps (stages are free now) -------------------------
@@ -606,22 +623,24 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::W * 32, Shape<TYPE, D, R>::
     float *wm = reinterpret_cast<float *>(wf + W * FRAG);      // [W][8]
     float *wl = wm + W * 8;                                     // [W][8]
     float *wus = wl + W * 8;                                    // [W]
+    if (warp < W) {
 #pragma unroll
-    for (int mt = 0; mt < S::NMT; ++mt)
-        wf[(warp * S::NMT + mt) * 32 + lane] = make_float4(acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3]);
-    // row sums: lanes gq = 0..7 hold different rows of the same heads
+        for (int mt = 0; mt < S::NMT; ++mt)
+            wf[(warp * S::NMT + mt) * 32 + lane] = make_float4(acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3]);
+        // row sums: lanes gq = 0..7 hold different rows of the same heads
 #pragma unroll
-    for (int m = 4; m < 32; m <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, m);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, m);
+        for (int m = 4; m < 32; m <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, m);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, m);
+        }
+        if (gq == 0) {
+            wm[warp * 8 + 2 * tq] = m0;
+            wm[warp * 8 + 2 * tq + 1] = m1;
+            wl[warp * 8 + 2 * tq] = l0;
+            wl[warp * 8 + 2 * tq + 1] = l1;
+        }
+        if (lane == 0) wus[warp] = have_s ? ldexpf(1.f, -sexp) : 0.f;
     }
-    if (gq == 0) {
-        wm[warp * 8 + 2 * tq] = m0;
-        wm[warp * 8 + 2 * tq + 1] = m1;
-        wl[warp * 8 + 2 * tq] = l0;
-        wl[warp * 8 + 2 * tq + 1] = l1;
-    }
-    if (lane == 0) wus[warp] = have_s ? ldexpf(1.f, -sexp) : 0.f;
     __syncthreads();
 
     const int n_chunks = sq.n_chunks;
@@ -783,7 +802,7 @@ cudaError_t launch_t(const AttnParams &p, const CUtensorMap *tmk, const CUtensor
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.total_chunks, p.Hk);
-    cfg.blockDim = dim3(S::W * 32);
+    cfg.blockDim = dim3(S::NTHREADS);
     cfg.dynamicSmemBytes = S::SMEM;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -807,7 +826,7 @@ int occupancy() {
     using S = Shape<TYPE, D, R>;
     int n = 0;
     cudaFuncSetAttribute(attn_kernel<TYPE, D, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<TYPE, D, R>, S::W * 32, S::SMEM) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<TYPE, D, R>, S::NTHREADS, S::SMEM) !=
         cudaSuccess) {
         cudaGetLastError();
         return 1;
