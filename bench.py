@@ -368,7 +368,7 @@ def attn_only_gbs(kvc, torch, dev, type_: str, n: int, reps: int = 50):
         cache.close()
 
 
-def ragged(kvc, torch, dev, type_: str, reps: int = 20):
+def ragged(kvc, torch, dev, type_: str, reps: int = 60):
     """32 sequences, lengths uniform in [1024, 32768] (seed 0), 32/8 heads,
     D 128, one layer; one attention call over the whole batch."""
     from kv_cache_decode_flash_gb300 import synth
@@ -387,7 +387,7 @@ def ragged(kvc, torch, dev, type_: str, reps: int = 20):
         q = torch.randn(32, Hq, D, device=dev)
         o = torch.empty_like(q)
         ids = list(range(32))
-        for _ in range(3):
+        for _ in range(10):
             cache.attn_decode(0, ids, q, o, 0.088)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -160,6 +160,11 @@ __device__ __forceinline__ float half_at(const uint32_t (&w)[N], int b) {
     return __half2float(__ushort_as_half((uint16_t)(w[b >> 1] >> (16 * (b & 1)))));
 }
 
+// 2^e for e in [-126, 127] (exact, from the exponent bits).
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) << 23); }
+// floor(log2 x) of a positive normal float (its unbiased exponent).
+__device__ __forceinline__ int ilogb_normal(float x) { return ((__float_as_int(x) >> 23) & 0xff) - 127; }
+
 // Slack of the lazily raised softmax maximum (log2 units): probabilities stay
 // below 2^RESCALE_SLACK between raises.
 constexpr int RESCALE_SLACK = 8;
@@ -529,12 +534,13 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
                 wm = __vmaxu2(wm, __shfl_xor_sync(0xffffffffu, wm, 2));
                 const float dmax = __half2float(__ushort_as_half((uint16_t)max(wm & 0xffffu, wm >> 16)));
                 // 2^S * max(p * d) < 2^15 with p <= 2^RESCALE_SLACK: hi and lo of P' stay in fp16 range
-                s_tile = (dmax > 0.f) ? 14 - RESCALE_SLACK - ilogbf(dmax) : (have_s ? sexp : 0);
+                // dmax is an fp16 value: a normal float in [2^-24, 2^16), so S stays in [-9, 30]
+                s_tile = (dmax > 0.f) ? 14 - RESCALE_SLACK - ilogb_normal(dmax) : (have_s ? sexp : 0);
             }
             const int s_new = have_s ? min(sexp, s_tile) : s_tile;
             // rescale the accumulators: the softmax maxima moved and/or S decreased
             if (raise || s_new != sexp || !have_s) {
-                const float sf = have_s ? ldexpf(1.f, s_new - sexp) : 1.f;
+                const float sf = have_s ? pow2i(s_new - sexp) : 1.f;
                 const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1); // 0 while m is -inf
                 const float f0 = al0 * sf, f1 = al1 * sf;
 #pragma unroll
@@ -550,7 +556,7 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
                 m1 = mn1;
             }
             // per-lane partial row sums, in the same 2^S domain as the accumulators
-            const float ps = ldexpf(1.f, s_new);
+            const float ps = pow2i(s_new);
             l0 = fmaf(pr[0] + pr[2], ps, l0);
             l1 = fmaf(pr[1] + pr[3], ps, l1);
             sexp = s_new;
@@ -639,7 +645,7 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
             wl[warp * 8 + 2 * tq] = l0;
             wl[warp * 8 + 2 * tq + 1] = l1;
         }
-        if (lane == 0) wus[warp] = have_s ? ldexpf(1.f, -sexp) : 0.f;
+        if (lane == 0) wus[warp] = have_s ? pow2i(-sexp) : 0.f;
     }
     __syncthreads();
 
