@@ -616,6 +616,8 @@ def run_ours(args, rank: int, world: int):
     if rank == 0 and not args.no_extra:
         ex = {}
         for name, fn in (("q8_0_4k", lambda: attn_only_gbs(kvc, torch, dev, "q8_0", 4096)),
+                         ("q8_0_64k", lambda: attn_only_gbs(kvc, torch, dev, "q8_0", 65536)),
+                         ("q8_0_256k", lambda: attn_only_gbs(kvc, torch, dev, "q8_0", 262144)),
                          ("f16_16k", lambda: attn_only_gbs(kvc, torch, dev, "f16", 16384)),
                          ("f16_4k", lambda: attn_only_gbs(kvc, torch, dev, "f16", 4096)),
                          ("ragged_q8_0", lambda: ragged(kvc, torch, dev, "q8_0")),
