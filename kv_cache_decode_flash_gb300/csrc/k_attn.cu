@@ -274,6 +274,15 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if constexpr (S::Q8) {
+        // Scale bytes past a tile's rows are never copied into: start them at 0
+        // (finite), so those rows' products stay 0 without masking
+        for (int i = tid; i < S::STAGES * (2 * S::SCALE_BUF / 16); i += NT) {
+            const int st_i = i / (2 * S::SCALE_BUF / 16), off = i % (2 * S::SCALE_BUF / 16);
+            reinterpret_cast<uint4 *>(stages + st_i * S::STAGE + S::KBYTES + S::VBYTES)[off] = make_uint4(0, 0, 0, 0);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); // before the bulk copies write there
+    }
     __syncthreads();
     const int n_tiles = s_flag;
     if (warp == 0)
@@ -420,7 +429,6 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
 
     // 2^-e for the two heads (2t, 2t+1) whose scores this lane accumulates
     const float hs0 = shs[2 * tq], hs1 = shs[2 * tq + 1];
-    const bool hv0 = 2 * tq < r_act, hv1 = 2 * tq + 1 < r_act;
 
     // ---- per-warp state -------------------------------------------------------
     // softmax state of heads 2t, 2t+1; PV accumulators O^T[dims][heads] as
@@ -504,10 +512,11 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
                 mn1 = fmaxf(m1, t1);
             }
             float pr[4];
-            pr[0] = hv0 ? ex2(s2v[0] - mn0) : 0.f;
-            pr[1] = hv1 ? ex2(s2v[1] - mn1) : 0.f;
-            pr[2] = hv0 ? ex2(s2v[2] - mn0) : 0.f;
-            pr[3] = hv1 ? ex2(s2v[3] - mn1) : 0.f;
+            // (head slots past the group have q = 0 and feed only columns that are never read)
+            pr[0] = ex2(s2v[0] - mn0);
+            pr[1] = ex2(s2v[1] - mn1);
+            pr[2] = ex2(s2v[2] - mn0);
+            pr[3] = ex2(s2v[3] - mn1);
             // probabilities to [head][row] for the PV B operand
             pw[(2 * tq) * S::PSTR + gq] = pr[0];
             pw[(2 * tq + 1) * S::PSTR + gq] = pr[1];
@@ -522,13 +531,11 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
                 uint32_t wm = 0;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
+                    // rows past the tile hold finite stale scales (or 0): their p is 0, and
+                    // the range exponent may only come out smaller than needed (safe)
                     load_scales<S::NB>(vsb + rr[i] * S::SB, vw[i]);
-                    // rows past the tile may hold stale bytes: their scales count as 0
 #pragma unroll
-                    for (int h = 0; h < S::NB / 2; ++h) {
-                        vw[i][h] = (rr[i] < rows_w) ? vw[i][h] : 0u;
-                        wm = __vmaxu2(wm, vw[i][h]); // non-negative fp16: integer order
-                    }
+                    for (int h = 0; h < S::NB / 2; ++h) wm = __vmaxu2(wm, vw[i][h]); // fp16 >= 0: integer order
                 }
                 wm = __vmaxu2(wm, __shfl_xor_sync(0xffffffffu, wm, 1));
                 wm = __vmaxu2(wm, __shfl_xor_sync(0xffffffffu, wm, 2));
