@@ -232,6 +232,9 @@ static RunCopyArgs payload_args(const Ctx *c, int64_t n, uint8_t *payload, bool 
     RunCopyArgs a = pool_args(c);
     a.payload = payload;
     a.to_payload = to_payload ? 1 : 0;
+    // the state format carries plain int8 codes
+    a.flip[0] = c->tk == KVC_Q8_0 ? CODE_FLIP : 0u;
+    a.flip[1] = c->tv == KVC_Q8_0 ? CODE_FLIP : 0u;
     const int64_t ks = section_bytes(c, c->tk, n);
     a.layer_bytes = ks + section_bytes(c, c->tv, n);
     a.toff[0] = 0;

@@ -72,10 +72,10 @@ __device__ __forceinline__ void store_tensor(int type, const TensorView &tv, int
         if constexpr (EPL == 4) {
             uint32_t w = (uint32_t)(uint8_t)q[0] | ((uint32_t)(uint8_t)q[1] << 8) |
                          ((uint32_t)(uint8_t)q[2] << 16) | ((uint32_t)(uint8_t)q[3] << 24);
-            reinterpret_cast<uint32_t *>(row)[lane] = w;
+            reinterpret_cast<uint32_t *>(row)[lane] = w ^ CODE_FLIP; // stored offset binary
         } else {
             uint16_t w = (uint16_t)((uint16_t)(uint8_t)q[0] | ((uint16_t)(uint8_t)q[1] << 8));
-            reinterpret_cast<uint16_t *>(row)[lane] = w;
+            reinterpret_cast<uint16_t *>(row)[lane] = (uint16_t)(w ^ (CODE_FLIP & 0xffffu)); // offset binary
         }
         if ((lane % LPB) == 0) tv.scales[R * (D / QK) + lane / LPB] = __half_as_ushort(__float2half_rn(d));
     } else {

@@ -89,11 +89,13 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Four int8 codes -> two half2 of their exact values: (c0,c1) and (c2,c3).
-// Bytes are flipped to offset binary u = c + 128 and placed in the low
-// mantissa byte of 0x64xx (= 1024 + u); subtracting 1152 gives c exactly.
+// Four codes -> two half2 of their exact values: (c0,c1) and (c2,c3).  The
+// offset-binary bytes u = c + 128 go into the low mantissa byte of 0x64xx
+// (= 1024 + u); subtracting 1152 gives c exactly.  RAW: the word holds plain
+// int8 codes, flipped to offset binary first.
+template <bool RAW>
 __device__ __forceinline__ void codes_to_half2(uint32_t w, uint32_t &h01, uint32_t &h23) {
-    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t u = RAW ? (w ^ CODE_FLIP) : w;
     asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(h01) : "r"(u), "r"(0x64646464u));
     asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(h23) : "r"(u), "r"(0x64646464u));
     const uint32_t bias = 0x64806480u; // half2(1152, 1152)
@@ -135,8 +137,9 @@ __device__ __forceinline__ void split_pack(float x0, float x1, uint32_t &hi, uin
 // A transposed V word holds codes (row 2t, dim 2g), (row 2t, dim 2g+1),
 // (row 2t+1, dim 2g), (row 2t+1, dim 2g+1); return the exact half2 of the
 // even dim (rows 2t, 2t+1) and of the odd dim.
+template <bool RAW>
 __device__ __forceinline__ void vcodes_to_half2(uint32_t w, uint32_t &ev, uint32_t &od) {
-    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t u = RAW ? (w ^ CODE_FLIP) : w;
     asm("prmt.b32 %0, %1, %2, 0x5240;" : "=r"(ev) : "r"(u), "r"(0x64646464u));
     asm("prmt.b32 %0, %1, %2, 0x5341;" : "=r"(od) : "r"(u), "r"(0x64646464u));
     const uint32_t bias = 0x64806480u; // half2(1152, 1152)
@@ -225,7 +228,7 @@ struct TileInfo {
     int delta; // scale rows skipped by the 16-byte alignment of the scale copy
 };
 
-template <int TYPE, int D, int R>
+template <int TYPE, int D, int R, bool RAW = false>
 __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmk,
                 const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmkb,
@@ -462,13 +465,13 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
                     ldsm_x4(st + swz<S::KROW>(lm_row, 2 * b + lm_hi), r0, r1, r2, r3);
                     float c[4] = {0.f, 0.f, 0.f, 0.f};
                     uint32_t a0, a1, a2, a3;
-                    codes_to_half2(r0, a0, a2);
-                    codes_to_half2(r1, a1, a3);
+                    codes_to_half2<RAW>(r0, a0, a2);
+                    codes_to_half2<RAW>(r1, a1, a3);
                     const uint4 qa = qfs[(2 * b) * 32 + lane], qb = qfs[(2 * b + 1) * 32 + lane];
                     mma16816(c, a0, a1, a2, a3, qa.x, qa.y);
                     mma16816(c, a0, a1, a2, a3, qa.z, qa.w);
-                    codes_to_half2(r2, a0, a2);
-                    codes_to_half2(r3, a1, a3);
+                    codes_to_half2<RAW>(r2, a0, a2);
+                    codes_to_half2<RAW>(r3, a1, a3);
                     mma16816(c, a0, a1, a2, a3, qb.x, qb.y);
                     mma16816(c, a0, a1, a2, a3, qb.z, qb.w);
                     const float da = half_at(kw[0], b), db = half_at(kw[1], b);
@@ -598,10 +601,10 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
                     // v0: rows 0-7 / bytes 0-15, v1: rows 8-15 / bytes 0-15,
                     // v2: rows 0-7 / bytes 16-31, v3: rows 8-15 / bytes 16-31 of block b
                     uint32_t e0, e1, e2, e3, o0, o1, o2, o3;
-                    vcodes_to_half2(v0, e0, o0);
-                    vcodes_to_half2(v2, e1, o1);
-                    vcodes_to_half2(v1, e2, o2);
-                    vcodes_to_half2(v3, e3, o3);
+                    vcodes_to_half2<RAW>(v0, e0, o0);
+                    vcodes_to_half2<RAW>(v2, e1, o1);
+                    vcodes_to_half2<RAW>(v1, e2, o2);
+                    vcodes_to_half2<RAW>(v3, e3, o3);
                     mma16816(acc[2 * b], e0, e1, e2, e3, b0h, b1h);
                     mma16816(acc[2 * b], e0, e1, e2, e3, b0l, b1l);
                     mma16816(acc[2 * b + 1], o0, o1, o2, o3, b0h, b1h);
@@ -802,13 +805,13 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
     }
 }
 
-template <int TYPE, int D, int R>
+template <int TYPE, int D, int R, bool RAW = false>
 cudaError_t launch_t(const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv, cudaStream_t st) {
     // tmk / tmv point at {16-row map, 128-row map} pairs
     using S = Shape<TYPE, D, R>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_kernel<TYPE, D, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(attn_kernel<TYPE, D, R, RAW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              S::SMEM);
         if (e != cudaSuccess) return e;
         configured = true;
@@ -823,11 +826,15 @@ cudaError_t launch_t(const AttnParams &p, const CUtensorMap *tmk, const CUtensor
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_kernel<TYPE, D, R>, p, tmk[0], tmv[0], tmk[1], tmv[1]);
+    return cudaLaunchKernelEx(&cfg, attn_kernel<TYPE, D, R, RAW>, p, tmk[0], tmv[0], tmk[1], tmv[1]);
 }
 
 template <int TYPE, int D>
-cudaError_t launch_d(const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv, cudaStream_t st) {
+cudaError_t launch_d(const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv, cudaStream_t st,
+                     bool raw) {
+    // plain int8 codes (caller buffers): one instance for every group size up to 8
+    if constexpr (TYPE == KVC_Q8_0)
+        if (raw) return p.r <= 8 ? launch_t<TYPE, D, 8, true>(p, tmk, tmv, st) : cudaErrorInvalidValue;
     if (p.r <= 4) return launch_t<TYPE, D, 4>(p, tmk, tmv, st);
     if (p.r == 5) return launch_t<TYPE, D, 5>(p, tmk, tmv, st);
     if (p.r <= 8) return launch_t<TYPE, D, 8>(p, tmk, tmv, st);
@@ -879,13 +886,13 @@ int attn_merge_cap(int type, int D, int r) {
 }
 
 cudaError_t launch_attn(int type, const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv,
-                        cudaStream_t st) {
+                        cudaStream_t st, bool raw_codes) {
     if (type == KVC_Q8_0) {
-        if (p.D == 128) return launch_d<KVC_Q8_0, 128>(p, tmk, tmv, st);
-        if (p.D == 64) return launch_d<KVC_Q8_0, 64>(p, tmk, tmv, st);
+        if (p.D == 128) return launch_d<KVC_Q8_0, 128>(p, tmk, tmv, st, raw_codes);
+        if (p.D == 64) return launch_d<KVC_Q8_0, 64>(p, tmk, tmv, st, raw_codes);
     } else {
-        if (p.D == 128) return launch_d<KVC_F16, 128>(p, tmk, tmv, st);
-        if (p.D == 64) return launch_d<KVC_F16, 64>(p, tmk, tmv, st);
+        if (p.D == 128) return launch_d<KVC_F16, 128>(p, tmk, tmv, st, false);
+        if (p.D == 64) return launch_d<KVC_F16, 64>(p, tmk, tmv, st, false);
     }
     return cudaErrorInvalidValue;
 }

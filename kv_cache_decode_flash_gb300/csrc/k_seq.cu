@@ -21,8 +21,13 @@ namespace {
 
 // Copy `bytes` (a multiple of sizeof(T)) with the CTA's threads; each
 // thread has U loads in flight before its stores.
+__device__ __forceinline__ uint4 flip_bits(uint4 v, uint32_t m) { return make_uint4(v.x ^ m, v.y ^ m, v.z ^ m, v.w ^ m); }
+__device__ __forceinline__ uint2 flip_bits(uint2 v, uint32_t m) { return make_uint2(v.x ^ m, v.y ^ m); }
+__device__ __forceinline__ uint32_t flip_bits(uint32_t v, uint32_t m) { return v ^ m; }
+__device__ __forceinline__ uint8_t flip_bits(uint8_t v, uint32_t m) { return (uint8_t)(v ^ (m & 255u)); }
+
 template <typename T, int U>
-__device__ __forceinline__ void copy_vec(const uint8_t *src, uint8_t *dst, int64_t bytes) {
+__device__ __forceinline__ void copy_vec(const uint8_t *src, uint8_t *dst, int64_t bytes, uint32_t flip = 0) {
     const T *s = reinterpret_cast<const T *>(src);
     T *d = reinterpret_cast<T *>(dst);
     const int64_t n = bytes / (int64_t)sizeof(T);
@@ -31,7 +36,7 @@ __device__ __forceinline__ void copy_vec(const uint8_t *src, uint8_t *dst, int64
         T v[U];
 #pragma unroll
         for (int u = 0; u < U; ++u)
-            if (i0 + u * blockDim.x < n) v[u] = s[i0 + u * blockDim.x];
+            if (i0 + u * blockDim.x < n) v[u] = flip_bits(s[i0 + u * blockDim.x], flip);
 #pragma unroll
         for (int u = 0; u < U; ++u)
             if (i0 + u * blockDim.x < n) d[i0 + u * blockDim.x] = v[u];
@@ -53,14 +58,15 @@ __global__ void __launch_bounds__(256) copy_runs_kernel(const __grid_constant__ 
     uint8_t *dst = (a.payload && !a.to_payload) ? pool : other;
     const int64_t bytes = (int64_t)rn.n * rb;
     const uintptr_t al = (uintptr_t)src | (uintptr_t)dst | (uintptr_t)bytes;
+    const uint32_t flip = a.flip[t];
     if ((al & 15) == 0)
-        copy_vec<uint4, 4>(src, dst, bytes);
+        copy_vec<uint4, 4>(src, dst, bytes, flip);
     else if ((al & 7) == 0)
-        copy_vec<uint2, 4>(src, dst, bytes);
+        copy_vec<uint2, 4>(src, dst, bytes, flip);
     else if ((al & 3) == 0)
-        copy_vec<uint32_t, 4>(src, dst, bytes);
+        copy_vec<uint32_t, 4>(src, dst, bytes, flip);
     else
-        copy_vec<uint8_t, 4>(src, dst, bytes);
+        copy_vec<uint8_t, 4>(src, dst, bytes, flip);
 }
 
 struct RopeArgs {
@@ -72,16 +78,17 @@ struct RopeArgs {
     float2 cs[64]; // (cos, sin) of delta * theta_i, i < D/2
 };
 
-__device__ __forceinline__ float code_at(const uint4 &w, int i) { // int8 code i of 16
+__device__ __forceinline__ float code_at(const uint4 &w, int i) { // code i of 16 stored offset binary
     const uint32_t u = i < 4 ? w.x : i < 8 ? w.y : i < 12 ? w.z : w.w;
-    return (float)(int8_t)(u >> (8 * (i & 3)));
+    return (float)((int)((u >> (8 * (i & 3))) & 255u) - 128);
 }
 __device__ __forceinline__ uint4 pack16(const int (&c)[16]) {
     uint32_t u[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-        u[j] = (uint32_t)(c[4 * j] & 255) | ((uint32_t)(c[4 * j + 1] & 255) << 8) |
-               ((uint32_t)(c[4 * j + 2] & 255) << 16) | ((uint32_t)(c[4 * j + 3] & 255) << 24);
+        u[j] = ((uint32_t)(c[4 * j] & 255) | ((uint32_t)(c[4 * j + 1] & 255) << 8) |
+                ((uint32_t)(c[4 * j + 2] & 255) << 16) | ((uint32_t)(c[4 * j + 3] & 255) << 24)) ^
+               CODE_FLIP; // stored offset binary
     return make_uint4(u[0], u[1], u[2], u[3]);
 }
 

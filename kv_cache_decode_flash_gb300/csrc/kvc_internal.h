@@ -13,6 +13,12 @@
 namespace kvc {
 
 constexpr int QK = 32;                 // elements per q8_0 block
+// q8_0 code bytes in device pools, host stores and staging slots are offset
+// binary: the byte holds code + 128 (the int8 code with its top bit flipped),
+// which the attention kernel turns into fp16 without a separate flip.  The
+// state format and the no-alloc entry point's caller buffers carry plain int8
+// codes; copies between the two flip the top bit of every code byte.
+constexpr uint32_t CODE_FLIP = 0x80808080u;
 constexpr int MAX_SEQ_PER_LAUNCH = 64; // sequences carried in one attention launch
 constexpr int MAX_GROUP = 8;           // query heads per KV head supported by the attention kernel
 constexpr int TMA_BOX_ROWS = 16;       // rows per small TMA box
@@ -68,8 +74,9 @@ struct AttnParams {
 // Launch the decode attention kernel for one layer.  tmk / tmv each point at
 // a pair of maps over the same rows: boxes of TMA_BOX_ROWS rows, then of
 // TMA_BIG_ROWS rows.
+// raw_codes: q8_0 codes are plain int8 (caller buffers) instead of offset binary.
 cudaError_t launch_attn(int type, const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv,
-                        cudaStream_t st);
+                        cudaStream_t st, bool raw_codes = false);
 int attn_ctas_per_sm(int type, int D, int r);
 int attn_merge_cap(int type, int D, int r); // most chunks per (sequence, kv head) one merge can take
 size_t attn_partial_floats(int r, int D); // floats per (chunk, kv head) partial
@@ -110,6 +117,7 @@ struct RunCopyArgs {
     int64_t layer_bytes; // payload bytes of one layer
     int64_t toff[4];     // offset of each tensor inside a payload layer
     int32_t to_payload;  // payload copies: 1 pool -> payload, 0 payload -> pool
+    uint32_t flip[4];    // XOR applied to every 4 bytes copied (offset-binary <-> int8 codes)
     int32_t l0;          // first layer
 };
 cudaError_t launch_copy_runs(const RunCopyArgs &a, const RowRun *runs_dev, int64_t n_runs, int n_layers,
