@@ -767,36 +767,25 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
     }
     __syncthreads();
     const float *sp = reinterpret_cast<const float *>(stg);
-    float *cw = reinterpret_cast<float *>(stg + items); // [n_chunks][R] weights
-    for (int h = warp; h < r_act; h += W) {
-        float M = -INFINITY;
-        for (int c = lane; c < n_chunks; c += 32) M = fmaxf(M, sp[c * S::PF + h]);
-#pragma unroll
-        for (int m = 16; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
-        float L = 0.f;
-        for (int c = lane; c < n_chunks; c += 32) {
-            const float f = (M == -INFINITY) ? 0.f : ex2(sp[c * S::PF + h] - M);
-            cw[c * R + h] = f;
-            L += f * sp[c * S::PF + R + h];
-        }
-        // fixed-order tree: the same bits on every call
-#pragma unroll
-        for (int m = 16; m > 0; m >>= 1) L += __shfl_xor_sync(0xffffffffu, L, m);
-        if (lane == 0) s_L[h] = L;
-    }
-    __syncthreads();
+    // every output column weighs the chunks itself (max, then weights and sums in
+    // chunk order: the same bits on every call), with no further barrier
     for (int col = tid; col < r_act * (D / 4); col += NT) {
         const int h = col / (D / 4), i4 = col % (D / 4);
+        float M = -INFINITY;
+        for (int c = 0; c < n_chunks; ++c) M = fmaxf(M, sp[c * S::PF + h]);
         float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c = 0; c < n_chunks; ++c) {
-            const float w = cw[c * R + h];
-            const float4 v = *reinterpret_cast<const float4 *>(sp + c * S::PF + S::OOFF + h * D + 4 * i4);
-            O.x += w * v.x;
-            O.y += w * v.y;
-            O.z += w * v.z;
-            O.w += w * v.w;
+        float L = 0.f;
+        if (M != -INFINITY) {
+            for (int c = 0; c < n_chunks; ++c) {
+                const float w = ex2(sp[c * S::PF + h] - M);
+                const float4 v = *reinterpret_cast<const float4 *>(sp + c * S::PF + S::OOFF + h * D + 4 * i4);
+                L = fmaf(w, sp[c * S::PF + R + h], L);
+                O.x = fmaf(w, v.x, O.x);
+                O.y = fmaf(w, v.y, O.y);
+                O.z = fmaf(w, v.z, O.z);
+                O.w = fmaf(w, v.w, O.w);
+            }
         }
-        const float L = s_L[h];
         float *dst = outp + h * D + 4 * i4;
         dst[0] = (L > 0.f) ? O.x / L : 0.f;
         dst[1] = (L > 0.f) ? O.y / L : 0.f;
