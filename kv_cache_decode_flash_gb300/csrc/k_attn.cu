@@ -248,8 +248,6 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
     uint4 *qfs = reinterpret_cast<uint4 *>(((uintptr_t)(s_tpage + S::MAXT) + 15) & ~(uintptr_t)15);
     float *shs = reinterpret_cast<float *>(qfs + S::KSTEPS * 32); // 2^-e of each head slot
     __shared__ int s_flag;
-    __shared__ float s_M[R], s_L[R];
-    __shared__ float s_ww[W * 8]; // per-warp merge weights [warp][head]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = blockIdx.y;
@@ -662,41 +660,32 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
     const int n_chunks = sq.n_chunks;
     float *part = p.part + ((int64_t)chunk * p.Hk + g) * S::PF;
     float *outp = p.out + ((int64_t)sq.out_row * p.H + (int64_t)g * r_act) * D;
-    // per-head weights of the warps (softmax rescale; the P' scale only weighs O):
-    // one warp per head, one lane per warp of the CTA
-    for (int h = warp; h < r_act; h += W) {
-        const float mw = (lane < W) ? wm[lane * 8 + h] : -INFINITY;
-        float M = mw;
-#pragma unroll
-        for (int m = 16; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
-        // O and l of a warp are both in its 2^S domain: one weight for both
-        const float f = (lane < W && M != -INFINITY) ? ex2(mw - M) * wus[lane] : 0.f;
-        if (lane < W) s_ww[lane * 8 + h] = f;
-        float L = (lane < W) ? wl[lane * 8 + h] * f : 0.f;
-#pragma unroll
-        for (int m = 16; m > 0; m >>= 1) L += __shfl_xor_sync(0xffffffffu, L, m);
-        if (lane == 0) {
-            s_M[h] = M;
-            s_L[h] = L;
-            if (n_chunks > 1) {
-                part[h] = M;
-                part[R + h] = L;
-            }
-        }
-    }
-    __syncthreads();
-    // fragment (mt, ln): heads 2t, 2t+1 of lane ln, dims of rows g and g+8
+    // fragment (mt, ln): heads 2t, 2t+1 of lane ln, dims of rows g and g+8.  Each
+    // fragment weighs the warps itself (softmax rescale and the warp's 2^-S: O
+    // and l of a warp share its 2^S domain), in warp order, with no barrier.
     for (int it = tid; it < FRAG; it += NT) {
         const int mt = it / 32, ln = it % 32, fg = ln >> 2, ft = ln & 3;
-        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int h0 = 2 * ft, h1 = 2 * ft + 1;
+        float M0 = -INFINITY, M1 = -INFINITY;
 #pragma unroll
         for (int w = 0; w < W; ++w) {
+            M0 = fmaxf(M0, wm[w * 8 + h0]);
+            M1 = fmaxf(M1, wm[w * 8 + h1]);
+        }
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        float L0 = 0.f, L1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            const float us = wus[w];
+            const float f0 = (M0 == -INFINITY) ? 0.f : ex2(wm[w * 8 + h0] - M0) * us;
+            const float f1 = (M1 == -INFINITY) ? 0.f : ex2(wm[w * 8 + h1] - M1) * us;
             const float4 v = wf[(w * S::NMT + mt) * 32 + ln];
-            const float f0 = s_ww[w * 8 + 2 * ft], f1 = s_ww[w * 8 + 2 * ft + 1];
-            O.x += f0 * v.x;
-            O.y += f1 * v.y;
-            O.z += f0 * v.z;
-            O.w += f1 * v.w;
+            O.x = fmaf(f0, v.x, O.x);
+            O.y = fmaf(f1, v.y, O.y);
+            O.z = fmaf(f0, v.z, O.z);
+            O.w = fmaf(f1, v.w, O.w);
+            L0 = fmaf(f0, wl[w * 8 + h0], L0);
+            L1 = fmaf(f1, wl[w * 8 + h1], L1);
         }
         int dA, dB;
         if constexpr (S::Q8) {
@@ -706,17 +695,14 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
             dA = 16 * mt + fg;
             dB = dA + 8;
         }
-        const int h0 = 2 * ft, h1 = 2 * ft + 1;
         if (n_chunks == 1) {
             if (h0 < r_act) {
-                const float L = s_L[h0];
-                outp[h0 * D + dA] = (L > 0.f) ? O.x / L : 0.f;
-                outp[h0 * D + dB] = (L > 0.f) ? O.z / L : 0.f;
+                outp[h0 * D + dA] = (L0 > 0.f) ? O.x / L0 : 0.f;
+                outp[h0 * D + dB] = (L0 > 0.f) ? O.z / L0 : 0.f;
             }
             if (h1 < r_act) {
-                const float L = s_L[h1];
-                outp[h1 * D + dA] = (L > 0.f) ? O.y / L : 0.f;
-                outp[h1 * D + dB] = (L > 0.f) ? O.w / L : 0.f;
+                outp[h1 * D + dA] = (L1 > 0.f) ? O.y / L1 : 0.f;
+                outp[h1 * D + dB] = (L1 > 0.f) ? O.w / L1 : 0.f;
             }
         } else {
             if (h0 < R) {
@@ -726,6 +712,16 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
             if (h1 < R) {
                 part[S::OOFF + h1 * D + dA] = O.y;
                 part[S::OOFF + h1 * D + dB] = O.w;
+            }
+            if (mt == 0 && fg == 0) { // one writer per head pair: the partial's max and sum
+                if (h0 < r_act) {
+                    part[h0] = M0;
+                    part[R + h0] = L0;
+                }
+                if (h1 < r_act) {
+                    part[h1] = M1;
+                    part[R + h1] = L1;
+                }
             }
         }
     }
