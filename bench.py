@@ -282,7 +282,7 @@ def host_pipeline(args, dev, torch, kvc, n=None, cells=HOST_CELLS, link=None):
     res = {}
     link = link or measure_link(torch, dev)
     scale = float(1.0 / np.sqrt(D))
-    cache = kvc.KVCache(L, H, HK, D, n + 64, 1, t, t, 1e6, 0, kvc.KVC_HOST_PINNED)
+    cache = kvc.KVCache(L, H, HK, D, n + 256, 1, t, t, 1e6, 0, kvc.KVC_HOST_PINNED)
     try:
         for l in range(L):
             for p0 in range(0, n - 1, 8192):
@@ -298,28 +298,34 @@ def host_pipeline(args, dev, torch, kvc, n=None, cells=HOST_CELLS, link=None):
         for name, depth, budget in cells:
             kvc.kvc_pipeline_depth(cache.ctx, depth)
             kvc.kvc_pipeline_budget(cache.ctx, budget)
-            times = []
-            for step in range(args.host_steps + 1):
-                if step == 1:
-                    torch.cuda.synchronize()
-                    t0 = time.perf_counter()
-                for l in range(L):
-                    cache.append(l, 0, pos, kn[l], vn[l])
-                    cache.attn_decode(l, [0], q[l], out[l], scale)
-                pos += 1
-            torch.cuda.synchronize()
-            dt = (time.perf_counter() - t0) / args.host_steps
+            # median of three timed runs of host_steps steps after one warm-up step: the
+            # host link is shared with other work on the machine and single runs vary
+            runs = []
+            for rep in range(3):
+                for step in range(args.host_steps + (1 if rep == 0 else 0)):
+                    if step == (1 if rep == 0 else 0):
+                        torch.cuda.synchronize()
+                        t0 = time.perf_counter()
+                    for l in range(L):
+                        cache.append(l, 0, pos, kn[l], vn[l])
+                        cache.attn_decode(l, [0], q[l], out[l], scale)
+                    pos += 1
+                torch.cuda.synchronize()
+                runs.append((time.perf_counter() - t0) / args.host_steps)
+            dt = statistics.median(runs)
             st = cache.stats()
             # bytes moved host->device per step: every layer's rows (stable prefix) once
             h2d = L * (pos - 1) * kv_bytes_per_row(args.type)
             res[name] = {"steps_per_s": round(1.0 / dt, 3), "ms_per_step": round(1000 * dt, 3),
                          "h2d_gbs": round(h2d / dt / GB, 2), "frac_of_link": round(h2d / dt / GB / link, 3),
                          "ring_engaged": st["ring_engaged"], "ring_declined": st["ring_declined"],
+                         "rolling": st["rolling"], "tile_rows": st["tile_rows"],
                          "ring_mib": round(st["ring_bytes"] / 2**20, 1)}
         res["n_kv"] = n
         res["link_gbs"] = round(link, 2)
         res["link"] = "pinned H2D, 256 MiB copies, measured in this run"
-        res["note"] = "n_kv grows by one row per step (decode); H2D counts every layer's rows once per step"
+        res["note"] = ("n_kv grows by one row per step (decode); H2D counts every layer's rows once per step; "
+                       "steps/s is the median of 3 runs")
     finally:
         cache.close()
     return res

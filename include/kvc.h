@@ -212,11 +212,17 @@ int kvc_pipeline_depth(kvc_ctx *c, int n);
 /* Device-memory budget of the staging ring, in bytes.  Default 128 MiB
  * ([R4] section Device memory: --kv-pipeline-budget).  The need,
  * (N+2) * bytes of one layer's K+V over the current context, is checked
- * before anything is allocated on every plan; a ring that does not fit is
- * declined and the decision is latched, the transfer stream and events are
- * created only when a ring is engaged and released with it, and a declined
- * context runs the ordered path.  Changing the budget releases the ring and
- * clears the latch.  Errors: KVC_EINVAL. */
+ * before anything is allocated on every plan.  A ring of whole layers that
+ * does not fit falls back to rolling mode ([F5] section Rolling KV): the
+ * N+2 slots hold tiles of a layer, each the largest whole number of 1024
+ * rows that lets N+2 of them fit the budget, and each layer is attended tile
+ * by tile while the next N tiles are delivered; tiles are whole chunks of the
+ * layer's split-K plan, so the output bytes equal the ordered path's.  When
+ * even a 1024-row tile (or one chunk) does not fit, the ring is declined and
+ * the decision is latched; the transfer stream and events are created only
+ * when a ring is engaged and released with it, and a declined context runs
+ * the ordered path.  Changing the budget releases the ring and clears the
+ * latch.  Errors: KVC_EINVAL. */
 int kvc_pipeline_budget(kvc_ctx *c, size_t bytes);
 
 /* Number of rows `seq` holds in every layer (after all appends of a step). */
@@ -242,6 +248,9 @@ typedef struct kvc_stats {
     int64_t pages_free;
     int64_t device_bytes;       /* all device memory held by the context */
     int64_t host_pinned_bytes;  /* pinned host memory held by the context */
+    int32_t rolling;            /* 1 while the ring holds tiles of a layer (rolling mode) */
+    int32_t tile_rows;          /* rows of one tile slot in rolling mode, else 0 */
+    int64_t tiles_delivered;    /* rolling mode: tile deliveries issued */
 } kvc_stats;
 
 int kvc_get_stats(const kvc_ctx *c, kvc_stats *out);

@@ -994,6 +994,9 @@ int kvc_get_stats(const kvc_ctx *cc, kvc_stats *o) {
     o->pages_free = (int64_t)c->free_pages.size();
     o->device_bytes = c->device_bytes;
     o->host_pinned_bytes = c->host_bytes;
+    o->rolling = c->tr.rolling ? 1 : 0;
+    o->tile_rows = c->tr.rolling && !c->tr.ring.empty() ? c->tr.ring[0].cap : 0;
+    o->tiles_delivered = c->tr.tiles;
     return KVC_OK;
 }
 

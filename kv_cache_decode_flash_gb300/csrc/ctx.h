@@ -40,7 +40,10 @@ struct Slot {
     CUtensorMap tmk[2], tmv[2]; // 16-row and 128-row boxes
     cudaEvent_t ready = nullptr, release = nullptr;
     int32_t layer = -1; // layer held (-1 none)
-    int32_t rows = 0;   // rows of that layer present
+    int32_t rows = 0;   // rows of that layer present (from row r0)
+    int32_t tile = -1;  // rolling mode: tile index of the rows held, first row r0
+    int32_t r0 = 0;
+    bool delivered = false; // a delivery was issued into the slot (its ready event is recorded)
     bool consumed_once = false;
 };
 
@@ -49,10 +52,11 @@ struct Transport {
     int64_t budget = 128ll << 20;
     bool latched = false;
     std::vector<Slot> ring; // engaged ring (depth + 2 slots) or empty
+    bool rolling = false;   // ring slots hold tiles of a layer (the whole-layer ring did not fit)
     Slot ordered;           // ordered-path buffer
     cudaStream_t xfer = nullptr;
     int64_t cursor = 0;     // deliveries issued into the ring
-    int64_t early = 0, in_order = 0, bytes = 0;
+    int64_t early = 0, in_order = 0, bytes = 0, tiles = 0;
 };
 
 struct Ctx {

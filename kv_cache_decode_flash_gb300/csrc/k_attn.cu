@@ -658,7 +658,7 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
     __syncthreads();
 
     const int n_chunks = sq.n_chunks;
-    float *part = p.part + ((int64_t)chunk * p.Hk + g) * S::PF;
+    float *part = p.part + ((int64_t)(sq.part0 + lc) * p.Hk + g) * S::PF;
     float *outp = p.out + ((int64_t)sq.out_row * p.H + (int64_t)g * r_act) * D;
     // fragment (mt, ln): heads 2t, 2t+1 of lane ln, dims of rows g and g+8.  Each
     // fragment weighs the warps itself (softmax rescale and the warp's 2^-S: O
@@ -740,7 +740,7 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
     }
     __syncthreads();
     if (!s_flag) return;
-    const float *part0 = p.part + ((int64_t)sq.chunk0 * p.Hk + g) * S::PF;
+    const float *part0 = p.part + ((int64_t)sq.part_first * p.Hk + g) * S::PF;
     const int64_t cstride = (int64_t)p.Hk * S::PF;
     // one round of independent loads stages every partial in shared memory
     // (the host keeps n_chunks <= MERGE_CAP)

@@ -52,6 +52,10 @@ struct AttnSeq {
     int32_t ticket;            // index of this sequence's ticket row
     int32_t stable_rows;       // leading rows no possibly in-flight kernel writes (readable before
                                // the programmatic-dependency wait)
+    int32_t part0;             // partial slot of this launch's first chunk of the sequence
+    int32_t part_first;        // partial slot of the sequence's chunk 0 (n_chunks slots from there
+                               // are merged); a sequence's chunks may span several launches, the
+                               // ticket counting all of them
 };
 
 struct AttnParams {

@@ -56,20 +56,40 @@ static int auto_chunk_rows(const Ctx *c, int64_t total_rows) {
     return (int)std::min<int64_t>(cmax, std::max<int64_t>(64, C));
 }
 
-int launch_attention(Ctx *c, const LayerView &lv, const CUtensorMap *tmk, const CUtensorMap *tmv, int P,
-                     int64_t scale_limit, int n_seq, const AttnSeq *seqs_in, const float *q, float *out,
-                     float kq_scale, cudaStream_t st) {
+// Chunk rows of one launch over sequences of the given row counts.
+static int chunk_rows_plan(const Ctx *c, int n_seq, const int32_t *rows) {
     int64_t total = 0;
-    for (int i = 0; i < n_seq; ++i) total += seqs_in[i].n_rows;
+    for (int i = 0; i < n_seq; ++i) total += rows[i];
     int C = c->chunk_override ? c->chunk_override : auto_chunk_rows(c, total);
     // one merge stages at most `cap` partials per (sequence, kv head)
     const int cap = attn_merge_cap(c->tk, c->D, c->r);
     for (int i = 0; i < n_seq; ++i) {
-        const int need = (seqs_in[i].n_rows + cap - 1) / cap;
+        const int need = (rows[i] + cap - 1) / cap;
         if (need > C) C = (need + 15) / 16 * 16;
     }
     // a chunk spans at most 512 tiles of at least 16 rows
-    C = std::min(C, 8000);
+    return std::min(C, 8000);
+}
+
+static int grow_partials(Ctx *c, int64_t need, cudaStream_t st) {
+    if (need <= c->part_floats) return KVC_OK;
+    // grows only for forced chunk sizes or unusual batches (not inside graph capture)
+    KVC_CU(c, cudaStreamSynchronize(st));
+    dev_free(c, c->part, c->part_floats * 4);
+    c->part = nullptr;
+    c->part_floats = 0;
+    int rc = dev_alloc(c, (void **)&c->part, need * 4, "partials");
+    if (rc) return rc;
+    c->part_floats = need;
+    return KVC_OK;
+}
+
+int launch_attention(Ctx *c, const LayerView &lv, const CUtensorMap *tmk, const CUtensorMap *tmv, int P,
+                     int64_t scale_limit, int n_seq, const AttnSeq *seqs_in, const float *q, float *out,
+                     float kq_scale, cudaStream_t st) {
+    std::vector<int32_t> rows((size_t)n_seq);
+    for (int i = 0; i < n_seq; ++i) rows[(size_t)i] = seqs_in[i].n_rows;
+    const int C = chunk_rows_plan(c, n_seq, rows.data());
     const int64_t pf = (int64_t)attn_partial_floats(c->r, c->D);
     for (int base = 0; base < n_seq; base += MAX_SEQ_PER_LAUNCH) {
         const int cnt = std::min(MAX_SEQ_PER_LAUNCH, n_seq - base);
@@ -95,22 +115,14 @@ int launch_attention(Ctx *c, const LayerView &lv, const CUtensorMap *tmk, const 
             AttnSeq a = seqs_in[base + i];
             a.chunk0 = chunks;
             a.n_chunks = std::max(1, (a.n_rows + C - 1) / C);
+            a.part0 = a.part_first = chunks;
             a.ticket = i;
             p.seq[i] = a;
             chunks += a.n_chunks;
         }
         p.total_chunks = chunks;
-        const int64_t need = (int64_t)chunks * c->Hk * pf;
-        if (need > c->part_floats) {
-            // grows only for forced chunk sizes or unusual batches (not inside graph capture)
-            KVC_CU(c, cudaStreamSynchronize(st));
-            dev_free(c, c->part, c->part_floats * 4);
-            c->part = nullptr;
-            c->part_floats = 0;
-            int rc = dev_alloc(c, (void **)&c->part, need * 4, "partials");
-            if (rc) return rc;
-            c->part_floats = need;
-        }
+        int rc = grow_partials(c, (int64_t)chunks * c->Hk * pf, st);
+        if (rc) return rc;
         p.part = c->part;
         cudaError_t e = launch_attn(c->tk, p, tmk, tmv, st);
         if (e != cudaSuccess) return cuda_fail(c, e, "attention kernel");
@@ -175,6 +187,7 @@ static int alloc_slot(Ctx *c, Slot &s, int32_t cap) {
 void transport_release(Ctx *c) {
     for (auto &s : c->tr.ring) free_slot(c, s);
     c->tr.ring.clear();
+    c->tr.rolling = false;
     if (c->tr.xfer) {
         cudaStreamDestroy(c->tr.xfer);
         c->tr.xfer = nullptr;
@@ -187,30 +200,33 @@ static void dev_free_slot_memory(Ctx *c, Slot &s) {
     free_slot(c, s);
 }
 
-// Decide ordered vs pipelined for a context of n rows; allocate or grow the
-// ring when it fits the budget.  Returns true when the ring is engaged.
+// Bytes of one row of every KV head (K and V codes and scales).
+static int64_t row_bytes_all(const Ctx *c) { return (int64_t)c->Hk * (c->krow + c->vrow + c->ksb + c->vsb); }
+
+// Rows of a rolling tile for a layer attended over `rows` rows: whole chunks
+// of that attention's chunk plan, as many as a tile slot holds.
+static int32_t tile_rows_for(const Ctx *c, int32_t rows) {
+    const int C = chunk_rows_plan(c, 1, &rows);
+    const int32_t cap = c->tr.ring.empty() ? 0 : c->tr.ring[0].cap;
+    return std::max(C, (cap / C) * C); // cap >= C when rolling is engaged
+}
+
+// Decide ordered / pipelined / rolling for a context of n rows; allocate or
+// regrow the ring when it fits the budget.  *engaged: the ring is in use
+// (c->tr.rolling tells whether it holds whole layers or tiles).
 static int plan(Ctx *c, int64_t n, cudaStream_t st, bool *engaged) {
     *engaged = false;
     Transport &t = c->tr;
     if (t.depth == 0 || t.latched) return KVC_OK;
-    const int32_t cap = cap_for(c, n);
-    const int64_t need = (int64_t)(t.depth + 2) * slot_bytes_for(c, cap);
-    if (need > t.budget) {
-        // declined before anything is allocated, and latched: the context only grows
+    auto drop_ring = [&]() -> int {
         if (!t.ring.empty()) {
             KVC_CU(c, cudaStreamSynchronize(st));
             if (t.xfer) KVC_CU(c, cudaStreamSynchronize(t.xfer));
             transport_release(c);
         }
-        t.latched = true;
         return KVC_OK;
-    }
-    if (t.ring.empty() || t.ring[0].cap < n) {
-        if (!t.ring.empty()) {
-            KVC_CU(c, cudaStreamSynchronize(st));
-            if (t.xfer) KVC_CU(c, cudaStreamSynchronize(t.xfer));
-            transport_release(c);
-        }
+    };
+    auto make_ring = [&](int32_t cap, bool rolling) -> int {
         t.ring.resize((size_t)(t.depth + 2));
         for (auto &s : t.ring) {
             int rc = alloc_slot(c, s, cap);
@@ -221,14 +237,48 @@ static int plan(Ctx *c, int64_t n, cudaStream_t st, bool *engaged) {
         }
         KVC_CU(c, cudaStreamCreateWithFlags(&t.xfer, cudaStreamNonBlocking));
         t.cursor = 0;
+        t.rolling = rolling;
+        return KVC_OK;
+    };
+    int rc;
+    const int32_t cap = cap_for(c, n);
+    const int64_t need = (int64_t)(t.depth + 2) * slot_bytes_for(c, cap);
+    if (need <= t.budget) {
+        // whole layers
+        if (t.ring.empty() || t.rolling || t.ring[0].cap < n) {
+            if ((rc = drop_ring())) return rc;
+            if ((rc = make_ring(cap, false))) return rc;
+        }
+        *engaged = true;
+        return KVC_OK;
+    }
+    // Rolling: the ring holds tiles of a layer, (N+2) tile slots within the
+    // budget, each a whole number of 1024-row blocks ("F5 - Advanced KV Cache
+    // Techniques", Rolling KV: tiles streamed through a small ring, merged
+    // with the online-softmax partials)
+    const int64_t tcap = (t.budget / (t.depth + 2) - 4 * 64) / row_bytes_all(c) / 1024 * 1024;
+    const int32_t rows = (int32_t)std::min<int64_t>(n, INT32_MAX);
+    if (tcap < 1024 || tcap < chunk_rows_plan(c, 1, &rows)) {
+        // declined before anything is allocated, and latched: the context only grows
+        if ((rc = drop_ring())) return rc;
+        t.latched = true;
+        return KVC_OK;
+    }
+    if (t.ring.empty() || !t.rolling || t.ring[0].cap != tcap) {
+        if ((rc = drop_ring())) return rc;
+        if ((rc = make_ring((int32_t)tcap, true))) return rc;
     }
     *engaged = true;
     return KVC_OK;
 }
 
-// Issue H2D copies of rows [0, rows) of `layer` from the host store into slot s.
-static int deliver(Ctx *c, Slot &s, int layer, int32_t rows, cudaStream_t x) {
+// Issue H2D copies of rows [r0, r0 + rows) of `layer` from the host store
+// into slot s (slot row 0 = layer row r0), after the slot's previous delivery
+// and its previous reader.
+static int deliver_range(Ctx *c, Slot &s, int layer, int32_t r0, int32_t rows, int tile, cudaStream_t x) {
     const int64_t hcap = c->P;
+    if (s.delivered) KVC_CU(c, cudaStreamWaitEvent(x, s.ready, 0));
+    if (s.consumed_once) KVC_CU(c, cudaStreamWaitEvent(x, s.release, 0));
     struct Part {
         uint8_t *host;
         void *dev;
@@ -237,20 +287,43 @@ static int deliver(Ctx *c, Slot &s, int layer, int32_t rows, cudaStream_t x) {
                   {c->hvs, s.vscales, c->vsb}};
     for (auto &pt : parts) {
         if (!pt.rowb || rows == 0) continue;
-        const uint8_t *src = pt.host + (int64_t)layer * c->Hk * hcap * pt.rowb;
+        const uint8_t *src = pt.host + ((int64_t)layer * c->Hk * hcap + r0) * pt.rowb;
         KVC_CU(c, cudaMemcpy2DAsync(pt.dev, (size_t)s.cap * pt.rowb, src, (size_t)hcap * pt.rowb,
                                     (size_t)rows * pt.rowb, (size_t)c->Hk, cudaMemcpyHostToDevice, x));
         c->tr.bytes += (int64_t)rows * pt.rowb * c->Hk;
     }
     s.layer = layer;
+    s.r0 = r0;
     s.rows = rows;
+    s.tile = tile;
+    KVC_CU(c, cudaEventRecord(s.ready, x));
+    s.delivered = true;
     return KVC_OK;
+}
+
+static int deliver(Ctx *c, Slot &s, int layer, int32_t rows, cudaStream_t x) {
+    return deliver_range(c, s, layer, 0, rows, -1, x);
 }
 
 static Slot *find_slot(Ctx *c, int layer, int32_t rows) {
     for (auto &s : c->tr.ring)
-        if (s.layer == layer && s.rows == rows) return &s;
+        if (s.layer == layer && s.tile < 0 && s.rows == rows) return &s;
     return nullptr;
+}
+
+// Rolling mode: the slot holding tile `tile` of `layer` from row r0 with
+// `rows` rows present.
+static Slot *find_tile(Ctx *c, int layer, int tile, int32_t r0, int32_t rows) {
+    for (auto &s : c->tr.ring)
+        if (s.layer == layer && s.tile == tile && s.r0 == r0 && s.rows == rows) return &s;
+    return nullptr;
+}
+
+static Slot &next_slot(Ctx *c) {
+    Transport &t = c->tr;
+    Slot &s = t.ring[(size_t)(t.cursor % (int64_t)t.ring.size())];
+    ++t.cursor;
+    return s;
 }
 
 // Early delivery into the next ring slot on the transfer stream.
@@ -259,15 +332,31 @@ static int deliver_early(Ctx *c, int layer) {
     const int32_t rows = c->seqs[0].lfill[(size_t)layer];
     if (rows == 0 || find_slot(c, layer, rows)) return KVC_OK;
     if (rows > t.ring[0].cap) return KVC_OK; // the next plan grows the ring
-    Slot &s = t.ring[(size_t)(t.cursor % (int64_t)t.ring.size())];
-    ++t.cursor;
-    if (s.consumed_once) KVC_CU(c, cudaStreamWaitEvent(t.xfer, s.release, 0));
+    Slot &s = next_slot(c);
     // the host rows being delivered were written by append kernels on the compute stream
     KVC_CU(c, cudaStreamWaitEvent(t.xfer, c->app_ev[(size_t)layer], 0));
     int rc = deliver(c, s, layer, rows, t.xfer);
     if (rc) return rc;
-    KVC_CU(c, cudaEventRecord(s.ready, t.xfer));
     ++t.early;
+    return KVC_OK;
+}
+
+// Rolling mode: rows the attention of `layer` will cover when it comes next
+// (this step for layers not yet attended, the next step for the others; one
+// token per step), and tile `tile`'s stable rows [r0, r0 + n) held now.
+static int deliver_tile_early(Ctx *c, int layer, int tile, int32_t att_rows) {
+    Transport &t = c->tr;
+    const int32_t TR = tile_rows_for(c, att_rows);
+    const int32_t r0 = tile * TR;
+    const int32_t held = c->seqs[0].lfill[(size_t)layer];
+    const int32_t n = std::min(held, std::min(att_rows, r0 + TR)) - r0;
+    if (n <= 0 || find_tile(c, layer, tile, r0, n)) return KVC_OK;
+    Slot &s = next_slot(c);
+    KVC_CU(c, cudaStreamWaitEvent(t.xfer, c->app_ev[(size_t)layer], 0));
+    int rc = deliver_range(c, s, layer, r0, n, tile, t.xfer);
+    if (rc) return rc;
+    ++t.early;
+    ++t.tiles;
     return KVC_OK;
 }
 
@@ -293,21 +382,110 @@ int transport_append(Ctx *c, int layer, int n_tok, const float *k, const float *
     d[0].row0 = fill;
     d[0].P = c->P;
     // rows written this step also go straight into the slot holding the
-    // layer's stable prefix, after that delivery has landed
-    Slot *s = find_slot(c, layer, fill);
-    if (s && fill + n_tok <= s->cap) {
+    // layer's stable prefix (rolling mode: the tile they fall in), after that
+    // delivery has landed
+    Slot *s = nullptr;
+    if (c->tr.rolling && !c->tr.ring.empty()) {
+        const int32_t TR = tile_rows_for(c, fill + n_tok);
+        const int tile = fill / TR;
+        s = find_tile(c, layer, tile, tile * TR, fill - tile * TR);
+        if (s && fill + n_tok > s->r0 + std::min(TR, s->cap)) s = nullptr;
+    } else {
+        s = find_slot(c, layer, fill);
+        if (s && fill + n_tok > s->cap) s = nullptr;
+    }
+    if (s) {
         KVC_CU(c, cudaStreamWaitEvent(st, s->ready, 0));
         slot_layer_view(*s, d[1].lv);
         d[1].pt = nullptr;
         d[1].off = 0;
-        d[1].row0 = fill;
+        d[1].row0 = fill - s->r0;
         d[1].P = s->cap;
         nd = 2;
     }
     cudaError_t e = launch_append(c->tk, c->tv, c->Hk, c->D, n_tok, k, v, d, nd, st);
     if (e != cudaSuccess) return cuda_fail(c, e, "append kernel");
     KVC_CU(c, cudaEventRecord(c->app_ev[(size_t)layer], st));
-    if (nd == 2) s->rows = fill + n_tok;
+    if (nd == 2) s->rows = fill + n_tok - s->r0;
+    return KVC_OK;
+}
+
+// Rolling mode: attention of `layer` over its tiles, each one launch writing
+// its chunks' partials at their place in the whole layer's chunk plan; the
+// ticket counts every chunk of the layer, so the last CTA of the last tile
+// merges them in chunk order.  The chunking is the ordered path's, so the
+// result is the same bytes.
+static int rolling_attn(Ctx *c, int layer, const float *q, float *out, float kq_scale, cudaStream_t st) {
+    Transport &t = c->tr;
+    Seq &sq = c->seqs[0];
+    const int32_t rows = sq.lfill[(size_t)layer];
+    const int C = chunk_rows_plan(c, 1, &rows);
+    const int32_t TR = tile_rows_for(c, rows);
+    const int n_tiles = std::max(1, (rows + TR - 1) / TR);
+    const int total = std::max(1, (rows + C - 1) / C);
+    int rc = grow_partials(c, (int64_t)total * c->Hk * (int64_t)attn_partial_floats(c->r, c->D), st);
+    if (rc) return rc;
+    const int32_t recent = c->recent[0][(size_t)layer];
+    for (int tile = 0; tile < n_tiles; ++tile) {
+        const int32_t r0 = tile * TR, n = std::min(rows, r0 + TR) - r0;
+        Slot *s = find_tile(c, layer, tile, r0, n);
+        if (!s) {
+            // not delivered ahead: deliver now, in stream order, into the next slot
+            s = &next_slot(c);
+            if ((rc = deliver_range(c, *s, layer, r0, n, tile, st))) return rc;
+            ++t.in_order;
+            ++t.tiles;
+        }
+        KVC_CU(c, cudaStreamWaitEvent(st, s->ready, 0));
+        AttnParams p;
+        std::memset(&p, 0, sizeof(p));
+        p.H = c->H;
+        p.Hk = c->Hk;
+        p.D = c->D;
+        p.r = c->r;
+        p.P = s->cap;
+        p.chunk_rows = C;
+        p.n_seq = 1;
+        p.kq_scale_log2 = (float)((double)kq_scale * 1.4426950408889634);
+        p.q = q;
+        p.out = out;
+        p.ks = reinterpret_cast<uint16_t *>(s->kscales);
+        p.vs = reinterpret_cast<uint16_t *>(s->vscales);
+        p.tickets = c->tickets;
+        p.err = c->err_dev;
+        p.scale_limit_bytes = s->scale_bytes;
+        p.part = c->part;
+        AttnSeq &a = p.seq[0];
+        a.page_table = c->zero_pt;
+        a.off = 0;
+        a.n_rows = n;
+        a.chunk0 = 0;
+        a.n_chunks = total;
+        a.out_row = 0;
+        a.ticket = 0;
+        a.stable_rows = std::max(0, std::min(n, rows - recent - r0));
+        a.part0 = r0 / C;
+        a.part_first = 0;
+        p.total_chunks = (n + C - 1) / C;
+        cudaError_t e = launch_attn(c->tk, p, s->tmk, s->tmv, st);
+        if (e != cudaSuccess) return cuda_fail(c, e, "attention kernel");
+        KVC_CU(c, cudaEventRecord(s->release, st));
+        s->consumed_once = true;
+        // look-ahead: the next N tiles, on into the following layers
+        int l2 = layer, t2 = tile;
+        int32_t rows2 = rows;
+        for (int k = 0; k < t.depth; ++k) {
+            if (++t2 >= std::max(1, (rows2 + tile_rows_for(c, rows2) - 1) / tile_rows_for(c, rows2))) {
+                l2 = (l2 + 1) % c->L;
+                t2 = 0;
+                // layers after this one in the step hold sq.n rows once appended; the
+                // ones before it come round again in the next step with one more row
+                rows2 = l2 > layer ? sq.n : sq.n + 1;
+            }
+            if ((rc = deliver_tile_early(c, l2, t2, rows2))) return rc;
+        }
+    }
+    c->clear_recent();
     return KVC_OK;
 }
 
@@ -317,18 +495,15 @@ int transport_attn(Ctx *c, int layer, const float *q, float *out, float kq_scale
     bool engaged = false;
     int rc = plan(c, sq.n, st, &engaged);
     if (rc) return rc;
+    if (engaged && c->tr.rolling) return rolling_attn(c, layer, q, out, kq_scale, st);
     Slot *s = nullptr;
     if (engaged) {
         s = find_slot(c, layer, rows);
         if (!s) {
             // not delivered ahead: deliver now, in stream order, into the next slot
-            Transport &t = c->tr;
-            s = &t.ring[(size_t)(t.cursor % (int64_t)t.ring.size())];
-            ++t.cursor;
-            if (s->consumed_once) KVC_CU(c, cudaStreamWaitEvent(st, s->release, 0));
+            s = &next_slot(c);
             if ((rc = deliver(c, *s, layer, rows, st))) return rc;
-            KVC_CU(c, cudaEventRecord(s->ready, st));
-            ++t.in_order;
+            ++c->tr.in_order;
         }
         KVC_CU(c, cudaStreamWaitEvent(st, s->ready, 0));
     } else {

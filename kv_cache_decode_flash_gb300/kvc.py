@@ -34,7 +34,8 @@ class kvc_stats(C.Structure):
     _fields_ = [(n, C.c_int32) for n in ("ring_engaged", "ring_declined", "ring_slots", "transfer_stream")] + [
         (n, C.c_int64) for n in ("slot_bytes", "ring_bytes", "ordered_bytes", "deliveries_early",
                                  "deliveries_ordered", "bytes_delivered", "pages_total", "pages_free",
-                                 "device_bytes", "host_pinned_bytes")]
+                                 "device_bytes", "host_pinned_bytes")] + [
+        (n, C.c_int32) for n in ("rolling", "tile_rows")] + [("tiles_delivered", C.c_int64)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

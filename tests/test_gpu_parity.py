@@ -267,7 +267,7 @@ def test_cold_store_cycle_small():
         tw.close()
 
 
-def _host_run(depth, budget, L=8, H=40, Hk=8, D=128, n=2000, steps=3):
+def _host_run(depth, budget, L=8, H=40, Hk=8, D=128, n=2000, steps=3, chunk=0):
     import torch
 
     from kv_cache_decode_flash_gb300 import kvc
@@ -275,6 +275,7 @@ def _host_run(depth, budget, L=8, H=40, Hk=8, D=128, n=2000, steps=3):
     cache = kvc.KVCache(L, H, Hk, D, 4096, 1, Q8, Q8, 1e6, 0, kvc.KVC_HOST_PINNED)
     kvc.kvc_pipeline_depth(cache.ctx, depth)
     kvc.kvc_pipeline_budget(cache.ctx, budget)
+    kvc.kvc_set_chunk_rows(cache.ctx, chunk)
     dev = torch.device("cuda:0")
     res = []
     try:
@@ -308,6 +309,55 @@ def test_host_resident_ordered_and_pipelined_byte_identical():
         else:
             assert st["ring_engaged"] == 0 and st["ring_declined"] == 1 and st["transfer_stream"] == 0
             assert st["ring_bytes"] == 0
+
+
+@pytest.mark.parametrize("depth,budget,chunk", [(1, 8 << 20, 0), (2, 12 << 20, 0), (1, 8 << 20, 64)])
+def test_host_resident_rolling_tiles_byte_identical(depth, budget, chunk):
+    """A budget below N+2 whole-layer slots but above N+2 tile slots streams
+    each layer in tiles of whole chunks through the ring (rolling mode); the
+    chunk plan is the ordered path's, so the bytes are the same.  chunk=64
+    forces many chunks, merged across the tile launches."""
+    base, _ = _host_run(0, 128 << 20, chunk=chunk)
+    out, st = _host_run(depth, budget, chunk=chunk)
+    assert np.array_equal(out, base)
+    assert st["rolling"] == 1 and st["ring_engaged"] == 1 and st["ring_declined"] == 0
+    assert st["ring_slots"] == depth + 2 and st["tile_rows"] >= 1024
+    assert st["tiles_delivered"] > 0 and st["deliveries_early"] > 0
+
+
+def test_host_resident_rolling_vs_oracle():
+    import torch
+
+    from kv_cache_decode_flash_gb300 import kvc
+
+    L, H, Hk, D, n = 3, 40, 8, 128, 5000
+    cache = kvc.KVCache(L, H, Hk, D, 8192, 1, Q8, Q8, 1e6, 0, kvc.KVC_HOST_PINNED)
+    kvc.kvc_pipeline_depth(cache.ctx, 2)
+    kvc.kvc_pipeline_budget(cache.ctx, 10 << 20)  # tiles of 1024 rows, several per layer
+    ref = oracle.OracleCache(L, H, Hk, D, Q8, Q8, 1e6, 0)
+    dev = torch.device("cuda:0")
+    try:
+        for l in range(L):
+            k, v = kv_inputs(17, l, n, Hk, D, sigma=0.5)
+            cache.append(l, 0, 0, torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev))
+            ref.append(l, 0, 0, k, v)
+        for step in range(3):
+            for l in range(L):
+                k, v = kv_inputs(18, l, 1, Hk, D, pos0=n + step, sigma=0.5)
+                cache.append(l, 0, n + step, torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev))
+                ref.append(l, 0, n + step, k, v)
+                q = q_inputs(18, l, 1, H, D, extra=step)
+                qd = torch.from_numpy(q).to(dev)
+                out = torch.empty_like(qd)
+                cache.attn_decode(l, [0], qd, out, float(1 / np.sqrt(D)))
+                torch.cuda.synchronize()
+                want = ref.attn(l, [0], q, float(np.float32(1 / np.sqrt(D))))
+                assert_attn_close(out.cpu().numpy().astype(np.float64), want, "rolling layer %d" % l)
+        st = cache.stats()
+        assert st["rolling"] == 1 and st["tiles_delivered"] > 0
+        assert kvc.kvc_check_device_error(cache.ctx) == 0
+    finally:
+        cache.close()
 
 
 def test_host_resident_pipelined_vs_oracle():
