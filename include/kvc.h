@@ -213,10 +213,10 @@ int kvc_pipeline_depth(kvc_ctx *c, int n);
  * ([R4] section Device memory: --kv-pipeline-budget).  The need,
  * (N+2) * bytes of one layer's K+V over the current context, is checked
  * before anything is allocated on every plan.  A ring of whole layers that
- * does not fit falls back to rolling mode ([F5] section Rolling KV): the
- * N+2 slots hold tiles of a layer, each the largest whole number of 1024
- * rows that lets N+2 of them fit the budget, and each layer is attended tile
- * by tile while the next N tiles are delivered; tiles are whole chunks of the
+ * does not fit falls back to rolling mode ([F5] section Rolling KV): three
+ * slots (at any N >= 1) hold tiles of a layer, each the largest whole number
+ * of 1024 rows that lets three fit the budget, and each layer is attended
+ * tile by tile while the next tile is delivered; tiles are whole chunks of the
  * layer's split-K plan, so the output bytes equal the ordered path's.  When
  * even a 1024-row tile (or one chunk) does not fit, the ring is declined and
  * the decision is latched; the transfer stream and events are created only

@@ -506,6 +506,8 @@ int kvc_create(const kvc_params *p, kvc_ctx **out) {
             return fail(rc);
         if ((rc = dev_alloc(c, (void **)&c->zero_pt, 4, "slot page table"))) return fail(rc);
         c->app_ev.assign((size_t)c->L, nullptr);
+        c->app_gen.assign((size_t)c->L, 0);
+        c->tr.app_waited.assign((size_t)c->L, -1);
         for (auto &ev : c->app_ev)
             if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
                 c->err = "event creation failed";

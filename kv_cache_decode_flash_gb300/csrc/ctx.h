@@ -44,6 +44,7 @@ struct Slot {
     int32_t tile = -1;  // rolling mode: tile index of the rows held, first row r0
     int32_t r0 = 0;
     bool delivered = false; // a delivery was issued into the slot (its ready event is recorded)
+    cudaStream_t ready_stream = nullptr; // the stream that recorded it
     bool consumed_once = false;
 };
 
@@ -57,6 +58,7 @@ struct Transport {
     cudaStream_t xfer = nullptr;
     int64_t cursor = 0;     // deliveries issued into the ring
     int64_t early = 0, in_order = 0, bytes = 0, tiles = 0;
+    std::vector<int64_t> app_waited; // per layer: append generation the transfer stream has waited for
 };
 
 struct Ctx {
@@ -95,6 +97,7 @@ struct Ctx {
     int64_t host_bytes = 0;
     Transport tr;
     std::vector<cudaEvent_t> app_ev; // per layer: recorded after each append (orders early deliveries)
+    std::vector<int64_t> app_gen;    // per layer: appends recorded into app_ev
     int32_t *zero_pt = nullptr;      // device page table {0} used for slots
 
     // attention work space

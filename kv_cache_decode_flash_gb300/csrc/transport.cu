@@ -193,12 +193,16 @@ void transport_release(Ctx *c) {
         c->tr.xfer = nullptr;
     }
     c->tr.cursor = 0;
+    std::fill(c->tr.app_waited.begin(), c->tr.app_waited.end(), -1); // a new transfer stream waits afresh
 }
 
 static void dev_free_slot_memory(Ctx *c, Slot &s) {
     // free_slot without touching the bookkeeping of device_bytes twice
     free_slot(c, s);
 }
+
+// Tile slots of the rolling mode (one tile delivered ahead).
+constexpr int ROLLING_SLOTS = 3;
 
 // Bytes of one row of every KV head (K and V codes and scales).
 static int64_t row_bytes_all(const Ctx *c) { return (int64_t)c->Hk * (c->krow + c->vrow + c->ksb + c->vsb); }
@@ -226,8 +230,8 @@ static int plan(Ctx *c, int64_t n, cudaStream_t st, bool *engaged) {
         }
         return KVC_OK;
     };
-    auto make_ring = [&](int32_t cap, bool rolling) -> int {
-        t.ring.resize((size_t)(t.depth + 2));
+    auto make_ring = [&](int32_t cap, bool rolling, int slots) -> int {
+        t.ring.resize((size_t)slots);
         for (auto &s : t.ring) {
             int rc = alloc_slot(c, s, cap);
             if (rc) {
@@ -247,16 +251,18 @@ static int plan(Ctx *c, int64_t n, cudaStream_t st, bool *engaged) {
         // whole layers
         if (t.ring.empty() || t.rolling || t.ring[0].cap < n) {
             if ((rc = drop_ring())) return rc;
-            if ((rc = make_ring(cap, false))) return rc;
+            if ((rc = make_ring(cap, false, t.depth + 2))) return rc;
         }
         *engaged = true;
         return KVC_OK;
     }
-    // Rolling: the ring holds tiles of a layer, (N+2) tile slots within the
-    // budget, each a whole number of 1024-row blocks ("F5 - Advanced KV Cache
+    // Rolling: the ring holds tiles of a layer ("F5 - Advanced KV Cache
     // Techniques", Rolling KV: tiles streamed through a small ring, merged
-    // with the online-softmax partials)
-    const int64_t tcap = (t.budget / (t.depth + 2) - 4 * 64) / row_bytes_all(c) / 1024 * 1024;
+    // with the online-softmax partials).  Three tile slots (one tile ahead,
+    // whatever the depth): each tile costs a fixed number of API calls and
+    // launches, so the budget goes into tile size rather than look-ahead;
+    // each slot is a whole number of 1024-row blocks.
+    const int64_t tcap = (t.budget / ROLLING_SLOTS - 4 * 64) / row_bytes_all(c) / 1024 * 1024;
     const int32_t rows = (int32_t)std::min<int64_t>(n, INT32_MAX);
     if (tcap < 1024 || tcap < chunk_rows_plan(c, 1, &rows)) {
         // declined before anything is allocated, and latched: the context only grows
@@ -266,7 +272,7 @@ static int plan(Ctx *c, int64_t n, cudaStream_t st, bool *engaged) {
     }
     if (t.ring.empty() || !t.rolling || t.ring[0].cap != tcap) {
         if ((rc = drop_ring())) return rc;
-        if ((rc = make_ring((int32_t)tcap, true))) return rc;
+        if ((rc = make_ring((int32_t)tcap, true, ROLLING_SLOTS))) return rc;
     }
     *engaged = true;
     return KVC_OK;
@@ -277,7 +283,7 @@ static int plan(Ctx *c, int64_t n, cudaStream_t st, bool *engaged) {
 // and its previous reader.
 static int deliver_range(Ctx *c, Slot &s, int layer, int32_t r0, int32_t rows, int tile, cudaStream_t x) {
     const int64_t hcap = c->P;
-    if (s.delivered) KVC_CU(c, cudaStreamWaitEvent(x, s.ready, 0));
+    if (s.delivered && s.ready_stream != x) KVC_CU(c, cudaStreamWaitEvent(x, s.ready, 0));
     if (s.consumed_once) KVC_CU(c, cudaStreamWaitEvent(x, s.release, 0));
     struct Part {
         uint8_t *host;
@@ -298,6 +304,7 @@ static int deliver_range(Ctx *c, Slot &s, int layer, int32_t r0, int32_t rows, i
     s.tile = tile;
     KVC_CU(c, cudaEventRecord(s.ready, x));
     s.delivered = true;
+    s.ready_stream = x;
     return KVC_OK;
 }
 
@@ -352,7 +359,11 @@ static int deliver_tile_early(Ctx *c, int layer, int tile, int32_t att_rows) {
     const int32_t n = std::min(held, std::min(att_rows, r0 + TR)) - r0;
     if (n <= 0 || find_tile(c, layer, tile, r0, n)) return KVC_OK;
     Slot &s = next_slot(c);
-    KVC_CU(c, cudaStreamWaitEvent(t.xfer, c->app_ev[(size_t)layer], 0));
+    if (t.app_waited[(size_t)layer] != c->app_gen[(size_t)layer]) {
+        // rows of this layer were appended since the transfer stream last waited
+        KVC_CU(c, cudaStreamWaitEvent(t.xfer, c->app_ev[(size_t)layer], 0));
+        t.app_waited[(size_t)layer] = c->app_gen[(size_t)layer];
+    }
     int rc = deliver_range(c, s, layer, r0, n, tile, t.xfer);
     if (rc) return rc;
     ++t.early;
@@ -406,6 +417,7 @@ int transport_append(Ctx *c, int layer, int n_tok, const float *k, const float *
     cudaError_t e = launch_append(c->tk, c->tv, c->Hk, c->D, n_tok, k, v, d, nd, st);
     if (e != cudaSuccess) return cuda_fail(c, e, "append kernel");
     KVC_CU(c, cudaEventRecord(c->app_ev[(size_t)layer], st));
+    ++c->app_gen[(size_t)layer];
     if (nd == 2) s->rows = fill + n_tok - s->r0;
     return KVC_OK;
 }
@@ -471,10 +483,10 @@ static int rolling_attn(Ctx *c, int layer, const float *q, float *out, float kq_
         if (e != cudaSuccess) return cuda_fail(c, e, "attention kernel");
         KVC_CU(c, cudaEventRecord(s->release, st));
         s->consumed_once = true;
-        // look-ahead: the next N tiles, on into the following layers
+        // look-ahead: the next tile(s), on into the following layers
         int l2 = layer, t2 = tile;
         int32_t rows2 = rows;
-        for (int k = 0; k < t.depth; ++k) {
+        for (int k = 0; k < ROLLING_SLOTS - 2; ++k) {
             if (++t2 >= std::max(1, (rows2 + tile_rows_for(c, rows2) - 1) / tile_rows_for(c, rows2))) {
                 l2 = (l2 + 1) % c->L;
                 t2 = 0;

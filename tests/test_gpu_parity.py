@@ -311,7 +311,7 @@ def test_host_resident_ordered_and_pipelined_byte_identical():
             assert st["ring_bytes"] == 0
 
 
-@pytest.mark.parametrize("depth,budget,chunk", [(1, 8 << 20, 0), (2, 12 << 20, 0), (1, 8 << 20, 64)])
+@pytest.mark.parametrize("depth,budget,chunk", [(1, 8 << 20, 0), (4, 8 << 20, 0), (1, 8 << 20, 64)])
 def test_host_resident_rolling_tiles_byte_identical(depth, budget, chunk):
     """A budget below N+2 whole-layer slots but above N+2 tile slots streams
     each layer in tiles of whole chunks through the ring (rolling mode); the
@@ -321,7 +321,7 @@ def test_host_resident_rolling_tiles_byte_identical(depth, budget, chunk):
     out, st = _host_run(depth, budget, chunk=chunk)
     assert np.array_equal(out, base)
     assert st["rolling"] == 1 and st["ring_engaged"] == 1 and st["ring_declined"] == 0
-    assert st["ring_slots"] == depth + 2 and st["tile_rows"] >= 1024
+    assert st["ring_slots"] == 3 and st["tile_rows"] >= 1024  # rolling: three tile slots at any depth
     assert st["tiles_delivered"] > 0 and st["deliveries_early"] > 0
 
 
