@@ -307,3 +307,78 @@ int orc_rope_shift_f16(uint16_t *h, int64_t n_rows, int D, int mode, double base
     free(x);
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* KeyDiff distinctiveness ("F5 - Advanced KV Cache Techniques", M1:   */
+/* retention-aware context shift)                                     */
+/* ------------------------------------------------------------------ */
+
+/* Cosine of two D-vectors; 0 when either norm is 0 (a reading: the page
+ * does not define the degenerate case). */
+static double orc_cos(const double *a, const double *b, int D) {
+    double ab = 0.0, aa = 0.0, bb = 0.0;
+    for (int i = 0; i < D; ++i) {
+        ab += a[i] * b[i];
+        aa += a[i] * a[i];
+        bb += b[i] * b[i];
+    }
+    if (aa == 0.0 || bb == 0.0) return 0.0;
+    return ab / (sqrt(aa) * sqrt(bb));
+}
+
+/* Per-row KeyDiff score of n rows of one layer's K, in the order given:
+ * mean_g = (1/n) sum_j K[j][g] for every KV head g, and
+ * score[j] = (1/Hk) sum_g (1 - cos(K[j][g], mean_g)).
+ * K as in orc_kv (q8_0 dequantised exactly, f16 decoded). */
+int orc_keydiff_scores(int type_k, const void *k, const uint16_t *ks, int64_t n, int Hk, int D, double *score) {
+    if (n <= 0) return 0;
+    orc_kv t = {type_k, k, ks};
+    double *mean = (double *)calloc((size_t)Hk * D, sizeof(double));
+    double *row = (double *)malloc((size_t)D * sizeof(double));
+    if (!mean || !row) {
+        free(mean);
+        free(row);
+        return -1;
+    }
+    for (int64_t j = 0; j < n; ++j)
+        for (int g = 0; g < Hk; ++g) {
+            orc_load_row(&t, j, g, Hk, D, row);
+            for (int i = 0; i < D; ++i) mean[(int64_t)g * D + i] += row[i];
+        }
+    for (int64_t i = 0; i < (int64_t)Hk * D; ++i) mean[i] /= (double)n;
+    for (int64_t j = 0; j < n; ++j) {
+        double s = 0.0;
+        for (int g = 0; g < Hk; ++g) {
+            orc_load_row(&t, j, g, Hk, D, row);
+            s += 1.0 - orc_cos(row, mean + (int64_t)g * D, D);
+        }
+        score[j] = s / (double)Hk;
+    }
+    free(mean);
+    free(row);
+    return 0;
+}
+
+/* Start w0 of the width-w window of consecutive entries of score[0..n)
+ * lying inside [lo, hi) whose sum is smallest (prefix sums in fp64; the
+ * first such window on ties).  -1 when no window fits. */
+int64_t orc_min_window(const double *score, int64_t n, int64_t lo, int64_t hi, int64_t w) {
+    if (lo < 0) lo = 0;
+    if (hi > n) hi = n;
+    if (w <= 0 || hi - lo < w) return -1;
+    double *pre = (double *)malloc((size_t)(n + 1) * sizeof(double));
+    if (!pre) return -1;
+    pre[0] = 0.0;
+    for (int64_t j = 0; j < n; ++j) pre[j + 1] = pre[j] + score[j];
+    int64_t best = lo;
+    double best_sum = pre[lo + w] - pre[lo];
+    for (int64_t s = lo + 1; s + w <= hi; ++s) {
+        const double sum = pre[s + w] - pre[s];
+        if (sum < best_sum) {
+            best_sum = sum;
+            best = s;
+        }
+    }
+    free(pre);
+    return best;
+}

@@ -198,6 +198,35 @@ class OracleCache:
             else:
                 t.a[sel] = L.rope_shift_f16(t.a[sel], self.rope_mode, self.rope_base, delta)
 
+    # -- KeyDiff retention-aware context shift ----------------------------
+    def key_scores(self, s: int, layer: int) -> np.ndarray:
+        """KeyDiff score of every row of sequence s in `layer`, rows in
+        position order ("F5 - Advanced KV Cache Techniques", M1: the per-position
+        score over a representative layer)."""
+        q = self._seq(s)
+        order = np.argsort(q.pos, kind="stable")
+        K = q.K[layer]
+        if len(K) == 0:
+            return np.zeros(0)
+        return L.keydiff_scores(K.type, K.a, K.s)[order]
+
+    def evict_window(self, s: int, layer: int, n_keep: int, n_discard: int, n_recent: int) -> int:
+        """Remove the width-n_discard window of position-ordered rows with the
+        smallest score sum inside [n_keep, n - n_recent), then slide the later
+        positions down over the gap (seq_rm + seq_add).  Returns the first
+        removed position, or -1 when no window fits (nothing changes)."""
+        q = self._seq(s)
+        sc = self.key_scores(s, layer)
+        n = len(sc)
+        w = L.min_window(sc, n_keep, n - n_recent, n_discard)
+        if w < 0:
+            return -1
+        pos = np.sort(q.pos)
+        p0, p1 = int(pos[w]), int(pos[w + n_discard - 1]) + 1
+        self.seq_rm(s, p0, p1)
+        self.seq_add(s, p1, -1, -(p1 - p0))
+        return p0
+
     # -- attention ---------------------------------------------------------
     def attn(self, layer: int, seq_ids, q: np.ndarray, kq_scale: float, heads=None) -> np.ndarray:
         """q fp32 [n_seq][H][D] -> fp64 [n_seq][H][D]."""

@@ -42,6 +42,10 @@ def _load():
     L.orc_rope_shift_q8_0.argtypes = [p, p, i64, i32, i32, f64, i64]
     L.orc_rope_shift_f16.restype = i32
     L.orc_rope_shift_f16.argtypes = [p, i64, i32, i32, f64, i64]
+    L.orc_keydiff_scores.restype = i32
+    L.orc_keydiff_scores.argtypes = [i32, p, p, i64, i32, i32, p]
+    L.orc_min_window.restype = i64
+    L.orc_min_window.argtypes = [p, i64, i64, i64, i64]
     return L
 
 
@@ -158,3 +162,21 @@ def rope_shift_f16(h, mode: int, base: float, delta: int) -> np.ndarray:
     if rc:
         raise ValueError("orc_rope_shift_f16 failed")
     return h
+
+
+def keydiff_scores(type_k, k, ks) -> np.ndarray:
+    """KeyDiff score of every row of one layer's K ([n][Hk][D] stored form),
+    in row order: mean over KV heads of 1 - cos(key, that head's mean key)."""
+    k, ks = _kv_args(type_k, k, ks)
+    n, Hk, D = k.shape
+    out = np.zeros(n, dtype=np.float64)
+    if lib.orc_keydiff_scores(type_k, _ptr(k), _ptr(ks), n, Hk, D, _ptr(out)):
+        raise ValueError("orc_keydiff_scores failed")
+    return out
+
+
+def min_window(score, lo: int, hi: int, w: int) -> int:
+    """Start of the width-w window inside [lo, hi) with the smallest score sum
+    (first on ties); -1 when none fits."""
+    score = np.ascontiguousarray(score, dtype=np.float64)
+    return int(lib.orc_min_window(_ptr(score), score.size, lo, hi, w))

@@ -379,3 +379,105 @@ def test_seq_add_rotates_k_only_for_selected_rows():
     assert np.array_equal(c.seqs[0].K[1].a[:32], k0[:32])
     assert np.array_equal(c.seqs[0].K[1].a[32:], oracle.rope_shift_f16(k0[32:], 0, 1e4, 1000))
     assert np.array_equal(c.positions(0), np.concatenate([np.arange(32), np.arange(1032, 1064)]))
+
+
+# ---------------------------------------------------------------- KeyDiff --
+# Pins of the KeyDiff score ("F5 - Advanced KV Cache Techniques", M1:
+# distinctiveness = mean over KV heads of 1 - cos(key, the head's mean key))
+# and of the minimum-sum window search.
+
+def _f16_keys(x):
+    return oracle.f32_to_f16(np.asarray(x, np.float32))
+
+
+def test_keydiff_closed_forms():
+    # two orthogonal unit keys: mean (1/2, 1/2), cos = 1/sqrt(2) for both
+    sc = oracle.keydiff_scores(oracle.F16, _f16_keys([[[1, 0]], [[0, 1]]]), None)
+    assert np.allclose(sc, 1 - 1 / math.sqrt(2), atol=1e-15, rtol=0)
+    # identical keys: every cosine is 1, every score 0
+    sc = oracle.keydiff_scores(oracle.F16, _f16_keys([[[3, -1, 2]]] * 5), None)
+    assert np.allclose(sc, 0, atol=1e-15)
+    # antipodal keys have a zero mean: the degenerate cosine is read as 0
+    sc = oracle.keydiff_scores(oracle.F16, _f16_keys([[[2, 0]], [[-2, 0]]]), None)
+    assert np.array_equal(sc, [1.0, 1.0])
+    # the score averages over heads: head 0 identical keys (0), head 1 orthogonal
+    sc = oracle.keydiff_scores(oracle.F16, _f16_keys([[[1, 1], [1, 0]], [[1, 1], [0, 1]]]), None)
+    assert np.allclose(sc, (1 - 1 / math.sqrt(2)) / 2, atol=1e-15)
+    # three unit axes in 3-d: mean (1,1,1)/3, cos = 1/sqrt(3)
+    sc = oracle.keydiff_scores(oracle.F16, _f16_keys([[[1, 0, 0]], [[0, 1, 0]], [[0, 0, 1]]]), None)
+    assert np.allclose(sc, 1 - 1 / math.sqrt(3), atol=1e-15)
+
+
+def test_keydiff_invariances():
+    rng = np.random.default_rng(5)
+    x = rng.normal(0, 1, (40, 3, 64)).astype(np.float32)
+    base = oracle.keydiff_scores(oracle.F16, _f16_keys(x), None)
+    # a positive power-of-two scale of every key (exact in fp16) leaves cosines alone
+    assert np.allclose(oracle.keydiff_scores(oracle.F16, _f16_keys(x * 4), None), base, atol=1e-12)
+    # permuting the rows permutes the scores (the mean is order-free)
+    perm = rng.permutation(40)
+    assert np.allclose(oracle.keydiff_scores(oracle.F16, _f16_keys(x[perm]), None), base[perm], atol=1e-12)
+    # permuting the dimensions of every key together changes nothing
+    dp = rng.permutation(64)
+    assert np.allclose(oracle.keydiff_scores(oracle.F16, _f16_keys(x[:, :, dp]), None), base, atol=1e-12)
+    # scores lie in [0, 2]
+    assert base.min() >= 0 and base.max() <= 2
+    # a row equal to its head's mean direction in every head scores 0
+    y = np.concatenate([x, x.mean(axis=0, keepdims=True)], axis=0)
+    sy = oracle.keydiff_scores(oracle.F16, _f16_keys(y), None)
+    assert abs(sy[-1]) < 1e-3  # fp16 rounding of the appended mean row
+
+
+def test_keydiff_q8_0_equals_f16_on_exact_values():
+    # integer keys with max |x| = 127 per block quantise to scale 1.0 and
+    # codes equal to the values: both storage types describe the same keys
+    rng = np.random.default_rng(6)
+    x = rng.integers(-126, 127, (30, 2, 64)).astype(np.float32)
+    x[:, :, ::32] = 127.0
+    codes, scales = oracle.q8_0_quantize(x)
+    assert np.all(oracle.f16_to_f64(scales) == 1.0) and np.array_equal(codes.astype(np.float32), x)
+    a = oracle.keydiff_scores(oracle.Q8_0, codes, scales)
+    b = oracle.keydiff_scores(oracle.F16, _f16_keys(x), None)
+    assert np.array_equal(a, b)
+
+
+def test_min_window_against_brute_force():
+    rng = np.random.default_rng(7)
+    for _ in range(300):
+        n = int(rng.integers(1, 40))
+        sc = rng.random(n)
+        lo, hi, w = int(rng.integers(0, n)), int(rng.integers(0, n + 1)), int(rng.integers(1, 8))
+        got = oracle.min_window(sc, lo, hi, w)
+        starts = [s for s in range(lo, hi - w + 1)]
+        if not starts:
+            assert got == -1
+            continue
+        sums = [sum(sc[s:s + w]) for s in starts]
+        assert got == starts[int(np.argmin(sums))]
+    # ties go to the first window
+    assert oracle.min_window(np.ones(10), 2, 9, 3) == 2
+    # the window never leaves [lo, hi)
+    assert oracle.min_window(np.array([5, 5, 0, 0, 5, 5.0]), 0, 3, 2) == 1
+
+
+def test_evict_window_removes_the_least_distinctive_rows():
+    # 24 rows; rows 10..13 repeat the mean direction of every head (score ~0):
+    # the width-4 window inside [4, 20) must be exactly those rows
+    rng = np.random.default_rng(8)
+    H, Hk, D, n = 4, 2, 64, 24
+    k = rng.normal(0, 1, (n, Hk, D)).astype(np.float32)
+    k[10:14] = k.mean(axis=0)
+    v = rng.normal(0, 1, (n, Hk, D)).astype(np.float32)
+    c = oracle.OracleCache(1, H, Hk, D, oracle.F16, oracle.F16, 1e4, 0)
+    c.append(0, 0, 0, k, v)
+    sc = c.key_scores(0, 0)
+    assert sc[10:14].max() < sc[np.r_[0:10, 14:24]].min()
+    v_before = c.seqs[0].V[0].a.copy()
+    p0 = c.evict_window(0, 0, n_keep=4, n_discard=4, n_recent=4)
+    assert p0 == 10
+    assert np.array_equal(c.positions(0), np.arange(n - 4))  # slid down over the gap
+    keep = np.r_[0:10, 14:24]
+    assert np.array_equal(c.seqs[0].V[0].a, v_before[keep])   # V untouched, window gone
+    # no window fits: nothing changes
+    assert c.evict_window(0, 0, n_keep=10, n_discard=8, n_recent=4) == -1
+    assert c.n_tokens(0) == n - 4
