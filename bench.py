@@ -474,6 +474,37 @@ def churn(kvc, torch, dev, n: int, cycles: int, layers: int):
         cache.close()
 
 
+def keydiff(kvc, torch, dev, n: int, layers: int, reps: int = 10):
+    """KeyDiff scores of one layer of an n-token q8_0 cache (two passes over
+    that layer's K) and one retention-aware context shift (scores, window,
+    seq_rm, slide of the later rows in every layer).  Synchronous API calls."""
+    from kv_cache_decode_flash_gb300 import synth
+
+    cache = kvc.KVCache(layers, H, HK, D, n + 512, 1, kvc.KVC_Q8_0, kvc.KVC_Q8_0, 1e6)
+    try:
+        for l in range(layers):
+            for p0 in range(0, n, 8192):
+                m = min(8192, n - p0)
+                k = synth.normal_torch(0, synth.stream_id("k", l, p0), m * HK * D, 0.5, dev).view(m, HK, D)
+                cache.append(l, 0, p0, k, k)
+        torch.cuda.synchronize()
+        cache.key_scores(0, -1)
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            sc = cache.key_scores(0, -1)
+        dt = (time.perf_counter() - t0) / reps
+        kbytes = n * HK * (D + (D // 32) * 2)  # one layer's K codes + scales
+        t0 = time.perf_counter()
+        p0 = cache.evict_window(0, -1, 4, 8192, 1024)
+        dt_evict = time.perf_counter() - t0
+        return {"n_kv": n, "layers": layers, "score_ms": round(dt * 1e3, 3),
+                "score_gbs": round(2 * kbytes / dt / GB, 1), "bytes": "2 passes over one layer's K",
+                "evict_ms": round(dt_evict * 1e3, 3), "evicted_from": p0, "rows_after": cache.n_tokens(0),
+                "score_range": [round(float(sc.min()), 4), round(float(sc.max()), 4)]}
+    finally:
+        cache.close()
+
+
 def run_ours(args, rank: int, world: int):
     import torch
 
@@ -628,7 +659,8 @@ def run_ours(args, rank: int, world: int):
                          ("f16_4k", lambda: attn_only_gbs(kvc, torch, dev, "f16", 4096)),
                          ("ragged_q8_0", lambda: ragged(kvc, torch, dev, "q8_0")),
                          ("ragged_f16", lambda: ragged(kvc, torch, dev, "f16")),
-                         ("churn", lambda: churn(kvc, torch, dev, args.churn_n, args.churn_cycles, args.layers))):
+                         ("churn", lambda: churn(kvc, torch, dev, args.churn_n, args.churn_cycles, args.layers)),
+                         ("keydiff", lambda: keydiff(kvc, torch, dev, args.churn_n, args.layers))):
             try:
                 ex[name] = fn()
             except Exception as e:  # reported, not fatal

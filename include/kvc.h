@@ -201,6 +201,30 @@ int kvc_state_get(kvc_ctx *c, int seq, int p0, int p1, void *dst, size_t cap,
  * Errors: KVC_EFORMAT (bad magic, version, geometry, length), KVC_ENOSPC. */
 int kvc_state_set(kvc_ctx *c, int seq, const void *src, size_t n, size_t *n_read);
 
+/* KeyDiff distinctiveness of every row of `seq` in one layer ([F5] section
+ * M1 - retention-aware context shift, which evicts the keys least
+ * distinctive by cosine similarity): score_j = (1/n_head_kv) * sum over KV
+ * heads g of (1 - cos(K_j,g, mu_g)), mu_g the mean of head g's keys over the
+ * sequence's rows, the cosine read as 0 when either norm is 0.  Keys are
+ * the stored (post-RoPE) K, q8_0 dequantised exactly; scores are fp32.
+ * Rows come in position order.  scores: HOST float[cap], or NULL to only
+ * receive the row count in *n.  layer < 0 selects n_layer / 2 (the page's
+ * default representative layer).  Device-resident contexts only.
+ * Errors: KVC_EINVAL, KVC_ENOSPC (cap below the row count). */
+int kvc_seq_key_scores(kvc_ctx *c, int seq, int layer, float *scores, int32_t cap, int32_t *n);
+
+/* Retention-aware context shift ([F5] section M1): among the windows of
+ * n_discard consecutive rows (position order) that lie inside
+ * [n_keep, rows - n_recent), remove the one with the smallest sum of
+ * KeyDiff scores (kvc_seq_key_scores of `layer`; sums in fp64, the first
+ * window on ties) with kvc_seq_rm over the positions it spans, then move
+ * every later position down over the gap with kvc_seq_add (which re-rotates
+ * those rows' K).  *p0 receives the first removed position, or -1 when no
+ * window fits (nothing changes).  Positions are taken to be distinct.
+ * Errors: KVC_EINVAL (n_discard < 1, n_keep or n_recent < 0), and those of
+ * the operations it runs. */
+int kvc_seq_evict_window(kvc_ctx *c, int seq, int layer, int n_keep, int n_discard, int n_recent, int32_t *p0);
+
 /* Pipeline depth N of the host-resident transport: deliveries are issued N
  * layers ahead into an (N+2)-slot ring; 0 is the ordered path exactly
  * (deliver, then attend, in stream order).  Default 1 ([R4] section What it

@@ -806,6 +806,117 @@ int kvc_seq_add(kvc_ctx *cc, int seq, int p0, int p1, int delta) {
     return KVC_OK;
 }
 
+int kvc_seq_key_scores(kvc_ctx *cc, int seq, int layer, float *scores, int32_t cap, int32_t *n) {
+    if (!cc || !n) return KVC_EINVAL;
+    Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (c->host) return c->fail(KVC_EINVAL, "sequence operations need a device-resident context");
+    if (seq < 0 || seq >= (int)c->seqs.size()) return c->fail(KVC_EINVAL, "sequence id out of range");
+    if (layer < 0) layer = c->L / 2;
+    if (layer >= c->L) return c->fail(KVC_EINVAL, "layer out of range");
+    Seq &q = c->seqs[(size_t)seq];
+    if (!q.synced()) return c->fail(KVC_EINVAL, "layers are not in sync");
+    const int64_t rows = q.n;
+    *n = (int32_t)rows;
+    if (!scores) return KVC_OK;
+    if (cap < rows) return c->fail(KVC_ENOSPC, "score buffer too small");
+    if (rows == 0) return KVC_OK;
+    int rc = enter_sync(c);
+    if (rc) return rc;
+    // rows in position order (head 0's layer-0 row of each), and the page runs
+    // of every KV head for the mean
+    std::vector<int64_t> order((size_t)rows);
+    for (int64_t r = 0; r < rows; ++r) order[(size_t)r] = r;
+    if (!std::is_sorted(q.pos.begin(), q.pos.end()))
+        std::stable_sort(order.begin(), order.end(),
+                         [&](int64_t a, int64_t b) { return q.pos[(size_t)a] < q.pos[(size_t)b]; });
+    std::vector<int64_t> base((size_t)rows);
+    for (int64_t j = 0; j < rows; ++j) {
+        int32_t pg, cl;
+        phys(c, q, order[(size_t)j], pg, cl);
+        base[(size_t)j] = prow(c, pg, 0, cl);
+    }
+    std::vector<RopeSpan> spans;
+    std::vector<int32_t> heads;
+    for (int64_t i = 0; i < rows;) {
+        int32_t pg, cl;
+        phys(c, q, i, pg, cl);
+        int64_t j = i + 1;
+        while (j < rows && (j - i) < ROPE_SPAN_MAX && cl + (j - i) < c->P) ++j;
+        for (int g = 0; g < c->Hk; ++g) {
+            spans.push_back(RopeSpan{prow(c, pg, g, cl), (int32_t)(j - i), 0});
+            heads.push_back(g);
+        }
+        i = j;
+    }
+    // device work space in the staging buffer
+    auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
+    const int64_t o_base = 0, o_spans = al(rows * 8), o_heads = o_spans + al((int64_t)spans.size() * 16);
+    const int64_t o_sum = o_heads + al((int64_t)heads.size() * 4);
+    const int64_t o_mean = o_sum + al((int64_t)spans.size() * c->D * 4);
+    const int64_t o_norm = o_mean + al((int64_t)c->Hk * c->D * 4), o_score = o_norm + al((int64_t)c->Hk * 4);
+    if ((rc = ensure_staging(c, o_score + al(rows * 4)))) return rc;
+    uint8_t *w = c->staging;
+    KVC_CU(c, cudaMemcpyAsync(w + o_base, base.data(), (size_t)rows * 8, cudaMemcpyHostToDevice, c->st));
+    KVC_CU(c, cudaMemcpyAsync(w + o_spans, spans.data(), spans.size() * 16, cudaMemcpyHostToDevice, c->st));
+    KVC_CU(c, cudaMemcpyAsync(w + o_heads, heads.data(), heads.size() * 4, cudaMemcpyHostToDevice, c->st));
+    KeyDiffArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.q8 = c->tk == KVC_Q8_0;
+    a.Hk = c->Hk;
+    a.D = c->D;
+    a.P = c->P;
+    a.kdata = c->kdata;
+    a.kscales = a.q8 ? reinterpret_cast<const uint16_t *>(c->kscales) : nullptr;
+    a.layer_off = (int64_t)layer * c->pool_rows;
+    a.spans = reinterpret_cast<const RopeSpan *>(w + o_spans);
+    a.span_head = reinterpret_cast<const int32_t *>(w + o_heads);
+    a.n_spans = (int32_t)spans.size();
+    a.row_base = reinterpret_cast<const int64_t *>(w + o_base);
+    a.n_rows = rows;
+    a.span_sum = reinterpret_cast<float *>(w + o_sum);
+    a.mean = reinterpret_cast<float *>(w + o_mean);
+    a.mean_norm = reinterpret_cast<float *>(w + o_norm);
+    a.score = reinterpret_cast<float *>(w + o_score);
+    cudaError_t e = launch_keydiff(a, c->st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "KeyDiff kernels");
+    KVC_CU(c, cudaMemcpyAsync(scores, w + o_score, (size_t)rows * 4, cudaMemcpyDeviceToHost, c->st));
+    return wait_internal(c);
+}
+
+int kvc_seq_evict_window(kvc_ctx *cc, int seq, int layer, int n_keep, int n_discard, int n_recent, int32_t *p0) {
+    if (!cc || !p0) return KVC_EINVAL;
+    Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (n_discard < 1 || n_keep < 0 || n_recent < 0) return c->fail(KVC_EINVAL, "bad window arguments");
+    *p0 = -1;
+    int32_t n = 0;
+    int rc = kvc_seq_key_scores(cc, seq, layer, nullptr, 0, &n);
+    if (rc) return rc;
+    std::vector<float> sc((size_t)n);
+    if (n > 0 && (rc = kvc_seq_key_scores(cc, seq, layer, sc.data(), n, &n))) return rc;
+    // smallest window sum by prefix sums in fp64 (the first on ties)
+    const int64_t lo = n_keep, hi = (int64_t)n - n_recent, wd = n_discard;
+    if (hi - lo < wd) return KVC_OK;
+    std::vector<double> pre((size_t)n + 1, 0.0);
+    for (int64_t j = 0; j < n; ++j) pre[(size_t)j + 1] = pre[(size_t)j] + (double)sc[(size_t)j];
+    int64_t best = lo;
+    double best_sum = pre[(size_t)(lo + wd)] - pre[(size_t)lo];
+    for (int64_t s = lo + 1; s + wd <= hi; ++s) {
+        const double sum = pre[(size_t)(s + wd)] - pre[(size_t)s];
+        if (sum < best_sum) {
+            best_sum = sum;
+            best = s;
+        }
+    }
+    Seq &q = c->seqs[(size_t)seq];
+    std::vector<int32_t> pos(q.pos.begin(), q.pos.end());
+    std::stable_sort(pos.begin(), pos.end());
+    const int32_t first = pos[(size_t)best], last = pos[(size_t)(best + wd - 1)];
+    if ((rc = kvc_seq_rm(cc, seq, first, last + 1))) return rc;
+    if ((rc = kvc_seq_add(cc, seq, last + 1, -1, -(last + 1 - first)))) return rc;
+    *p0 = first;
+    return KVC_OK;
+}
+
 int kvc_state_get(kvc_ctx *cc, int seq, int p0, int p1, void *dst, size_t cap, size_t *n_written) {
     if (!cc) return KVC_EINVAL;
     Ctx *c = reinterpret_cast<Ctx *>(cc);

@@ -141,6 +141,25 @@ cudaError_t launch_rope_shift(int type_k, int D, int mode, void *kdata, uint16_t
                               int n_layer, const RopeSpan *spans_dev, int64_t n_spans, const float2 *cs,
                               cudaStream_t st);
 
+// KeyDiff scan over one layer's K of one sequence (k_keydiff.cu).
+struct KeyDiffArgs {
+    bool q8;                   // K type q8_0 (offset-binary codes + fp16 scales) or f16
+    int32_t Hk, D, P;          // P: rows per page (head g's row = head 0's row + g * P)
+    const uint8_t *kdata;      // K pool base (codes or halves)
+    const uint16_t *kscales;   // q8_0 scales (else null)
+    int64_t layer_off;         // first row of the layer in the pool
+    const RopeSpan *spans;     // page runs of the sequence, one per KV head (row0: layer-0 row)
+    const int32_t *span_head;  // KV head of every span
+    int32_t n_spans;
+    const int64_t *row_base;   // per row in position order: head 0's layer-0 row
+    int64_t n_rows;
+    float *span_sum;           // work: [n_spans][D]
+    float *mean;               // work: [Hk][D]
+    float *mean_norm;          // work: [Hk]
+    float *score;              // out: [n_rows]
+};
+cudaError_t launch_keydiff(const KeyDiffArgs &a, cudaStream_t st);
+
 // Encode a 2D tiled tensor map (rows x row_bytes) for the attention kernel.
 bool encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int row_bytes, int type, bool swizzle,
                      std::string *why, int box_rows = TMA_BOX_ROWS);

@@ -72,6 +72,8 @@ def load():
         "kvc_seq_add": (i32, [p, i32, i32, i32, i32]),
         "kvc_state_get": (i32, [p, i32, i32, i32, p, sz, C.POINTER(sz)]),
         "kvc_state_set": (i32, [p, i32, p, sz, C.POINTER(sz)]),
+        "kvc_seq_key_scores": (i32, [p, i32, i32, p, C.c_int32, C.POINTER(C.c_int32)]),
+        "kvc_seq_evict_window": (i32, [p, i32, i32, i32, i32, i32, C.POINTER(C.c_int32)]),
         "kvc_pipeline_depth": (i32, [p, i32]),
         "kvc_pipeline_budget": (i32, [p, sz]),
         "kvc_seq_n_tokens": (i32, [p, i32, C.POINTER(C.c_int32)]),
@@ -213,6 +215,25 @@ def _host_buffer(b):
     raise TypeError("expected a host buffer")
 
 
+def kvc_seq_key_scores(ctx, seq, layer=-1):
+    """KeyDiff score of every row of `seq` in `layer` (position order), fp32."""
+    import numpy as np
+
+    n = C.c_int32()
+    _check(ctx, load().kvc_seq_key_scores(ctx, seq, layer, None, 0, C.byref(n)))
+    out = np.zeros(n.value, np.float32)
+    if n.value:
+        _check(ctx, load().kvc_seq_key_scores(ctx, seq, layer, out.ctypes.data, n.value, C.byref(n)))
+    return out
+
+
+def kvc_seq_evict_window(ctx, seq, layer, n_keep, n_discard, n_recent) -> int:
+    """Retention-aware context shift; returns the first removed position or -1."""
+    p0 = C.c_int32()
+    _check(ctx, load().kvc_seq_evict_window(ctx, seq, layer, n_keep, n_discard, n_recent, C.byref(p0)))
+    return p0.value
+
+
 def kvc_pipeline_depth(ctx, n):
     _check(ctx, load().kvc_pipeline_depth(ctx, n))
 
@@ -306,6 +327,12 @@ class KVCache:
 
     def state_set(self, seq, src, n=None):
         return kvc_state_set(self.ctx, seq, src, n)
+
+    def key_scores(self, seq, layer=-1):
+        return kvc_seq_key_scores(self.ctx, seq, layer)
+
+    def evict_window(self, seq, layer, n_keep, n_discard, n_recent):
+        return kvc_seq_evict_window(self.ctx, seq, layer, n_keep, n_discard, n_recent)
 
     def n_tokens(self, seq):
         return kvc_seq_n_tokens(self.ctx, seq)

@@ -422,3 +422,61 @@ def test_enospc_leaves_cache_unchanged():
         assert tw.gpu.state_get(0, -1, -1) == before
     finally:
         tw.close()
+
+
+# ------------------------------------------------------------- KeyDiff --
+@pytest.mark.parametrize("type_,D,Hk", [(Q8, 128, 8), (F16, 128, 8), (Q8, 64, 2), (F16, 64, 4)])
+def test_key_scores_match_oracle(type_, D, Hk):
+    """KeyDiff scores of a multi-page sequence whose row order differs from
+    its position order (a block copied in from another sequence)."""
+    tw = Twin(3, 2 * Hk, Hk, D, 4096, n_seq_max=2, type_=type_, page_rows=64)
+    try:
+        tw.fill(0, 900, seed=20, sigma=0.5)
+        tw.fill(1, 300, seed=21, pos0=100, sigma=0.5)
+        tw.gpu.seq_rm(0, 100, 250)
+        tw.ref.seq_rm(0, 100, 250)
+        tw.gpu.seq_cp(1, 0, 100, 250)  # appended rows that sort before most of the sequence
+        tw.ref.seq_cp(1, 0, 100, 250)
+        assert not np.all(np.diff(tw.gpu.positions(0)) > 0)
+        for layer in (-1, 0, 2):
+            got = tw.gpu.key_scores(0, layer).astype(np.float64)
+            want = tw.ref.key_scores(0, layer if layer >= 0 else 1)
+            assert got.shape == want.shape
+            assert np.abs(got - want).max() <= 1e-4, (layer, np.abs(got - want).max())
+    finally:
+        tw.close()
+
+
+@pytest.mark.parametrize("type_", [Q8, F16])
+def test_evict_window_matches_oracle(type_):
+    """Rows 700..763 of a 1200-row sequence repeat each head's mean key, so
+    they are the least distinctive window: both sides remove exactly them and
+    slide the rest down (RoPE re-rotation of the later K rows)."""
+    H, Hk, D, n = 16, 4, 128, 1200
+    tw = Twin(2, H, Hk, D, 2048, type_=type_, rope_base=1e6, page_rows=256)
+    try:
+        for l in range(2):
+            k, v = kv_inputs(22, l, n, Hk, D, sigma=0.5)
+            k[700:764] = k.mean(axis=0)
+            tw.append(l, 0, 0, k, v)
+        sc = tw.gpu.key_scores(0, 1)
+        assert sc[700:764].max() < np.delete(sc, np.s_[700:764]).min()
+        p_gpu = tw.gpu.evict_window(0, 1, 128, 64, 128)
+        p_ref = tw.ref.evict_window(0, 1, 128, 64, 128)
+        assert p_gpu == p_ref == 700
+        assert np.array_equal(tw.gpu.positions(0), tw.ref.positions(0))
+        assert np.array_equal(tw.gpu.positions(0), np.arange(n - 64))
+        if type_ == Q8:
+            _check_shifted_q8(tw, 0)
+        else:
+            pos_g, Kg, Vg = tw.ref.parse_state(tw.gpu.state_get(0, -1, -1))
+            for l in range(2):
+                assert np.array_equal(Vg[l].a, tw.ref.seqs[0].V[l].a)
+                a = oracle.f16_to_f64(Kg[l].a)
+                b = oracle.f16_to_f64(tw.ref.seqs[0].K[l].a)
+                assert np.abs(a - b).max() <= 2e-3
+        # no window fits: nothing changes
+        assert tw.gpu.evict_window(0, 1, 600, 600, 100) == -1
+        assert tw.gpu.n_tokens(0) == n - 64
+    finally:
+        tw.close()
