@@ -54,7 +54,8 @@ void dev_free(Ctx *c, void *p, int64_t bytes) {
     c->device_bytes -= bytes;
 }
 
-// Wait for the internal stream with a deadline (polling; never an unbounded block).
+// Wait for the internal stream with a deadline (polling; never an unbounded
+// block).  Short waits spin; past 2 ms the poll sleeps between queries.
 int wait_internal(Ctx *c) {
     KVC_CU(c, cudaEventRecord(c->done, c->st));
     auto t0 = std::chrono::steady_clock::now();
@@ -62,9 +63,9 @@ int wait_internal(Ctx *c) {
         cudaError_t e = cudaEventQuery(c->done);
         if (e == cudaSuccess) break;
         if (e != cudaErrorNotReady) return cuda_fail(c, e, "device work of a synchronous operation");
-        auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(std::chrono::steady_clock::now() - t0).count();
-        if (ms > c->timeout_ms) return c->fail(KVC_ETIMEDOUT, "timed out waiting for device work");
-        std::this_thread::sleep_for(std::chrono::microseconds(50));
+        auto us = std::chrono::duration_cast<std::chrono::microseconds>(std::chrono::steady_clock::now() - t0).count();
+        if (us > (int64_t)c->timeout_ms * 1000) return c->fail(KVC_ETIMEDOUT, "timed out waiting for device work");
+        if (us > 2000) std::this_thread::sleep_for(std::chrono::microseconds(50));
     }
     uint32_t word = 0;
     KVC_CU(c, cudaMemcpyAsync(&word, c->err_dev, 4, cudaMemcpyDeviceToHost, c->st));
@@ -822,43 +823,27 @@ int kvc_seq_key_scores(kvc_ctx *cc, int seq, int layer, float *scores, int32_t c
     if (rows == 0) return KVC_OK;
     int rc = enter_sync(c);
     if (rc) return rc;
-    // rows in position order (head 0's layer-0 row of each), and the page runs
-    // of every KV head for the mean
-    std::vector<int64_t> order((size_t)rows);
-    for (int64_t r = 0; r < rows; ++r) order[(size_t)r] = r;
-    if (!std::is_sorted(q.pos.begin(), q.pos.end()))
-        std::stable_sort(order.begin(), order.end(),
-                         [&](int64_t a, int64_t b) { return q.pos[(size_t)a] < q.pos[(size_t)b]; });
-    std::vector<int64_t> base((size_t)rows);
-    for (int64_t j = 0; j < rows; ++j) {
-        int32_t pg, cl;
-        phys(c, q, order[(size_t)j], pg, cl);
-        base[(size_t)j] = prow(c, pg, 0, cl);
-    }
-    std::vector<RopeSpan> spans;
-    std::vector<int32_t> heads;
+    // the rows in storage order as blocks of consecutive rows of one page;
+    // the scores come back in that order and are put in position order here
+    std::vector<KeyDiffBlock> blocks;
+    const int br = keydiff_block_rows(c->tk == KVC_Q8_0, c->Hk, c->D);
     for (int64_t i = 0; i < rows;) {
         int32_t pg, cl;
         phys(c, q, i, pg, cl);
-        int64_t j = i + 1;
-        while (j < rows && (j - i) < ROPE_SPAN_MAX && cl + (j - i) < c->P) ++j;
-        for (int g = 0; g < c->Hk; ++g) {
-            spans.push_back(RopeSpan{prow(c, pg, g, cl), (int32_t)(j - i), 0});
-            heads.push_back(g);
-        }
-        i = j;
+        const int64_t n = std::min<int64_t>({(int64_t)br, rows - i, (int64_t)(c->P - cl)});
+        blocks.push_back(KeyDiffBlock{prow(c, pg, 0, cl), (int32_t)n, (int32_t)i});
+        i += n;
     }
-    // device work space in the staging buffer
+    const int64_t nb = (int64_t)blocks.size();
+    const int64_t slices = (nb + keydiff_slice_blocks() - 1) / keydiff_slice_blocks();
     auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
-    const int64_t o_base = 0, o_spans = al(rows * 8), o_heads = o_spans + al((int64_t)spans.size() * 16);
-    const int64_t o_sum = o_heads + al((int64_t)heads.size() * 4);
-    const int64_t o_mean = o_sum + al((int64_t)spans.size() * c->D * 4);
+    const int64_t o_blocks = 0, o_sum = al(nb * (int64_t)sizeof(KeyDiffBlock));
+    const int64_t o_mean = o_sum + al((int64_t)c->Hk * slices * c->D * 4);
     const int64_t o_norm = o_mean + al((int64_t)c->Hk * c->D * 4), o_score = o_norm + al((int64_t)c->Hk * 4);
     if ((rc = ensure_staging(c, o_score + al(rows * 4)))) return rc;
     uint8_t *w = c->staging;
-    KVC_CU(c, cudaMemcpyAsync(w + o_base, base.data(), (size_t)rows * 8, cudaMemcpyHostToDevice, c->st));
-    KVC_CU(c, cudaMemcpyAsync(w + o_spans, spans.data(), spans.size() * 16, cudaMemcpyHostToDevice, c->st));
-    KVC_CU(c, cudaMemcpyAsync(w + o_heads, heads.data(), heads.size() * 4, cudaMemcpyHostToDevice, c->st));
+    KVC_CU(c, cudaMemcpyAsync(w + o_blocks, blocks.data(), blocks.size() * sizeof(KeyDiffBlock),
+                              cudaMemcpyHostToDevice, c->st));
     KeyDiffArgs a;
     std::memset(&a, 0, sizeof(a));
     a.q8 = c->tk == KVC_Q8_0;
@@ -868,19 +853,31 @@ int kvc_seq_key_scores(kvc_ctx *cc, int seq, int layer, float *scores, int32_t c
     a.kdata = c->kdata;
     a.kscales = a.q8 ? reinterpret_cast<const uint16_t *>(c->kscales) : nullptr;
     a.layer_off = (int64_t)layer * c->pool_rows;
-    a.spans = reinterpret_cast<const RopeSpan *>(w + o_spans);
-    a.span_head = reinterpret_cast<const int32_t *>(w + o_heads);
-    a.n_spans = (int32_t)spans.size();
-    a.row_base = reinterpret_cast<const int64_t *>(w + o_base);
+    a.blocks = reinterpret_cast<const KeyDiffBlock *>(w + o_blocks);
+    a.n_blocks = (int32_t)nb;
+    a.block_rows = br;
+    a.n_slices = (int32_t)slices;
     a.n_rows = rows;
-    a.span_sum = reinterpret_cast<float *>(w + o_sum);
+    a.slice_sum = reinterpret_cast<float *>(w + o_sum);
     a.mean = reinterpret_cast<float *>(w + o_mean);
     a.mean_norm = reinterpret_cast<float *>(w + o_norm);
     a.score = reinterpret_cast<float *>(w + o_score);
-    cudaError_t e = launch_keydiff(a, c->st);
+    a.err = c->err_dev;
+    cudaError_t e = launch_keydiff(a, c->sms, c->st);
     if (e != cudaSuccess) return cuda_fail(c, e, "KeyDiff kernels");
-    KVC_CU(c, cudaMemcpyAsync(scores, w + o_score, (size_t)rows * 4, cudaMemcpyDeviceToHost, c->st));
-    return wait_internal(c);
+    if (std::is_sorted(q.pos.begin(), q.pos.end())) {
+        KVC_CU(c, cudaMemcpyAsync(scores, w + o_score, (size_t)rows * 4, cudaMemcpyDeviceToHost, c->st));
+        return wait_internal(c);
+    }
+    std::vector<float> tmp((size_t)rows);
+    KVC_CU(c, cudaMemcpyAsync(tmp.data(), w + o_score, (size_t)rows * 4, cudaMemcpyDeviceToHost, c->st));
+    if ((rc = wait_internal(c))) return rc;
+    std::vector<int64_t> order((size_t)rows);
+    for (int64_t r = 0; r < rows; ++r) order[(size_t)r] = r;
+    std::stable_sort(order.begin(), order.end(),
+                     [&](int64_t x, int64_t y) { return q.pos[(size_t)x] < q.pos[(size_t)y]; });
+    for (int64_t j = 0; j < rows; ++j) scores[j] = tmp[(size_t)order[(size_t)j]];
+    return KVC_OK;
 }
 
 int kvc_seq_evict_window(kvc_ctx *cc, int seq, int layer, int n_keep, int n_discard, int n_recent, int32_t *p0) {

@@ -142,23 +142,35 @@ cudaError_t launch_rope_shift(int type_k, int D, int mode, void *kdata, uint16_t
                               cudaStream_t st);
 
 // KeyDiff scan over one layer's K of one sequence (k_keydiff.cu).
+// A block of n <= block_rows consecutive rows of one page: row0 is head
+// 0's layer-0 row of the first, i0 the first row's index in the output.
+struct KeyDiffBlock {
+    int64_t row0;
+    int32_t n;
+    int32_t i0;
+};
+// Rows per block for a K type / head count / head size (the score kernel's
+// stages must fit in shared memory), and blocks per pass-1 slice.
+int keydiff_block_rows(bool q8, int Hk, int D);
+int keydiff_slice_blocks();
 struct KeyDiffArgs {
     bool q8;                   // K type q8_0 (offset-binary codes + fp16 scales) or f16
     int32_t Hk, D, P;          // P: rows per page (head g's row = head 0's row + g * P)
     const uint8_t *kdata;      // K pool base (codes or halves)
     const uint16_t *kscales;   // q8_0 scales (else null)
     int64_t layer_off;         // first row of the layer in the pool
-    const RopeSpan *spans;     // page runs of the sequence, one per KV head (row0: layer-0 row)
-    const int32_t *span_head;  // KV head of every span
-    int32_t n_spans;
-    const int64_t *row_base;   // per row in position order: head 0's layer-0 row
+    const KeyDiffBlock *blocks; // the sequence's rows
+    int32_t n_blocks;
+    int32_t block_rows;
+    int32_t n_slices;          // pass 1: every head's blocks in slices of keydiff_slice_blocks()
     int64_t n_rows;
-    float *span_sum;           // work: [n_spans][D]
+    float *slice_sum;          // work: [Hk][n_slices][D]
     float *mean;               // work: [Hk][D]
     float *mean_norm;          // work: [Hk]
-    float *score;              // out: [n_rows]
+    float *score;              // out: [n_rows], by the blocks' i0
+    uint32_t *err;             // device error word (ERR_WAIT_TIMEOUT)
 };
-cudaError_t launch_keydiff(const KeyDiffArgs &a, cudaStream_t st);
+cudaError_t launch_keydiff(const KeyDiffArgs &a, int sms, cudaStream_t st);
 
 // Encode a 2D tiled tensor map (rows x row_bytes) for the attention kernel.
 bool encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int row_bytes, int type, bool swizzle,
