@@ -431,10 +431,10 @@ int kvc_create(const kvc_params *p, kvc_ctx **out) {
         return fail(KVC_ECUDA);
     }
     if ((rc = dev_alloc(c, (void **)&c->err_dev, 4, "error word"))) return fail(rc);
-    cudaMemset(c->err_dev, 0, 4);
+    cudaMemsetAsync(c->err_dev, 0, 4, c->st);
     if ((rc = dev_alloc(c, (void **)&c->tickets, (int64_t)MAX_SEQ_PER_LAUNCH * c->Hk * 4, "tickets")))
         return fail(rc);
-    cudaMemset(c->tickets, 0, (size_t)MAX_SEQ_PER_LAUNCH * c->Hk * 4);
+    cudaMemsetAsync(c->tickets, 0, (size_t)MAX_SEQ_PER_LAUNCH * c->Hk * 4, c->st);
 
     if (!c->host) {
         c->P = page_rows;
@@ -1138,7 +1138,8 @@ int kvc_check_device_error(kvc_ctx *cc, uint32_t *word) {
     KVC_CU(c, cudaSetDevice(c->dev));
     KVC_CU(c, cudaDeviceSynchronize());
     KVC_CU(c, cudaMemcpy(word, c->err_dev, 4, cudaMemcpyDeviceToHost));
-    KVC_CU(c, cudaMemset(c->err_dev, 0, 4));
+    KVC_CU(c, cudaMemsetAsync(c->err_dev, 0, 4, c->st)); // the internal stream is non-blocking: wait for it
+    KVC_CU(c, cudaStreamSynchronize(c->st));
     return KVC_OK;
 }
 

@@ -154,7 +154,10 @@ static void free_slot(Ctx *c, Slot &s) {
     s = Slot();
 }
 
-static int alloc_slot(Ctx *c, Slot &s, int32_t cap) {
+// Allocate and zero a slot.  The zeroing runs on `st`; the slot's ready
+// event is recorded after it, so a delivery issued on any other stream (the
+// non-blocking transfer stream) waits for it instead of racing it.
+static int alloc_slot(Ctx *c, Slot &s, int32_t cap, cudaStream_t st) {
     s = Slot();
     const int64_t rows = (int64_t)c->Hk * cap;
     int rc;
@@ -168,10 +171,10 @@ static int alloc_slot(Ctx *c, Slot &s, int32_t cap) {
     c->device_bytes = before + s.bytes;
     s.scale_bytes = c->ksb ? rows * c->ksb + 64 : 0;
     s.cap = cap;
-    KVC_CU(c, cudaMemset(s.kdata, 0, (size_t)(rows * c->krow + 64)));
-    KVC_CU(c, cudaMemset(s.vdata, 0, (size_t)(rows * c->vrow + 64)));
-    if (s.kscales) KVC_CU(c, cudaMemset(s.kscales, 0, (size_t)(rows * c->ksb + 64)));
-    if (s.vscales) KVC_CU(c, cudaMemset(s.vscales, 0, (size_t)(rows * c->vsb + 64)));
+    KVC_CU(c, cudaMemsetAsync(s.kdata, 0, (size_t)(rows * c->krow + 64), st));
+    KVC_CU(c, cudaMemsetAsync(s.vdata, 0, (size_t)(rows * c->vrow + 64), st));
+    if (s.kscales) KVC_CU(c, cudaMemsetAsync(s.kscales, 0, (size_t)(rows * c->ksb + 64), st));
+    if (s.vscales) KVC_CU(c, cudaMemsetAsync(s.vscales, 0, (size_t)(rows * c->vsb + 64), st));
     std::string why;
     for (int b = 0; b < 2; ++b) {
         const int box = b ? (int)std::min<int64_t>(TMA_BIG_ROWS, rows) : TMA_BOX_ROWS;
@@ -181,6 +184,9 @@ static int alloc_slot(Ctx *c, Slot &s, int32_t cap) {
     }
     KVC_CU(c, cudaEventCreateWithFlags(&s.ready, cudaEventDisableTiming));
     KVC_CU(c, cudaEventCreateWithFlags(&s.release, cudaEventDisableTiming));
+    KVC_CU(c, cudaEventRecord(s.ready, st));
+    s.delivered = true; // holds no layer (layer -1), but a copy into it must follow the zeroing
+    s.ready_stream = st;
     return KVC_OK;
 }
 
@@ -233,7 +239,7 @@ static int plan(Ctx *c, int64_t n, cudaStream_t st, bool *engaged) {
     auto make_ring = [&](int32_t cap, bool rolling, int slots) -> int {
         t.ring.resize((size_t)slots);
         for (auto &s : t.ring) {
-            int rc = alloc_slot(c, s, cap);
+            int rc = alloc_slot(c, s, cap, st);
             if (rc) {
                 transport_release(c);
                 return rc;
@@ -525,7 +531,7 @@ int transport_attn(Ctx *c, int layer, const float *q, float *out, float kq_scale
                 KVC_CU(c, cudaStreamSynchronize(st));
                 dev_free_slot_memory(c, o);
             }
-            if ((rc = alloc_slot(c, o, cap_for(c, std::max<int64_t>(rows, sq.n))))) return rc;
+            if ((rc = alloc_slot(c, o, cap_for(c, std::max<int64_t>(rows, sq.n)), st))) return rc;
         }
         if ((rc = deliver(c, o, layer, rows, st))) return rc;
         ++c->tr.in_order;

@@ -294,6 +294,47 @@ def _host_run(depth, budget, L=8, H=40, Hk=8, D=128, n=2000, steps=3, chunk=0):
         cache.close()
 
 
+def test_host_resident_ring_built_behind_busy_stream():
+    """The ring is built by the first attention after a fill, while the
+    compute stream is still busy (a bounded spin): the slots' zeroing is
+    queued behind that work, and the first look-ahead delivery on the
+    non-blocking transfer stream must wait for it rather than land first and
+    be wiped.  Ring (depth 1 and 4) and rolling tiles against ordered."""
+    import torch
+
+    from kv_cache_decode_flash_gb300 import kvc
+
+    L, H, Hk, D, n = 8, 40, 8, 128, 4000
+    dev = torch.device("cuda:0")
+    kv = [[torch.from_numpy(a).to(dev) for a in kv_inputs(15, l, n, Hk, D, sigma=0.5)] for l in range(L)]
+    new = [[torch.from_numpy(a).to(dev) for a in kv_inputs(15, l, 1, Hk, D, pos0=n, sigma=0.5)] for l in range(L)]
+    q = torch.from_numpy(q_inputs(15, 0, L, H, D)).to(dev)
+
+    def run(depth, budget):
+        cache = kvc.KVCache(L, H, Hk, D, n + 64, 1, Q8, Q8, 1e6, 0, kvc.KVC_HOST_PINNED)
+        try:
+            kvc.kvc_pipeline_depth(cache.ctx, depth)
+            kvc.kvc_pipeline_budget(cache.ctx, budget)
+            for l in range(L):
+                cache.append(l, 0, 0, *kv[l])
+            out = torch.empty_like(q)
+            torch.cuda.synchronize()
+            torch.cuda._sleep(40_000_000)
+            for l in range(L):
+                cache.append(l, 0, n, *new[l])
+                cache.attn_decode(l, [0], q[l:l + 1], out[l:l + 1], 0.0884)
+            torch.cuda.synchronize()
+            return out.cpu().numpy(), cache.stats()
+        finally:
+            cache.close()
+
+    base, _ = run(0, 128 << 20)
+    for depth, budget, rolling in ((1, 512 << 20, 0), (4, 512 << 20, 0), (1, 16 << 20, 1)):
+        out, st = run(depth, budget)
+        assert st["ring_engaged"] == 1 and st["rolling"] == rolling and st["deliveries_early"] > 0, st
+        assert np.array_equal(out, base), (depth, budget)
+
+
 def test_host_resident_ordered_and_pipelined_byte_identical():
     """Depth 0 (ordered), pipelined rings of depth 1 and 4, and a ring the
     budget declines all produce the same bytes.  Eight layers, so even the
