@@ -61,6 +61,7 @@ def parse():
     ap.add_argument("--host-matrix", action="store_true",
                     help="host-resident decline matrix: n_kv 32k/64k/128k x depth 0/1/4 x budget 128/512 MiB")
     ap.add_argument("--churn-n", type=int, default=131072)
+    ap.add_argument("--rows", default="", help="comma-separated subset of the extra rows to run (default: all)")
     return ap.parse_args()
 
 
@@ -661,6 +662,8 @@ def run_ours(args, rank: int, world: int):
                          ("ragged_f16", lambda: ragged(kvc, torch, dev, "f16")),
                          ("churn", lambda: churn(kvc, torch, dev, args.churn_n, args.churn_cycles, args.layers)),
                          ("keydiff", lambda: keydiff(kvc, torch, dev, args.churn_n, args.layers))):
+            if args.rows and name not in args.rows.split(","):
+                continue
             try:
                 ex[name] = fn()
             except Exception as e:  # reported, not fatal
