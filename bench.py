@@ -270,11 +270,16 @@ MATRIX_CELLS = (("N0", 0, 128 << 20), ("N1_128MiB", 1, 128 << 20), ("N1_512MiB",
                 ("N4_128MiB", 4, 128 << 20), ("N4_512MiB", 4, 512 << 20))
 
 
-def host_pipeline(args, dev, torch, kvc, n=None, cells=HOST_CELLS, link=None):
+SPLIT_CELLS = (("ordered", 0, 128 << 20), ("pipelined", 1, 512 << 20))
+
+
+def host_pipeline(args, dev, torch, kvc, n=None, cells=HOST_CELLS, link=None, gpu_heads=0):
     """Host-resident KV at n (default args.host_n): steps/s and H2D GB/s for
     each (name, depth, budget) cell, run one after another on one cache (the
-    context grows by host_steps + 1 rows per cell).  Ordered/pipelined byte
-    identity is a parity test, not measured here."""
+    context grows by host_steps + 1 rows per cell).  With gpu_heads > 0 the
+    context splits by head: KV heads 0..gpu_heads-1 stay in HBM and only the
+    others cross the link.  Ordered/pipelined byte identity is a parity test,
+    not measured here."""
     from kv_cache_decode_flash_gb300 import synth
 
     n = n or args.host_n
@@ -283,7 +288,11 @@ def host_pipeline(args, dev, torch, kvc, n=None, cells=HOST_CELLS, link=None):
     res = {}
     link = link or measure_link(torch, dev)
     scale = float(1.0 / np.sqrt(D))
-    cache = kvc.KVCache(L, H, HK, D, n + 256, 1, t, t, 1e6, 0, kvc.KVC_HOST_PINNED)
+    if gpu_heads:
+        cache = kvc.KVCache(L, H, HK, D, n + 256, 1, t, t, 1e6, 0, kvc.KVC_SPLIT_HEADS, 0, 0, gpu_heads)
+    else:
+        cache = kvc.KVCache(L, H, HK, D, n + 256, 1, t, t, 1e6, 0, kvc.KVC_HOST_PINNED)
+    host_frac = (HK - gpu_heads) / HK  # share of each row that lives in host memory
     try:
         for l in range(L):
             for p0 in range(0, n - 1, 8192):
@@ -301,6 +310,8 @@ def host_pipeline(args, dev, torch, kvc, n=None, cells=HOST_CELLS, link=None):
             kvc.kvc_pipeline_budget(cache.ctx, budget)
             # median of three timed runs of host_steps steps after one warm-up step: the
             # host link is shared with other work on the machine and single runs vary
+            # the host link is shared with other work on the machine: measure it around the cell too
+            link_cell = measure_link(torch, dev)
             runs = []
             for rep in range(3):
                 for step in range(args.host_steps + (1 if rep == 0 else 0)):
@@ -314,19 +325,28 @@ def host_pipeline(args, dev, torch, kvc, n=None, cells=HOST_CELLS, link=None):
                 torch.cuda.synchronize()
                 runs.append((time.perf_counter() - t0) / args.host_steps)
             dt = statistics.median(runs)
+            link_cell = max(link_cell, measure_link(torch, dev))
             st = cache.stats()
             # bytes moved host->device per step: every layer's rows (stable prefix) once
-            h2d = L * (pos - 1) * kv_bytes_per_row(args.type)
+            h2d = L * (pos - 1) * kv_bytes_per_row(args.type) * host_frac
             res[name] = {"steps_per_s": round(1.0 / dt, 3), "ms_per_step": round(1000 * dt, 3),
                          "h2d_gbs": round(h2d / dt / GB, 2), "frac_of_link": round(h2d / dt / GB / link, 3),
+                         "link_gbs_around": round(link_cell, 2),
+                         "frac_of_link_around": round(h2d / dt / GB / link_cell, 3),
                          "ring_engaged": st["ring_engaged"], "ring_declined": st["ring_declined"],
                          "rolling": st["rolling"], "tile_rows": st["tile_rows"],
-                         "ring_mib": round(st["ring_bytes"] / 2**20, 1)}
+                         "ring_mib": round(st["ring_bytes"] / 2**20, 1),
+                         "device_mib": round(st["device_bytes"] / 2**20, 1),
+                         "host_mib": round(st["host_pinned_bytes"] / 2**20, 1)}
         res["n_kv"] = n
+        if gpu_heads:
+            res["gpu_heads"] = gpu_heads
+            res["bytes"] = "H2D counts the host heads' rows only (%d of %d KV heads)" % (HK - gpu_heads, HK)
         res["link_gbs"] = round(link, 2)
         res["link"] = "pinned H2D, 256 MiB copies, measured in this run"
         res["note"] = ("n_kv grows by one row per step (decode); H2D counts every layer's rows once per step; "
-                       "steps/s is the median of 3 runs")
+                       "steps/s is the median of 3 runs; link_gbs_around = the best of two link measurements "
+                       "taken just before and after the cell (the host link is shared)")
     finally:
         cache.close()
     return res
@@ -661,7 +681,9 @@ def run_ours(args, rank: int, world: int):
                          ("ragged_q8_0", lambda: ragged(kvc, torch, dev, "q8_0")),
                          ("ragged_f16", lambda: ragged(kvc, torch, dev, "f16")),
                          ("churn", lambda: churn(kvc, torch, dev, args.churn_n, args.churn_cycles, args.layers)),
-                         ("keydiff", lambda: keydiff(kvc, torch, dev, args.churn_n, args.layers))):
+                         ("keydiff", lambda: keydiff(kvc, torch, dev, args.churn_n, args.layers)),
+                         ("split_32k_g4", lambda: host_pipeline(args, dev, torch, kvc, 32768, SPLIT_CELLS,
+                                                                gpu_heads=4))):
             if args.rows and name not in args.rows.split(","):
                 continue
             try:

@@ -71,8 +71,18 @@ typedef enum kvc_type { KVC_F16 = 1, KVC_Q8_0 = 8 } kvc_type;
  * KVC_HOST_PINNED: pinned host RAM, one sequence (id 0); each layer's rows
  * are delivered to the device through a staging ring before attention
  * ([R4] section What it does).  Only kvc_append and kvc_attn_decode are
- * available; the sequence and state operations return KVC_EINVAL. */
-typedef enum kvc_residency { KVC_DEVICE = 0, KVC_HOST_PINNED = 1 } kvc_residency;
+ * available; the sequence and state operations return KVC_EINVAL.
+ * KVC_SPLIT_HEADS: a per-head residency split ("F5 - Advanced KV Cache
+ * Techniques", sections M2 HeadInfer and M3 NEO): KV heads 0 .. gpu_heads-1
+ * (whole GQA groups: query heads 0 .. gpu_heads*H/Hk - 1) live in device HBM
+ * as with KVC_DEVICE, the others in pinned host RAM as with
+ * KVC_HOST_PINNED, delivered through the staging ring.  kvc_attn_decode runs
+ * two attention launches on the disjoint head ranges (device heads first, so
+ * they overlap the host heads' transfers) whose outputs sit side by side on
+ * the head axis.  One sequence (id 0); only kvc_append, kvc_attn_decode and
+ * the pipeline / introspection calls apply.
+ */
+typedef enum kvc_residency { KVC_DEVICE = 0, KVC_HOST_PINNED = 1, KVC_SPLIT_HEADS = 2 } kvc_residency;
 
 /* Rotary pairing used by kvc_seq_add.  NEOX pairs (i, i + D/2); NORM pairs
  * (2i, 2i + 1).  The pages do not say which; NEOX is the default. */
@@ -94,6 +104,8 @@ typedef struct kvc_params {
     int32_t device;     /* CUDA device ordinal */
     int32_t page_rows;  /* device residency: cells per page, a multiple of 16
                            in [16, 4096]; 0 selects 256 */
+    int32_t gpu_heads;  /* KVC_SPLIT_HEADS: KV heads kept on the device,
+                           1 .. n_head_kv-1; ignored otherwise */
 } kvc_params;
 
 /* Fill *p with defaults: 1 layer, 8 heads, 2 KV heads, D 64, 512 cells,

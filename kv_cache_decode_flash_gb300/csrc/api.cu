@@ -284,7 +284,7 @@ using namespace kvc;
 // -------------------------------------------------------------- transport --
 namespace kvc {
 int transport_attn(Ctx *c, int layer, const float *q, float *out, float kq_scale, cudaStream_t st);
-int transport_append(Ctx *c, int layer, int n_tok, const float *k, const float *v, cudaStream_t st);
+int transport_append(Ctx *c, int layer, int n_tok, const float *k, const float *v, int in_heads, cudaStream_t st);
 void transport_release(Ctx *c);
 int launch_attention(Ctx *c, const LayerView &lv, const CUtensorMap *tmk, const CUtensorMap *tmv, int P,
                      int64_t scale_limit, int n_seq, const AttnSeq *seqs_in, const float *q, float *out,
@@ -311,6 +311,7 @@ void kvc_params_init(kvc_params *p) {
     p->residency = KVC_DEVICE;
     p->device = 0;
     p->page_rows = 0;
+    p->gpu_heads = 0;
 }
 
 const char *kvc_status_str(int s) {
@@ -336,6 +337,12 @@ const char *kvc_last_error(const kvc_ctx *c) {
 void kvc_destroy(kvc_ctx *cc) {
     if (!cc) return;
     Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (c->split) {
+        kvc_destroy(reinterpret_cast<kvc_ctx *>(c->part_dev));
+        kvc_destroy(reinterpret_cast<kvc_ctx *>(c->part_host));
+        delete c;
+        return;
+    }
     cudaSetDevice(c->dev);
     cudaDeviceSynchronize();
     transport_release(c);
@@ -391,10 +398,48 @@ int kvc_create(const kvc_params *p, kvc_ctx **out) {
     if (p->type_k != p->type_v) return bad("K and V must have the same type");
     if (p->rope_mode != KVC_ROPE_NEOX && p->rope_mode != KVC_ROPE_NORM) return bad("bad rope_mode");
     if (!(p->rope_base > 1.0f) || !std::isfinite(p->rope_base)) return bad("rope_base must be > 1");
-    if (p->residency != KVC_DEVICE && p->residency != KVC_HOST_PINNED) return bad("bad residency");
+    if (p->residency != KVC_DEVICE && p->residency != KVC_HOST_PINNED && p->residency != KVC_SPLIT_HEADS)
+        return bad("bad residency");
     int page_rows = p->page_rows ? p->page_rows : 256;
     if (page_rows < 16 || page_rows > 4096 || page_rows % 16) return bad("page_rows must be a multiple of 16 in [16, 4096]");
     if (p->residency == KVC_HOST_PINNED && p->n_seq_max != 1) return bad("host-resident contexts hold one sequence");
+    if (p->residency == KVC_SPLIT_HEADS) {
+        if (p->n_seq_max != 1) return bad("split contexts hold one sequence");
+        if (p->gpu_heads < 1 || p->gpu_heads >= p->n_head_kv) return bad("gpu_heads must be in [1, n_head_kv - 1]");
+        // two whole contexts on the disjoint KV-head ranges (whole GQA groups)
+        const int r = p->n_head / p->n_head_kv;
+        kvc_params dp = *p, hp = *p;
+        dp.residency = KVC_DEVICE;
+        dp.n_head_kv = p->gpu_heads;
+        dp.n_head = p->gpu_heads * r;
+        hp.residency = KVC_HOST_PINNED;
+        hp.n_head_kv = p->n_head_kv - p->gpu_heads;
+        hp.n_head = hp.n_head_kv * r;
+        kvc_ctx *d = nullptr, *h = nullptr;
+        int rc = kvc_create(&dp, &d);
+        if (rc == KVC_OK) rc = kvc_create(&hp, &h);
+        if (rc != KVC_OK) {
+            kvc_destroy(d);
+            c->err = "creating a part of the split context failed";
+            delete c;
+            return rc;
+        }
+        c->split = true;
+        c->host = true; // the sequence and state operations are not available
+        c->gpu_heads = p->gpu_heads;
+        c->part_dev = reinterpret_cast<Ctx *>(d);
+        c->part_host = reinterpret_cast<Ctx *>(h);
+        c->dev = p->device;
+        c->H = p->n_head;
+        c->Hk = p->n_head_kv;
+        c->D = p->head_dim;
+        c->r = r;
+        c->L = p->n_layer;
+        c->tk = p->type_k;
+        c->tv = p->type_v;
+        *out = reinterpret_cast<kvc_ctx *>(c);
+        return KVC_OK;
+    }
 
     int ndev = 0;
     if (cudaGetDeviceCount(&ndev) != cudaSuccess || p->device < 0 || p->device >= ndev) {
@@ -530,10 +575,34 @@ int kvc_create(const kvc_params *p, kvc_ctx **out) {
     return KVC_OK;
 }
 
+// Append n_tok rows of every KV head of c; k / v hold in_heads head-rows per
+// token, of which the first Hk are c's.
+static int append_impl(Ctx *c, int layer, int seq, int pos0, int n_tok, const float *k, const float *v,
+                       void *stream, int in_heads);
+
 int kvc_append(kvc_ctx *cc, int layer, int seq, int pos0, int n_tok, const float *k, const float *v,
                void *stream) {
     if (!cc) return KVC_EINVAL;
     Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (c->split) {
+        if (layer < 0 || layer >= c->L) return c->fail(KVC_EINVAL, "layer out of range");
+        if (seq != 0) return c->fail(KVC_EINVAL, "sequence id out of range");
+        if (n_tok < 1 || !k || !v) return c->fail(KVC_EINVAL, "n_tok must be >= 1 and k, v non-null");
+        if (((uintptr_t)k | (uintptr_t)v) & 15) return c->fail(KVC_EINVAL, "k and v must be 16-byte aligned");
+        // the host half first: the host store is the one that can be full (the device half holds the
+        // same number of cells in pages); the two halves carry identical positions
+        const int64_t skip = (int64_t)c->gpu_heads * c->D;
+        int rc = append_impl(c->part_host, layer, seq, pos0, n_tok, k + skip, v + skip, stream, c->Hk);
+        if (rc) return c->fail(rc, c->part_host->err);
+        rc = append_impl(c->part_dev, layer, seq, pos0, n_tok, k, v, stream, c->Hk);
+        if (rc) return c->fail(rc, "device half: " + c->part_dev->err + " (the host half took the rows)");
+        return KVC_OK;
+    }
+    return append_impl(c, layer, seq, pos0, n_tok, k, v, stream, c->Hk);
+}
+
+static int append_impl(Ctx *c, int layer, int seq, int pos0, int n_tok, const float *k, const float *v,
+                       void *stream, int in_heads) {
     if (layer < 0 || layer >= c->L) return c->fail(KVC_EINVAL, "layer out of range");
     if (seq < 0 || seq >= (int)c->seqs.size()) return c->fail(KVC_EINVAL, "sequence id out of range");
     if (n_tok < 1 || !k || !v) return c->fail(KVC_EINVAL, "n_tok must be >= 1 and k, v non-null");
@@ -552,7 +621,7 @@ int kvc_append(kvc_ctx *cc, int layer, int seq, int pos0, int n_tok, const float
     }
     if (c->host) {
         if (creates && (int64_t)q.n + n_tok > c->P) return c->fail(KVC_ENOSPC, "host store is full");
-        int rc = transport_append(c, layer, n_tok, k, v, st);
+        int rc = transport_append(c, layer, n_tok, k, v, in_heads, st);
         if (rc) return rc;
     } else {
         if (creates) {
@@ -581,7 +650,7 @@ int kvc_append(kvc_ctx *cc, int layer, int seq, int pos0, int n_tok, const float
         d.off = q.off;
         d.row0 = fill;
         d.P = c->P;
-        cudaError_t e = launch_append(c->tk, c->tv, c->Hk, c->D, n_tok, k, v, &d, 1, st);
+        cudaError_t e = launch_append(c->tk, c->tv, c->Hk, in_heads, c->D, n_tok, k, v, &d, 1, st);
         if (e != cudaSuccess) return cuda_fail(c, e, "append kernel");
     }
     if (creates) {
@@ -597,6 +666,21 @@ int kvc_attn_decode(kvc_ctx *cc, int layer, int n_seq, const int32_t *seq_ids, c
                     float kq_scale, void *stream) {
     if (!cc) return KVC_EINVAL;
     Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (c->split) {
+        if (n_seq != 1 || !seq_ids || seq_ids[0] != 0)
+            return c->fail(KVC_EINVAL, "split contexts attend sequence 0 only");
+        if (!q || !out) return c->fail(KVC_EINVAL, "q and out must be non-null");
+        // device heads first (they need no transfer), then the host heads, whose launch waits for
+        // their delivery; query heads of a KV head are contiguous, so the two outputs sit side by side
+        int rc = kvc_attn_decode(reinterpret_cast<kvc_ctx *>(c->part_dev), layer, 1, seq_ids, q, out, kq_scale,
+                                 stream);
+        if (rc) return c->fail(rc, c->part_dev->err);
+        const int64_t skip = (int64_t)c->gpu_heads * c->r * c->D;
+        rc = kvc_attn_decode(reinterpret_cast<kvc_ctx *>(c->part_host), layer, 1, seq_ids, q + skip, out + skip,
+                             kq_scale, stream);
+        if (rc) return c->fail(rc, c->part_host->err);
+        return KVC_OK;
+    }
     if (layer < 0 || layer >= c->L) return c->fail(KVC_EINVAL, "layer out of range");
     if (n_seq < 1 || !seq_ids || !q || !out) return c->fail(KVC_EINVAL, "n_seq >= 1 and non-null pointers required");
     if (!std::isfinite(kq_scale)) return c->fail(KVC_EINVAL, "kq_scale must be finite");
@@ -1040,6 +1124,10 @@ int kvc_state_set(kvc_ctx *cc, int seq, const void *src, size_t nbytes, size_t *
 int kvc_pipeline_depth(kvc_ctx *cc, int n) {
     if (!cc) return KVC_EINVAL;
     Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (c->split) {
+        int rc = kvc_pipeline_depth(reinterpret_cast<kvc_ctx *>(c->part_host), n);
+        return rc ? c->fail(rc, c->part_host->err) : KVC_OK;
+    }
     if (n < 0 || n > 16) return c->fail(KVC_EINVAL, "depth must be in [0, 16]");
     if (c->host) {
         cudaSetDevice(c->dev);
@@ -1054,6 +1142,10 @@ int kvc_pipeline_depth(kvc_ctx *cc, int n) {
 int kvc_pipeline_budget(kvc_ctx *cc, size_t bytes) {
     if (!cc) return KVC_EINVAL;
     Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (c->split) {
+        int rc = kvc_pipeline_budget(reinterpret_cast<kvc_ctx *>(c->part_host), bytes);
+        return rc ? c->fail(rc, c->part_host->err) : KVC_OK;
+    }
     if (bytes > ((size_t)1 << 50)) return c->fail(KVC_EINVAL, "budget too large");
     if (c->host) {
         cudaSetDevice(c->dev);
@@ -1068,6 +1160,7 @@ int kvc_pipeline_budget(kvc_ctx *cc, size_t bytes) {
 int kvc_seq_n_tokens(const kvc_ctx *cc, int seq, int32_t *n) {
     if (!cc || !n) return KVC_EINVAL;
     const Ctx *c = reinterpret_cast<const Ctx *>(cc);
+    if (c->split) return kvc_seq_n_tokens(reinterpret_cast<const kvc_ctx *>(c->part_dev), seq, n);
     if (seq < 0 || seq >= (int)c->seqs.size()) return KVC_EINVAL;
     *n = c->seqs[(size_t)seq].n;
     return KVC_OK;
@@ -1076,6 +1169,7 @@ int kvc_seq_n_tokens(const kvc_ctx *cc, int seq, int32_t *n) {
 int kvc_seq_positions(const kvc_ctx *cc, int seq, int32_t *pos, int32_t cap, int32_t *n) {
     if (!cc || !n) return KVC_EINVAL;
     const Ctx *c = reinterpret_cast<const Ctx *>(cc);
+    if (c->split) return kvc_seq_positions(reinterpret_cast<const kvc_ctx *>(c->part_dev), seq, pos, cap, n);
     if (seq < 0 || seq >= (int)c->seqs.size()) return KVC_EINVAL;
     const Seq &q = c->seqs[(size_t)seq];
     *n = q.n;
@@ -1089,6 +1183,16 @@ int kvc_seq_positions(const kvc_ctx *cc, int seq, int32_t *pos, int32_t cap, int
 int kvc_get_stats(const kvc_ctx *cc, kvc_stats *o) {
     if (!cc || !o) return KVC_EINVAL;
     const Ctx *c = reinterpret_cast<const Ctx *>(cc);
+    if (c->split) {
+        // the transport is the host half's; memory is both halves'
+        kvc_get_stats(reinterpret_cast<const kvc_ctx *>(c->part_host), o);
+        kvc_stats d;
+        kvc_get_stats(reinterpret_cast<const kvc_ctx *>(c->part_dev), &d);
+        o->pages_total = d.pages_total;
+        o->pages_free = d.pages_free;
+        o->device_bytes += d.device_bytes;
+        return KVC_OK;
+    }
     std::memset(o, 0, sizeof(*o));
     o->ring_engaged = c->tr.ring.empty() ? 0 : 1;
     o->ring_declined = c->tr.latched ? 1 : 0;
@@ -1113,6 +1217,11 @@ int kvc_get_stats(const kvc_ctx *cc, kvc_stats *o) {
 int kvc_set_chunk_rows(kvc_ctx *cc, int rows) {
     if (!cc) return KVC_EINVAL;
     Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (c->split) {
+        int rc = kvc_set_chunk_rows(reinterpret_cast<kvc_ctx *>(c->part_dev), rows);
+        if (!rc) rc = kvc_set_chunk_rows(reinterpret_cast<kvc_ctx *>(c->part_host), rows);
+        return rc ? c->fail(rc, "bad chunk rows") : KVC_OK;
+    }
     if (rows < 0 || rows % 16) return c->fail(KVC_EINVAL, "chunk rows must be a non-negative multiple of 16");
     c->chunk_override = rows;
     return KVC_OK;
@@ -1121,6 +1230,11 @@ int kvc_set_chunk_rows(kvc_ctx *cc, int rows) {
 int kvc_set_timeout_ms(kvc_ctx *cc, int ms) {
     if (!cc) return KVC_EINVAL;
     Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (c->split) {
+        int rc = kvc_set_timeout_ms(reinterpret_cast<kvc_ctx *>(c->part_dev), ms);
+        if (!rc) rc = kvc_set_timeout_ms(reinterpret_cast<kvc_ctx *>(c->part_host), ms);
+        return rc ? c->fail(rc, "bad timeout") : KVC_OK;
+    }
     if (ms < 1) return c->fail(KVC_EINVAL, "timeout must be positive");
     c->timeout_ms = ms;
     return KVC_OK;
@@ -1128,13 +1242,26 @@ int kvc_set_timeout_ms(kvc_ctx *cc, int ms) {
 
 int kvc_debug_fail_alloc_after(kvc_ctx *cc, int n) {
     if (!cc) return KVC_EINVAL;
-    reinterpret_cast<Ctx *>(cc)->fail_after = n < 0 ? -1 : n;
+    Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (c->split) {
+        kvc_debug_fail_alloc_after(reinterpret_cast<kvc_ctx *>(c->part_dev), n);
+        kvc_debug_fail_alloc_after(reinterpret_cast<kvc_ctx *>(c->part_host), n);
+        return KVC_OK;
+    }
+    c->fail_after = n < 0 ? -1 : n;
     return KVC_OK;
 }
 
 int kvc_check_device_error(kvc_ctx *cc, uint32_t *word) {
     if (!cc || !word) return KVC_EINVAL;
     Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (c->split) {
+        uint32_t a = 0, b = 0;
+        int rc = kvc_check_device_error(reinterpret_cast<kvc_ctx *>(c->part_dev), &a);
+        if (!rc) rc = kvc_check_device_error(reinterpret_cast<kvc_ctx *>(c->part_host), &b);
+        *word = a | b;
+        return rc;
+    }
     KVC_CU(c, cudaSetDevice(c->dev));
     KVC_CU(c, cudaDeviceSynchronize());
     KVC_CU(c, cudaMemcpy(word, c->err_dev, 4, cudaMemcpyDeviceToHost));

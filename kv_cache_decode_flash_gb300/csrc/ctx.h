@@ -71,6 +71,10 @@ struct Ctx {
     int tk = 0, tv = 0;
     int krow = 0, vrow = 0, ksb = 0, vsb = 0; // data row bytes, scale row bytes (0 for f16)
     bool host = false;
+    // per-head residency split: the two halves are whole contexts of their own
+    bool split = false;
+    int gpu_heads = 0;
+    Ctx *part_dev = nullptr, *part_host = nullptr;
 
     // device residency
     int32_t n_pages = 0;

@@ -87,6 +87,7 @@ __device__ __forceinline__ void store_tensor(int type, const TensorView &tv, int
 
 struct AppendArgs {
     int type_k, type_v, Hk, n_tok, n_dst;
+    int in_heads; // head-rows per token in k / v (>= Hk: a context holding a subset of the heads)
     const float *k, *v;
     AppendDst dst[2];
 };
@@ -105,8 +106,9 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
     if (w >= (int64_t)a.n_tok * a.Hk) return;
     const int t = (int)(w / a.Hk), g = (int)(w % a.Hk);
     float xk[EPL], xv[EPL];
-    load_row<EPL>(a.k + w * D, lane, xk);
-    load_row<EPL>(a.v + w * D, lane, xv);
+    const int64_t in = ((int64_t)t * a.in_heads + g) * D;
+    load_row<EPL>(a.k + in, lane, xk);
+    load_row<EPL>(a.v + in, lane, xv);
     for (int i = 0; i < a.n_dst; ++i) {
         const int64_t R = dst_row(a.dst[i], t, g, a.Hk);
         store_tensor<D>(a.type_k, a.dst[i].lv.k, R, lane, xk);
@@ -128,12 +130,13 @@ __global__ void pt_update_kernel(const __grid_constant__ PtArgs a) {
 
 } // namespace
 
-cudaError_t launch_append(int type_k, int type_v, int Hk, int D, int n_tok, const float *k, const float *v,
-                          const AppendDst *dst, int n_dst, cudaStream_t st) {
+cudaError_t launch_append(int type_k, int type_v, int Hk, int in_heads, int D, int n_tok, const float *k,
+                          const float *v, const AppendDst *dst, int n_dst, cudaStream_t st) {
     AppendArgs a;
     a.type_k = type_k;
     a.type_v = type_v;
     a.Hk = Hk;
+    a.in_heads = in_heads;
     a.n_tok = n_tok;
     a.n_dst = n_dst;
     a.k = k;

@@ -95,8 +95,9 @@ struct AppendDst {
     int32_t row0;
     int32_t P;
 };
-cudaError_t launch_append(int type_k, int type_v, int Hk, int D, int n_tok, const float *k, const float *v,
-                          const AppendDst *dst, int n_dst, cudaStream_t st);
+// k / v hold in_heads head-rows per token; the first Hk of them are stored.
+cudaError_t launch_append(int type_k, int type_v, int Hk, int in_heads, int D, int n_tok, const float *k,
+                          const float *v, const AppendDst *dst, int n_dst, cudaStream_t st);
 
 // Write page-table entries: pt[idx[i]] = val[i], up to 32 per launch.
 cudaError_t launch_pt_update(int32_t *pt, int n, const int32_t *idx, const int32_t *val, cudaStream_t st);

@@ -384,7 +384,7 @@ static void slot_layer_view(const Slot &s, LayerView &lv) {
     lv.v.scales = reinterpret_cast<uint16_t *>(s.vscales);
 }
 
-int transport_append(Ctx *c, int layer, int n_tok, const float *k, const float *v, cudaStream_t st) {
+int transport_append(Ctx *c, int layer, int n_tok, const float *k, const float *v, int in_heads, cudaStream_t st) {
     Seq &q = c->seqs[0];
     const int32_t fill = q.lfill[(size_t)layer];
     AppendDst d[2];
@@ -420,7 +420,7 @@ int transport_append(Ctx *c, int layer, int n_tok, const float *k, const float *
         d[1].P = s->cap;
         nd = 2;
     }
-    cudaError_t e = launch_append(c->tk, c->tv, c->Hk, c->D, n_tok, k, v, d, nd, st);
+    cudaError_t e = launch_append(c->tk, c->tv, c->Hk, in_heads, c->D, n_tok, k, v, d, nd, st);
     if (e != cudaSuccess) return cuda_fail(c, e, "append kernel");
     KVC_CU(c, cudaEventRecord(c->app_ev[(size_t)layer], st));
     ++c->app_gen[(size_t)layer];

@@ -20,14 +20,14 @@ LIB_PATH = os.path.join(HERE, "libkvc.so")
 KVC_OK, KVC_EINVAL, KVC_ENOMEM, KVC_ENOSPC, KVC_ERANGE = 0, -1, -2, -3, -4
 KVC_EFORMAT, KVC_ECUDA, KVC_ETIMEDOUT, KVC_EINTERNAL = -5, -6, -7, -8
 KVC_F16, KVC_Q8_0 = 1, 8
-KVC_DEVICE, KVC_HOST_PINNED = 0, 1
+KVC_DEVICE, KVC_HOST_PINNED, KVC_SPLIT_HEADS = 0, 1, 2
 KVC_ROPE_NEOX, KVC_ROPE_NORM = 0, 1
 
 
 class kvc_params(C.Structure):
     _fields_ = [(n, C.c_int32) for n in ("n_layer", "n_head", "n_head_kv", "head_dim", "n_ctx", "n_seq_max",
                                           "type_k", "type_v")] + [("rope_base", C.c_float)] + [
-        (n, C.c_int32) for n in ("rope_mode", "residency", "device", "page_rows")]
+        (n, C.c_int32) for n in ("rope_mode", "residency", "device", "page_rows", "gpu_heads")]
 
 
 class kvc_stats(C.Structure):
@@ -287,11 +287,12 @@ class KVCache:
 
     def __init__(self, n_layer, n_head, n_head_kv, head_dim, n_ctx, n_seq_max=1, type_k=KVC_Q8_0,
                  type_v=KVC_Q8_0, rope_base=10000.0, rope_mode=KVC_ROPE_NEOX, residency=KVC_DEVICE, device=0,
-                 page_rows=0):
+                 page_rows=0, gpu_heads=0):
         p = kvc_params_init()
         p.n_layer, p.n_head, p.n_head_kv, p.head_dim = n_layer, n_head, n_head_kv, head_dim
         p.n_ctx, p.n_seq_max, p.type_k, p.type_v = n_ctx, n_seq_max, type_k, type_v
         p.rope_base, p.rope_mode, p.residency, p.device, p.page_rows = rope_base, rope_mode, residency, device, page_rows
+        p.gpu_heads = gpu_heads
         self.params = p
         self.device = device
         self.ctx = kvc_create(p)

@@ -48,3 +48,10 @@ def test_create_rejects_bad_geometry_without_touching_a_gpu():
         with pytest.raises(kvc.KvcError) as e:
             kvc.kvc_create(p)
         assert e.value.status == kvc.KVC_EINVAL, field
+    # split residency: gpu_heads must leave at least one KV head on each side; one sequence
+    for gpu_heads, n_seq in ((0, 1), (2, 1), (5, 1), (1, 2)):
+        p = kvc.kvc_params_init()
+        p.residency, p.gpu_heads, p.n_seq_max = kvc.KVC_SPLIT_HEADS, gpu_heads, n_seq
+        with pytest.raises(kvc.KvcError) as e:
+            kvc.kvc_create(p)
+        assert e.value.status == kvc.KVC_EINVAL, (gpu_heads, n_seq)

@@ -335,6 +335,76 @@ def test_host_resident_ring_built_behind_busy_stream():
         assert np.array_equal(out, base), (depth, budget)
 
 
+# ------------------------------------------------- per-head residency split --
+@pytest.mark.parametrize("type_,G", [(Q8, 4), (F16, 2), (Q8, 7)])
+def test_split_heads_vs_oracle_and_pipelined(type_, G):
+    """KV heads 0..G-1 in device HBM, the others in pinned host memory: three
+    decode steps of 6 layers against the oracle (which holds every head in
+    one cache); the host half ordered, through the ring and on a small budget
+    (rolling tiles or declined) gives byte-identical outputs."""
+    import torch
+
+    from kv_cache_decode_flash_gb300 import kvc
+
+    L, H, Hk, D, n = 6, 40, 8, 128, 3000
+    dev = torch.device("cuda:0")
+    ref = oracle.OracleCache(L, H, Hk, D, type_, type_, 1e6, 0)
+    fill = [kv_inputs(16, l, n, Hk, D, sigma=0.5) for l in range(L)]
+    for l in range(L):
+        ref.append(l, 0, 0, *fill[l])
+    steps = []
+    for s_ in range(3):
+        new = [kv_inputs(16, l, 1, Hk, D, pos0=n + s_, sigma=0.5) for l in range(L)]
+        steps.append((new, [q_inputs(16, l, 1, H, D, extra=s_) for l in range(L)]))
+    want = []
+    for s_, (new, qs) in enumerate(steps):
+        for l in range(L):
+            ref.append(l, 0, n + s_, *new[l])
+            want.append(ref.attn(l, [0], qs[l], float(np.float32(0.0884)))[0])
+    outs = []
+    for depth, budget in ((0, 128 << 20), (1, 512 << 20), (1, 4 << 20)):
+        cache = kvc.KVCache(L, H, Hk, D, n + 64, 1, type_, type_, 1e6, 0, kvc.KVC_SPLIT_HEADS, 0, 0, G)
+        try:
+            kvc.kvc_pipeline_depth(cache.ctx, depth)
+            kvc.kvc_pipeline_budget(cache.ctx, budget)
+            for l in range(L):
+                cache.append(l, 0, 0, *[torch.from_numpy(a).to(dev) for a in fill[l]])
+            got = []
+            for s_, (new, qs) in enumerate(steps):
+                for l in range(L):
+                    cache.append(l, 0, n + s_, *[torch.from_numpy(a).to(dev) for a in new[l]])
+                    q = torch.from_numpy(qs[l]).to(dev)
+                    o = torch.empty_like(q)
+                    cache.attn_decode(l, [0], q, o, 0.0884)
+                    got.append(o.cpu().numpy()[0])
+            assert cache.n_tokens(0) == n + 3
+            st = cache.stats()
+            if depth:
+                assert st["deliveries_early"] + st["deliveries_ordered"] > 0
+            outs.append(np.stack(got))
+        finally:
+            cache.close()
+    for i, w in enumerate(want):
+        assert_attn_close(outs[0][i].astype(np.float64), w, "split G=%d, launch %d" % (G, i))
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+
+
+def test_split_heads_rejects_sequence_and_state_ops():
+    from kv_cache_decode_flash_gb300 import kvc
+
+    cache = kvc.KVCache(2, 8, 2, 64, 256, 1, Q8, Q8, 1e4, 0, kvc.KVC_SPLIT_HEADS, 0, 0, 1)
+    try:
+        for call in (lambda: cache.seq_rm(0, 0, 1), lambda: cache.seq_cp(0, 0, 0, 1),
+                     lambda: cache.seq_add(0, 0, 1, 1), lambda: cache.state_get(0, -1, -1),
+                     lambda: cache.key_scores(0, 0)):
+            with pytest.raises(kvc.KvcError) as e:
+                call()
+            assert e.value.status == kvc.KVC_EINVAL
+    finally:
+        cache.close()
+
+
 def test_host_resident_ordered_and_pipelined_byte_identical():
     """Depth 0 (ordered), pipelined rings of depth 1 and 4, and a ring the
     budget declines all produce the same bytes.  Eight layers, so even the
