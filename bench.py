@@ -526,6 +526,55 @@ def keydiff(kvc, torch, dev, n: int, layers: int, reps: int = 10):
         cache.close()
 
 
+def cold_store(kvc, torch, dev, n: int, layers: int, cycles: int = 8):
+    """Host-RAM cold store over an n-token q8_0 cache: each cycle evicts the
+    oldest 8192 rows into the store (copy to a scratch sequence, export into
+    pinned host memory, remove, slide) and admits them back at the tail
+    (import, shift, copy in), then admits an absent key (a miss).
+    Synchronous calls, wall time per operation; the first cycle, which pins
+    the store's buffers, is not timed."""
+    from kv_cache_decode_flash_gb300 import synth
+
+    blk = 8192
+    cache = kvc.KVCache(layers, H, HK, D, n + 2 * blk + 512, 2, kvc.KVC_Q8_0, kvc.KVC_Q8_0, 1e6)
+    store = kvc.ColdStore(2 * blk)
+    try:
+        for l in range(layers):
+            for p0 in range(0, n, 8192):
+                m = min(8192, n - p0)
+                k = synth.normal_torch(0, synth.stream_id("k", l, p0), m * HK * D, 0.5, dev).view(m, HK, D)
+                v = synth.normal_torch(0, synth.stream_id("v", l, p0), m * HK * D, 0.5, dev).view(m, HK, D)
+                cache.append(l, 0, p0, k, v)
+        torch.cuda.synchronize()
+        size = kvc.kvc_state_size(cache.ctx, 0, 0, blk)
+        t_ev = t_ad = t_miss = 0.0
+        ok = True
+        for c in range(cycles + 1):
+            t0 = time.perf_counter()
+            stored, _ = store.evict(cache, 0, 1, 0, blk, 1000 + c, c % 3)
+            t1 = time.perf_counter()
+            hit, _ = store.admit(cache, 0, 1, 1000 + c)
+            t2 = time.perf_counter()
+            miss, _ = store.admit(cache, 0, 1, 1)
+            t3 = time.perf_counter()
+            ok = ok and stored == 1 and hit == 1 and miss == 0
+            if c:
+                t_ev += t1 - t0
+                t_ad += t2 - t1
+                t_miss += t3 - t2
+        ok = ok and bool((np.sort(cache.positions(0)) == np.arange(n)).all())
+        return {"n_kv": n, "block": blk, "layers": layers, "cycles": cycles, "block_state_bytes": size,
+                "evict_ms": round(t_ev / cycles * 1e3, 3), "admit_ms": round(t_ad / cycles * 1e3, 3),
+                "miss_us": round(t_miss / cycles * 1e6, 1),
+                "evict_state_gbs": round(size / (t_ev / cycles) / GB, 1),
+                "admit_state_gbs": round(size / (t_ad / cycles) / GB, 1), "ok": ok, "store": store.stats(),
+                "note": "evict = seq_cp + export (D2H) + remove + slide of the rest; admit = import (H2D) + "
+                        "shift + copy in; GB/s = state bytes of the block / operation time"}
+    finally:
+        store.close()
+        cache.close()
+
+
 def run_ours(args, rank: int, world: int):
     import torch
 
@@ -683,7 +732,8 @@ def run_ours(args, rank: int, world: int):
                          ("churn", lambda: churn(kvc, torch, dev, args.churn_n, args.churn_cycles, args.layers)),
                          ("keydiff", lambda: keydiff(kvc, torch, dev, args.churn_n, args.layers)),
                          ("split_32k_g4", lambda: host_pipeline(args, dev, torch, kvc, 32768, SPLIT_CELLS,
-                                                                gpu_heads=4))):
+                                                                gpu_heads=4)),
+                         ("cold_store", lambda: cold_store(kvc, torch, dev, args.churn_n, args.layers))):
             if args.rows and name not in args.rows.split(","):
                 continue
             try:

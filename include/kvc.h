@@ -340,6 +340,70 @@ int kvc_attn_decode_static(int type, int n_head, int n_head_kv, int head_dim, in
                            const uint16_t *ks, const void *v, const uint16_t *vs, const float *q,
                            float *out, float kq_scale, void *stream);
 
+/* ---------------------------------------------------------------------
+ * Host-RAM cold store ("Plan: lossless long context", #3 Host-RAM KV cold
+ * store + retrieval, llama KV-byte offload): token ranges evicted from a
+ * device-resident context are kept as state bytes (kvc_state_get format) in
+ * pinned host memory, keyed by a caller-supplied 64-bit token hash, so they
+ * can be paged back losslessly.  The store is bounded in tokens.  When a new
+ * block does not fit, blocks are dropped most evictable class first and,
+ * within a class, least recently stored first; only blocks at least as
+ * evictable as the new one are dropped, otherwise the new block is not kept
+ * (loss happens only at the cold tier, for the most evictable classes).
+ * A block lives in one tier: admitting it removes it from the store.  On a
+ * miss the caller recomputes the tokens (re-prefill), the pages' fallback.
+ * Not thread-safe; a store may serve several contexts of the same geometry.
+ * ------------------------------------------------------------------- */
+typedef struct kvc_cold kvc_cold;
+
+typedef struct kvc_cold_stats {
+    int64_t budget_tokens;
+    int64_t tokens;      /* tokens held */
+    int64_t bytes;       /* state bytes held (pinned host memory) */
+    int32_t blocks;
+    int32_t pad;
+    int64_t stored;      /* evictions whose block was kept */
+    int64_t rejected;    /* evictions whose block was not kept (too large, or only less
+                            evictable blocks to drop) */
+    int64_t dropped;     /* blocks dropped to make room */
+    int64_t hits;        /* admits that found their block */
+    int64_t misses;      /* admits that did not */
+} kvc_cold_stats;
+
+/* A store holding at most budget_tokens tokens (>= 1).  Errors: KVC_EINVAL, KVC_ENOMEM. */
+int kvc_cold_create(int64_t budget_tokens, kvc_cold **out);
+/* Free the store and its blocks.  NULL is a no-op. */
+void kvc_cold_destroy(kvc_cold *s);
+/* Detail of the store's last error (empty when none). */
+const char *kvc_cold_last_error(const kvc_cold *s);
+
+/* Evict the rows of `seq` with positions in [p0, p1) (p0 >= 0, p1 > p0)
+ * from device-resident context c: copy them into sequence `scratch` (which
+ * must be empty), export it into the store under `key` with class `cls`
+ * (>= 0; larger = more evictable), drop the scratch, remove the rows from
+ * `seq` and slide the later positions down by p1 - p0 (kvc_seq_cp,
+ * kvc_state_get, kvc_seq_rm, kvc_seq_add).  The rows leave the context even
+ * when the block is not kept: *stored tells (1 kept, 0 not).  A block
+ * already stored under `key` is replaced.  *n_tok: rows evicted.
+ * Errors: KVC_EINVAL (arguments, a non-empty scratch, a host-resident
+ * context), the context calls' errors (c's kvc_last_error has the detail),
+ * KVC_ENOMEM (pinned host memory). */
+int kvc_cold_evict(kvc_ctx *c, kvc_cold *s, int seq, int scratch, int p0, int p1, uint64_t key, int cls,
+                   int *stored, int32_t *n_tok);
+
+/* Admit the block stored under `key` at the tail of `seq` (append mode):
+ * import it into sequence `scratch` (empty), shift it so that its first row
+ * lands at the position after the last row of `seq` (0 if empty), copy it
+ * into `seq` and drop the scratch; the block leaves the store.  *hit = 1 and
+ * *n_tok = its rows when found; *hit = 0 and *n_tok = 0 on a miss (nothing
+ * changes).  Errors as for kvc_cold_evict; on an error the block stays in
+ * the store and the scratch is emptied. */
+int kvc_cold_admit(kvc_ctx *c, kvc_cold *s, int seq, int scratch, uint64_t key, int *hit, int32_t *n_tok);
+
+/* The rows (*n_tok, 0 when absent) and class of the block under `key`. */
+int kvc_cold_find(const kvc_cold *s, uint64_t key, int32_t *n_tok, int32_t *cls);
+int kvc_cold_get_stats(const kvc_cold *s, kvc_cold_stats *out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -41,6 +41,15 @@ class kvc_stats(C.Structure):
         return {n: getattr(self, n) for n, _ in self._fields_}
 
 
+class kvc_cold_stats(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in ("budget_tokens", "tokens", "bytes")] + [
+        (n, C.c_int32) for n in ("blocks", "pad")] + [
+        (n, C.c_int64) for n in ("stored", "rejected", "dropped", "hits", "misses")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_ if n != "pad"}
+
+
 class KvcError(RuntimeError):
     def __init__(self, status: int, msg: str):
         super().__init__("%s (%d): %s" % (_status_str(status), status, msg))
@@ -83,6 +92,14 @@ def load():
         "kvc_set_timeout_ms": (i32, [p, i32]),
         "kvc_debug_fail_alloc_after": (i32, [p, i32]),
         "kvc_check_device_error": (i32, [p, C.POINTER(C.c_uint32)]),
+        "kvc_cold_create": (i32, [C.c_int64, C.POINTER(p)]),
+        "kvc_cold_destroy": (None, [p]),
+        "kvc_cold_last_error": (C.c_char_p, [p]),
+        "kvc_cold_evict": (i32, [p, p, i32, i32, i32, i32, C.c_uint64, i32, C.POINTER(C.c_int),
+                                 C.POINTER(C.c_int32)]),
+        "kvc_cold_admit": (i32, [p, p, i32, i32, C.c_uint64, C.POINTER(C.c_int), C.POINTER(C.c_int32)]),
+        "kvc_cold_find": (i32, [p, C.c_uint64, C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
+        "kvc_cold_get_stats": (i32, [p, C.POINTER(kvc_cold_stats)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -343,3 +360,84 @@ class KVCache:
 
     def stats(self):
         return kvc_get_stats(self.ctx)
+
+
+# ------------------------------------------------------------ cold store --
+def _check_cold(store, ctx, status: int):
+    if status != KVC_OK:
+        msg = load().kvc_cold_last_error(store).decode() if store else ""
+        if ctx:
+            detail = load().kvc_last_error(ctx).decode()
+            if detail:
+                msg = "%s (context: %s)" % (msg, detail)
+        raise KvcError(status, msg)
+
+
+def kvc_cold_create(budget_tokens: int) -> int:
+    h = C.c_void_p()
+    _check_cold(None, None, load().kvc_cold_create(int(budget_tokens), C.byref(h)))
+    return h.value
+
+
+def kvc_cold_destroy(store: int) -> None:
+    if store:
+        load().kvc_cold_destroy(store)
+
+
+def kvc_cold_evict(ctx, store, seq, scratch, p0, p1, key, cls):
+    """Returns (stored, n_tok)."""
+    stored, n = C.c_int(), C.c_int32()
+    _check_cold(store, ctx, load().kvc_cold_evict(ctx, store, seq, scratch, p0, p1, C.c_uint64(key), cls,
+                                                  C.byref(stored), C.byref(n)))
+    return stored.value, n.value
+
+
+def kvc_cold_admit(ctx, store, seq, scratch, key):
+    """Returns (hit, n_tok)."""
+    hit, n = C.c_int(), C.c_int32()
+    _check_cold(store, ctx, load().kvc_cold_admit(ctx, store, seq, scratch, C.c_uint64(key), C.byref(hit),
+                                                  C.byref(n)))
+    return hit.value, n.value
+
+
+def kvc_cold_find(store, key):
+    """Returns (n_tok, cls); (0, -1) when absent."""
+    n, cls = C.c_int32(), C.c_int32()
+    _check_cold(store, None, load().kvc_cold_find(store, C.c_uint64(key), C.byref(n), C.byref(cls)))
+    return n.value, cls.value
+
+
+def kvc_cold_get_stats(store) -> dict:
+    st = kvc_cold_stats()
+    _check_cold(store, None, load().kvc_cold_get_stats(store, C.byref(st)))
+    return st.as_dict()
+
+
+class ColdStore:
+    """Owns one cold store; evict / admit take the KVCache they act on."""
+
+    def __init__(self, budget_tokens):
+        self.handle = kvc_cold_create(budget_tokens)
+
+    def close(self):
+        if self.handle:
+            kvc_cold_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def evict(self, cache, seq, scratch, p0, p1, key, cls):
+        return kvc_cold_evict(cache.ctx, self.handle, seq, scratch, p0, p1, key, cls)
+
+    def admit(self, cache, seq, scratch, key):
+        return kvc_cold_admit(cache.ctx, self.handle, seq, scratch, key)
+
+    def find(self, key):
+        return kvc_cold_find(self.handle, key)
+
+    def stats(self):
+        return kvc_cold_get_stats(self.handle)

@@ -13,11 +13,11 @@ row-list model of the sequence operations and the state byte format
 """
 from .numerics import lib, F16, Q8_0, f16_to_f64, f32_to_f16, q8_0_quantize, q8_0_dequantize, attn, attn_bruteforce
 from .numerics import rope_rotate, rope_shift_q8_0, rope_shift_f16, keydiff_scores, min_window
-from .model import OracleCache, STATE_MAGIC, STATE_VERSION, state_size
+from .model import OracleCache, ColdStore, STATE_MAGIC, STATE_VERSION, state_size
 
 __all__ = [
     "lib", "F16", "Q8_0", "f16_to_f64", "f32_to_f16", "q8_0_quantize", "q8_0_dequantize", "attn",
     "attn_bruteforce", "rope_rotate", "rope_shift_q8_0", "rope_shift_f16", "keydiff_scores", "min_window",
-    "OracleCache",
+    "OracleCache", "ColdStore",
     "STATE_MAGIC", "STATE_VERSION", "state_size",
 ]

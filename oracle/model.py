@@ -308,3 +308,105 @@ class OracleCache:
             q.K[l].extend(K[l])
             q.V[l].extend(V[l])
         return state_size(self.n_layer, self.Hk, self.D, self.type_k, self.type_v, len(pos))
+
+
+class ColdStore:
+    """Host-RAM cold store of evicted ranges (Plan: lossless long context,
+    #3 Host-RAM KV cold store + retrieval, section llama - KV-byte offload).
+
+    Evict: copy the range to a scratch sequence, export it as state bytes,
+    keep them under the range's token hash with its cache class, drop the
+    scratch, then remove the range and slide the later rows down.  The store
+    is bounded in tokens; when a block does not fit, blocks are dropped by
+    class (the more evictable first: a larger class number here) and least
+    recently stored first within a class, but never a block less evictable
+    than the new one: then the new block is not kept (the pages: lossy only
+    at the cold tier, only for the most evictable classes).  Admit (append
+    mode): import the bytes into the scratch sequence, shift them so that the
+    first row follows the sequence's last position, copy them into the
+    sequence, drop the scratch.  A block lives in one tier, so an admitted
+    block leaves the store; a miss changes nothing (the caller recomputes).
+    """
+
+    def __init__(self, budget_tokens: int):
+        if budget_tokens < 1:
+            raise ValueError("budget must be positive")
+        self.budget = int(budget_tokens)
+        self.blocks = []  # dicts: key, cls, n, first, stamp, blob
+        self.clock = 0
+        self.stats = {"stored": 0, "rejected": 0, "dropped": 0, "hits": 0, "misses": 0}
+
+    @property
+    def tokens(self) -> int:
+        return sum(b["n"] for b in self.blocks)
+
+    def find(self, key: int):
+        for b in self.blocks:
+            if b["key"] == key:
+                return b
+        return None
+
+    def victims(self, n: int, cls: int):
+        """Blocks to drop so that n tokens of class cls fit, in drop order, or
+        None when they cannot make room."""
+        if n > self.budget:
+            return None
+        cand = sorted((b for b in self.blocks if b["cls"] >= cls), key=lambda b: (-b["cls"], b["stamp"]))
+        used, out = self.tokens, []
+        for b in cand:
+            if used + n <= self.budget:
+                break
+            out.append(b)
+            used -= b["n"]
+        return out if used + n <= self.budget else None
+
+    def evict(self, cache: "OracleCache", seq: int, scratch: int, p0: int, p1: int, key: int, cls: int):
+        """Returns (stored, n_tok)."""
+        q = cache._seq(seq)
+        if cache.n_tokens(scratch) != 0:
+            raise ValueError("scratch sequence not empty")
+        sel = (q.pos >= p0) & (q.pos < p1)
+        n = int(sel.sum())
+        if n == 0:
+            return 0, 0
+        first = int(q.pos[sel].min())
+        old = self.find(key)
+        if old is not None:
+            self.blocks.remove(old)
+        vict = self.victims(n, cls)
+        stored = 0
+        if vict is not None:
+            cache.seq_cp(seq, scratch, p0, p1)
+            blob = cache.state_get(scratch, -1, -1)
+            cache.seq_rm(scratch, -1, -1)
+            for b in vict:
+                self.blocks.remove(b)
+                self.stats["dropped"] += 1
+            self.clock += 1
+            self.blocks.append({"key": key, "cls": cls, "n": n, "first": first, "stamp": self.clock, "blob": blob})
+            self.stats["stored"] += 1
+            stored = 1
+        else:
+            self.stats["rejected"] += 1
+        cache.seq_rm(seq, p0, p1)
+        cache.seq_add(seq, p1, -1, -(p1 - p0))
+        return stored, n
+
+    def admit(self, cache: "OracleCache", seq: int, scratch: int, key: int):
+        """Returns (hit, n_tok)."""
+        if cache.n_tokens(scratch) != 0:
+            raise ValueError("scratch sequence not empty")
+        b = self.find(key)
+        if b is None:
+            self.stats["misses"] += 1
+            return 0, 0
+        pos = cache.positions(seq)
+        tail = int(pos.max()) + 1 if len(pos) else 0
+        cache.state_set(scratch, b["blob"])
+        if tail != b["first"]:
+            cache.seq_add(scratch, -1, -1, tail - b["first"])
+        cache.seq_cp(scratch, seq, -1, -1)
+        cache.seq_rm(scratch, -1, -1)
+        self.blocks.remove(b)
+        self.stats["hits"] += 1
+        return 1, b["n"]

@@ -335,6 +335,48 @@ def test_host_resident_ring_built_behind_busy_stream():
         assert np.array_equal(out, base), (depth, budget)
 
 
+# ------------------------------------------------------------- cold store --
+def test_cold_store_scenario_matches_oracle():
+    """Evictions into a bounded host cold store and admits back at the tail,
+    on the library and on the oracle with the same calls: the kept / not
+    kept and hit / miss results and the store statistics agree exactly, and
+    the final sequence matches (positions and V exact, shifted K within the
+    requantisation tolerance).  Every row is shifted at most once: tail
+    evictions slide nothing, the one head eviction slides the rest once, and
+    the admitted blocks were never shifted before."""
+    from kv_cache_decode_flash_gb300 import kvc
+
+    tw = Twin(2, 8, 2, 128, 4096, n_seq_max=2, type_=Q8, rope_base=1e6, page_rows=64)
+    store = kvc.ColdStore(400)
+    ref = oracle.ColdStore(400)
+    try:
+        tw.fill(0, 1200, seed=17, sigma=0.5)
+        ops = [("evict", 1000, 1200, 11, 0), ("evict", 900, 1000, 12, 1), ("evict", 800, 900, 13, 1),
+               ("evict", 0, 100, 14, 2), ("evict", 600, 700, 15, 0), ("admit", 12), ("admit", 13),
+               ("admit", 11)]
+        for op in ops:
+            if op[0] == "evict":
+                _, p0, p1, key, cls = op
+                got = store.evict(tw.gpu, 0, 1, p0, p1, key, cls)
+                want = ref.evict(tw.ref, 0, 1, p0, p1, key, cls)
+            else:
+                got = store.admit(tw.gpu, 0, 1, op[1])
+                want = ref.admit(tw.ref, 0, 1, op[1])
+            assert got == want, (op, got, want)
+            assert np.array_equal(tw.gpu.positions(0), tw.ref.positions(0)), op
+            assert tw.gpu.n_tokens(1) == 0
+        st = store.stats()
+        assert {k: st[k] for k in ref.stats} == ref.stats
+        assert st["tokens"] == ref.tokens and st["blocks"] == len(ref.blocks)
+        assert [store.find(b["key"]) for b in ref.blocks] == [(b["n"], b["cls"]) for b in ref.blocks]
+        assert ref.stats == {"stored": 4, "rejected": 1, "dropped": 1, "hits": 2, "misses": 1}
+        assert np.array_equal(np.sort(tw.gpu.positions(0)), np.arange(900))
+        _check_shifted_q8(tw, 0)
+    finally:
+        store.close()
+        tw.close()
+
+
 # ------------------------------------------------- per-head residency split --
 @pytest.mark.parametrize("type_,G", [(Q8, 4), (F16, 2), (Q8, 7)])
 def test_split_heads_vs_oracle_and_pipelined(type_, G):

@@ -481,3 +481,98 @@ def test_evict_window_removes_the_least_distinctive_rows():
     # no window fits: nothing changes
     assert c.evict_window(0, 0, n_keep=10, n_discard=8, n_recent=4) == -1
     assert c.n_tokens(0) == n - 4
+
+
+# Pins of the host-RAM cold store policy (Plan: lossless long context, #3
+# Host-RAM KV cold store + retrieval, llama - KV-byte offload): bounded in
+# tokens, blocks dropped most evictable class first and least recently
+# stored first within a class, never a less evictable block for a more
+# evictable one; admit in append mode; evict -> admit is lossless.
+
+def _cold_cache(n, n_seq=2, seed=9):
+    rng = np.random.default_rng(seed)
+    c = oracle.OracleCache(2, 4, 2, 64, oracle.Q8_0, oracle.Q8_0, 1e4, 0)
+    for l in range(2):
+        c.append(l, 0, 0, rng.normal(0, 1, (n, 2, 64)).astype(np.float32),
+                 rng.normal(0, 1, (n, 2, 64)).astype(np.float32))
+    return c
+
+
+def test_cold_store_victim_order_closed_case():
+    c = _cold_cache(100)
+    s = oracle.ColdStore(10)
+    # evicting from the tail keeps the arithmetic simple: no slide
+    assert s.evict(c, 0, 1, 96, 100, key=1, cls=0) == (1, 4)    # A: 4 tokens, class 0
+    assert s.evict(c, 0, 1, 93, 96, key=2, cls=1) == (1, 3)     # B: 3, class 1
+    assert s.evict(c, 0, 1, 90, 93, key=3, cls=1) == (1, 3)     # C: 3, class 1 -> store full (10)
+    assert s.evict(c, 0, 1, 87, 90, key=4, cls=1) == (1, 3)     # D: drops B (class 1, oldest)
+    assert [b["key"] for b in s.blocks] == [1, 3, 4] and s.stats["dropped"] == 1
+    assert s.evict(c, 0, 1, 82, 87, key=5, cls=0) == (1, 5)     # E (5, class 0): drops C then D, keeps A
+    assert [b["key"] for b in s.blocks] == [1, 5] and s.tokens == 9 and s.stats["dropped"] == 3
+    assert s.evict(c, 0, 1, 80, 82, key=6, cls=2) == (0, 2)     # class 2 may drop nothing here: not kept
+    assert s.evict(c, 0, 1, 69, 80, key=7, cls=9) == (0, 11)    # larger than the budget: not kept
+    assert s.stats["rejected"] == 2 and s.tokens == 9
+    assert c.n_tokens(0) == 69 and c.n_tokens(1) == 0           # evicted rows left the cache either way
+    assert s.admit(c, 0, 1, key=3) == (0, 0) and s.stats["misses"] == 1
+
+
+def test_cold_store_tail_round_trip_is_lossless():
+    c = _cold_cache(64)
+    before = c.state_get(0, -1, -1)
+    s = oracle.ColdStore(1000)
+    assert s.evict(c, 0, 1, 40, 64, key=7, cls=0) == (1, 24)
+    assert c.n_tokens(0) == 40
+    assert s.admit(c, 0, 1, key=7) == (1, 24)                   # back at position 40: no shift
+    assert c.state_get(0, -1, -1) == before and s.blocks == [] and c.n_tokens(1) == 0
+
+
+def test_cold_store_admit_after_slide_equals_manual_ops():
+    # evict the head, which slides the rest down; admit returns it at the tail, shifted
+    a, b = _cold_cache(80), _cold_cache(80)
+    s = oracle.ColdStore(100)
+    assert s.evict(a, 0, 1, 0, 16, key=3, cls=0) == (1, 16)
+    assert np.array_equal(a.positions(0), np.arange(64))
+    assert s.admit(a, 0, 1, key=3) == (1, 16)
+    assert np.array_equal(a.positions(0), np.arange(80))
+    # the same steps by hand
+    b.seq_cp(0, 1, 0, 16)
+    blob = b.state_get(1, -1, -1)
+    b.seq_rm(1, -1, -1)
+    b.seq_rm(0, 0, 16)
+    b.seq_add(0, 16, -1, -16)
+    b.state_set(1, blob)
+    b.seq_add(1, -1, -1, 64)
+    b.seq_cp(1, 0, -1, -1)
+    b.seq_rm(1, -1, -1)
+    assert a.state_get(0, -1, -1) == b.state_get(0, -1, -1)
+
+
+def test_cold_store_invariants_random():
+    rng = np.random.default_rng(11)
+    for trial in range(20):
+        c = _cold_cache(400, seed=trial)
+        s = oracle.ColdStore(int(rng.integers(20, 120)))
+        key = 0
+        for _ in range(12):
+            n = c.n_tokens(0)
+            if n < 2:
+                break
+            w = int(rng.integers(1, min(40, n) + 1))
+            p0 = int(rng.integers(0, n - w + 1))
+            cls = int(rng.integers(0, 3))
+            before = [(b["key"], b["cls"], b["stamp"], b["n"]) for b in s.blocks]
+            key += 1
+            stored, got = s.evict(c, 0, 1, p0, p0 + w, key=key, cls=cls)
+            assert got == w and s.tokens <= s.budget
+            after = {b["key"] for b in s.blocks}
+            gone = [x for x in before if x[0] not in after]
+            # every dropped block was at least as evictable as the new one, and a kept block of a
+            # class above a dropped one's, or older in the same class, was not passed over
+            assert all(g[1] >= cls for g in gone)
+            for g in gone:
+                for x in before:
+                    if x[0] in after and x[1] >= cls:
+                        assert (x[1], -x[2]) <= (g[1], -g[2])
+            assert stored == (key in after)
+            if not stored:
+                assert gone == []
