@@ -463,7 +463,8 @@ int kvc_create(const kvc_params *p, kvc_ctx **out) {
     c->ksb = c->tk == KVC_Q8_0 ? (c->D / QK) * 2 : 0;
     c->vsb = c->tv == KVC_Q8_0 ? (c->D / QK) * 2 : 0;
     c->host = p->residency == KVC_HOST_PINNED;
-    c->occ = attn_ctas_per_sm(c->tk, c->D, c->r);
+    c->occ = attn_ctas_per_sm(c->tk, c->D, c->r, 0);
+    c->occ2 = attn_ctas_per_sm(c->tk, c->D, c->r, 1);
 
     auto fail = [&](int rc) {
         kvc_destroy(reinterpret_cast<kvc_ctx *>(c));

@@ -66,7 +66,8 @@ struct Ctx {
     std::string err;
     int dev = 0;
     int sms = 0;
-    int occ = 1; // attention CTAs resident per SM (from the occupancy calculator)
+    int occ = 1;  // attention CTAs resident per SM (from the occupancy calculator), configuration 0
+    int occ2 = 0; // the same for configuration 1 (two CTAs per SM; 0 where it does not exist)
     int H = 0, Hk = 0, D = 0, r = 0, L = 0, P = 0;
     int tk = 0, tv = 0;
     int krow = 0, vrow = 0, ksb = 0, vsb = 0; // data row bytes, scale row bytes (0 for f16)

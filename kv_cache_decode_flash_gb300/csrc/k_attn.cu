@@ -180,10 +180,13 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 // Static shape of one kernel instance.  W compute warps in groups of GW;
 // group j takes tiles j, j + G, j + 2G, ... and each of its warps owns 16
 // rows of a tile.  One more warp issues the tile loads.
-template <int TYPE, int D, int R>
+template <int TYPE, int D, int R, int CFG = 0>
 struct Shape {
     static constexpr bool Q8 = TYPE == KVC_Q8_0;
-    static constexpr int W = Q8 ? 16 : 8;             // compute warps per CTA (one CTA per SM)
+    // CFG 0: one CTA per SM (16 compute warps for q8_0); CFG 1 (q8_0): two CTAs
+    // per SM of 8 compute warps, each with half the SM's shared memory, for
+    // launches whose work exceeds one wave of CFG 0 at the longest chunks
+    static constexpr int W = (Q8 && CFG == 0) ? 16 : 8; // compute warps per CTA
     static constexpr int GW = 8;                      // warps per group
     static constexpr int G = W / GW;                  // groups
     static constexpr int NTHREADS = (W + 1) * 32;     // compute warps + the load warp
@@ -203,13 +206,18 @@ struct Shape {
     static constexpr int MAXT = 512;                  // tiles per chunk (host keeps chunks within it)
     // as many stages (2..8) as fit next to the exchange buffers in one SM's shared memory
     static constexpr int QF_BYTES = KSTEPS * 32 * 16 + 64; // q fragments (one copy for all warps) + head scales
-    static constexpr int FIT = (232448 - 4096 - W * PBUF * 4 - 1024 - MAXT * 8 - 256 - QF_BYTES) / STAGE;
+    static constexpr int SM_BUDGET = CFG == 1 ? 115712 : 232448; // shared memory one CTA may take
+    static constexpr int MINB = CFG == 1 ? 2 : 1;                 // CTAs per SM the registers allow for
+    static constexpr int FIT = (SM_BUDGET - 4096 - W * PBUF * 4 - 1024 - MAXT * 8 - 256 - QF_BYTES) / STAGE;
     static constexpr int STAGES = FIT < 2 ? 2 : (FIT > 8 ? 8 : FIT);
     static constexpr int OOFF = ((2 * R + 3) / 4) * 4;  // partial: m[R], l[R], pad, then o[R][D] 16-byte aligned
     static constexpr int PF = OOFF + R * D;            // floats of one partial
     static constexpr int SMEM =
         STAGES * STAGE + W * PBUF * 4 + 2 * STAGES * 8 + STAGES * 8 + 64 + MAXT * 8 + QF_BYTES + 1024;
-    static constexpr int MERGE_CAP = (STAGES * STAGE) / (4 * (PF + R)); // chunks the grid merge can stage
+    static constexpr int MERGE_CAP = (STAGES * STAGE) / (4 * (PF + R)); // chunks one merge round stages
+    // chunks per (sequence, kv head) the planner may use: CFG 0 merges in one
+    // round; CFG 1 has little staging room and merges in rounds
+    static constexpr int CHUNK_CAP = CFG == 1 ? 256 : MERGE_CAP;
     static constexpr int BIG = 128;                    // rows of a large TMA box (small boxes are 16 rows)
     static constexpr int NMT = D / 16;                 // PV m-tiles of 16 dims
 };
@@ -228,12 +236,12 @@ struct TileInfo {
     int delta; // scale rows skipped by the 16-byte alignment of the scale copy
 };
 
-template <int TYPE, int D, int R, bool RAW = false>
-__global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
+template <int TYPE, int D, int R, bool RAW = false, int CFG = 0>
+__global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, D, R, CFG>::MINB)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmk,
                 const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmkb,
                 const __grid_constant__ CUtensorMap tmvb) {
-    using S = Shape<TYPE, D, R>;
+    using S = Shape<TYPE, D, R, CFG>;
     constexpr int W = S::W, T = S::T, NT = S::NTHREADS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -287,7 +295,16 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
     __syncthreads();
     const int n_tiles = s_flag;
     if (warp == 0)
-        for (int k = lane; k < n_tiles; k += 32) s_tpage[k] = sq.page_table[(sq.off + s_tstart[k]) / p.P];
+        for (int k = lane; k < n_tiles; k += 32) {
+            // a page outside the page table or the tensor maps is reported and its tile skipped
+            const int idx = (sq.off + s_tstart[k]) / p.P;
+            int page = idx < sq.pt_len ? sq.page_table[idx] : -1;
+            if (page < 0 || ((int64_t)page * p.Hk + p.Hk) * p.P > p.map_rows) {
+                atomicOr(p.err, ERR_BAD_PAGE);
+                page = -1;
+            }
+            s_tpage[k] = page;
+        }
     __syncthreads();
 
     // ---- tile loads, all issued by lane 0 of the load warp (warp W) -----------
@@ -296,6 +313,12 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
         const int r0 = s_tstart[k];
         const int n = tile_rows(r0);
         const int page = s_tpage[k];
+        if (page < 0) { // reported: the stage completes with nothing copied
+            tinfo[s].n = n;
+            tinfo[s].delta = 0;
+            mbar_expect_tx(&full[s], 0);
+            return;
+        }
         const int cell = (sq.off + r0) % p.P;
         const int64_t R0 = ((int64_t)page * p.Hk + g) * p.P + cell;
         uint8_t *st = stages + s * S::STAGE;
@@ -312,7 +335,7 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
             delta = (int)((start - saligned) / S::SB);
             const int64_t end = (start + (int64_t)n * S::SB + 15) & ~(int64_t)15;
             sbytes = (unsigned)(end - saligned);
-            if (saligned + (int64_t)sbytes > p.scale_limit_bytes) {
+            if (saligned < 0 || saligned + (int64_t)sbytes > p.scale_limit_bytes) {
                 atomicOr(p.err, ERR_BAD_INDEX);
                 sbytes = 0;
             }
@@ -659,6 +682,8 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
 
     const int n_chunks = sq.n_chunks;
     float *part = p.part + ((int64_t)(sq.part0 + lc) * p.Hk + g) * S::PF;
+    const bool part_ok = ((int64_t)(sq.part0 + lc) * p.Hk + g + 1) * S::PF <= p.part_cap;
+    if (!part_ok && tid == 0 && n_chunks > 1) atomicOr(p.err, ERR_BAD_PART);
     float *outp = p.out + ((int64_t)sq.out_row * p.H + (int64_t)g * r_act) * D;
     // fragment (mt, ln): heads 2t, 2t+1 of lane ln, dims of rows g and g+8.  Each
     // fragment weighs the warps itself (softmax rescale and the warp's 2^-S: O
@@ -704,7 +729,7 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
                 outp[h1 * D + dA] = (L1 > 0.f) ? O.y / L1 : 0.f;
                 outp[h1 * D + dB] = (L1 > 0.f) ? O.w / L1 : 0.f;
             }
-        } else {
+        } else if (part_ok) {
             if (h0 < R) {
                 part[S::OOFF + h0 * D + dA] = O.x;
                 part[S::OOFF + h0 * D + dB] = O.z;
@@ -742,46 +767,72 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
     if (!s_flag) return;
     const float *part0 = p.part + ((int64_t)sq.part_first * p.Hk + g) * S::PF;
     const int64_t cstride = (int64_t)p.Hk * S::PF;
-    // one round of independent loads stages every partial in shared memory
-    // (the host keeps n_chunks <= MERGE_CAP)
+    if (((int64_t)(sq.part_first + n_chunks - 1) * p.Hk + g + 1) * S::PF > p.part_cap) {
+        // reported above or by the CTA that wrote past the buffer: nothing to merge
+        if (tid == 0) atomicOr(p.err, ERR_BAD_PART);
+        return;
+    }
+    // The partials are merged in rounds of at most MERGE_CAP chunks, each
+    // staged in shared memory by one round of independent loads.  A thread
+    // owns one output column (4 dims of one head) and keeps its running
+    // maximum, weight sum and weighted output across rounds, rescaled when a
+    // round raises the maximum; within a round the chunks go in chunk order.
+    // The same bits on every call; one round gives the plain merge.
+    static_assert(8 * (D / 4) <= NT, "one output column per thread");
     constexpr int Q4 = S::PF / 4; // float4 per partial
     float4 *stg = reinterpret_cast<float4 *>(stages);
-    const int items = n_chunks * Q4;
-    for (int base = 0; base < items; base += 8 * NT) {
-        float4 v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int it = base + u * NT + tid;
-            v[u] = (it < items) ? __ldcg(reinterpret_cast<const float4 *>(part0 + (it / Q4) * cstride) + it % Q4)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int it = base + u * NT + tid;
-            if (it < items) stg[it] = v[u];
-        }
-    }
-    __syncthreads();
     const float *sp = reinterpret_cast<const float *>(stg);
-    // every output column weighs the chunks itself (max, then weights and sums in
-    // chunk order: the same bits on every call), with no further barrier
-    for (int col = tid; col < r_act * (D / 4); col += NT) {
-        const int h = col / (D / 4), i4 = col % (D / 4);
-        float M = -INFINITY;
-        for (int c = 0; c < n_chunks; ++c) M = fmaxf(M, sp[c * S::PF + h]);
-        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-        float L = 0.f;
-        if (M != -INFINITY) {
-            for (int c = 0; c < n_chunks; ++c) {
-                const float w = ex2(sp[c * S::PF + h] - M);
-                const float4 v = *reinterpret_cast<const float4 *>(sp + c * S::PF + S::OOFF + h * D + 4 * i4);
-                L = fmaf(w, sp[c * S::PF + R + h], L);
-                O.x = fmaf(w, v.x, O.x);
-                O.y = fmaf(w, v.y, O.y);
-                O.z = fmaf(w, v.z, O.z);
-                O.w = fmaf(w, v.w, O.w);
+    const int col = tid, ncol = r_act * (D / 4);
+    const int h = col / (D / 4), i4 = col % (D / 4);
+    float Mrun = -INFINITY, L = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < n_chunks; c0 += S::MERGE_CAP) {
+        const int nc = min(S::MERGE_CAP, n_chunks - c0);
+        if (c0 > 0) __syncthreads(); // the previous round's reads of the staging are done
+        const int items = nc * Q4;
+        for (int base = 0; base < items; base += 8 * NT) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int it = base + u * NT + tid;
+                v[u] = (it < items)
+                           ? __ldcg(reinterpret_cast<const float4 *>(part0 + (c0 + it / Q4) * cstride) + it % Q4)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int it = base + u * NT + tid;
+                if (it < items) stg[it] = v[u];
             }
         }
+        __syncthreads();
+        if (col < ncol) {
+            float M = -INFINITY;
+            for (int c = 0; c < nc; ++c) M = fmaxf(M, sp[c * S::PF + h]);
+            if (M != -INFINITY) {
+                const float Mn = fmaxf(Mrun, M);
+                if (Mrun != -INFINITY && Mn != Mrun) {
+                    const float a = ex2(Mrun - Mn);
+                    O.x *= a;
+                    O.y *= a;
+                    O.z *= a;
+                    O.w *= a;
+                    L *= a;
+                }
+                for (int c = 0; c < nc; ++c) {
+                    const float w = ex2(sp[c * S::PF + h] - Mn);
+                    const float4 v = *reinterpret_cast<const float4 *>(sp + c * S::PF + S::OOFF + h * D + 4 * i4);
+                    L = fmaf(w, sp[c * S::PF + R + h], L);
+                    O.x = fmaf(w, v.x, O.x);
+                    O.y = fmaf(w, v.y, O.y);
+                    O.z = fmaf(w, v.z, O.z);
+                    O.w = fmaf(w, v.w, O.w);
+                }
+                Mrun = Mn;
+            }
+        }
+    }
+    if (col < ncol) {
         float *dst = outp + h * D + 4 * i4;
         dst[0] = (L > 0.f) ? O.x / L : 0.f;
         dst[1] = (L > 0.f) ? O.y / L : 0.f;
@@ -790,14 +841,14 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R>::NTHREADS, 1)
     }
 }
 
-template <int TYPE, int D, int R, bool RAW = false>
+template <int TYPE, int D, int R, bool RAW = false, int CFG = 0>
 cudaError_t launch_t(const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv, cudaStream_t st) {
     // tmk / tmv point at {16-row map, 128-row map} pairs
-    using S = Shape<TYPE, D, R>;
+    using S = Shape<TYPE, D, R, CFG>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_kernel<TYPE, D, R, RAW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             S::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(attn_kernel<TYPE, D, R, RAW, CFG>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
         if (e != cudaSuccess) return e;
         configured = true;
     }
@@ -811,46 +862,53 @@ cudaError_t launch_t(const AttnParams &p, const CUtensorMap *tmk, const CUtensor
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_kernel<TYPE, D, R, RAW>, p, tmk[0], tmv[0], tmk[1], tmv[1]);
+    return cudaLaunchKernelEx(&cfg, attn_kernel<TYPE, D, R, RAW, CFG>, p, tmk[0], tmv[0], tmk[1], tmv[1]);
 }
 
 template <int TYPE, int D>
 cudaError_t launch_d(const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv, cudaStream_t st,
-                     bool raw) {
+                     bool raw, int cfg) {
     // plain int8 codes (caller buffers): one instance for every group size up to 8
-    if constexpr (TYPE == KVC_Q8_0)
+    if constexpr (TYPE == KVC_Q8_0) {
         if (raw) return p.r <= 8 ? launch_t<TYPE, D, 8, true>(p, tmk, tmv, st) : cudaErrorInvalidValue;
+        if (cfg == 1) {
+            if (p.r <= 4) return launch_t<TYPE, D, 4, false, 1>(p, tmk, tmv, st);
+            if (p.r == 5) return launch_t<TYPE, D, 5, false, 1>(p, tmk, tmv, st);
+            if (p.r <= 8) return launch_t<TYPE, D, 8, false, 1>(p, tmk, tmv, st);
+            return cudaErrorInvalidValue;
+        }
+    }
     if (p.r <= 4) return launch_t<TYPE, D, 4>(p, tmk, tmv, st);
     if (p.r == 5) return launch_t<TYPE, D, 5>(p, tmk, tmv, st);
     if (p.r <= 8) return launch_t<TYPE, D, 8>(p, tmk, tmv, st);
     return cudaErrorInvalidValue;
 }
 
-template <int TYPE, int D, int R>
+template <int TYPE, int D, int R, int CFG>
 int occupancy() {
-    using S = Shape<TYPE, D, R>;
+    using S = Shape<TYPE, D, R, CFG>;
     int n = 0;
-    cudaFuncSetAttribute(attn_kernel<TYPE, D, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<TYPE, D, R>, S::NTHREADS, S::SMEM) !=
-        cudaSuccess) {
+    cudaFuncSetAttribute(attn_kernel<TYPE, D, R, false, CFG>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<TYPE, D, R, false, CFG>, S::NTHREADS,
+                                                      S::SMEM) != cudaSuccess) {
         cudaGetLastError();
         return 1;
     }
     return n > 0 ? n : 1;
 }
 
-template <int TYPE, int D>
+template <int TYPE, int D, int CFG>
 int occupancy_d(int r) {
-    if (r <= 4) return occupancy<TYPE, D, 4>();
-    if (r == 5) return occupancy<TYPE, D, 5>();
-    return occupancy<TYPE, D, 8>();
+    if (r <= 4) return occupancy<TYPE, D, 4, CFG>();
+    if (r == 5) return occupancy<TYPE, D, 5, CFG>();
+    return occupancy<TYPE, D, 8, CFG>();
 }
 
-template <int TYPE, int D>
-int merge_cap_d(int r) {
-    if (r <= 4) return Shape<TYPE, D, 4>::MERGE_CAP;
-    if (r == 5) return Shape<TYPE, D, 5>::MERGE_CAP;
-    return Shape<TYPE, D, 8>::MERGE_CAP;
+template <int TYPE, int D, int CFG>
+int chunk_cap_d(int r) {
+    if (r <= 4) return Shape<TYPE, D, 4, CFG>::CHUNK_CAP;
+    if (r == 5) return Shape<TYPE, D, 5, CFG>::CHUNK_CAP;
+    return Shape<TYPE, D, 8, CFG>::CHUNK_CAP;
 }
 
 } // namespace
@@ -860,24 +918,32 @@ size_t attn_partial_floats(int r, int D) {
     return (size_t)(((2 * R + 3) / 4) * 4 + R * D);
 }
 
-int attn_ctas_per_sm(int type, int D, int r) {
-    if (type == KVC_Q8_0) return D == 128 ? occupancy_d<KVC_Q8_0, 128>(r) : occupancy_d<KVC_Q8_0, 64>(r);
-    return D == 128 ? occupancy_d<KVC_F16, 128>(r) : occupancy_d<KVC_F16, 64>(r);
+int attn_ctas_per_sm(int type, int D, int r, int cfg) {
+    if (type == KVC_Q8_0) {
+        if (cfg == 1) return D == 128 ? occupancy_d<KVC_Q8_0, 128, 1>(r) : occupancy_d<KVC_Q8_0, 64, 1>(r);
+        return D == 128 ? occupancy_d<KVC_Q8_0, 128, 0>(r) : occupancy_d<KVC_Q8_0, 64, 0>(r);
+    }
+    if (cfg == 1) return 0; // f16 has one configuration
+    return D == 128 ? occupancy_d<KVC_F16, 128, 0>(r) : occupancy_d<KVC_F16, 64, 0>(r);
 }
 
-int attn_merge_cap(int type, int D, int r) {
-    if (type == KVC_Q8_0) return D == 128 ? merge_cap_d<KVC_Q8_0, 128>(r) : merge_cap_d<KVC_Q8_0, 64>(r);
-    return D == 128 ? merge_cap_d<KVC_F16, 128>(r) : merge_cap_d<KVC_F16, 64>(r);
+int attn_merge_cap(int type, int D, int r, int cfg) {
+    if (type == KVC_Q8_0) {
+        if (cfg == 1) return D == 128 ? chunk_cap_d<KVC_Q8_0, 128, 1>(r) : chunk_cap_d<KVC_Q8_0, 64, 1>(r);
+        return D == 128 ? chunk_cap_d<KVC_Q8_0, 128, 0>(r) : chunk_cap_d<KVC_Q8_0, 64, 0>(r);
+    }
+    return D == 128 ? chunk_cap_d<KVC_F16, 128, 0>(r) : chunk_cap_d<KVC_F16, 64, 0>(r);
 }
 
 cudaError_t launch_attn(int type, const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv,
-                        cudaStream_t st, bool raw_codes) {
+                        cudaStream_t st, bool raw_codes, int cfg) {
     if (type == KVC_Q8_0) {
-        if (p.D == 128) return launch_d<KVC_Q8_0, 128>(p, tmk, tmv, st, raw_codes);
-        if (p.D == 64) return launch_d<KVC_Q8_0, 64>(p, tmk, tmv, st, raw_codes);
+        if (p.D == 128) return launch_d<KVC_Q8_0, 128>(p, tmk, tmv, st, raw_codes, cfg);
+        if (p.D == 64) return launch_d<KVC_Q8_0, 64>(p, tmk, tmv, st, raw_codes, cfg);
     } else {
-        if (p.D == 128) return launch_d<KVC_F16, 128>(p, tmk, tmv, st, false);
-        if (p.D == 64) return launch_d<KVC_F16, 64>(p, tmk, tmv, st, false);
+        if (cfg != 0) return cudaErrorInvalidValue;
+        if (p.D == 128) return launch_d<KVC_F16, 128>(p, tmk, tmv, st, false, 0);
+        if (p.D == 64) return launch_d<KVC_F16, 64>(p, tmk, tmv, st, false, 0);
     }
     return cudaErrorInvalidValue;
 }

@@ -71,16 +71,17 @@ extern "C" int kvc_attn_decode_static(int type, int n_head, int n_head_kv, int h
     unsigned char *base = g_scratch_dev[dev];
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
-    // split-K plan: whole waves of CTAs, 64..2048 rows per chunk
-    const int occ = attn_ctas_per_sm(type, head_dim, r);
+    // split-K plan (one CTA per SM): whole waves of CTAs, 64..ATTN_MAX_CHUNK_ROWS rows per chunk
+    const int occ = attn_ctas_per_sm(type, head_dim, r, 0);
     const int64_t slots = (int64_t)g_sms[dev] * occ;
     const int64_t work = std::max<int64_t>((int64_t)n_kv * n_head_kv, 1);
-    const int64_t waves = std::max<int64_t>(1, (work + slots * 2048 - 1) / (slots * 2048));
+    const int64_t cmax = ATTN_MAX_CHUNK_ROWS;
+    const int64_t waves = std::max<int64_t>(1, (work + slots * cmax - 1) / (slots * cmax));
     int64_t C = (work + waves * slots - 1) / (waves * slots);
-    C = std::min<int64_t>(2048, std::max<int64_t>(64, (C + 15) / 16 * 16));
-    const int cap = attn_merge_cap(type, head_dim, r);
+    C = std::min<int64_t>(cmax, std::max<int64_t>(64, (C + 15) / 16 * 16));
+    const int cap = attn_merge_cap(type, head_dim, r, 0);
     if ((n_kv + cap - 1) / cap > C) C = ((n_kv + cap - 1) / cap + 15) / 16 * 16;
-    C = std::min<int64_t>(C, 8000); // a chunk spans at most 512 tiles
+    C = std::min<int64_t>(C, cmax);
     const int n_chunks = std::max<int>(1, (int)((n_kv + C - 1) / C));
     const size_t part_bytes = (size_t)n_chunks * n_head_kv * attn_partial_floats(r, head_dim) * sizeof(float);
     if (part_bytes > STATIC_SCRATCH_BYTES - HEADER_BYTES) return KVC_ERANGE; // beyond the fixed work space
@@ -125,6 +126,8 @@ extern "C" int kvc_attn_decode_static(int type, int n_head, int n_head_kv, int h
     // the next multiple of 16 bytes
     const int sb = type == KVC_Q8_0 ? (head_dim / QK) * 2 : 0;
     p.scale_limit_bytes = ((int64_t)n_head_kv * n_kv * sb + 15) / 16 * 16;
+    p.map_rows = (int64_t)n_head_kv * std::max(n_kv, 1);
+    p.part_cap = (int64_t)((STATIC_SCRATCH_BYTES - HEADER_BYTES) / sizeof(float));
     AttnSeq &a = p.seq[0];
     a.page_table = reinterpret_cast<const int32_t *>(base + TICKET_BYTES + 16);
     a.off = 0;
@@ -134,5 +137,6 @@ extern "C" int kvc_attn_decode_static(int type, int n_head, int n_head_kv, int h
     a.out_row = 0;
     a.ticket = 0;
     a.stable_rows = 0; // caller buffers: nothing is read before the dependency wait
+    a.pt_len = 1;
     return launch_attn(type, p, tmk, tmv, st, /*raw_codes=*/true) == cudaSuccess ? KVC_OK : KVC_ECUDA;
 }

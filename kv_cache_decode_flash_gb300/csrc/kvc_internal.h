@@ -28,6 +28,8 @@ constexpr int TMA_BIG_ROWS = 128;      // rows per large TMA box
 constexpr uint32_t ERR_WAIT_TIMEOUT = 1u << 0;
 constexpr uint32_t ERR_BAD_INDEX = 1u << 1;
 constexpr uint32_t ERR_BAD_CONFIG = 1u << 2;
+constexpr uint32_t ERR_BAD_PAGE = 1u << 3; // attention: a page-table entry outside the tensor maps
+constexpr uint32_t ERR_BAD_PART = 1u << 4; // attention: a split-K partial outside the partial buffer
 
 // Addressing of one layer's K or V store.  Row index of (page, kv head g,
 // cell) is (page * Hk + g) * P + cell; data rows are `row_bytes` long,
@@ -56,6 +58,7 @@ struct AttnSeq {
     int32_t part_first;        // partial slot of the sequence's chunk 0 (n_chunks slots from there
                                // are merged); a sequence's chunks may span several launches, the
                                // ticket counting all of them
+    int32_t pt_len;            // entries of page_table
 };
 
 struct AttnParams {
@@ -72,6 +75,8 @@ struct AttnParams {
     int32_t *tickets;   // [MAX_SEQ_PER_LAUNCH * Hk] arrival counters, self-resetting
     uint32_t *err;      // device error word
     int64_t scale_limit_bytes; // bytes readable from ks / vs (bounds of the bulk copies)
+    int64_t map_rows;          // rows the K / V tensor maps cover (pages must lie inside)
+    int64_t part_cap;          // floats of the partial buffer
     AttnSeq seq[MAX_SEQ_PER_LAUNCH];
 };
 
@@ -79,10 +84,13 @@ struct AttnParams {
 // a pair of maps over the same rows: boxes of TMA_BOX_ROWS rows, then of
 // TMA_BIG_ROWS rows.
 // raw_codes: q8_0 codes are plain int8 (caller buffers) instead of offset binary.
+// cfg 0: one CTA per SM; cfg 1 (q8_0 only): two CTAs per SM, for launches whose
+// work exceeds one wave of cfg 0 at the longest chunks.
 cudaError_t launch_attn(int type, const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv,
-                        cudaStream_t st, bool raw_codes = false);
-int attn_ctas_per_sm(int type, int D, int r);
-int attn_merge_cap(int type, int D, int r); // most chunks per (sequence, kv head) one merge can take
+                        cudaStream_t st, bool raw_codes = false, int cfg = 0);
+int attn_ctas_per_sm(int type, int D, int r, int cfg = 0); // 0: the configuration does not exist
+int attn_merge_cap(int type, int D, int r, int cfg = 0);   // most chunks per (sequence, kv head) a launch may use
+constexpr int ATTN_MAX_CHUNK_ROWS = 8000;                  // a chunk spans at most 512 tiles
 size_t attn_partial_floats(int r, int D); // floats per (chunk, kv head) partial
 
 // Quantise-on-append.  Destination of token t: logical row row0 + t of a

@@ -42,33 +42,48 @@ void dev_free(Ctx *c, void *p, int64_t bytes);
 
 // ------------------------------------------------------ split-K planning ----
 
+// Split-K plan of one launch: rows per chunk and the kernel configuration.
 // Rows per chunk: enough chunks that every SM gets work in whole waves, no
-// chunk longer than 2048 rows (bounded merge fan-in and tail), at least 64
-// rows (partials stay a small fraction of the bytes read).  Depends only on
-// the row counts, the geometry and the SM count.
-static int auto_chunk_rows(const Ctx *c, int64_t total_rows) {
-    const int64_t slots = (int64_t)c->sms * c->occ;
-    const int64_t work = std::max<int64_t>(total_rows * c->Hk, 1);
-    const int64_t cmax = 2048;
-    const int64_t waves = std::max<int64_t>(1, (work + slots * cmax - 1) / (slots * cmax));
-    int64_t C = (work + waves * slots - 1) / (waves * slots);
-    C = (C + 15) / 16 * 16;
-    return (int)std::min<int64_t>(cmax, std::max<int64_t>(64, C));
-}
+// chunk longer than ATTN_MAX_CHUNK_ROWS (few long chunks amortise each CTA's
+// prologue and merge: one wave of long chunks beats several of short ones),
+// at least 64 rows (partials stay a small fraction of the bytes read).
+// Configuration 1 (two CTAs per SM, q8_0) takes over when the work exceeds
+// one wave of configuration 0 at the longest chunks: measured, it streams such
+// long contexts faster, and below that it is slower.  Depends only on the row
+// counts, the geometry and the SM count.
+struct ChunkPlan {
+    int C;
+    int cfg;
+};
 
-// Chunk rows of one launch over sequences of the given row counts.
-static int chunk_rows_plan(const Ctx *c, int n_seq, const int32_t *rows) {
+static ChunkPlan chunk_plan(const Ctx *c, int n_seq, const int32_t *rows) {
     int64_t total = 0;
     for (int i = 0; i < n_seq; ++i) total += rows[i];
-    int C = c->chunk_override ? c->chunk_override : auto_chunk_rows(c, total);
-    // one merge stages at most `cap` partials per (sequence, kv head)
-    const int cap = attn_merge_cap(c->tk, c->D, c->r);
+    const int64_t work = std::max<int64_t>(total * c->Hk, 1);
+    const int64_t cmax = ATTN_MAX_CHUNK_ROWS;
+    ChunkPlan pl;
+    pl.cfg = (c->occ2 > 0 && work > (int64_t)c->sms * c->occ * cmax) ? 1 : 0;
+    int64_t C;
+    if (c->chunk_override) {
+        C = c->chunk_override;
+    } else {
+        const int64_t slots = (int64_t)c->sms * (pl.cfg ? c->occ2 : c->occ);
+        const int64_t waves = std::max<int64_t>(1, (work + slots * cmax - 1) / (slots * cmax));
+        C = (work + waves * slots - 1) / (waves * slots);
+        C = std::min<int64_t>(cmax, std::max<int64_t>(64, (C + 15) / 16 * 16));
+    }
+    // at most `cap` chunks per (sequence, kv head)
+    const int cap = attn_merge_cap(c->tk, c->D, c->r, pl.cfg);
     for (int i = 0; i < n_seq; ++i) {
-        const int need = (rows[i] + cap - 1) / cap;
+        const int64_t need = ((int64_t)rows[i] + cap - 1) / cap;
         if (need > C) C = (need + 15) / 16 * 16;
     }
-    // a chunk spans at most 512 tiles of at least 16 rows
-    return std::min(C, 8000);
+    pl.C = (int)std::min<int64_t>(C, cmax);
+    return pl;
+}
+
+static int chunk_rows_plan(const Ctx *c, int n_seq, const int32_t *rows) {
+    return chunk_plan(c, n_seq, rows).C;
 }
 
 static int grow_partials(Ctx *c, int64_t need, cudaStream_t st) {
@@ -89,7 +104,8 @@ int launch_attention(Ctx *c, const LayerView &lv, const CUtensorMap *tmk, const 
                      float kq_scale, cudaStream_t st) {
     std::vector<int32_t> rows((size_t)n_seq);
     for (int i = 0; i < n_seq; ++i) rows[(size_t)i] = seqs_in[i].n_rows;
-    const int C = chunk_rows_plan(c, n_seq, rows.data());
+    const ChunkPlan pl = chunk_plan(c, n_seq, rows.data());
+    const int C = pl.C;
     const int64_t pf = (int64_t)attn_partial_floats(c->r, c->D);
     for (int base = 0; base < n_seq; base += MAX_SEQ_PER_LAUNCH) {
         const int cnt = std::min(MAX_SEQ_PER_LAUNCH, n_seq - base);
@@ -110,6 +126,8 @@ int launch_attention(Ctx *c, const LayerView &lv, const CUtensorMap *tmk, const 
         p.tickets = c->tickets;
         p.err = c->err_dev;
         p.scale_limit_bytes = scale_limit;
+        // the tensor maps cover one slot (Hk x P rows) on the host paths, the layer's pool otherwise
+        p.map_rows = c->host ? (int64_t)c->Hk * P : c->pool_rows;
         int32_t chunks = 0;
         for (int i = 0; i < cnt; ++i) {
             AttnSeq a = seqs_in[base + i];
@@ -124,7 +142,9 @@ int launch_attention(Ctx *c, const LayerView &lv, const CUtensorMap *tmk, const 
         int rc = grow_partials(c, (int64_t)chunks * c->Hk * pf, st);
         if (rc) return rc;
         p.part = c->part;
-        cudaError_t e = launch_attn(c->tk, p, tmk, tmv, st);
+        p.part_cap = c->part_floats;
+        for (int i = 0; i < cnt; ++i) p.seq[i].pt_len = c->host ? 1 : c->max_pages;
+        cudaError_t e = launch_attn(c->tk, p, tmk, tmv, st, false, pl.cfg);
         if (e != cudaSuccess) return cuda_fail(c, e, "attention kernel");
     }
     return KVC_OK;
@@ -437,7 +457,8 @@ static int rolling_attn(Ctx *c, int layer, const float *q, float *out, float kq_
     Transport &t = c->tr;
     Seq &sq = c->seqs[0];
     const int32_t rows = sq.lfill[(size_t)layer];
-    const int C = chunk_rows_plan(c, 1, &rows);
+    const ChunkPlan pl = chunk_plan(c, 1, &rows);
+    const int C = pl.C;
     const int32_t TR = tile_rows_for(c, rows);
     const int n_tiles = std::max(1, (rows + TR - 1) / TR);
     const int total = std::max(1, (rows + C - 1) / C);
@@ -472,7 +493,9 @@ static int rolling_attn(Ctx *c, int layer, const float *q, float *out, float kq_
         p.tickets = c->tickets;
         p.err = c->err_dev;
         p.scale_limit_bytes = s->scale_bytes;
+        p.map_rows = (int64_t)c->Hk * s->cap;
         p.part = c->part;
+        p.part_cap = c->part_floats;
         AttnSeq &a = p.seq[0];
         a.page_table = c->zero_pt;
         a.off = 0;
@@ -484,8 +507,9 @@ static int rolling_attn(Ctx *c, int layer, const float *q, float *out, float kq_
         a.stable_rows = std::max(0, std::min(n, rows - recent - r0));
         a.part0 = r0 / C;
         a.part_first = 0;
+        a.pt_len = 1;
         p.total_chunks = (n + C - 1) / C;
-        cudaError_t e = launch_attn(c->tk, p, s->tmk, s->tmv, st);
+        cudaError_t e = launch_attn(c->tk, p, s->tmk, s->tmv, st, false, pl.cfg);
         if (e != cudaSuccess) return cuda_fail(c, e, "attention kernel");
         KVC_CU(c, cudaEventRecord(s->release, st));
         s->consumed_once = true;

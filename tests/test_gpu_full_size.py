@@ -20,6 +20,7 @@ scales within 1 fp16 ulp; V and unshifted K bit-exact; KeyDiff scores 1e-4.
 """
 import os
 from concurrent.futures import ThreadPoolExecutor
+from ctypes import byref as C_byref, c_uint32 as C_uint32
 
 import numpy as np
 import pytest
@@ -126,6 +127,44 @@ def test_full_device_resident_decode_step(type_, n):
             v = np.concatenate([host[l][1], vnh[l]])
             want = _oracle_attn(qh[l, 0], type_, k, v, scale, range(H))
             _close_on_heads(got[l, 0], want, range(H), "layer %d at n %d" % (l, n))
+    finally:
+        cache.close()
+
+
+# ---------------------------------------------- long-context attention --
+@pytest.mark.parametrize("n", [65536, 262144])
+def test_full_long_context_attention(n):
+    """The benchmark's long-context attention rows (q8_0, 40/8 heads): at
+    65536 rows one wave of long chunks, at 262144 rows the configuration with
+    two CTAs per SM (its work exceeds one wave of the other at the longest
+    chunks) and a merge of the split-K partials in several rounds; layer 1 of
+    two against the oracle on one query head per KV group."""
+    torch, kvc, dev = _env()
+    scale = float(1.0 / np.sqrt(D))
+    Lr = 2
+    cache = kvc.KVCache(Lr, H, HK, D, n + 64, 1, Q8, Q8, BASE)
+    try:
+        host = {}
+        for l in range(Lr):
+            ks, vs = [], []
+            for p0 in range(0, n, 8192):
+                m = min(8192, n - p0)
+                k, v = _draw(torch, dev, "k", l, p0, m), _draw(torch, dev, "v", l, p0, m)
+                cache.append(l, 0, p0, k, v)
+                if l == 1:
+                    ks.append(k.cpu().numpy())
+                    vs.append(v.cpu().numpy())
+            if l == 1:
+                host = (np.concatenate(ks), np.concatenate(vs))
+        q = synth.normal_torch(0, synth.stream_id("q", 1, n), Lr * H * D, 1.0, dev).view(Lr, H, D)
+        out = torch.empty_like(q)
+        for l in range(Lr):
+            cache.attn_decode(l, [0], q[l:l + 1], out[l:l + 1], scale)
+        torch.cuda.synchronize()
+        got = out.cpu().numpy()
+        assert np.isfinite(got).all()
+        want = _oracle_attn(q.cpu().numpy()[1], Q8, host[0], host[1], scale, SAMPLED_HEADS)
+        _close_on_heads(got[1], want, SAMPLED_HEADS, "n %d" % n)
     finally:
         cache.close()
 
@@ -302,6 +341,9 @@ def test_full_cold_store_churn():
             for l in range(L):
                 cache.attn_decode(l, [0], q[l], o[l], 0.088)
             torch.cuda.synchronize()
+            word = C_uint32()
+            kvc.load().kvc_check_device_error(cache.ctx, C_byref(word))
+            assert word.value == 0, "device error word %#x after the decode of cycle %d" % (word.value, c)
             assert np.array_equal(np.sort(cache.positions(0)), np.arange(n)), "positions, cycle %d" % c
             if c == 0:
                 ref.seq_cp(0, 1, 0, blk)
