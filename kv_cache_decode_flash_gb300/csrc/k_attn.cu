@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
             int page = idx < sq.pt_len ? sq.page_table[idx] : -1;
             if (page < 0 || ((int64_t)page * p.Hk + p.Hk) * p.P > p.map_rows) {
                 atomicOr(p.err, ERR_BAD_PAGE);
-                page = -1;
+                page = 0; // inside every map: the tile reads valid memory, the result is flagged
             }
             s_tpage[k] = page;
         }
@@ -313,12 +313,6 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
         const int r0 = s_tstart[k];
         const int n = tile_rows(r0);
         const int page = s_tpage[k];
-        if (page < 0) { // reported: the stage completes with nothing copied
-            tinfo[s].n = n;
-            tinfo[s].delta = 0;
-            mbar_expect_tx(&full[s], 0);
-            return;
-        }
         const int cell = (sq.off + r0) % p.P;
         const int64_t R0 = ((int64_t)page * p.Hk + g) * p.P + cell;
         uint8_t *st = stages + s * S::STAGE;
