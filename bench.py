@@ -17,7 +17,7 @@ host memory and its outputs copied back inside the timed region; host = the
 host-resident pipeline at 32k (steps/s, H2D GB/s against the measured pinned
 link); cpu_baseline = the CPU oracle on a bounded sample, on the host cores.
 
---impl reference times the CPU oracle (the only reference this build has) on
+--impl reference times the CPU oracle (there is no other reference implementation) on
 the same workload, a bounded sample per step.
 Multi-GPU: replicas only (one independent cache per rank, no collective on
 the data path); value = bytes of all ranks / max time over ranks.
