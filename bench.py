@@ -154,6 +154,8 @@ def attn_traffic(type_: str, n_kv: int):
     return int(t.group(1))
 
 
+L_STACK = 64  # layers of the decode stack the host-resident rows run
+
 # ------------------------------------------------------------- CPU oracle --
 def oracle_sample(n_kv: int, n_layers: int, type_: str, seed: int = 0):
     """Quantised sample layers for the oracle (not timed)."""
@@ -193,6 +195,56 @@ def time_oracle(layers, n_kv: int, type_: str):
     dt = time.perf_counter() - t0
     nbytes = len(layers) * n_kv * kv_bytes_per_row(type_)
     return nbytes / dt / GB, dt, threads
+
+
+def oracle_rows(args) -> dict:
+    """The oracle timed beside the other rows, each on a bounded sample (a few
+    seconds of host time in all), on every host core where the work splits:
+    host-resident attention over one layer's pinned-store-sized arrays at 32k
+    (the CPU attending where the data lives), a ragged-batch sample, one
+    layer's RoPE shift of an 8192-row block (the churn's shift), and KeyDiff
+    scores of one 32768-row layer."""
+    import oracle
+    from kv_cache_decode_flash_gb300 import synth
+
+    res = {}
+    # host-resident 32k: one layer, all query heads; steps/s for the 64-layer stack
+    lay = oracle_sample(32768, 1, "q8_0", seed=3)
+    gbs, dt, threads = time_oracle(lay, 32768, "q8_0")
+    res["host_32k_attention"] = {"gbs": round(gbs, 3), "steps_per_s": round(gbs * GB / (L_STACK * 32768 *
+                                kv_bytes_per_row("q8_0")), 4), "cores": threads,
+                                 "sample": "1 of 64 layers at 32768 rows, 40 query heads (%.1f s)" % dt}
+    # ragged batch: the four shortest of the benchmark's 32 lengths, 32 query heads
+    lens = sorted(synth.randint(0, synth.stream_id("len"), 32, 1024, 32768).tolist())[:4]
+    seqs = []
+    for i, n in enumerate(lens):
+        k = synth.normal(4, synth.stream_id("k", 0, i), n * HK * D).reshape(n, HK, D)
+        v = synth.normal(4, synth.stream_id("v", 0, i), n * HK * D).reshape(n, HK, D)
+        q = synth.normal(4, synth.stream_id("q", 0, i), 32 * D).reshape(32, D)
+        seqs.append((q, *oracle.q8_0_quantize(k), *oracle.q8_0_quantize(v), n))
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(lambda a: oracle.attn(a[0][0], oracle.Q8_0, a[0][1], a[0][2], oracle.Q8_0, a[0][3], a[0][4],
+                                          0.088, heads=(a[1], a[1] + 1)), [(sq, h) for sq in seqs for h in range(32)]))
+    dt = time.perf_counter() - t0
+    rows = sum(lens)
+    res["ragged_q8_0"] = {"gbs": round(rows * kv_bytes_per_row("q8_0") / dt / GB, 3), "cores": threads,
+                          "sample": "the 4 shortest of the 32 sequences (%d rows), 32 query heads (%.1f s)"
+                                    % (rows, dt)}
+    # churn shift: one layer's K of an 8192-row block, RoPE shift with requantisation (one thread)
+    kc, ks = lay[0][2][:8192], lay[0][3][:8192]
+    t0 = time.perf_counter()
+    oracle.rope_shift_q8_0(kc, ks, 0, 1e6, 131072 - 8192)
+    dt = time.perf_counter() - t0
+    res["churn_shift"] = {"gbs": round(2 * 8192 * HK * (D + (D // 32) * 2) / dt / GB, 3), "cores": 1,
+                          "sample": "one layer of an 8192-row block, K read + write (%.2f s)" % dt}
+    # KeyDiff: one 32768-row layer, two passes over its K (one thread)
+    t0 = time.perf_counter()
+    oracle.keydiff_scores(oracle.Q8_0, lay[0][2], lay[0][3])
+    dt = time.perf_counter() - t0
+    res["keydiff_scores"] = {"gbs": round(2 * 32768 * HK * (D + (D // 32) * 2) / dt / GB, 3), "cores": 1,
+                             "sample": "one 32768-row layer, two passes over its K (%.2f s)" % dt}
+    return res
 
 
 # ------------------------------------------------------------ reference --
@@ -742,6 +794,11 @@ def run_ours(args, rank: int, world: int):
                 ex[name] = {"error": str(e)[:300]}
             torch.cuda.empty_cache()
         out["rows"] = ex
+    if rank == 0 and not args.no_cpu_baseline and not args.no_extra:
+        try:
+            out["cpu_rows"] = oracle_rows(args)
+        except Exception as e:  # reported, not fatal
+            out["cpu_rows"] = {"error": str(e)[:300]}
     if rank == 0 and not args.no_cpu_baseline:
         layers = oracle_sample(n, args.cpu_sample_layers, args.type)
         passes, dt, threads = 0, 0.0, 1
