@@ -600,6 +600,67 @@ def test_key_scores_match_oracle(type_, D, Hk):
         tw.close()
 
 
+def test_key_scores_edge_cases():
+    """An empty sequence scores nothing; a one-row sequence scores 0 (its key
+    is its head's mean); a sequence whose keys are all zero scores 1 in every
+    row (the degenerate cosine is 0); a window that does not fit evicts
+    nothing; odd head counts and tiny pages (blocks of a few rows)."""
+    for Hk, page_rows in ((3, 16), (1, 32), (8, 16)):
+        tw = Twin(2, 2 * Hk, Hk, 128, 512, n_seq_max=3, type_=Q8, page_rows=page_rows)
+        try:
+            assert tw.gpu.key_scores(0, 1).shape == (0,)
+            k, v = kv_inputs(30, 0, 1, Hk, 128, sigma=0.5)
+            for l in range(2):
+                tw.append(l, 1, 0, k, v)
+            assert np.allclose(tw.gpu.key_scores(1, 1), 0.0, atol=1e-5)
+            z = np.zeros((100, Hk, 128), np.float32)
+            for l in range(2):
+                tw.append(l, 2, 0, z, z)
+            assert np.array_equal(tw.gpu.key_scores(2, 0), np.ones(100, np.float32))
+            assert tw.gpu.evict_window(2, 0, 50, 60, 0) == -1
+            assert tw.gpu.n_tokens(2) == 100
+            fill = [kv_inputs(31, l, 333, Hk, 128, sigma=0.5) for l in range(2)]
+            for l in range(2):
+                tw.append(l, 0, 0, *fill[l])
+            got = tw.gpu.key_scores(0, 1).astype(np.float64)
+            want = tw.ref.key_scores(0, 1)
+            assert np.abs(got - want).max() <= 1e-4, (Hk, page_rows)
+        finally:
+            tw.close()
+
+
+def test_cold_store_rejects_bad_calls():
+    from kv_cache_decode_flash_gb300 import kvc
+
+    tw = Twin(1, 8, 2, 64, 512, n_seq_max=3, type_=Q8, page_rows=16)
+    store = kvc.ColdStore(100)
+    try:
+        tw.fill(0, 50, seed=32)
+        tw.fill(2, 10, seed=33)  # sequence 1 stays empty
+        for call in (lambda: store.evict(tw.gpu, 0, 2, 0, 10, 1, 0),   # scratch not empty
+                     lambda: store.evict(tw.gpu, 0, 0, 0, 10, 1, 0),   # scratch == seq
+                     lambda: store.evict(tw.gpu, 0, 5, 0, 10, 1, 0),   # no such scratch
+                     lambda: store.evict(tw.gpu, 0, 1, 5, 5, 1, 0),    # empty range
+                     lambda: store.evict(tw.gpu, 0, 1, 0, 5, 1, -1),   # negative class
+                     lambda: store.admit(tw.gpu, 0, 2, 1)):            # scratch not empty
+            with pytest.raises(kvc.KvcError) as e:
+                call()
+            assert e.value.status == kvc.KVC_EINVAL
+        assert store.evict(tw.gpu, 0, 1, 1000, 2000, 1, 0) == (0, 0)  # no rows there: nothing happens
+        assert tw.gpu.n_tokens(0) == 50
+        host = kvc.KVCache(1, 8, 2, 64, 64, 1, Q8, Q8, 1e4, 0, kvc.KVC_HOST_PINNED)
+        try:
+            with pytest.raises(kvc.KvcError) as e:
+                store.evict(host, 0, 0, 0, 1, 1, 0)
+            assert e.value.status == kvc.KVC_EINVAL
+        finally:
+            host.close()
+        assert store.stats()["stored"] == 0
+    finally:
+        store.close()
+        tw.close()
+
+
 @pytest.mark.parametrize("type_", [Q8, F16])
 def test_evict_window_matches_oracle(type_):
     """Rows 700..763 of a 1200-row sequence repeat each head's mean key, so
