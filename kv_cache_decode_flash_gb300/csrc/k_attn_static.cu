@@ -73,8 +73,11 @@ extern "C" int kvc_attn_decode_static(int type, int n_head, int n_head_kv, int h
 
     // split-K plan (one CTA per SM): whole waves of CTAs, 64..ATTN_MAX_CHUNK_ROWS rows per chunk
     const int occ = attn_ctas_per_sm(type, head_dim, r, 0);
-    const int64_t slots = (int64_t)g_sms[dev] * occ;
+    int64_t slots = (int64_t)g_sms[dev] * occ;
     const int64_t work = std::max<int64_t>((int64_t)n_kv * n_head_kv, 1);
+    // short chunks: leave the SMs of a previous launch's last (merging) CTAs free, as the
+    // context planner does
+    if (occ == 1 && (int64_t)n_head_kv * 8 <= slots && work <= (slots - n_head_kv) * 4096) slots -= n_head_kv;
     const int64_t cmax = ATTN_MAX_CHUNK_ROWS;
     const int64_t waves = std::max<int64_t>(1, (work + slots * cmax - 1) / (slots * cmax));
     int64_t C = (work + waves * slots - 1) / (waves * slots);
