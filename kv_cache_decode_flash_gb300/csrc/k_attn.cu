@@ -366,6 +366,13 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
     // Tiles made only of rows no in-flight kernel writes (the stable prefix)
     // are requested before waiting for the preceding kernel.
     const bool loader = warp == W && lane == 0;
+    // Warm L2 with this head group's query rows.  They are read only after the
+    // wait below (a preceding kernel may write them); L2 is coherent, so a line
+    // brought in early is simply updated by such a write.
+    if (warp == 0 && lane < r_act * (D * 4 / 128)) {
+        const char *qb = reinterpret_cast<const char *>(p.q + ((int64_t)sq.out_row * p.H + (int64_t)g * r_act) * D);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(qb + lane * 128));
+    }
     int prod_k = 0; // tiles issued before the wait
     if (loader) {
         while (prod_k < n_tiles && prod_k < S::STAGES && s_tstart[prod_k] + tile_rows(s_tstart[prod_k]) <= sq.stable_rows)
