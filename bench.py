@@ -3,8 +3,9 @@
 Workload (default): 64 layers, 40 query heads / 8 KV heads, head_dim 128,
 q8_0 K/V from N(0,1)*0.5, RoPE base 1e6, n_kv = 16384.  One step is one
 decode token through the layer stack: for every layer, quantise-on-append of
-the new K/V row, then split-K decode attention over all n_kv rows.  The step
-is captured once as a CUDA graph of 128 launches and replayed; each replay
+the new K/V row, then split-K decode attention over all n_kv rows, as one
+fused launch (kvc_decode_step).  The step is captured once as a CUDA graph of
+64 launches and replayed; each replay
 rewrites row n_kv-1 with the same values, so every step does the full work of
 a decode step at n_kv.  The 64 layers read 2.28 GB of distinct KV per step,
 far more than the 129 MB L2, so nothing is served from L2 across steps.
@@ -15,7 +16,8 @@ the step / device time of the step); roofline = the attention kernel alone
 bandwidth; e2e = the same metric with the step's inputs copied from pinned
 host memory and its outputs copied back inside the timed region; host = the
 host-resident pipeline at 32k (steps/s, H2D GB/s against the measured pinned
-link); cpu_baseline = the CPU oracle on a bounded sample, on the host cores.
+link); cpu_baseline = the CPU oracle on a bounded sample, on the host cores;
+step_two_calls = the same step with a separate append kernel per layer.
 
 --impl reference times the CPU oracle (there is no other reference implementation) on
 the same workload, a bounded sample per step.
@@ -651,15 +653,22 @@ def run_ours(args, rank: int, world: int):
     # one eager step creates row n-1 in every layer (allocations happen here, not in capture)
     with torch.cuda.stream(s):
         for l in range(L):
-            cache.append(l, 0, n - 1, kbuf[l], vbuf[l], stream=s)
-            cache.attn_decode(l, [0], qbuf[l], obuf[l], scale, stream=s)
+            cache.decode_step(l, [0], [n - 1], kbuf[l], vbuf[l], qbuf[l], obuf[l], scale, stream=s)
     s.synchronize()
     # the captured step rewrites row n-1: roll the host bookkeeping back by one row
     # (seq_rm of the last position keeps the device pages; the graph re-appends it)
     cache.seq_rm(0, n - 1, -1)
 
+    # the step: one fused append + attention launch per layer
     step_graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(step_graph, stream=s):
+        for l in range(L):
+            cache.decode_step(l, [0], [n - 1], kbuf[l], vbuf[l], qbuf[l], obuf[l], scale,
+                              stream=torch.cuda.current_stream())
+    cache.seq_rm(0, n - 1, -1)
+    # the same step as two calls per layer (append kernel, then attention), for comparison
+    two_call_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(two_call_graph, stream=s):
         for l in range(L):
             cache.append(l, 0, n - 1, kbuf[l], vbuf[l], stream=torch.cuda.current_stream())
             cache.attn_decode(l, [0], qbuf[l], obuf[l], scale, stream=torch.cuda.current_stream())
@@ -698,6 +707,9 @@ def run_ours(args, rank: int, world: int):
     for _ in range(3):
         attn_graph.replay()
     t_attn = timed(attn_graph.replay, args.steps)
+    for _ in range(3):
+        two_call_graph.replay()
+    t_two = timed(two_call_graph.replay, args.steps)
 
     # end to end through the public API: inputs from pinned host memory, outputs back
     hq = torch.empty_like(qbuf, device="cpu").pin_memory()
@@ -721,12 +733,12 @@ def run_ours(args, rank: int, world: int):
     t_e2e = timed(e2e_step, args.steps)
 
     # max over ranks
-    times = torch.tensor([t_step, t_attn, t_e2e], dtype=torch.float64, device=dev)
+    times = torch.tensor([t_step, t_attn, t_e2e, t_two], dtype=torch.float64, device=dev)
     if world > 1:
         import torch.distributed as dist
 
         dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    t_step, t_attn, t_e2e = [float(x) for x in times.cpu()]
+    t_step, t_attn, t_e2e, t_two = [float(x) for x in times.cpu()]
 
     row_bytes = kv_bytes_per_row(args.type)
     step_bytes = L * n * row_bytes
@@ -751,7 +763,10 @@ def run_ours(args, rank: int, world: int):
         "e2e": {"value": round(world * step_bytes * args.steps / t_e2e / GB, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(hq.numel() * 4 + hk.numel() * 4 + hv.numel() * 4),
                 "d2h_bytes_per_step": int(ho.numel() * 4)},
-        "gpu_launches": 2 * L * args.steps,
+        "gpu_launches": L * args.steps,
+        "step_two_calls": {"ms_per_step": round(1000 * t_two / args.steps, 4),
+                           "value": round(world * step_bytes * args.steps / t_two / GB, 2), "unit": "GB/s",
+                           "note": "the same step with a separate append kernel before each attention launch"},
         "clocks": clk,
     }
     cache.close()

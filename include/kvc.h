@@ -160,6 +160,29 @@ int kvc_append(kvc_ctx *c, int layer, int seq, int pos0, int n_tok, const float 
 int kvc_attn_decode(kvc_ctx *c, int layer, int n_seq, const int32_t *seq_ids, const float *q,
                     float *out, float kq_scale, void *stream);
 
+/* One decode step of one layer for n_seq sequences: sequence seq_ids[i]
+ * appends one token at position pos[i] (its K/V head-rows are row i of k / v)
+ * and then attends over all its rows with query row i of q.  The result, out
+ * and the stored rows, is bitwise that of kvc_append(c, layer, seq_ids[i],
+ * pos[i], 1, k + i*n_head_kv*head_dim, v + ..., stream) for every i followed
+ * by kvc_attn_decode(c, layer, n_seq, seq_ids, q, out, kq_scale, stream)
+ * ([F5] section M2 - HeadInfer: the per-layer cpy_k/cpy_v writes, then the
+ * attention over the cache; the q8_0 block of the decode-attention statement).
+ * On device-resident contexts it is one launch: the CTA that attends over a
+ * sequence's last chunk quantises the new row, stores it and reads it back
+ * like the others, so no separate append kernel sits between the producer of
+ * k/v/q and the attention.  Host-resident and split contexts take n_seq 1,
+ * sequence 0, and run the two calls.
+ * seq_ids, pos: HOST int32[n_seq].  k, v: device fp32 [n_seq][n_head_kv]
+ * [head_dim]; q, out: device fp32 [n_seq][n_head][head_dim]; all 16-byte
+ * aligned; out may not alias q.
+ * Errors: as kvc_append and kvc_attn_decode; every check (ids, positions, free
+ * pages) is made before anything changes, so a failed call leaves the context
+ * as it was (except KVC_ECUDA). */
+int kvc_decode_step(kvc_ctx *c, int layer, int n_seq, const int32_t *seq_ids, const int32_t *pos,
+                    const float *k, const float *v, const float *q, float *out, float kq_scale,
+                    void *stream);
+
 /* Remove the rows of `seq` whose position is in [p0, p1), in every layer
  * (MemorySeqRemove, [COLD] section llama - KV-byte offload; the context
  * shift's discard, [F5] section M1).  Rows after the removed ones keep their

@@ -288,7 +288,8 @@ int transport_append(Ctx *c, int layer, int n_tok, const float *k, const float *
 void transport_release(Ctx *c);
 int launch_attention(Ctx *c, const LayerView &lv, const CUtensorMap *tmk, const CUtensorMap *tmv, int P,
                      int64_t scale_limit, int n_seq, const AttnSeq *seqs_in, const float *q, float *out,
-                     float kq_scale, cudaStream_t st);
+                     float kq_scale, cudaStream_t st, const float *app_k = nullptr,
+                     const float *app_v = nullptr);
 } // namespace kvc
 
 // ------------------------------------------------------------------ ABI ----
@@ -602,64 +603,88 @@ int kvc_append(kvc_ctx *cc, int layer, int seq, int pos0, int n_tok, const float
     return append_impl(c, layer, seq, pos0, n_tok, k, v, stream, c->Hk);
 }
 
-static int append_impl(Ctx *c, int layer, int seq, int pos0, int n_tok, const float *k, const float *v,
-                       void *stream, int in_heads) {
+// Checks of an append that change nothing; *creates: the layer is the first to
+// append these positions (it allocates the rows).
+static int append_check(Ctx *c, int layer, int seq, int pos0, int n_tok, bool *creates) {
     if (layer < 0 || layer >= c->L) return c->fail(KVC_EINVAL, "layer out of range");
     if (seq < 0 || seq >= (int)c->seqs.size()) return c->fail(KVC_EINVAL, "sequence id out of range");
-    if (n_tok < 1 || !k || !v) return c->fail(KVC_EINVAL, "n_tok must be >= 1 and k, v non-null");
-    if (((uintptr_t)k | (uintptr_t)v) & 15) return c->fail(KVC_EINVAL, "k and v must be 16-byte aligned");
     if (pos0 < 0 || (int64_t)pos0 + n_tok - 1 > INT32_MAX) return c->fail(KVC_ERANGE, "positions out of range");
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    KVC_CU(c, cudaSetDevice(c->dev));
-    Seq &q = c->seqs[seq];
+    const Seq &q = c->seqs[seq];
     const int32_t fill = q.lfill[layer];
-    const bool creates = fill == q.n;
-    if (!creates) {
+    *creates = fill == q.n;
+    if (!*creates) {
         if ((int64_t)fill + n_tok > q.n) return c->fail(KVC_EINVAL, "append runs past the rows other layers created");
         for (int i = 0; i < n_tok; ++i)
             if (q.pos[(size_t)fill + i] != pos0 + i)
                 return c->fail(KVC_EINVAL, "append positions differ from the rows other layers created");
     }
-    if (c->host) {
-        if (creates && (int64_t)q.n + n_tok > c->P) return c->fail(KVC_ENOSPC, "host store is full");
-        int rc = transport_append(c, layer, n_tok, k, v, in_heads, st);
+    return KVC_OK;
+}
+
+// Destination of the next n_tok rows of `seq` in `layer` of a device context;
+// when the layer creates them, their pages are allocated and new page-table
+// entries are sent on st (as kernel arguments, no host copy).
+static int device_append_dst(Ctx *c, int layer, int seq, bool creates, int n_tok, cudaStream_t st, AppendDst *d) {
+    Seq &q = c->seqs[seq];
+    if (creates) {
+        size_t first_new;
+        int rc = grow_pages(c, q, n_tok, &first_new);
         if (rc) return rc;
-    } else {
-        if (creates) {
-            size_t first_new;
-            int rc = grow_pages(c, q, n_tok, &first_new);
-            if (rc) return rc;
-            // new page-table entries travel as kernel arguments (no host copy)
-            std::vector<int32_t> idx, val;
-            for (size_t i = (size_t)q.dev_pages; i < q.pages.size(); ++i) {
-                idx.push_back((int32_t)((int64_t)seq * c->max_pages + (int64_t)i));
-                val.push_back(q.pages[i]);
-            }
-            if (!idx.empty()) {
-                cudaError_t e = launch_pt_update(c->pt_dev, (int)idx.size(), idx.data(), val.data(), st);
-                if (e != cudaSuccess) return cuda_fail(c, e, "page table update");
-                q.dev_pages = (int32_t)q.pages.size();
-            }
+        std::vector<int32_t> idx, val;
+        for (size_t i = (size_t)q.dev_pages; i < q.pages.size(); ++i) {
+            idx.push_back((int32_t)((int64_t)seq * c->max_pages + (int64_t)i));
+            val.push_back(q.pages[i]);
         }
-        AppendDst d;
-        const int64_t lo = (int64_t)layer * c->pool_rows;
-        d.lv.k.data = c->kdata + lo * c->krow;
-        d.lv.k.scales = c->ksb ? reinterpret_cast<uint16_t *>(c->kscales + lo * c->ksb) : nullptr;
-        d.lv.v.data = c->vdata + lo * c->vrow;
-        d.lv.v.scales = c->vsb ? reinterpret_cast<uint16_t *>(c->vscales + lo * c->vsb) : nullptr;
-        d.pt = c->pt_dev + (int64_t)seq * c->max_pages;
-        d.off = q.off;
-        d.row0 = fill;
-        d.P = c->P;
-        cudaError_t e = launch_append(c->tk, c->tv, c->Hk, in_heads, c->D, n_tok, k, v, &d, 1, st);
-        if (e != cudaSuccess) return cuda_fail(c, e, "append kernel");
+        if (!idx.empty()) {
+            cudaError_t e = launch_pt_update(c->pt_dev, (int)idx.size(), idx.data(), val.data(), st);
+            if (e != cudaSuccess) return cuda_fail(c, e, "page table update");
+            q.dev_pages = (int32_t)q.pages.size();
+        }
     }
+    const int64_t lo = (int64_t)layer * c->pool_rows;
+    d->lv.k.data = c->kdata + lo * c->krow;
+    d->lv.k.scales = c->ksb ? reinterpret_cast<uint16_t *>(c->kscales + lo * c->ksb) : nullptr;
+    d->lv.v.data = c->vdata + lo * c->vrow;
+    d->lv.v.scales = c->vsb ? reinterpret_cast<uint16_t *>(c->vscales + lo * c->vsb) : nullptr;
+    d->pt = c->pt_dev + (int64_t)seq * c->max_pages;
+    d->off = q.off;
+    d->row0 = q.lfill[layer];
+    d->P = c->P;
+    return KVC_OK;
+}
+
+// Host bookkeeping of an append whose writes are enqueued.
+static void append_commit(Ctx *c, int layer, int seq, int pos0, int n_tok, bool creates) {
+    Seq &q = c->seqs[seq];
     if (creates) {
         for (int i = 0; i < n_tok; ++i) q.pos.push_back(pos0 + i);
         q.n += n_tok;
     }
     q.lfill[layer] += n_tok;
     c->recent[(size_t)seq][(size_t)layer] += n_tok;
+}
+
+static int append_impl(Ctx *c, int layer, int seq, int pos0, int n_tok, const float *k, const float *v,
+                       void *stream, int in_heads) {
+    if (n_tok < 1 || !k || !v) return c->fail(KVC_EINVAL, "n_tok must be >= 1 and k, v non-null");
+    if (((uintptr_t)k | (uintptr_t)v) & 15) return c->fail(KVC_EINVAL, "k and v must be 16-byte aligned");
+    bool creates = false;
+    int rc = append_check(c, layer, seq, pos0, n_tok, &creates);
+    if (rc) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    KVC_CU(c, cudaSetDevice(c->dev));
+    if (c->host) {
+        if (creates && (int64_t)c->seqs[seq].n + n_tok > c->P) return c->fail(KVC_ENOSPC, "host store is full");
+        rc = transport_append(c, layer, n_tok, k, v, in_heads, st);
+        if (rc) return rc;
+    } else {
+        AppendDst d;
+        rc = device_append_dst(c, layer, seq, creates, n_tok, st, &d);
+        if (rc) return rc;
+        cudaError_t e = launch_append(c->tk, c->tv, c->Hk, in_heads, c->D, n_tok, k, v, &d, 1, st);
+        if (e != cudaSuccess) return cuda_fail(c, e, "append kernel");
+    }
+    append_commit(c, layer, seq, pos0, n_tok, creates);
     return KVC_OK;
 }
 
@@ -708,6 +733,7 @@ int kvc_attn_decode(kvc_ctx *cc, int layer, int n_seq, const int32_t *seq_ids, c
         a.n_rows = s.lfill[layer];
         a.out_row = i;
         a.stable_rows = std::max(0, a.n_rows - c->recent[(size_t)seq_ids[i]][(size_t)layer]);
+        a.app_row = -1;
     }
     LayerView lv;
     const int64_t lo = (int64_t)layer * c->pool_rows;
@@ -720,6 +746,82 @@ int kvc_attn_decode(kvc_ctx *cc, int layer, int n_seq, const int32_t *seq_ids, c
                               seqs.data(), q, out, kq_scale, st);
     if (rc == KVC_OK) c->clear_recent(); // kernels after this one start only once it has waited
     return rc;
+}
+
+int kvc_decode_step(kvc_ctx *cc, int layer, int n_seq, const int32_t *seq_ids, const int32_t *pos, const float *k,
+                    const float *v, const float *q, float *out, float kq_scale, void *stream) {
+    if (!cc) return KVC_EINVAL;
+    Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (n_seq < 1 || !seq_ids || !pos || !k || !v || !q || !out)
+        return c->fail(KVC_EINVAL, "n_seq >= 1 and non-null pointers required");
+    if (((uintptr_t)k | (uintptr_t)v) & 15) return c->fail(KVC_EINVAL, "k and v must be 16-byte aligned");
+    if (c->split || c->host) {
+        // one sequence; the append and the attention as two launches (the rows go through the
+        // host store and the staging ring)
+        if (n_seq != 1 || seq_ids[0] != 0) return c->fail(KVC_EINVAL, "this context decodes sequence 0 only");
+        int rc = kvc_append(cc, layer, 0, pos[0], 1, k, v, stream);
+        if (rc) return rc;
+        return kvc_attn_decode(cc, layer, 1, seq_ids, q, out, kq_scale, stream);
+    }
+    if (layer < 0 || layer >= c->L) return c->fail(KVC_EINVAL, "layer out of range");
+    if (!std::isfinite(kq_scale)) return c->fail(KVC_EINVAL, "kq_scale must be finite");
+    if (q == out) return c->fail(KVC_EINVAL, "out may not alias q");
+    if (((uintptr_t)q | (uintptr_t)out) & 15) return c->fail(KVC_EINVAL, "q and out must be 16-byte aligned");
+    std::vector<char> seen(c->seqs.size(), 0);
+    std::vector<char> creates((size_t)n_seq, 0);
+    int64_t new_pages = 0;
+    for (int i = 0; i < n_seq; ++i) {
+        const int id = seq_ids[i];
+        if (id < 0 || id >= (int)c->seqs.size()) return c->fail(KVC_EINVAL, "sequence id out of range");
+        if (seen[(size_t)id]) return c->fail(KVC_EINVAL, "duplicate sequence id");
+        seen[(size_t)id] = 1;
+        bool cr = false;
+        int rc = append_check(c, layer, id, pos[i], 1, &cr);
+        if (rc) return rc;
+        creates[(size_t)i] = cr;
+        if (cr) {
+            const Seq &s = c->seqs[(size_t)id];
+            const int32_t need = pages_for(c, s.off, (int64_t)s.n + 1);
+            if (need > c->max_pages) return c->fail(KVC_ENOSPC, "sequence would exceed the page table");
+            new_pages += std::max<int64_t>(0, need - (int64_t)s.pages.size());
+        }
+    }
+    if (new_pages > (int64_t)c->free_pages.size()) return c->fail(KVC_ENOSPC, "no free pages");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    KVC_CU(c, cudaSetDevice(c->dev));
+    // cells and page-table entries first (the checks above leave nothing to fail but CUDA)
+    for (int i = 0; i < n_seq; ++i) {
+        AppendDst d;
+        int rc = device_append_dst(c, layer, seq_ids[i], creates[(size_t)i] != 0, 1, st, &d);
+        if (rc) return rc;
+        append_commit(c, layer, seq_ids[i], pos[i], 1, creates[(size_t)i] != 0);
+    }
+    std::vector<AttnSeq> seqs((size_t)n_seq);
+    for (int i = 0; i < n_seq; ++i) {
+        const Seq &s = c->seqs[(size_t)seq_ids[i]];
+        AttnSeq &a = seqs[(size_t)i];
+        a.page_table = c->pt_dev + (int64_t)seq_ids[i] * c->max_pages;
+        a.off = s.off;
+        a.n_rows = s.lfill[layer];
+        a.out_row = i;
+        a.stable_rows = std::max(0, a.n_rows - c->recent[(size_t)seq_ids[i]][(size_t)layer]);
+        a.app_row = a.n_rows - 1;
+    }
+    LayerView lv;
+    const int64_t lo = (int64_t)layer * c->pool_rows;
+    lv.k.data = c->kdata + lo * c->krow;
+    lv.k.scales = c->ksb ? reinterpret_cast<uint16_t *>(c->kscales + lo * c->ksb) : nullptr;
+    lv.v.data = c->vdata + lo * c->vrow;
+    lv.v.scales = c->vsb ? reinterpret_cast<uint16_t *>(c->vscales + lo * c->vsb) : nullptr;
+    const int64_t scale_limit = c->ksb ? c->kscale_bytes - lo * c->ksb : 0;
+    int rc = launch_attention(c, lv, &c->tmk[2 * (size_t)layer], &c->tmv[2 * (size_t)layer], c->P, scale_limit, n_seq,
+                              seqs.data(), q, out, kq_scale, st, k, v);
+    if (rc) return rc;
+    // Everything before this launch is complete once the next kernel starts, but the new rows
+    // are stored after this kernel lets the next one start: they stay recent for it.
+    c->clear_recent();
+    for (int i = 0; i < n_seq; ++i) c->recent[(size_t)seq_ids[i]][(size_t)layer] = 1;
+    return KVC_OK;
 }
 
 int kvc_seq_rm(kvc_ctx *cc, int seq, int p0, int p1) {

@@ -7,44 +7,10 @@
 // round-half-away(x * (1/d)) and the scale stored as fp16(d), rounded to
 // nearest even; f16 stores fp16(x).  The fp32 step order is fixed, so the
 // codes are bit-exact with any implementation of the same steps.
-#include "kvc_internal.h"
-
-#include <cuda_fp16.h>
+#include "quant_row.cuh"
 
 namespace kvc {
 namespace {
-
-// Elements per lane for a head-row of D values handled by one warp.
-template <int D>
-struct RowShape {
-    static constexpr int EPL = D / 32;          // 2 (D=64) or 4 (D=128)
-    static constexpr int LPB = QK / EPL;        // lanes per q8_0 block
-};
-
-template <int EPL>
-__device__ __forceinline__ void load_row(const float *src, int lane, float (&x)[EPL]) {
-    if constexpr (EPL == 4) {
-        float4 t = reinterpret_cast<const float4 *>(src)[lane];
-        x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
-    } else {
-        float2 t = reinterpret_cast<const float2 *>(src)[lane];
-        x[0] = t.x; x[1] = t.y;
-    }
-}
-
-// q8_0 of the lane's EPL values within its block of 32 (LPB lanes per block).
-template <int EPL, int LPB>
-__device__ __forceinline__ void quantise(const float (&x)[EPL], int8_t (&q)[EPL], float &d) {
-    float a = 0.0f;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) a = fmaxf(a, fabsf(x[i]));
-#pragma unroll
-    for (int m = 1; m < LPB; m <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
-    d = __fdiv_rn(a, 127.0f);
-    float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) q[i] = (int8_t)(int)roundf(__fmul_rn(x[i], id));
-}
 
 __device__ __forceinline__ int64_t dst_row(const AppendDst &d, int t, int g, int Hk) {
     int64_t L = (int64_t)d.row0 + t;
@@ -58,31 +24,6 @@ __device__ __forceinline__ int64_t dst_row(const AppendDst &d, int t, int g, int
         cell = L;
     }
     return (page * Hk + g) * (int64_t)d.P + cell;
-}
-
-template <int D>
-__device__ __forceinline__ void store_tensor(int type, const TensorView &tv, int64_t R, int lane,
-                                             const float (&x)[D / 32]) {
-    constexpr int EPL = RowShape<D>::EPL, LPB = RowShape<D>::LPB;
-    if (type == KVC_Q8_0) {
-        int8_t q[EPL];
-        float d;
-        quantise<EPL, LPB>(x, q, d);
-        int8_t *row = reinterpret_cast<int8_t *>(tv.data) + R * D;
-        if constexpr (EPL == 4) {
-            uint32_t w = (uint32_t)(uint8_t)q[0] | ((uint32_t)(uint8_t)q[1] << 8) |
-                         ((uint32_t)(uint8_t)q[2] << 16) | ((uint32_t)(uint8_t)q[3] << 24);
-            reinterpret_cast<uint32_t *>(row)[lane] = w ^ CODE_FLIP; // stored offset binary
-        } else {
-            uint16_t w = (uint16_t)((uint16_t)(uint8_t)q[0] | ((uint16_t)(uint8_t)q[1] << 8));
-            reinterpret_cast<uint16_t *>(row)[lane] = (uint16_t)(w ^ (CODE_FLIP & 0xffffu)); // offset binary
-        }
-        if ((lane % LPB) == 0) tv.scales[R * (D / QK) + lane / LPB] = __half_as_ushort(__float2half_rn(d));
-    } else {
-        __half *row = reinterpret_cast<__half *>(tv.data) + R * D;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) row[lane * EPL + i] = __float2half_rn(x[i]);
-    }
 }
 
 struct AppendArgs {
@@ -111,8 +52,8 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
     load_row<EPL>(a.v + in, lane, xv);
     for (int i = 0; i < a.n_dst; ++i) {
         const int64_t R = dst_row(a.dst[i], t, g, a.Hk);
-        store_tensor<D>(a.type_k, a.dst[i].lv.k, R, lane, xk);
-        store_tensor<D>(a.type_v, a.dst[i].lv.v, R, lane, xv);
+        store_row<D>(a.type_k, a.dst[i].lv.k, R, lane, xk);
+        store_row<D>(a.type_v, a.dst[i].lv.v, R, lane, xv);
     }
 }
 

@@ -25,6 +25,7 @@
 // global partials, the last CTA to arrive (an atomic ticket, no waiting)
 // combining them in fixed chunk order, so results are bitwise repeatable.
 #include "kvc_internal.h"
+#include "quant_row.cuh"
 
 #include <cuda_fp16.h>
 
@@ -270,6 +271,8 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
     const int r_act = p.r;
     const int row_begin = lc * p.chunk_rows;
     const int row_end = min(sq.n_rows, row_begin + p.chunk_rows);
+    // fused quantise-on-append: this CTA's chunk holds the row it stores before reading it
+    const bool app = p.app_k != nullptr && sq.app_row >= row_begin && sq.app_row < row_end;
 
     // tiles never cross a page: their sizes follow from (off, rows, P) alone
     auto tile_rows = [&](int r0) { return min(min(T, row_end - r0), p.P - (sq.off + r0) % p.P); };
@@ -381,7 +384,11 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
     pdl_wait();
     pdl_trigger();
     if (loader) {
-        for (; prod_k < n_tiles && prod_k < S::STAGES; ++prod_k) issue(prod_k);
+        // (the tile of a fused append's row waits until the row is stored)
+        for (; prod_k < n_tiles && prod_k < S::STAGES; ++prod_k) {
+            if (app && s_tstart[prod_k] + tile_rows(s_tstart[prod_k]) > sq.app_row) break;
+            issue(prod_k);
+        }
     }
 
     // per-warp results of the compute warps (read by the CTA merge)
@@ -439,11 +446,32 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
         }
         if (tq == 0) shs[gq] = ldexpf(1.0f, -e_q);
     }
+    if (app && warp == 1) {
+        // the new row of KV head g, quantised by the same steps (and to the same bytes) as the
+        // append kernel; its cell comes from the page table like every tile's
+        const int64_t lr = (int64_t)sq.off + sq.app_row;
+        const int64_t idx = lr / p.P;
+        const int page = idx < sq.pt_len ? sq.page_table[idx] : -1;
+        if (page < 0 || ((int64_t)page * p.Hk + p.Hk) * p.P > p.map_rows) {
+            if (lane == 0) atomicOr(p.err, ERR_BAD_PAGE);
+        } else {
+            const int64_t R = ((int64_t)page * p.Hk + g) * p.P + lr % p.P;
+            const int64_t in = ((int64_t)sq.out_row * p.app_heads + g) * D;
+            float xk[D / 32], xv[D / 32];
+            load_row<D / 32>(p.app_k + in, lane, xk);
+            load_row<D / 32>(p.app_v + in, lane, xv);
+            store_row<D>(TYPE, p.app_lv.k, R, lane, xk);
+            store_row<D>(TYPE, p.app_lv.v, R, lane, xv);
+            // order the stores before the bulk copies (async proxy) issued after the barrier
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+    }
     __syncthreads();
 
     if (warp == W) {
         // the load warp: refill each stage as soon as its group has released it
         if (lane == 0) {
+            for (; prod_k < n_tiles && prod_k < S::STAGES; ++prod_k) issue(prod_k);
             for (int k = S::STAGES; k < n_tiles; ++k) {
                 const int s = k % S::STAGES;
                 if (!mbar_wait(&empty[s], ((k / S::STAGES) - 1) & 1, p.err)) break;

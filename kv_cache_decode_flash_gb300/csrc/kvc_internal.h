@@ -59,6 +59,7 @@ struct AttnSeq {
                                // are merged); a sequence's chunks may span several launches, the
                                // ticket counting all of them
     int32_t pt_len;            // entries of page_table
+    int32_t app_row;           // row this launch quantises and stores itself (fused append), or -1
 };
 
 struct AttnParams {
@@ -77,6 +78,13 @@ struct AttnParams {
     int64_t scale_limit_bytes; // bytes readable from ks / vs (bounds of the bulk copies)
     int64_t map_rows;          // rows the K / V tensor maps cover (pages must lie inside)
     int64_t part_cap;          // floats of the partial buffer
+    // Fused quantise-on-append (the decode step): for each sequence with
+    // app_row >= 0, the CTA whose chunk holds that row quantises it from
+    // app_k / app_v (fp32 [.][app_heads][D], the sequence's token at index
+    // out_row) into app_lv, then reads it like any other row.  app_k == nullptr: none.
+    const float *app_k, *app_v;
+    int32_t app_heads;
+    LayerView app_lv;
     AttnSeq seq[MAX_SEQ_PER_LAUNCH];
 };
 

@@ -107,7 +107,7 @@ static int grow_partials(Ctx *c, int64_t need, cudaStream_t st) {
 
 int launch_attention(Ctx *c, const LayerView &lv, const CUtensorMap *tmk, const CUtensorMap *tmv, int P,
                      int64_t scale_limit, int n_seq, const AttnSeq *seqs_in, const float *q, float *out,
-                     float kq_scale, cudaStream_t st) {
+                     float kq_scale, cudaStream_t st, const float *app_k, const float *app_v) {
     std::vector<int32_t> rows((size_t)n_seq);
     for (int i = 0; i < n_seq; ++i) rows[(size_t)i] = seqs_in[i].n_rows;
     const ChunkPlan pl = chunk_plan(c, n_seq, rows.data());
@@ -134,6 +134,10 @@ int launch_attention(Ctx *c, const LayerView &lv, const CUtensorMap *tmk, const 
         p.scale_limit_bytes = scale_limit;
         // the tensor maps cover one slot (Hk x P rows) on the host paths, the layer's pool otherwise
         p.map_rows = c->host ? (int64_t)c->Hk * P : c->pool_rows;
+        p.app_k = app_k;
+        p.app_v = app_v;
+        p.app_heads = c->Hk;
+        p.app_lv = lv;
         int32_t chunks = 0;
         for (int i = 0; i < cnt; ++i) {
             AttnSeq a = seqs_in[base + i];
@@ -576,7 +580,8 @@ int transport_attn(Ctx *c, int layer, const float *q, float *out, float kq_scale
     a.n_rows = rows;
     a.out_row = 0;
     a.stable_rows = std::max(0, rows - c->recent[0][(size_t)layer]);
-    rc = launch_attention(c, lv, s->tmk, s->tmv, s->cap, s->scale_bytes, 1, &a, q, out, kq_scale, st);
+    rc = launch_attention(c, lv, s->tmk, s->tmv, s->cap, s->scale_bytes, 1, &a, q, out, kq_scale, st, nullptr,
+                          nullptr);
     if (rc) return rc;
     c->clear_recent();
     if (engaged) {

@@ -76,6 +76,7 @@ def load():
         "kvc_status_str": (C.c_char_p, [i32]),
         "kvc_append": (i32, [p, i32, i32, i32, i32, p, p, p]),
         "kvc_attn_decode": (i32, [p, i32, i32, p, p, p, C.c_float, p]),
+        "kvc_decode_step": (i32, [p, i32, i32, p, p, p, p, p, p, C.c_float, p]),
         "kvc_seq_rm": (i32, [p, i32, i32, i32]),
         "kvc_seq_cp": (i32, [p, i32, i32, i32, i32]),
         "kvc_seq_add": (i32, [p, i32, i32, i32, i32]),
@@ -171,6 +172,15 @@ def kvc_attn_decode(ctx, layer, seq_ids, q, out, kq_scale, stream=None, device=0
     ids = (C.c_int32 * len(seq_ids))(*[int(s) for s in seq_ids])
     _check(ctx, load().kvc_attn_decode(ctx, layer, len(seq_ids), ids, _addr(q), _addr(out), float(kq_scale),
                                        _stream(stream, device)))
+
+
+def kvc_decode_step(ctx, layer, seq_ids, pos, k, v, q, out, kq_scale, stream=None, device=0):
+    if len(pos) != len(seq_ids):
+        raise ValueError("one position per sequence")
+    ids = (C.c_int32 * len(seq_ids))(*[int(s) for s in seq_ids])
+    ps = (C.c_int32 * len(pos))(*[int(x) for x in pos])
+    _check(ctx, load().kvc_decode_step(ctx, layer, len(seq_ids), ids, ps, _addr(k), _addr(v), _addr(q), _addr(out),
+                                       float(kq_scale), _stream(stream, device)))
 
 
 def kvc_seq_rm(ctx, seq, p0, p1):
@@ -330,6 +340,9 @@ class KVCache:
 
     def attn_decode(self, layer, seq_ids, q, out, kq_scale, stream=None):
         kvc_attn_decode(self.ctx, layer, seq_ids, q, out, kq_scale, stream, self.device)
+
+    def decode_step(self, layer, seq_ids, pos, k, v, q, out, kq_scale, stream=None):
+        kvc_decode_step(self.ctx, layer, seq_ids, pos, k, v, q, out, kq_scale, stream, self.device)
 
     def seq_rm(self, seq, p0, p1):
         kvc_seq_rm(self.ctx, seq, p0, p1)
