@@ -689,6 +689,8 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
     float *wm = reinterpret_cast<float *>(wf + W * FRAG);      // [W][8]
     float *wl = wm + W * 8;                                     // [W][8]
     float *wus = wl + W * 8;                                    // [W]
+    float *wwt = wus + W;                                       // [W][8] merge weights
+    float *wmx = wwt + W * 8;                                   // [8] the CTA's maxima
     if (warp < W) {
 #pragma unroll
         for (int mt = 0; mt < S::NMT; ++mt)
@@ -708,31 +710,35 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
         if (lane == 0) wus[warp] = have_s ? pow2i(-sexp) : 0.f;
     }
     __syncthreads();
+    // the weight of warp w in head slot h: 2^(m_w - M) * 2^-S_w (0 for a warp without rows)
+    if (tid < W * 8) {
+        const int h = tid & 7;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < W; ++w) M = fmaxf(M, wm[w * 8 + h]);
+        wwt[tid] = (M == -INFINITY) ? 0.f : ex2(wm[tid] - M) * wus[tid >> 3];
+        if (tid < 8) wmx[h] = M;
+    }
+    __syncthreads();
 
     const int n_chunks = sq.n_chunks;
     float *part = p.part + ((int64_t)(sq.part0 + lc) * p.Hk + g) * S::PF;
     const bool part_ok = ((int64_t)(sq.part0 + lc) * p.Hk + g + 1) * S::PF <= p.part_cap;
     if (!part_ok && tid == 0 && n_chunks > 1) atomicOr(p.err, ERR_BAD_PART);
     float *outp = p.out + ((int64_t)sq.out_row * p.H + (int64_t)g * r_act) * D;
-    // fragment (mt, ln): heads 2t, 2t+1 of lane ln, dims of rows g and g+8.  Each
-    // fragment weighs the warps itself (softmax rescale and the warp's 2^-S: O
-    // and l of a warp share its 2^S domain), in warp order, with no barrier.
+    // fragment (mt, ln): heads 2t, 2t+1 of lane ln, dims of rows g and g+8: the
+    // warps' fragments summed with those weights (softmax rescale and the warp's
+    // 2^-S: O and l of a warp share its 2^S domain), in warp order.
     for (int it = tid; it < FRAG; it += NT) {
         const int mt = it / 32, ln = it % 32, fg = ln >> 2, ft = ln & 3;
         const int h0 = 2 * ft, h1 = 2 * ft + 1;
-        float M0 = -INFINITY, M1 = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < W; ++w) {
-            M0 = fmaxf(M0, wm[w * 8 + h0]);
-            M1 = fmaxf(M1, wm[w * 8 + h1]);
-        }
+        const float M0 = wmx[h0], M1 = wmx[h1];
         float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
         float L0 = 0.f, L1 = 0.f;
 #pragma unroll
         for (int w = 0; w < W; ++w) {
-            const float us = wus[w];
-            const float f0 = (M0 == -INFINITY) ? 0.f : ex2(wm[w * 8 + h0] - M0) * us;
-            const float f1 = (M1 == -INFINITY) ? 0.f : ex2(wm[w * 8 + h1] - M1) * us;
+            const float2 f = *reinterpret_cast<const float2 *>(wwt + w * 8 + h0); // h0 even: (h0, h1)
+            const float f0 = f.x, f1 = f.y;
             const float4 v = wf[(w * S::NMT + mt) * 32 + ln];
             O.x = fmaf(f0, v.x, O.x);
             O.y = fmaf(f1, v.y, O.y);
