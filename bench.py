@@ -64,6 +64,7 @@ def parse():
                     help="host-resident decline matrix: n_kv 32k/64k/128k x depth 0/1/4 x budget 128/512 MiB")
     ap.add_argument("--churn-n", type=int, default=131072)
     ap.add_argument("--rows", default="", help="comma-separated subset of the extra rows to run (default: all)")
+    ap.add_argument("--child", default="", help=argparse.SUPPRESS)  # one optional phase, in a process of its own
     return ap.parse_args()
 
 
@@ -629,6 +630,70 @@ def cold_store(kvc, torch, dev, n: int, layers: int, cycles: int = 8):
         cache.close()
 
 
+EXTRA_ROWS = ("q8_0_4k", "q8_0_64k", "q8_0_256k", "f16_16k", "f16_4k", "ragged_q8_0", "ragged_f16", "churn",
+              "keydiff", "split_32k_g4", "cold_store")
+
+
+def run_child(args, name: str) -> dict:
+    """Run one optional phase in a child process and return its JSON result
+    (or the error it ended with)."""
+    t0 = time.perf_counter()
+    log("phase %s" % name)
+    cmd = [sys.executable, os.path.abspath(__file__), "--child", name] + [a for a in sys.argv[1:]]
+    try:
+        r = subprocess.run(cmd, capture_output=True, text=True, timeout=1800)
+    except subprocess.TimeoutExpired:
+        return {"error": "phase %s: no result within 1800 s" % name}
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    if r.returncode != 0 or not lines:
+        tail = " | ".join((r.stderr or "").strip().splitlines()[-4:])
+        log("phase %s failed (exit %d)" % (name, r.returncode))
+        return {"error": ("exit %d: %s" % (r.returncode, tail))[:400]}
+    log("phase %s done in %.1f s" % (name, time.perf_counter() - t0))
+    return json.loads(lines[-1])
+
+
+def child_phase(args) -> dict:
+    import torch
+
+    from kv_cache_decode_flash_gb300 import kvc
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    name = args.child
+    if name == "host":
+        return host_pipeline(args, dev, torch, kvc)
+    if name == "host_matrix":
+        link = measure_link(torch, dev)
+        mat = {}
+        for hn in (32768, 65536, 131072):
+            try:
+                mat[str(hn)] = host_pipeline(args, dev, torch, kvc, hn, MATRIX_CELLS, link)
+            except Exception as e:  # reported, not fatal
+                mat[str(hn)] = {"error": str(e)[:300]}
+            torch.cuda.empty_cache()
+        return mat
+    rows = {
+        "q8_0_4k": lambda: attn_only_gbs(kvc, torch, dev, "q8_0", 4096),
+        "q8_0_64k": lambda: attn_only_gbs(kvc, torch, dev, "q8_0", 65536),
+        "q8_0_256k": lambda: attn_only_gbs(kvc, torch, dev, "q8_0", 262144),
+        "f16_16k": lambda: attn_only_gbs(kvc, torch, dev, "f16", 16384),
+        "f16_4k": lambda: attn_only_gbs(kvc, torch, dev, "f16", 4096),
+        "ragged_q8_0": lambda: ragged(kvc, torch, dev, "q8_0"),
+        "ragged_f16": lambda: ragged(kvc, torch, dev, "f16"),
+        "churn": lambda: churn(kvc, torch, dev, args.churn_n, args.churn_cycles, args.layers),
+        "keydiff": lambda: keydiff(kvc, torch, dev, args.churn_n, args.layers),
+        "split_32k_g4": lambda: host_pipeline(args, dev, torch, kvc, 32768, SPLIT_CELLS, gpu_heads=4),
+        "cold_store": lambda: cold_store(kvc, torch, dev, args.churn_n, args.layers),
+    }
+    return rows[name]()
+
+
+def log(msg: str):
+    print("bench: %s" % msg, file=sys.stderr, flush=True)
+
+
 def run_ours(args, rank: int, world: int):
     import torch
 
@@ -772,43 +837,20 @@ def run_ours(args, rank: int, world: int):
     cache.close()
     del cache
     torch.cuda.empty_cache()
-    if rank == 0 and args.host_n > 0:
-        try:
-            out["host"] = host_pipeline(args, dev, torch, kvc)
-        except Exception as e:  # reported, not fatal
-            out["host"] = {"error": str(e)[:300]}
-    if rank == 0 and args.host_matrix:
-        link = measure_link(torch, dev)
-        mat = {}
-        for hn in (32768, 65536, 131072):
-            try:
-                mat[str(hn)] = host_pipeline(args, dev, torch, kvc, hn, MATRIX_CELLS, link)
-            except Exception as e:  # reported, not fatal
-                mat[str(hn)] = {"error": str(e)[:300]}
-            torch.cuda.empty_cache()
-        out["host_matrix"] = mat
-    if rank == 0 and not args.no_extra:
-        ex = {}
-        for name, fn in (("q8_0_4k", lambda: attn_only_gbs(kvc, torch, dev, "q8_0", 4096)),
-                         ("q8_0_64k", lambda: attn_only_gbs(kvc, torch, dev, "q8_0", 65536)),
-                         ("q8_0_256k", lambda: attn_only_gbs(kvc, torch, dev, "q8_0", 262144)),
-                         ("f16_16k", lambda: attn_only_gbs(kvc, torch, dev, "f16", 16384)),
-                         ("f16_4k", lambda: attn_only_gbs(kvc, torch, dev, "f16", 4096)),
-                         ("ragged_q8_0", lambda: ragged(kvc, torch, dev, "q8_0")),
-                         ("ragged_f16", lambda: ragged(kvc, torch, dev, "f16")),
-                         ("churn", lambda: churn(kvc, torch, dev, args.churn_n, args.churn_cycles, args.layers)),
-                         ("keydiff", lambda: keydiff(kvc, torch, dev, args.churn_n, args.layers)),
-                         ("split_32k_g4", lambda: host_pipeline(args, dev, torch, kvc, 32768, SPLIT_CELLS,
-                                                                gpu_heads=4)),
-                         ("cold_store", lambda: cold_store(kvc, torch, dev, args.churn_n, args.layers))):
-            if args.rows and name not in args.rows.split(","):
-                continue
-            try:
-                ex[name] = fn()
-            except Exception as e:  # reported, not fatal
-                ex[name] = {"error": str(e)[:300]}
-            torch.cuda.empty_cache()
-        out["rows"] = ex
+    if rank == 0:
+        # The optional phases run one per child process (a fresh CUDA context each), so
+        # that a failing phase is reported as that phase's error and the line above stands.
+        if args.host_n > 0:
+            out["host"] = run_child(args, "host")
+        if args.host_matrix:
+            out["host_matrix"] = run_child(args, "host_matrix")
+        if not args.no_extra:
+            ex = {}
+            for name in EXTRA_ROWS:
+                if args.rows and name not in args.rows.split(","):
+                    continue
+                ex[name] = run_child(args, name)
+            out["rows"] = ex
     if rank == 0 and not args.no_cpu_baseline and not args.no_extra:
         try:
             out["cpu_rows"] = oracle_rows(args)
@@ -832,6 +874,12 @@ def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.child:
+        import __graft_entry__
+
+        __graft_entry__.build()
+        print(json.dumps(child_phase(args)), flush=True)
+        return
     if world > 1:
         import torch
         import torch.distributed as dist

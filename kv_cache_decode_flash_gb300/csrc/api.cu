@@ -181,6 +181,7 @@ static RunCopyArgs pool_args(const Ctx *c) {
     a.rowb[2] = c->ksb;
     a.rowb[3] = c->vsb;
     a.pool_rows = c->pool_rows;
+    a.err = c->err_dev;
     return a;
 }
 
@@ -242,6 +243,7 @@ static RunCopyArgs payload_args(const Ctx *c, int64_t n, uint8_t *payload, bool 
     a.toff[2] = pad16((int64_t)c->Hk * n * c->krow);
     a.toff[1] = ks;
     a.toff[3] = ks + pad16((int64_t)c->Hk * n * c->vrow);
+    a.payload_rows = (int64_t)c->Hk * n;
     return a;
 }
 
@@ -987,7 +989,7 @@ int kvc_seq_add(kvc_ctx *cc, int seq, int p0, int p1, int delta) {
     }
     cudaError_t e = launch_rope_shift(c->tk, c->D, c->prm.rope_mode, c->kdata,
                                       reinterpret_cast<uint16_t *>(c->kscales), c->pool_rows, c->L, c->spans_dev,
-                                      n_spans, cs, c->st);
+                                      n_spans, cs, c->err_dev, c->st);
     if (e != cudaSuccess) return cuda_fail(c, e, "rope shift kernel");
     if ((rc = wait_internal(c))) return rc;
     for (int64_t r : sel) q.pos[(size_t)r] += delta;

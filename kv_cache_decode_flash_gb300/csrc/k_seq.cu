@@ -51,6 +51,11 @@ __global__ void __launch_bounds__(256) copy_runs_kernel(const __grid_constant__ 
     const RowRun rn = runs[blockIdx.x];
     const int64_t l = a.l0 + (int64_t)blockIdx.y;
     const int64_t rb = a.rowb[t];
+    const int64_t other_rows = a.payload ? a.payload_rows : a.pool_rows;
+    if (rn.n < 0 || rn.row0 < 0 || rn.row0 + rn.n > a.pool_rows || rn.other < 0 || rn.other + rn.n > other_rows) {
+        if (threadIdx.x == 0 && a.err) atomicOr(a.err, ERR_BAD_INDEX);
+        return;
+    }
     uint8_t *pool = a.base[t] + (rn.row0 + l * a.pool_rows) * rb;
     uint8_t *other = a.payload ? a.payload + l * a.layer_bytes + a.toff[t] + rn.other * rb
                                : a.base[t] + (rn.other + l * a.pool_rows) * rb;
@@ -75,6 +80,7 @@ struct RopeArgs {
     uint16_t *kscales;
     int64_t layer_rows;
     const RopeSpan *spans;
+    uint32_t *err; // a span outside the layer pool is reported and skipped
     float2 cs[64]; // (cos, sin) of delta * theta_i, i < D/2
 };
 
@@ -109,6 +115,10 @@ __global__ void __launch_bounds__(256, 4) rope_shift_kernel(const __grid_constan
     constexpr int NB = D / QK;
     constexpr int HALF = D / 2;
     const RopeSpan sp = a.spans[blockIdx.x];
+    if (sp.n < 0 || sp.row0 < 0 || sp.row0 + sp.n > a.layer_rows) { // the whole CTA leaves
+        if (threadIdx.x == 0 && a.err) atomicOr(a.err, ERR_BAD_INDEX);
+        return;
+    }
     const int64_t base = sp.row0 + (int64_t)blockIdx.y * a.layer_rows;
     const int k = threadIdx.x % TPR;
     const int da = MODE == KVC_ROPE_NEOX ? V * k : 2 * V * k; // first dim of A
@@ -220,7 +230,7 @@ cudaError_t launch_copy_runs(const RunCopyArgs &a, const RowRun *runs_dev, int64
 
 cudaError_t launch_rope_shift(int type_k, int D, int mode, void *kdata, uint16_t *kscales, int64_t layer_rows,
                               int n_layer, const RopeSpan *spans_dev, int64_t n_spans, const float2 *cs,
-                              cudaStream_t st) {
+                              uint32_t *err, cudaStream_t st) {
     if (n_spans <= 0 || n_layer <= 0) return cudaSuccess;
     if (n_spans > 0x7fffffff || n_layer > 65535) return cudaErrorInvalidValue;
     if ((uintptr_t)kdata & 15) return cudaErrorMisalignedAddress; // 16-byte row pieces
@@ -231,6 +241,7 @@ cudaError_t launch_rope_shift(int type_k, int D, int mode, void *kdata, uint16_t
     a.kscales = kscales;
     a.layer_rows = layer_rows;
     a.spans = spans_dev;
+    a.err = err;
     for (int i = 0; i < 64; ++i) a.cs[i] = i < D / 2 ? cs[i] : make_float2(1.f, 0.f);
     const dim3 grid((unsigned)n_spans, (unsigned)n_layer);
     const bool q8 = type_k == KVC_Q8_0, neox = mode == KVC_ROPE_NEOX;

@@ -140,6 +140,8 @@ struct RunCopyArgs {
     int32_t to_payload;  // payload copies: 1 pool -> payload, 0 payload -> pool
     uint32_t flip[4];    // XOR applied to every 4 bytes copied (offset-binary <-> int8 codes)
     int32_t l0;          // first layer
+    int64_t payload_rows; // rows of each tensor section of a payload layer (Hk x rows)
+    uint32_t *err;        // device error word: a run outside its buffers is reported and skipped
 };
 cudaError_t launch_copy_runs(const RunCopyArgs &a, const RowRun *runs_dev, int64_t n_runs, int n_layers,
                              cudaStream_t st);
@@ -156,7 +158,7 @@ struct RopeSpan {
 constexpr int ROPE_SPAN_MAX = 512; // rows of one span (one CTA)
 cudaError_t launch_rope_shift(int type_k, int D, int mode, void *kdata, uint16_t *kscales, int64_t layer_rows,
                               int n_layer, const RopeSpan *spans_dev, int64_t n_spans, const float2 *cs,
-                              cudaStream_t st);
+                              uint32_t *err, cudaStream_t st);
 
 // KeyDiff scan over one layer's K of one sequence (k_keydiff.cu).
 // A block of n <= block_rows consecutive rows of one page: row0 is head
