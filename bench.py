@@ -694,6 +694,18 @@ def log(msg: str):
     print("bench: %s" % msg, file=sys.stderr, flush=True)
 
 
+def max_over_ranks(vals, device, world: int):
+    """Element-wise maximum of the ranks' timed durations (every rank gets it)."""
+    import torch
+
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
 def run_ours(args, rank: int, world: int):
     import torch
 
@@ -797,13 +809,7 @@ def run_ours(args, rank: int, world: int):
             e2e_step()
     t_e2e = timed(e2e_step, args.steps)
 
-    # max over ranks
-    times = torch.tensor([t_step, t_attn, t_e2e, t_two], dtype=torch.float64, device=dev)
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    t_step, t_attn, t_e2e, t_two = [float(x) for x in times.cpu()]
+    t_step, t_attn, t_e2e, t_two = max_over_ranks([t_step, t_attn, t_e2e, t_two], dev, world)
 
     row_bytes = kv_bytes_per_row(args.type)
     step_bytes = L * n * row_bytes
