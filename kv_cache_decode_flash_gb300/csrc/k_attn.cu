@@ -402,7 +402,13 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
     int sexp = 0;        // P' range exponent S of this warp (valid once have_s)
     bool have_s = false;
     const int gq = lane >> 2, tq = lane & 3;
-    // ---- query fragments (B operand of QK), hi + lo fp16, built once by warp 0
+    // ---- query fragments (B operand of QK), hi + lo fp16.  Warp 0 reads the
+    // head group's rows (scaled by kq_scale log2 e) and their maxima, and leaves
+    // the values in the exchange buffers (not in use before the tile loop);
+    // after a barrier warp ks converts k-step ks.
+    static_assert(S::KSTEPS <= W, "one converting warp per k-step");
+    float4 *qraw = reinterpret_cast<float4 *>(pbuf_all); // [KSTEPS][32 lanes]
+    int *s_eq = reinterpret_cast<int *>(shs + 8);        // e of each head slot
     if (warp == 0) {
         const bool hq = gq < r_act; // head slot this lane feeds into the MMA B operand
         const float *qrow = p.q + ((int64_t)sq.out_row * p.H + (int64_t)g * r_act + (hq ? gq : 0)) * D;
@@ -432,19 +438,11 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
         // power-of-two scaling that puts max|q| in [2^13, 2^14): hi and lo stay normal fp16
         const int e_q = (amax > 0.0f) ? 13 - ilogbf(amax) : 0;
 #pragma unroll
-        for (int ks = 0; ks < S::KSTEPS; ++ks) {
-            uint32_t bh[2], bl[2];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const float x0 = ldexpf(qv[ks][2 * j], e_q), x1 = ldexpf(qv[ks][2 * j + 1], e_q);
-                const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-                const __half l0 = __float2half_rn(x0 - __half2float(h0)), l1 = __float2half_rn(x1 - __half2float(h1));
-                bh[j] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
-                bl[j] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
-            }
-            qfs[ks * 32 + lane] = make_uint4(bh[0], bh[1], bl[0], bl[1]);
+        for (int ks = 0; ks < S::KSTEPS; ++ks) qraw[ks * 32 + lane] = make_float4(qv[ks][0], qv[ks][1], qv[ks][2], qv[ks][3]);
+        if (tq == 0) {
+            shs[gq] = ldexpf(1.0f, -e_q);
+            s_eq[gq] = e_q;
         }
-        if (tq == 0) shs[gq] = ldexpf(1.0f, -e_q);
     }
     if (app && warp == 1) {
         // the new row of KV head g, quantised by the same steps (and to the same bytes) as the
@@ -465,6 +463,23 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
             // order the stores before the bulk copies (async proxy) issued after the barrier
             asm volatile("fence.proxy.async.global;" ::: "memory");
         }
+    }
+    __syncthreads();
+    if (warp < S::KSTEPS) {
+        const int ks = warp;
+        const float4 x = qraw[ks * 32 + lane];
+        const int e_q = s_eq[gq];
+        const float xs[4] = {x.x, x.y, x.z, x.w};
+        uint32_t bh[2], bl[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float x0 = ldexpf(xs[2 * j], e_q), x1 = ldexpf(xs[2 * j + 1], e_q);
+            const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+            const __half l0 = __float2half_rn(x0 - __half2float(h0)), l1 = __float2half_rn(x1 - __half2float(h1));
+            bh[j] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+            bl[j] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+        }
+        qfs[ks * 32 + lane] = make_uint4(bh[0], bh[1], bl[0], bl[1]);
     }
     __syncthreads();
 
