@@ -10,20 +10,28 @@
 // online-softmax merge; section F5-opt W4: inter-tile online softmax).
 //
 // Layout of the work: grid (chunk, kv head).  A CTA streams its chunk in
-// tiles of 128 rows through a multi-stage shared-memory ring filled by TMA
-// (K and V rows as 2-D boxes of 16 rows, K with the 128-/64-byte swizzle so
-// the tensor-core fragment loads are bank-conflict free; q8_0 scales by
-// 1-D bulk copies).  Each of the 8 warps owns 16 rows of every tile and runs
-// its own online softmax:
+// tiles of 128 rows (never across a page) through a multi-stage shared-memory
+// ring filled by one lane of a load warp with TMA: K and V rows as 2-D boxes
+// of 128 (and 16) rows, swizzled so that the tensor-core fragment loads are
+// bank-conflict free, and the q8_0 scales as 1-D bulk copies.  Tiles of rows
+// no in-flight kernel writes are requested before the programmatic-dependency
+// wait, so a launch prefetches under the end of the previous one.  The compute
+// warps form groups of 8 that take alternate tiles; a warp owns 16 rows of each
+// tile its group takes and runs its own online softmax:
 //   QK  on the tensor cores (mma.sync m16n8k16, fp32 accumulate): int8 codes
 //       become exact fp16 values in registers, q is split into fp16 hi + lo
 //       parts (about 22 significant bits), and each 32-element block gets its
 //       own accumulator so the block scale is applied in fp32 afterwards;
-//   PV  on the CUDA cores with packed fp32x2 FMAs (fp32 accumulate); the
-//       q8_0 V scale is folded into the probability (p * d_v per block).
+//   PV  on the tensor cores as O^T = V^T (P' hi + lo)^T, the q8_0 V scale
+//       folded into the probability (P' = p * d_v * 2^S per block, with a
+//       per-warp range exponent S that keeps hi and lo normal fp16).
 // Warps merge inside the CTA; CTAs of one (sequence, kv head) merge through
 // global partials, the last CTA to arrive (an atomic ticket, no waiting)
 // combining them in fixed chunk order, so results are bitwise repeatable.
+// A decode step may also hand the kernel each sequence's new K/V row: the
+// CTA whose chunk holds it quantises and stores it before reading its tile.
+// Configuration 0 runs one CTA per SM (16 compute warps for q8_0, 8 for f16);
+// configuration 1 (q8_0) two CTAs of 8 compute warps per SM.
 #include "kvc_internal.h"
 #include "quant_row.cuh"
 
