@@ -342,6 +342,9 @@ class KVCache:
         kvc_attn_decode(self.ctx, layer, seq_ids, q, out, kq_scale, stream, self.device)
 
     def decode_step(self, layer, seq_ids, pos, k, v, q, out, kq_scale, stream=None):
+        """Append one token per sequence (k, v: [n_seq][n_head_kv][head_dim] fp32 on the
+        device, at positions pos) and attend with q ([n_seq][n_head][head_dim]) into out;
+        one launch on device-resident contexts (kvc_decode_step)."""
         kvc_decode_step(self.ctx, layer, seq_ids, pos, k, v, q, out, kq_scale, stream, self.device)
 
     def seq_rm(self, seq, p0, p1):
