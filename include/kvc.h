@@ -319,6 +319,15 @@ int kvc_get_stats(const kvc_ctx *c, kvc_stats *out);
  * the row counts, the geometry and the device's SM count.  Errors: KVC_EINVAL. */
 int kvc_set_chunk_rows(kvc_ctx *c, int rows);
 
+/* Test hook, no context and no GPU needed: the split-K plan an attention
+ * launch over n_seq sequences of rows[i] rows would use, for a KV type,
+ * head_dim and head counts, on a device of `sms` SMs where configuration 0
+ * fits occ CTAs per SM and configuration 1 (q8_0, two CTAs of half the
+ * size) occ2 (0: not available).  *chunk_rows: rows per chunk; *cfg: the
+ * configuration.  rows: HOST int32[n_seq].  Errors: KVC_EINVAL. */
+int kvc_debug_chunk_plan(int type, int head_dim, int n_head, int n_head_kv, int sms, int occ, int occ2,
+                         int n_seq, const int32_t *rows, int32_t *chunk_rows, int32_t *cfg);
+
 /* Limit, in milliseconds, of every bounded host wait of the synchronous
  * operations (default 120000).  A wait that runs out returns KVC_ETIMEDOUT. */
 int kvc_set_timeout_ms(kvc_ctx *c, int ms);

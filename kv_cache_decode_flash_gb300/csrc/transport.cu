@@ -92,6 +92,34 @@ static int chunk_rows_plan(const Ctx *c, int n_seq, const int32_t *rows) {
     return chunk_plan(c, n_seq, rows).C;
 }
 
+} // namespace kvc
+
+extern "C" int kvc_debug_chunk_plan(int type, int head_dim, int n_head, int n_head_kv, int sms, int occ, int occ2,
+                                    int n_seq, const int32_t *rows, int32_t *chunk_rows, int32_t *cfg) {
+    using namespace kvc;
+    if (!rows || !chunk_rows || !cfg || n_seq < 1 || sms < 1 || occ < 1 || occ2 < 0) return KVC_EINVAL;
+    if (type != KVC_Q8_0 && type != KVC_F16) return KVC_EINVAL;
+    if (head_dim != 64 && head_dim != 128) return KVC_EINVAL;
+    if (n_head_kv < 1 || n_head < 1 || n_head % n_head_kv || n_head / n_head_kv > MAX_GROUP) return KVC_EINVAL;
+    if (type == KVC_F16 && occ2 != 0) return KVC_EINVAL; // f16 has one configuration
+    for (int i = 0; i < n_seq; ++i)
+        if (rows[i] < 0) return KVC_EINVAL;
+    Ctx c;
+    c.tk = c.tv = type;
+    c.D = head_dim;
+    c.Hk = n_head_kv;
+    c.r = n_head / n_head_kv;
+    c.sms = sms;
+    c.occ = occ;
+    c.occ2 = occ2;
+    const ChunkPlan pl = chunk_plan(&c, n_seq, rows);
+    *chunk_rows = pl.C;
+    *cfg = pl.cfg;
+    return KVC_OK;
+}
+
+namespace kvc {
+
 static int grow_partials(Ctx *c, int64_t need, cudaStream_t st) {
     if (need <= c->part_floats) return KVC_OK;
     // grows only for forced chunk sizes or unusual batches (not inside graph capture)

@@ -90,6 +90,8 @@ def load():
         "kvc_seq_positions": (i32, [p, i32, p, C.c_int32, C.POINTER(C.c_int32)]),
         "kvc_get_stats": (i32, [p, C.POINTER(kvc_stats)]),
         "kvc_set_chunk_rows": (i32, [p, i32]),
+        "kvc_debug_chunk_plan": (i32, [i32, i32, i32, i32, i32, i32, i32, i32, p, C.POINTER(C.c_int32),
+                                       C.POINTER(C.c_int32)]),
         "kvc_set_timeout_ms": (i32, [p, i32]),
         "kvc_debug_fail_alloc_after": (i32, [p, i32]),
         "kvc_check_device_error": (i32, [p, C.POINTER(C.c_uint32)]),
@@ -297,6 +299,18 @@ def kvc_set_chunk_rows(ctx, rows):
 
 def kvc_set_timeout_ms(ctx, ms):
     _check(ctx, load().kvc_set_timeout_ms(ctx, ms))
+
+
+def kvc_debug_chunk_plan(type_, head_dim, n_head, n_head_kv, sms, occ, occ2, rows):
+    """The split-K plan (chunk rows, configuration) of an attention launch over
+    sequences of `rows` rows, without a context or a GPU."""
+    arr = (C.c_int32 * len(rows))(*[int(r) for r in rows])
+    cr, cfg = C.c_int32(), C.c_int32()
+    st = load().kvc_debug_chunk_plan(type_, head_dim, n_head, n_head_kv, sms, occ, occ2, len(rows), arr,
+                                     C.byref(cr), C.byref(cfg))
+    if st != KVC_OK:
+        raise KvcError(st, "bad chunk-plan arguments")
+    return cr.value, cfg.value
 
 
 def kvc_debug_fail_alloc_after(ctx, n):

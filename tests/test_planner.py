@@ -1,0 +1,70 @@
+"""The split-K chunk planner (host logic, no GPU): whole waves of chunks of
+at most 8000 rows, the SM reserve for short chunks, the switch to two CTAs per
+SM for long launches, and argument checks.  GB300 figures: 152 SMs, one
+attention CTA per SM in configuration 0, two in configuration 1 (q8_0)."""
+import random
+
+import pytest
+
+from kv_cache_decode_flash_gb300 import kvc
+
+SMS, OCC, OCC2 = 152, 1, 2
+Q8, F16 = kvc.KVC_Q8_0, kvc.KVC_F16
+
+
+def plan(rows, type_=Q8, D=128, H=40, Hk=8, sms=SMS, occ=OCC, occ2=None):
+    if occ2 is None:
+        occ2 = OCC2 if type_ == Q8 else 0
+    return kvc.kvc_debug_chunk_plan(type_, D, H, Hk, sms, occ, occ2, rows)
+
+
+def ctas(rows, C, Hk=8):
+    return Hk * sum(max(1, -(-r // C)) for r in rows)
+
+
+def test_decode_16k_leaves_the_merging_ctas_their_sms():
+    # 16384 rows x 8 KV heads: 144 CTAs of 912 rows, 8 SMs left to the previous launch's last CTAs
+    C, cfg = plan([16384])
+    assert (C, cfg) == (912, 0)
+    assert ctas([16384], C) == 144
+
+
+def test_long_single_sequence_fills_one_wave():
+    C, cfg = plan([131072])        # 1,048,576 row-heads: one wave of one CTA per SM
+    assert (C, cfg) == (6912, 0) and ctas([131072], C) == 152
+    C, cfg = plan([262144])        # above one wave of 8000-row chunks: two CTAs per SM
+    assert (C, cfg) == (6912, 1) and ctas([262144], C) == 304
+
+
+def test_f16_has_one_configuration():
+    for n in (4096, 262144, 1 << 20):
+        assert plan([n], type_=F16)[1] == 0
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_invariants_on_random_batches(seed):
+    rng = random.Random(seed)
+    for _ in range(200):
+        n_seq = rng.choice([1, 1, 2, 7, 32, 64])
+        rows = [rng.choice([0, 1, rng.randint(1, 40000), rng.randint(1, 600000)]) for _ in range(n_seq)]
+        D = rng.choice([64, 128])
+        Hk = rng.choice([1, 2, 4, 8])
+        H = Hk * rng.choice([1, 3, 4, 5, 8])
+        type_ = rng.choice([Q8, F16])
+        C, cfg = plan(rows, type_=type_, D=D, H=H, Hk=Hk)
+        assert C % 16 == 0 and 64 <= C <= 8000
+        assert cfg in (0, 1) and (type_ == Q8 or cfg == 0)
+        work = max(sum(rows) * Hk, 1)
+        assert cfg == (1 if type_ == Q8 and work > SMS * OCC * 8000 else 0)
+        if n_seq == 1 and rows[0] > 0:
+            slots = SMS * (OCC2 if cfg else OCC)
+            waves = -(-work // (slots * 8000))
+            assert ctas(rows, C, Hk) <= waves * slots  # whole waves
+
+
+def test_rejects_bad_arguments():
+    for args in [(Q8, 96, 40, 8, SMS, 1, 2, [10]), (Q8, 128, 41, 8, SMS, 1, 2, [10]),
+                 (Q8, 128, 72, 8, SMS, 1, 2, [10]), (F16, 128, 40, 8, SMS, 1, 2, [10]),
+                 (Q8, 128, 40, 8, 0, 1, 2, [10]), (Q8, 128, 40, 8, SMS, 1, 2, [-1]), (7, 128, 40, 8, SMS, 1, 2, [10])]:
+        with pytest.raises(kvc.KvcError):
+            kvc.kvc_debug_chunk_plan(*args)
