@@ -641,9 +641,9 @@ def run_child(args, name: str) -> dict:
     log("phase %s" % name)
     cmd = [sys.executable, os.path.abspath(__file__), "--child", name] + [a for a in sys.argv[1:]]
     try:
-        r = subprocess.run(cmd, capture_output=True, text=True, timeout=1800)
+        r = subprocess.run(cmd, capture_output=True, text=True, timeout=600)  # each phase takes about a minute
     except subprocess.TimeoutExpired:
-        return {"error": "phase %s: no result within 1800 s" % name}
+        return {"error": "phase %s: no result within 600 s" % name}
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
     if r.returncode != 0 or not lines:
         tail = " | ".join((r.stderr or "").strip().splitlines()[-4:])
