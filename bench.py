@@ -630,6 +630,40 @@ def cold_store(kvc, torch, dev, n: int, layers: int, cycles: int = 8):
         cache.close()
 
 
+def step_line(args, world: int, L: int, n: int, t_step: float, t_attn: float, t_e2e: float, t_two: float,
+              h2d_bytes: int, d2h_bytes: int, clk: dict) -> dict:
+    """The JSON line of the decode step from its measured durations (seconds for
+    args.steps steps; t_attn: the attention-only graph)."""
+    row_bytes = kv_bytes_per_row(args.type)
+    step_bytes = L * n * row_bytes
+    value = world * step_bytes * args.steps / t_step / GB
+    attn_launch_s = t_attn / (args.steps * L)
+    achieved = n * row_bytes / attn_launch_s / GB
+    peak, peak_kind = peaks()
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1000 * t_step / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "%s KV, fp32 accumulate" % args.type,
+        "data": "synthetic (splitmix64 + Box-Muller, N(0,1)*0.5 K/V)", "config": config_dict(args),
+        "steps_per_s": round(args.steps / t_step, 2),
+        "hbm_frac": round(value / world / peak, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": attn_traffic(args.type, n),
+                     "kernel": "attn_kernel (decode attention), %d bytes per launch" % (n * row_bytes),
+                     "peak_kind": "%s (MEASURED_PEAKS.json hbm_gbs, burst copy)" % peak_kind,
+                     "launch_us": round(attn_launch_s * 1e6, 3),
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, "
+                                       "profiles/attn_kernel_q8_0_16k.md (null when the kernel changed)"},
+        "e2e": {"value": round(world * step_bytes * args.steps / t_e2e / GB, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes},
+        "gpu_launches": L * args.steps,
+        "step_two_calls": {"ms_per_step": round(1000 * t_two / args.steps, 4),
+                           "value": round(world * step_bytes * args.steps / t_two / GB, 2), "unit": "GB/s",
+                           "note": "the same step with a separate append kernel before each attention launch"},
+        "clocks": clk,
+    }
+
+
 EXTRA_ROWS = ("q8_0_4k", "q8_0_64k", "q8_0_256k", "f16_16k", "f16_4k", "ragged_q8_0", "ragged_f16", "churn",
               "keydiff", "split_32k_g4", "cold_store")
 
@@ -812,35 +846,8 @@ def run_ours(args, rank: int, world: int):
 
     t_step, t_attn, t_e2e, t_two = max_over_ranks([t_step, t_attn, t_e2e, t_two], dev, world)
 
-    row_bytes = kv_bytes_per_row(args.type)
-    step_bytes = L * n * row_bytes
-    value = world * step_bytes * args.steps / t_step / GB
-    attn_launch_s = t_attn / (args.steps * L)
-    achieved = n * row_bytes / attn_launch_s / GB
-    peak, peak_kind = peaks()
-    out = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(1000 * t_step / args.steps, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "%s KV, fp32 accumulate" % args.type,
-        "data": "synthetic (splitmix64 + Box-Muller, N(0,1)*0.5 K/V)", "config": config_dict(args),
-        "steps_per_s": round(args.steps / t_step, 2),
-        "hbm_frac": round(value / world / peak, 4),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": attn_traffic(args.type, n),
-                     "kernel": "attn_kernel (decode attention), %d bytes per launch" % (n * row_bytes),
-                     "peak_kind": "%s (MEASURED_PEAKS.json hbm_gbs, burst copy)" % peak_kind,
-                     "launch_us": round(attn_launch_s * 1e6, 3),
-                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, "
-                                       "profiles/attn_kernel_q8_0_16k.md (null when the kernel changed)"},
-        "e2e": {"value": round(world * step_bytes * args.steps / t_e2e / GB, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": int(hin.numel() * 4),
-                "d2h_bytes_per_step": int(ho.numel() * 4)},
-        "gpu_launches": L * args.steps,
-        "step_two_calls": {"ms_per_step": round(1000 * t_two / args.steps, 4),
-                           "value": round(world * step_bytes * args.steps / t_two / GB, 2), "unit": "GB/s",
-                           "note": "the same step with a separate append kernel before each attention launch"},
-        "clocks": clk,
-    }
+    out = step_line(args, world, L, n, t_step, t_attn, t_e2e, t_two, int(hin.numel() * 4), int(ho.numel() * 4),
+                    clk)
     cache.close()
     del cache
     torch.cuda.empty_cache()

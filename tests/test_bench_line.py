@@ -1,0 +1,49 @@
+"""The benchmark's JSON line (no GPU): the keys the measurement contract asks
+for, and the arithmetic of value, e2e and the roofline from given durations."""
+import json
+
+import bench
+
+GB = 1e9
+
+
+def _args(**kw):
+    class A:
+        pass
+
+    a = A()
+    a.type, a.steps, a.warmup, a.layers, a.n_kv = "q8_0", 500, 5, 64, 16384
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_step_line_keys_and_arithmetic():
+    a = _args()
+    L, n = 64, 16384
+    # 0.9 ms per step, 14 us per attention launch, e2e 0.94 ms, two calls 1.03 ms
+    line = bench.step_line(a, 1, L, n, 0.9e-3 * 500, 14e-6 * 64 * 500, 0.94e-3 * 500, 1.03e-3 * 500,
+                           1835008, 1310720, {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []})
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+              "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "gpu_launches", "clocks"):
+        assert k in line, k
+    json.dumps(line)
+    step_bytes = L * n * 2176
+    assert abs(line["value"] - step_bytes / 0.9e-3 / GB) < 0.01
+    assert line["ms_per_step"] == 0.9 and line["steps"] == 500 and line["warmup"] == 5
+    assert line["higher_is_better"] is True and line["scaling"] == "weak" and line["vs_baseline"] is None
+    assert line["gpu_launches"] == L * 500
+    r = line["roofline"]
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["achieved"] - n * 2176 / 14e-6 / GB) < 0.1 and abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-4
+    assert abs(line["e2e"]["value"] - step_bytes / 0.94e-3 / GB) < 0.01
+    assert line["e2e"]["h2d_bytes_per_step"] == 1835008 and line["e2e"]["d2h_bytes_per_step"] == 1310720
+    assert line["config"]["workload"].startswith("decode, 64 layers")
+
+
+def test_value_is_whole_job_over_ranks():
+    a = _args()
+    one = bench.step_line(a, 1, 64, 16384, 0.45, 0.448, 0.47, 0.52, 1, 1, {})
+    two = bench.step_line(a, 2, 64, 16384, 0.45, 0.448, 0.47, 0.52, 1, 1, {})
+    assert abs(two["value"] - 2 * one["value"]) < 0.02 and two["n_gpus"] == 2
+    assert abs(two["hbm_frac"] - one["hbm_frac"]) < 1e-4  # per-GPU fraction
