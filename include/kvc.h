@@ -23,8 +23,8 @@
  *    pointers, e.g. torch tensors) and all host byte buffers; the library
  *    never keeps a caller pointer after a call returns.
  *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
- *    default stream).  kvc_append and kvc_attn_decode only enqueue work on it
- *    and return without waiting; calls on one context must be issued from one
+ *    default stream).  kvc_append, kvc_attn_decode and kvc_decode_step only
+ *    enqueue work on it and return without waiting; calls on one context must be issued from one
  *    host thread and be ordered on the device (one stream, or events).
  *    The sequence and state operations are synchronous: they wait for all
  *    device work already issued in the process, run, and return when their
