@@ -357,14 +357,22 @@ int kvc_check_device_error(kvc_ctx *c, uint32_t *word);
  *         [n_head_kv][n_kv][head_dim], ks = vs = NULL.
  * q, out: device fp32 [n_head][head_dim].  Every pointer 16-byte aligned;
  * scale buffers readable up to the next multiple of 16 bytes.
+ * n_kv = 0 gives out = 0, as kvc_attn_decode does for an empty sequence
+ * (k, v, ks and vs may then be NULL).
  * Work space (split-K partials, arrival tickets, error word) lives in one
  * fixed 8 MiB device array inside the library, which every GPU that loads
  * the library holds until the process exits.  The first call on a device
- * looks up that array's device address (set-up, no allocation), so make it
- * before recording work you cannot interrupt.  All calls share the array and
- * it keeps the previous call's contents: the call clears what must start at
- * zero in stream order, and calls whose kernels overlap on the GPU (other
- * streams, other threads) race on it, so order them.
+ * (and the first in a new context of it, e.g. after a device reset) does a
+ * set-up with that device current: it looks up the array's device address
+ * and the SM count, which allocates nothing.  Make that first call before
+ * any stream capture.  All calls share the array and it keeps the previous
+ * call's contents: the call clears what must start at zero in stream order,
+ * and calls whose kernels overlap on the GPU (other streams, other threads)
+ * race on it, so order them.
+ * The kernel's own guards (a bounded wait that gave up, an index outside its
+ * buffers) set a word in that work space that this call does not report:
+ * there is no context whose later calls could read it.  Arguments that pass
+ * the host checks below cannot trigger them.
  * Errors: KVC_EINVAL (types, shapes, null or misaligned pointers),
  * KVC_ERANGE (n_kv so large that the partials do not fit the 8 MiB work
  * space; plain kvc_attn_decode has no such limit), KVC_ECUDA. */

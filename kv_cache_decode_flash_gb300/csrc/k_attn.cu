@@ -67,8 +67,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait: gives up after WAIT_LIMIT polls and reports it in *err.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, uint32_t *err) {
+// Bounded wait: gives up after WAIT_LIMIT polls (reported in *err, and *abort
+// set so that the CTA's other waits give up too), or as soon as *abort is set.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, uint32_t *err, volatile int *abort) {
+    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+    }
+    atomicOr(err, ERR_WAIT_TIMEOUT);
+    *abort = 1;
+    return false;
+}
+// Bounded wait for copies already issued (the drain before a CTA reuses or
+// gives back its shared memory): no early exit.
+__device__ __forceinline__ bool mbar_wait_landed(uint64_t *bar, unsigned parity, uint32_t *err) {
     for (uint32_t i = 0; i < WAIT_LIMIT; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     atomicOr(err, ERR_WAIT_TIMEOUT);
@@ -205,25 +217,39 @@ struct Shape {
     static constexpr int VROW = KROW;                 // bytes per V row
     static constexpr int SB = Q8 ? NB * 2 : 0;        // scale bytes per row
     static constexpr int KSUB = Q8 ? 1 : (D == 128 ? 2 : 1); // f16 K sub-tiles of 64 halves
-    static constexpr int SCALE_BUF = Q8 ? ((T * SB + 32 + 127) / 128) * 128 : 0;
+    // scale copies start on the 16-byte boundary at or below a tile's first scale row: up to
+    // 16 bytes more than the tile's rows hold
+    static constexpr int SCALE_BUF = Q8 ? T * SB + 16 : 0;
     static constexpr int KBYTES = T * KROW, VBYTES = T * VROW;
-    static constexpr int STAGE = ((KBYTES + VBYTES + 2 * SCALE_BUF + 1023) / 1024) * 1024; // 1024-aligned stages
+    // K and V tiles of one stage; the swizzled boxes need 1024-byte aligned destinations.
+    // The scales of all stages sit after all the tiles.
+    static constexpr int STAGE = KBYTES + VBYTES;
+    static_assert(STAGE % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
     static constexpr int KSTEPS = D / 16;
     static constexpr int NBX = Q8 ? NB : 1;           // scale blocks per row (1 for f16)
     static constexpr int PSTR = 24;                   // floats per head slot in the exchange (16 rows + pad)
     static constexpr int PBUF = 8 * PSTR;             // floats per warp: p[8 head slots][rows]
     static constexpr int MAXT = 512;                  // tiles per chunk (host keeps chunks within it)
-    // as many stages (2..8) as fit next to the exchange buffers in one SM's shared memory
     static constexpr int QF_BYTES = KSTEPS * 32 * 16 + 64; // q fragments (one copy for all warps) + head scales
     static constexpr int SM_BUDGET = CFG == 1 ? 115712 : 232448; // shared memory one CTA may take
     static constexpr int MINB = CFG == 1 ? 2 : 1;                 // CTAs per SM the registers allow for
-    static constexpr int FIT = (SM_BUDGET - 4096 - W * PBUF * 4 - 1024 - MAXT * 8 - 256 - QF_BYTES) / STAGE;
-    static constexpr int STAGES = FIT < 2 ? 2 : (FIT > 8 ? 8 : FIT);
+    // shared memory besides the stages: base alignment, exchange buffers, tile tables, q
+    // fragments, and a margin for the kernel's static shared variables
+    static constexpr int FIXED = 1024 + W * PBUF * 4 + MAXT * 8 + 16 + QF_BYTES + 64;
+    static constexpr int PER_STAGE = STAGE + 2 * SCALE_BUF + 3 * 8; // tiles, scales, full/empty, tile info
+    // as many stages (2..8) as fit, a whole number per group: group j takes tiles
+    // j, j + G, ..., so with STAGES a multiple of G every phase of a stage belongs to
+    // one group, whose warps consumed the stage's previous tile before waiting on it
+    static constexpr int FIT = (SM_BUDGET - FIXED) / PER_STAGE;
+    static constexpr int FIT_G = FIT - FIT % G;
+    static constexpr int STAGES = FIT_G < 2 ? 2 : (FIT_G > 8 ? 8 : FIT_G);
+    static_assert(STAGES % G == 0, "a stage's phases must all belong to one group");
     static constexpr int OOFF = ((2 * R + 3) / 4) * 4;  // partial: m[R], l[R], pad, then o[R][D] 16-byte aligned
     static constexpr int PF = OOFF + R * D;            // floats of one partial
-    static constexpr int SMEM =
-        STAGES * STAGE + W * PBUF * 4 + 2 * STAGES * 8 + STAGES * 8 + 64 + MAXT * 8 + QF_BYTES + 1024;
-    static constexpr int MERGE_CAP = (STAGES * STAGE) / (4 * (PF + R)); // chunks one merge round stages
+    static constexpr int SMEM = FIXED + STAGES * PER_STAGE;
+    static_assert(SMEM <= SM_BUDGET, "shared memory");
+    static constexpr int RING = STAGES * (STAGE + 2 * SCALE_BUF); // tiles + scales, contiguous
+    static constexpr int MERGE_CAP = RING / (4 * (PF + R)); // chunks one merge round stages
     // chunks per (sequence, kv head) the planner may use: CFG 0 merges in one
     // round; CFG 1 has little staging room and merges in rounds
     static constexpr int CHUNK_CAP = CFG == 1 ? 256 : MERGE_CAP;
@@ -254,8 +280,9 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
     constexpr int W = S::W, T = S::T, NT = S::NTHREADS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t *stages = smem;
-    float *pbuf_all = reinterpret_cast<float *>(smem + S::STAGES * S::STAGE);
+    uint8_t *stages = smem;                                  // [STAGES][K tile, V tile]
+    uint8_t *scales = smem + S::STAGES * S::STAGE;           // [STAGES][K scales, V scales]
+    float *pbuf_all = reinterpret_cast<float *>(smem + S::RING);
     uint64_t *full = reinterpret_cast<uint64_t *>(pbuf_all + W * S::PBUF);
     uint64_t *empty = full + S::STAGES;
     TileInfo *tinfo = reinterpret_cast<TileInfo *>(empty + S::STAGES);
@@ -265,6 +292,9 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
     uint4 *qfs = reinterpret_cast<uint4 *>(((uintptr_t)(s_tpage + S::MAXT) + 15) & ~(uintptr_t)15);
     float *shs = reinterpret_cast<float *>(qfs + S::KSTEPS * 32); // 2^-e of each head slot
     __shared__ int s_flag;
+    __shared__ int s_nstable; // leading tiles made only of stable rows
+    // set by a wait that gave up: the load lane stops issuing and every other wait gives up too
+    __shared__ int s_abort;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = blockIdx.y;
@@ -285,9 +315,14 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
     // tiles never cross a page: their sizes follow from (off, rows, P) alone
     auto tile_rows = [&](int r0) { return min(min(T, row_end - r0), p.P - (sq.off + r0) % p.P); };
     if (tid == 0) {
-        int nt = 0;
-        for (int r0 = row_begin; r0 < row_end && nt < S::MAXT; r0 += tile_rows(r0)) s_tstart[nt++] = r0;
+        int nt = 0, ns = 0;
+        for (int r0 = row_begin; r0 < row_end && nt < S::MAXT; r0 += tile_rows(r0)) {
+            s_tstart[nt++] = r0;
+            if (r0 + tile_rows(r0) <= sq.stable_rows) ns = nt;
+        }
         s_flag = nt;
+        s_nstable = ns;
+        s_abort = 0;
         for (int s = 0; s < S::STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], S::GW); // the group of warps that reads the stage
@@ -297,25 +332,30 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
     if constexpr (S::Q8) {
         // Scale bytes past a tile's rows are never copied into: start them at 0
         // (finite), so those rows' products stay 0 without masking
-        for (int i = tid; i < S::STAGES * (2 * S::SCALE_BUF / 16); i += NT) {
-            const int st_i = i / (2 * S::SCALE_BUF / 16), off = i % (2 * S::SCALE_BUF / 16);
-            reinterpret_cast<uint4 *>(stages + st_i * S::STAGE + S::KBYTES + S::VBYTES)[off] = make_uint4(0, 0, 0, 0);
-        }
+        for (int i = tid; i < S::STAGES * (2 * S::SCALE_BUF / 16); i += NT)
+            reinterpret_cast<uint4 *>(scales)[i] = make_uint4(0, 0, 0, 0);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); // before the bulk copies write there
     }
     __syncthreads();
     const int n_tiles = s_flag;
-    if (warp == 0)
-        for (int k = lane; k < n_tiles; k += 32) {
-            // a page outside the page table or the tensor maps is reported and its tile skipped
-            const int idx = (sq.off + s_tstart[k]) / p.P;
-            int page = idx < sq.pt_len ? sq.page_table[idx] : -1;
-            if (page < 0 || ((int64_t)page * p.Hk + p.Hk) * p.P > p.map_rows) {
-                atomicOr(p.err, ERR_BAD_PAGE);
-                page = 0; // inside every map: the tile reads valid memory, the result is flagged
-            }
-            s_tpage[k] = page;
+    const int n_stable = s_nstable;
+    // Physical page of tile k.  A page outside the page table or the tensor
+    // maps is reported and replaced by page 0 (inside every map: the tile reads
+    // valid memory, the result is flagged).
+    auto tile_page = [&](int k) {
+        const int idx = (sq.off + s_tstart[k]) / p.P;
+        int page = idx < sq.pt_len ? sq.page_table[idx] : -1;
+        if (page < 0 || ((int64_t)page * p.Hk + p.Hk) * p.P > p.map_rows) {
+            atomicOr(p.err, ERR_BAD_PAGE);
+            page = 0;
         }
+        return page;
+    };
+    // Page-table entries of stable tiles were written by kernels that completed
+    // before the preceding launch passed its wait; the others (a page a preceding
+    // kernel may just have added) are read after this launch's wait, below.
+    if (warp == 0)
+        for (int k = lane; k < n_stable; k += 32) s_tpage[k] = tile_page(k);
     __syncthreads();
 
     // ---- tile loads, all issued by lane 0 of the load warp (warp W) -----------
@@ -367,10 +407,9 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
         for (int b = 0; b < nsmall; ++b) box(&tmk, &tmv, nbig * S::BIG + b * TMA_BOX_ROWS);
         if constexpr (S::Q8) {
             if (sbytes) {
-                bulk_load(st + S::KBYTES + S::VBYTES, reinterpret_cast<const uint8_t *>(p.ks) + saligned, sbytes,
-                          &full[s]);
-                bulk_load(st + S::KBYTES + S::VBYTES + S::SCALE_BUF,
-                          reinterpret_cast<const uint8_t *>(p.vs) + saligned, sbytes, &full[s]);
+                uint8_t *sc = scales + s * (2 * S::SCALE_BUF);
+                bulk_load(sc, reinterpret_cast<const uint8_t *>(p.ks) + saligned, sbytes, &full[s]);
+                bulk_load(sc + S::SCALE_BUF, reinterpret_cast<const uint8_t *>(p.vs) + saligned, sbytes, &full[s]);
             }
         }
     };
@@ -384,18 +423,21 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
         const char *qb = reinterpret_cast<const char *>(p.q + ((int64_t)sq.out_row * p.H + (int64_t)g * r_act) * D);
         asm volatile("prefetch.global.L2 [%0];" ::"l"(qb + lane * 128));
     }
-    int prod_k = 0; // tiles issued before the wait
-    if (loader) {
-        while (prod_k < n_tiles && prod_k < S::STAGES && s_tstart[prod_k] + tile_rows(s_tstart[prod_k]) <= sq.stable_rows)
-            issue(prod_k++);
-    }
+    int prod_k = 0; // tiles issued so far (by the load lane)
+    if (loader)
+        while (prod_k < n_stable && prod_k < S::STAGES) issue(prod_k++);
     pdl_wait();
     pdl_trigger();
-    if (loader) {
-        // (the tile of a fused append's row waits until the row is stored)
-        for (; prod_k < n_tiles && prod_k < S::STAGES; ++prod_k) {
-            if (app && s_tstart[prod_k] + tile_rows(s_tstart[prod_k]) > sq.app_row) break;
-            issue(prod_k);
+    if (warp == W) {
+        // pages of the tiles past the stable prefix, now that preceding kernels are complete
+        for (int k = n_stable + lane; k < n_tiles; k += 32) s_tpage[k] = tile_page(k);
+        __syncwarp();
+        if (lane == 0) {
+            // (the tile of a fused append's row waits until the row is stored)
+            for (; prod_k < n_tiles && prod_k < S::STAGES; ++prod_k) {
+                if (app && s_tstart[prod_k] + tile_rows(s_tstart[prod_k]) > sq.app_row) break;
+                issue(prod_k);
+            }
         }
     }
 
@@ -495,11 +537,17 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
         // the load warp: refill each stage as soon as its group has released it
         if (lane == 0) {
             for (; prod_k < n_tiles && prod_k < S::STAGES; ++prod_k) issue(prod_k);
-            for (int k = S::STAGES; k < n_tiles; ++k) {
-                const int s = k % S::STAGES;
-                if (!mbar_wait(&empty[s], ((k / S::STAGES) - 1) & 1, p.err)) break;
-                issue(k);
+            for (; prod_k < n_tiles; ++prod_k) {
+                const int s = prod_k % S::STAGES;
+                if (!mbar_wait(&empty[s], ((prod_k / S::STAGES) - 1) & 1, p.err, &s_abort)) break;
+                issue(prod_k);
             }
+            // Drain: the last tile issued into each stage has landed before the
+            // CTA reuses its shared memory (or exits), also when a wait gave up.
+            // The stage's earlier tiles were consumed before that tile was issued,
+            // so its full barrier is at most one phase behind and the parity is exact.
+            for (int k = max(prod_k - S::STAGES, 0); k < prod_k; ++k)
+                mbar_wait_landed(&full[k % S::STAGES], (k / S::STAGES) & 1, p.err);
         }
     } else {
 
@@ -514,9 +562,10 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
 
     for (int k = warp / S::GW; k < n_tiles; k += S::G) {
         const int s = k % S::STAGES;
-        if (!mbar_wait(&full[s], (k / S::STAGES) & 1, p.err)) break;
+        if (!mbar_wait(&full[s], (k / S::STAGES) & 1, p.err, &s_abort)) break;
         const uint8_t *st = stages + s * S::STAGE;
         const uint8_t *vt = st + S::KBYTES;
+        const uint8_t *sct = scales + s * (2 * S::SCALE_BUF); // K scales, then V scales
         const int n = tinfo[s].n;
         const int rows_w = min(max(n - rbase, 0), 16);
         if (rows_w > 0) {
@@ -528,7 +577,7 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
             const int lm_hi = lane >> 4;
             if constexpr (S::Q8) {
                 // K scales of rows ra, rb: NB halves each, one 8- (or 4-) byte load per row
-                const uint8_t *ksb = st + S::KBYTES + S::VBYTES + (tinfo[s].delta + rbase) * S::SB;
+                const uint8_t *ksb = sct + (tinfo[s].delta + rbase) * S::SB;
                 uint32_t kw[2][S::NB / 2];
                 load_scales<S::NB>(ksb + gq * S::SB, kw[0]);
                 load_scales<S::NB>(ksb + (gq + 8) * S::SB, kw[1]);
@@ -603,7 +652,7 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
             uint32_t vw[4][S::NBX / 2 > 0 ? S::NBX / 2 : 1];
             int s_tile = 14 - RESCALE_SLACK; // f16: P' = p <= 2^RESCALE_SLACK
             if constexpr (S::Q8) {
-                const uint8_t *vsb = st + S::KBYTES + S::VBYTES + S::SCALE_BUF + (tinfo[s].delta + rbase) * S::SB;
+                const uint8_t *vsb = sct + S::SCALE_BUF + (tinfo[s].delta + rbase) * S::SB;
                 uint32_t wm = 0;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -903,12 +952,18 @@ template <int TYPE, int D, int R, bool RAW = false, int CFG = 0>
 cudaError_t launch_t(const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv, cudaStream_t st) {
     // tmk / tmv point at {16-row map, 128-row map} pairs
     using S = Shape<TYPE, D, R, CFG>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_kernel<TYPE, D, R, RAW, CFG>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+    // the shared-memory attribute belongs to the current context: set it once per
+    // context of each device (a reset device or another context gets it again)
+    static uint64_t configured[MAX_DEVICES];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t ctx = current_context_id();
+    if (dev < 0 || dev >= MAX_DEVICES || ctx == 0 || configured[dev] != ctx) {
+        e = cudaFuncSetAttribute(attn_kernel<TYPE, D, R, RAW, CFG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 S::SMEM);
         if (e != cudaSuccess) return e;
-        configured = true;
+        if (dev >= 0 && dev < MAX_DEVICES) configured[dev] = ctx;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.total_chunks, p.Hk);
@@ -970,6 +1025,35 @@ int chunk_cap_d(int r) {
 }
 
 } // namespace
+
+uint64_t current_context_id() {
+    using GetCurrentFn = CUresult (*)(CUcontext *);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    if (!get_current || !get_id) {
+        cudaDriverEntryPointQueryResult q1, q2;
+        void *p1 = nullptr, *p2 = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p1, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+            q1 != cudaDriverEntryPointSuccess || !p1 ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &p2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+            q2 != cudaDriverEntryPointSuccess || !p2) {
+            cudaGetLastError();
+            return 0;
+        }
+        get_current = reinterpret_cast<GetCurrentFn>(p1);
+        get_id = reinterpret_cast<GetIdFn>(p2);
+    }
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+    return (uint64_t)id + 1; // 0 stays "unknown"
+}
+
+int attn_instance_r(int type, int r, bool raw_codes) {
+    if (type == KVC_Q8_0 && raw_codes) return 8; // one instance for every group size
+    return r <= 4 ? 4 : (r == 5 ? 5 : 8);
+}
 
 size_t attn_partial_floats(int r, int D) {
     const int R = r <= 4 ? 4 : (r == 5 ? 5 : 8);

@@ -28,14 +28,18 @@ static_assert(TICKET_BYTES + 256 <= HEADER_BYTES, "header too small");
 
 static __device__ __align__(256) unsigned char g_attn_scratch[STATIC_SCRATCH_BYTES];
 
-constexpr int MAX_DEVICES = 64;
-unsigned char *g_scratch_dev[MAX_DEVICES]; // device address of g_attn_scratch, per device
+// Per device: the context the entries below belong to, the array's device
+// address in that context and the SM count.
+uint64_t g_ctx[MAX_DEVICES];
+unsigned char *g_scratch_dev[MAX_DEVICES];
 int g_sms[MAX_DEVICES];
 
-// First call on a device: resolve the array's device address (the host-side
-// name is only a stand-in for it) and the SM count.
+// First call on a device (and again in a new context of it, e.g. after a
+// reset): resolve the array's device address, with the device current (the
+// host-side name is only a stand-in for it), and the SM count.
 int setup(int dev) {
-    if (g_scratch_dev[dev]) return KVC_OK;
+    const uint64_t ctx = current_context_id();
+    if (ctx != 0 && g_ctx[dev] == ctx && g_scratch_dev[dev]) return KVC_OK;
     void *ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_attn_scratch) != cudaSuccess || !ptr) {
         cudaGetLastError();
@@ -45,6 +49,7 @@ int setup(int dev) {
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KVC_ECUDA;
     g_sms[dev] = sms;
     g_scratch_dev[dev] = (unsigned char *)ptr;
+    g_ctx[dev] = ctx;
     return KVC_OK;
 }
 
@@ -71,8 +76,11 @@ extern "C" int kvc_attn_decode_static(int type, int n_head, int n_head_kv, int h
     unsigned char *base = g_scratch_dev[dev];
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
-    // split-K plan (one CTA per SM): whole waves of CTAs, 64..ATTN_MAX_CHUNK_ROWS rows per chunk
-    const int occ = attn_ctas_per_sm(type, head_dim, r, 0);
+    // split-K plan (one CTA per SM): whole waves of CTAs, 64..ATTN_MAX_CHUNK_ROWS rows per chunk.
+    // Occupancy, merge capacity and partial size are those of the instance that runs: plain
+    // int8 q8_0 codes run the group-size-8 instance for every group size.
+    const int ri = attn_instance_r(type, r, /*raw_codes=*/true);
+    const int occ = attn_ctas_per_sm(type, head_dim, ri, 0);
     int64_t slots = (int64_t)g_sms[dev] * occ;
     const int64_t work = std::max<int64_t>((int64_t)n_kv * n_head_kv, 1);
     // short chunks: leave the SMs of a previous launch's last (merging) CTAs free, as the
@@ -82,11 +90,11 @@ extern "C" int kvc_attn_decode_static(int type, int n_head, int n_head_kv, int h
     const int64_t waves = std::max<int64_t>(1, (work + slots * cmax - 1) / (slots * cmax));
     int64_t C = (work + waves * slots - 1) / (waves * slots);
     C = std::min<int64_t>(cmax, std::max<int64_t>(64, (C + 15) / 16 * 16));
-    const int cap = attn_merge_cap(type, head_dim, r, 0);
+    const int cap = attn_merge_cap(type, head_dim, ri, 0);
     if ((n_kv + cap - 1) / cap > C) C = ((n_kv + cap - 1) / cap + 15) / 16 * 16;
     C = std::min<int64_t>(C, cmax);
     const int n_chunks = std::max<int>(1, (int)((n_kv + C - 1) / C));
-    const size_t part_bytes = (size_t)n_chunks * n_head_kv * attn_partial_floats(r, head_dim) * sizeof(float);
+    const size_t part_bytes = (size_t)n_chunks * n_head_kv * attn_partial_floats(ri, head_dim) * sizeof(float);
     if (part_bytes > STATIC_SCRATCH_BYTES - HEADER_BYTES) return KVC_ERANGE; // beyond the fixed work space
 
     const int row_bytes = type == KVC_Q8_0 ? head_dim : 2 * head_dim;

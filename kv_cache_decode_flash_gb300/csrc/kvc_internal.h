@@ -100,6 +100,15 @@ int attn_ctas_per_sm(int type, int D, int r, int cfg = 0); // 0: the configurati
 int attn_merge_cap(int type, int D, int r, int cfg = 0);   // most chunks per (sequence, kv head) a launch may use
 constexpr int ATTN_MAX_CHUNK_ROWS = 8000;                  // a chunk spans at most 512 tiles
 size_t attn_partial_floats(int r, int D); // floats per (chunk, kv head) partial
+// Group size of the kernel instance a launch with group size r runs (partials,
+// merge capacity and occupancy follow that instance): plain int8 q8_0 codes run
+// the one instance for groups of up to 8.
+int attn_instance_r(int type, int r, bool raw_codes);
+constexpr int MAX_DEVICES = 64; // devices whose per-device state the library caches
+// A process-unique id of the current CUDA context (0 if it cannot be read):
+// state that belongs to a context is cached under it, so a reset device or
+// another context is set up again.
+uint64_t current_context_id();
 
 // Quantise-on-append.  Destination of token t: logical row row0 + t of a
 // sequence with page table pt and first-page offset off (pt == nullptr:

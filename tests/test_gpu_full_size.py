@@ -91,6 +91,14 @@ def _oracle_attn(q, type_, k, v, kq_scale, heads):
         return sum(ex.map(one, heads))
 
 
+def _oracle_attn_stored(q, kc, ks, vc, vs, kq_scale, heads):
+    """Oracle outputs fp64 [H][D] over stored q8_0 rows, listed heads only."""
+    scale = float(np.float32(kq_scale))
+    one = lambda h: oracle.attn(q, Q8, kc, ks, Q8, vc, vs, scale, heads=(h, h + 1))
+    with ThreadPoolExecutor(max(1, min(len(heads), os.cpu_count() or 1))) as ex:
+        return sum(ex.map(one, heads))
+
+
 def _close_on_heads(got, want, heads, what):
     idx = list(heads)
     assert_attn_close(got[idx].astype(np.float64), want[idx], what)
@@ -127,6 +135,58 @@ def test_full_device_resident_decode_step(type_, n):
             v = np.concatenate([host[l][1], vnh[l]])
             want = _oracle_attn(qh[l, 0], type_, k, v, scale, range(H))
             _close_on_heads(got[l, 0], want, range(H), "layer %d at n %d" % (l, n))
+    finally:
+        cache.close()
+
+
+@pytest.mark.parametrize("type_", [Q8, F16])
+def test_full_fused_decode_step_graph_replay(type_):
+    """The benchmark's step exactly as it times it: n_kv 16384, 64 layers,
+    one fused kvc_decode_step launch per layer (row n-1 quantised inside the
+    attention launch), run once eagerly, then captured as a CUDA graph and
+    replayed three times (each replay rewrites row n-1).  The eager step and
+    every replay give the same bits; layers 0, 31 and 63 of the last replay
+    against the oracle on all 40 query heads."""
+    torch, kvc, dev = _env()
+    n = 16384
+    sampled = (0, 31, 63)
+    scale = float(1.0 / np.sqrt(D))
+    cache = kvc.KVCache(L, H, HK, D, n + 256, 1, type_, type_, BASE, 0, kvc.KVC_DEVICE, 0)
+    try:
+        host = _fill([cache], torch, dev, n - 1, 4096, keep=sampled)
+        q = synth.normal_torch(0, synth.stream_id("q", 0, n + 7), L * H * D, 1.0, dev).view(L, 1, H, D)
+        kn = _draw(torch, dev, "knew", 0, n + 7, L).view(L, 1, HK, D)
+        vn = _draw(torch, dev, "vnew", 0, n + 7, L).view(L, 1, HK, D)
+        out = torch.empty_like(q)
+        s = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(s):
+            for l in range(L):
+                cache.decode_step(l, [0], [n - 1], kn[l], vn[l], q[l], out[l], scale, stream=s)
+        s.synchronize()
+        eager = out.clone()
+        cache.seq_rm(0, n - 1, -1)  # the captured step re-appends row n-1 (the pages stay)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=s):
+            for l in range(L):
+                cache.decode_step(l, [0], [n - 1], kn[l], vn[l], q[l], out[l], scale,
+                                  stream=torch.cuda.current_stream())
+        for rep in range(3):
+            out.fill_(float("nan"))
+            with torch.cuda.stream(s):
+                gr.replay()
+            s.synchronize()
+            assert torch.equal(out, eager), "replay %d differs from the eager step" % rep
+        word = C_uint32()
+        kvc.load().kvc_check_device_error(cache.ctx, C_byref(word))
+        assert word.value == 0, "device error word %#x" % word.value
+        got = out.cpu().numpy()
+        qh, knh, vnh = q.cpu().numpy(), kn.cpu().numpy(), vn.cpu().numpy()
+        for l in sampled:
+            k = np.concatenate([host[l][0], knh[l]])
+            v = np.concatenate([host[l][1], vnh[l]])
+            want = _oracle_attn(qh[l, 0], type_, k, v, scale, range(H))
+            _close_on_heads(got[l, 0], want, range(H), "fused step, graph replay, layer %d" % l)
+        del gr
     finally:
         cache.close()
 
@@ -303,15 +363,54 @@ def _compare_shifted(gpu, ref, what):
     assert np.abs(Kg.s.astype(int) - Ko.s.astype(int)).max() <= 1, what
 
 
+def _layer_of_state(blob, n, layer, hk=HK, d=D):
+    """Layer `layer`'s q8_0 K and V of a 64-layer state blob of n rows, as the
+    oracle stores them: codes int8 [n][Hk][D], scales u16 [n][Hk][D/32]."""
+    pad = lambda x: (x + 15) // 16 * 16
+    codes, scl = pad(hk * n * d), pad(hk * n * (d // 32) * 2)
+    off = 64 + pad(4 * n) + layer * 2 * (codes + scl)
+    out = []
+    for _ in range(2):  # K then V
+        c = np.frombuffer(blob, np.int8, hk * n * d, off).reshape(hk, n, d)
+        sc = np.frombuffer(blob, "<u2", hk * n * (d // 32), off + codes).reshape(hk, n, d // 32)
+        out.append((np.ascontiguousarray(c.transpose(1, 0, 2)), np.ascontiguousarray(sc.transpose(1, 0, 2))))
+        off += codes + scl
+    return out
+
+
+def _export_layer(cache, kvc, torch, n, layer, piece=16384):
+    """K and V of one layer of sequence 0 (positions 0..n-1), exported in
+    pieces of `piece` positions through the state format."""
+    size = kvc.kvc_state_size(cache.ctx, 0, 0, piece)
+    buf = torch.empty(size, dtype=torch.uint8, pin_memory=True)
+    parts = []
+    for p0 in range(0, n, piece):
+        cache.state_get(0, p0, p0 + piece, buf)
+        blob = buf.numpy().tobytes()
+        cnt = int(np.frombuffer(blob, "<u4", 1, 28)[0])  # header: rows in the blob
+        parts.append(_layer_of_state(blob, cnt, layer))
+    kc = np.concatenate([p[0][0] for p in parts])
+    ks = np.concatenate([p[0][1] for p in parts])
+    vc = np.concatenate([p[1][0] for p in parts])
+    vs = np.concatenate([p[1][1] for p in parts])
+    return kc, ks, vc, vs
+
+
 def test_full_cold_store_churn():
     """131072-token q8_0 cache, 64 layers, 64 cycles of: copy the oldest
     8192 rows to a scratch sequence, export them, drop the scratch, remove
     them and slide the rest down; import into the scratch, shift it to the
     tail, copy it in, drop the scratch; one decode step.  Every cycle:
-    positions 0..n-1; first and last cycle: export -> import -> export is
+    positions 0..n-1, and layer 32's decode output bitwise equal to a second
+    launch of that layer; first and last cycle: export -> import -> export is
     byte-exact.  After the first cycle, layer 32 is checked against the
     oracle running the same operations (the exported block bit-exact; slid
-    and re-admitted rows within the shift tolerances)."""
+    and re-admitted rows within the shift tolerances), and so is its decode
+    output (one query head per KV group).  Every 16 cycles the decode output
+    is checked against the oracle's attention over the rows the cache holds
+    then: requantisation after each shift is lossy, so two caches evolved
+    independently drift apart by more than the attention tolerance after
+    many cycles, and each cycle's shifts are compared one op at a time."""
     torch, kvc, dev = _env()
     n, blk, cycles, lay = 131072, 8192, 64, 32
     cache = kvc.KVCache(L, H, HK, D, n + 2 * blk + 512, 2, Q8, Q8, BASE)
@@ -325,6 +424,8 @@ def test_full_cold_store_churn():
         again = torch.empty(size, dtype=torch.uint8, pin_memory=True)
         q = synth.normal_torch(0, synth.stream_id("q", 0, 5), L * H * D, 1.0, dev).view(L, 1, H, D)
         o = torch.empty_like(q)
+        o2 = torch.empty_like(q[0])
+        qh = q.cpu().numpy()[lay, 0]
         for c in range(cycles):
             cache.seq_cp(0, 1, 0, blk)
             cache.state_get(1, -1, -1, blob)
@@ -340,7 +441,10 @@ def test_full_cold_store_churn():
             cache.seq_rm(1, -1, -1)
             for l in range(L):
                 cache.attn_decode(l, [0], q[l], o[l], 0.088)
+            cache.attn_decode(lay, [0], q[lay], o2, 0.088)
             torch.cuda.synchronize()
+            assert torch.equal(o[lay], o2), "decode of layer %d not repeatable, cycle %d" % (lay, c)
+            assert torch.isfinite(o).all(), "cycle %d" % c
             word = C_uint32()
             kvc.load().kvc_check_device_error(cache.ctx, C_byref(word))
             assert word.value == 0, "device error word %#x after the decode of cycle %d" % (word.value, c)
@@ -364,6 +468,15 @@ def test_full_cold_store_churn():
                     gpu = _layer_rows(parser, cache.state_get(0, p0, p1), lay)
                     po, Ko, Vo = ref.parse_state(ref.state_get(0, p0, p1))
                     _compare_shifted(gpu, (po, Ko[0], Vo[0]), "rows [%d, %d)" % (p0, p1))
+                want = ref.attn(0, [0], qh[None], 0.088)[0]
+                got = o[lay, 0].cpu().numpy().astype(np.float64)
+                for g in SAMPLED_HEADS:
+                    assert_attn_close(got[g:g + 1], want[g:g + 1], "cycle 0 decode, head %d" % g)
+            if c % 16 == 15:
+                kc, ks, vc, vs = _export_layer(cache, kvc, torch, n, lay)
+                assert kc.shape[0] == n
+                want = _oracle_attn_stored(qh, kc, ks, vc, vs, 0.088, SAMPLED_HEADS)
+                _close_on_heads(o[lay, 0].cpu().numpy(), want, SAMPLED_HEADS, "cycle %d decode" % c)
     finally:
         cache.close()
 
