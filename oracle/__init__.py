@@ -11,12 +11,13 @@ definition is fp32); this file loads them through ctypes and adds the
 row-list model of the sequence operations and the state byte format
 (model.py).
 """
-from .numerics import lib, F16, Q8_0, f16_to_f64, f32_to_f16, q8_0_quantize, q8_0_dequantize, attn, attn_bruteforce
+from .numerics import lib, F16, Q4_0, Q8_0, f16_to_f64, f32_to_f16, q8_0_quantize, q8_0_dequantize, attn, attn_bruteforce
+from .numerics import q4_0_quantize, q4_0_dequantize
 from .numerics import rope_rotate, rope_shift_q8_0, rope_shift_f16, keydiff_scores, min_window
 from .model import OracleCache, ColdStore, STATE_MAGIC, STATE_VERSION, state_size
 
 __all__ = [
-    "lib", "F16", "Q8_0", "f16_to_f64", "f32_to_f16", "q8_0_quantize", "q8_0_dequantize", "attn",
+    "lib", "F16", "Q4_0", "Q8_0", "q4_0_quantize", "q4_0_dequantize", "f16_to_f64", "f32_to_f16", "q8_0_quantize", "q8_0_dequantize", "attn",
     "attn_bruteforce", "rope_rotate", "rope_shift_q8_0", "rope_shift_f16", "keydiff_scores", "min_window",
     "OracleCache", "ColdStore",
     "STATE_MAGIC", "STATE_VERSION", "state_size",

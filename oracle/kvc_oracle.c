@@ -11,6 +11,8 @@
  *
  *   - fp16 (IEEE-754 binary16) encode/decode, round to nearest even, with
  *     subnormals and overflow to infinity.
+ *   - q4_0 block quantisation (V): 32 4-bit codes plus one fp16 scale per
+ *     block, a reading stated at orc_q4_0_quantize_block.
  *   - q8_0 block quantisation: 32 int8 codes plus one fp16 scale per block.
  *     The pages only name the type ("-ctk q8_0", F5 - Advanced KV Cache
  *     Techniques, section M6 - PolyKV; "q8_0 K/V", sched: pipeline the
@@ -138,11 +140,66 @@ void orc_q8_0_dequantize_row(const int8_t *q, const uint16_t *scale, int64_t n, 
 }
 
 /* ------------------------------------------------------------------ */
+/* q4_0 (V only)                                                       */
+/* ------------------------------------------------------------------ */
+
+/* The pages name "-ctv q4_0" (F5 - Advanced KV Cache Techniques, section
+ * M6 - PolyKV: asymmetric K/V compression) but do not define it.  The
+ * reading used, the plainest 4-bit counterpart of q8_0 with one fp16 scale
+ * per block of 32:
+ *   m = the element of largest magnitude, sign kept (the first one on ties);
+ *   d = m / -8; id = 1/d (0 if d == 0); code_i = min(15, trunc(x_i * id + 8.5))
+ *   with the product and the sum each rounded to fp32; scale = fp16(d).
+ *   Value of a code: (code - 8) * fp16(d)  (m itself maps to code 0).
+ *   Packing: byte j (0..15) of a block holds code j in its low four bits
+ *   and code j + 16 in its high four bits. */
+void orc_q4_0_quantize_block(const float *x, uint8_t *packed, uint16_t *scale) {
+    float amax = 0.0f, m = 0.0f;
+    for (int i = 0; i < ORC_QK; ++i) {
+        float ax = fabsf(x[i]);
+        if (ax > amax) {
+            amax = ax;
+            m = x[i];
+        }
+    }
+    volatile float d = m / -8.0f;
+    volatile float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+    int code[ORC_QK];
+    for (int i = 0; i < ORC_QK; ++i) {
+        volatile float t = x[i] * id;
+        volatile float u = t + 8.5f;
+        int c = (int)u; /* u > 0: truncation is the floor */
+        code[i] = c > 15 ? 15 : c;
+    }
+    for (int j = 0; j < ORC_QK / 2; ++j) packed[j] = (uint8_t)(code[j] | (code[j + ORC_QK / 2] << 4));
+    *scale = orc_f32_to_f16(d);
+}
+
+/* n values (n a multiple of 32) -> n/2 packed bytes and n/32 scales. */
+void orc_q4_0_quantize_row(const float *x, int64_t n, uint8_t *packed, uint16_t *scale) {
+    for (int64_t b = 0; b < n / ORC_QK; ++b)
+        orc_q4_0_quantize_block(x + b * ORC_QK, packed + b * (ORC_QK / 2), scale + b);
+}
+
+/* Code of element i of a row of packed blocks. */
+static int orc_q4_0_code(const uint8_t *packed, int64_t i) {
+    const uint8_t *blk = packed + (i / ORC_QK) * (ORC_QK / 2);
+    int k = (int)(i % ORC_QK);
+    return k < ORC_QK / 2 ? (blk[k] & 15) : (blk[k - ORC_QK / 2] >> 4);
+}
+
+/* Dequantised values of n elements: (code - 8) * fp16(d), exact in double. */
+void orc_q4_0_dequantize_row(const uint8_t *packed, const uint16_t *scale, int64_t n, double *x) {
+    for (int64_t i = 0; i < n; ++i) x[i] = (double)(orc_q4_0_code(packed, i) - 8) * orc_f16_to_f64(scale[i / ORC_QK]);
+}
+
+/* ------------------------------------------------------------------ */
 /* Attention                                                           */
 /* ------------------------------------------------------------------ */
 
 /* KV storage description used by the attention and rope routines.
  * type 8 = q8_0: codes int8 [n][Hk][D], scales fp16 bits [n][Hk][D/32].
+ * type 2 = q4_0: packed bytes [n][Hk][D/2], scales fp16 bits [n][Hk][D/32].
  * type 1 = f16 : values fp16 bits [n][Hk][D] (codes pointer), scales NULL. */
 typedef struct {
     int type;
@@ -157,6 +214,10 @@ static void orc_load_row(const orc_kv *t, int64_t j, int g, int Hk, int D, doubl
         const int8_t *c = (const int8_t *)t->data + base;
         const uint16_t *s = t->scales + (j * Hk + g) * (int64_t)(D / ORC_QK);
         for (int i = 0; i < D; ++i) out[i] = orc_f16_to_f64(s[i / ORC_QK]) * (double)c[i];
+    } else if (t->type == 2) {
+        const uint8_t *c = (const uint8_t *)t->data + (j * Hk + g) * (int64_t)(D / 2);
+        const uint16_t *s = t->scales + (j * Hk + g) * (int64_t)(D / ORC_QK);
+        orc_q4_0_dequantize_row(c, s, D, out);
     } else {
         const uint16_t *h = (const uint16_t *)t->data + base;
         for (int i = 0; i < D; ++i) out[i] = orc_f16_to_f64(h[i]);

@@ -35,6 +35,8 @@ to a multiple of 16 bytes:
   payload:     for each layer: the K section, then the V section;
                q8_0 section = codes int8 [Hk][n_tok][D] (padded),
                               then scales u16 [Hk][n_tok][D/32] (padded)
+               q4_0 section = packed codes u8 [Hk][n_tok][D/2] (padded),
+                              then scales u16 [Hk][n_tok][D/32] (padded)
                f16 section  = halves u16 [Hk][n_tok][D] (padded)
 """
 from __future__ import annotations
@@ -58,6 +60,8 @@ def _pad16(n: int) -> int:
 def section_bytes(type_: int, n_tok: int, Hk: int, D: int) -> int:
     if type_ == L.Q8_0:
         return _pad16(Hk * n_tok * D) + _pad16(Hk * n_tok * (D // 32) * 2)
+    if type_ == L.Q4_0:
+        return _pad16(Hk * n_tok * (D // 2)) + _pad16(Hk * n_tok * (D // 32) * 2)
     return _pad16(Hk * n_tok * D * 2)
 
 
@@ -71,12 +75,16 @@ def _norm_range(p0: int, p1: int) -> tuple[int, int]:
 
 
 class _Tensor:
-    """One layer's K or V rows: q8_0 (codes, scales) or f16 (halves, None)."""
+    """One layer's K or V rows: q8_0 (codes, scales), q4_0 (packed codes,
+    scales; V only) or f16 (halves, None)."""
 
     def __init__(self, type_: int, Hk: int, D: int):
         self.type = type_
         if type_ == L.Q8_0:
             self.a = np.zeros((0, Hk, D), np.int8)
+            self.s = np.zeros((0, Hk, D // 32), np.uint16)
+        elif type_ == L.Q4_0:
+            self.a = np.zeros((0, Hk, D // 2), np.uint8)
             self.s = np.zeros((0, Hk, D // 32), np.uint16)
         else:
             self.a = np.zeros((0, Hk, D), np.uint16)
@@ -102,6 +110,8 @@ class _Tensor:
         t.type = self.type
         if self.type == L.Q8_0:
             t.a, t.s = L.q8_0_quantize(x)
+        elif self.type == L.Q4_0:
+            t.a, t.s = L.q4_0_quantize(x)
         else:
             t.a, t.s = L.f32_to_f16(x), None
         return t
@@ -121,6 +131,7 @@ class OracleCache:
     def __init__(self, n_layer, n_head, n_head_kv, head_dim, type_k=L.Q8_0, type_v=L.Q8_0,
                  rope_base=10000.0, rope_mode=0):
         assert n_head % n_head_kv == 0 and head_dim % 32 == 0
+        assert type_k != L.Q4_0, "q4_0 is a V type (the keys are rotated and requantised by seq_add)"
         self.n_layer, self.H, self.Hk, self.D = n_layer, n_head, n_head_kv, head_dim
         self.type_k, self.type_v = type_k, type_v
         self.rope_base, self.rope_mode = float(rope_base), int(rope_mode)
@@ -283,9 +294,10 @@ class OracleCache:
             for dst, type_ in ((K, tk), (V, tv)):
                 t = object.__new__(_Tensor)
                 t.type = type_
-                if type_ == L.Q8_0:
-                    a = np.frombuffer(blob, np.int8, hk * n * d, off).reshape(hk, n, d)
-                    off += _pad16(hk * n * d)
+                if type_ in (L.Q8_0, L.Q4_0):
+                    w, dt = (d, np.int8) if type_ == L.Q8_0 else (d // 2, np.uint8)
+                    a = np.frombuffer(blob, dt, hk * n * w, off).reshape(hk, n, w)
+                    off += _pad16(hk * n * w)
                     sc = np.frombuffer(blob, "<u2", hk * n * (d // 32), off).reshape(hk, n, d // 32)
                     off += _pad16(hk * n * (d // 32) * 2)
                     t.a = np.ascontiguousarray(a.transpose(1, 0, 2))

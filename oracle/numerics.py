@@ -13,7 +13,7 @@ from . import build as _build
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
-F16, Q8_0 = 1, 8
+F16, Q4_0, Q8_0 = 1, 2, 8
 
 
 def _load():
@@ -33,6 +33,9 @@ def _load():
     L.orc_q8_0_value.restype = f64
     L.orc_q8_0_value.argtypes = [C.c_int8, C.c_uint16]
     L.orc_q8_0_dequantize_row.argtypes = [p, p, i64, p]
+    L.orc_q4_0_quantize_block.argtypes = [p, p, p]
+    L.orc_q4_0_quantize_row.argtypes = [p, i64, p, p]
+    L.orc_q4_0_dequantize_row.argtypes = [p, p, i64, p]
     L.orc_attn.restype = i32
     L.orc_attn.argtypes = [p, i32, i32, i32, i64, i32, p, p, i32, p, p, f64, i32, i32, p]
     L.orc_attn_bruteforce.restype = i32
@@ -91,8 +94,30 @@ def q8_0_dequantize(codes, scales) -> np.ndarray:
     return out
 
 
+def q4_0_quantize(x) -> tuple[np.ndarray, np.ndarray]:
+    """x fp32 [..., D] (D % 32 == 0) -> (packed u8 [..., D/2], scales u16 [..., D/32]).
+    Byte j of a block holds code j (low four bits) and code j + 16 (high)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    D = x.shape[-1]
+    assert D % 32 == 0
+    packed = np.empty(x.shape[:-1] + (D // 2,), dtype=np.uint8)
+    scales = np.empty(x.shape[:-1] + (D // 32,), dtype=np.uint16)
+    lib.orc_q4_0_quantize_row(_ptr(x), x.size, _ptr(packed), _ptr(scales))
+    return packed, scales
+
+
+def q4_0_dequantize(packed, scales) -> np.ndarray:
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    assert packed.shape[:-1] == scales.shape[:-1] and packed.shape[-1] == 16 * scales.shape[-1]
+    out = np.empty(packed.shape[:-1] + (2 * packed.shape[-1],), dtype=np.float64)
+    lib.orc_q4_0_dequantize_row(_ptr(packed), _ptr(scales), out.size, _ptr(out))
+    return out
+
+
 def _kv_args(type_, data, scales):
-    data = np.ascontiguousarray(data, dtype=np.int8 if type_ == Q8_0 else np.uint16)
+    dt = {Q8_0: np.int8, Q4_0: np.uint8}.get(type_, np.uint16)
+    data = np.ascontiguousarray(data, dtype=dt)
     scales = None if type_ == F16 else np.ascontiguousarray(scales, dtype=np.uint16)
     return data, scales
 
@@ -101,7 +126,8 @@ def attn(q, type_k, k, ks, type_v, v, vs, kq_scale, heads=None) -> np.ndarray:
     """Single-query attention for one sequence.
 
     q fp32 [H][D]; k/v: q8_0 codes int8 [n][Hk][D] + scales u16 [n][Hk][D/32],
-    or f16 bits u16 [n][Hk][D] (scales None).  Returns fp64 [H][D]; rows
+    q4_0 packed u8 [n][Hk][D/2] + scales u16 [n][Hk][D/32] (V only), or f16
+    bits u16 [n][Hk][D] (scales None).  Returns fp64 [H][D]; rows
     outside `heads` (a (h0, h1) range) are left zero."""
     q = np.ascontiguousarray(q, dtype=np.float32)
     H, D = q.shape

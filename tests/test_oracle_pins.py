@@ -14,7 +14,7 @@ import scipy.special
 import oracle
 from oracle import numerics as L
 from kv_cache_decode_flash_gb300 import synth
-from golden_io import q8_0_blocks, hexfile
+from golden_io import q4_0_blocks, q8_0_blocks, hexfile
 
 # ---------------------------------------------------------------- fp16 ----
 
@@ -121,6 +121,109 @@ def test_q8_0_dequant_exact_in_fp32():
         v64 = oracle.q8_0_dequantize(codes.reshape(8, 32), np.full((8, 1), s, np.uint16)).ravel()
         v32 = np.float32(np.array([s], np.uint16).view(np.float16)[0]) * codes.astype(np.float32)
         assert np.array_equal(v64, v32.astype(np.float64))
+
+
+# ---------------------------------------------------------------- q4_0 ----
+
+
+def _nibble_decode(packed, scale_bits):
+    """Values of one packed q4_0 block read directly off the stated layout:
+    element i sits in byte i % 16, low four bits for i < 16, high for i >= 16."""
+    d = oracle.f16_to_f64(np.array([scale_bits], np.uint16))[0]
+    return np.array([(((int(packed[i % 16]) >> (4 * (i // 16))) & 15) - 8) * d for i in range(32)])
+
+
+@pytest.mark.parametrize("blk", q4_0_blocks(), ids=lambda b: b[0])
+def test_q4_0_golden_blocks(blk):
+    name, x, codes, packed, scale = blk
+    got_p, got_s = oracle.q4_0_quantize(x.reshape(1, 32))
+    assert got_p[0].tobytes() == packed.tobytes(), name
+    assert int(got_s[0, 0]) == scale, name
+    # the codes of the fixture, packed by hand, are the fixture's bytes
+    assert bytes(int(codes[j]) | (int(codes[j + 16]) << 4) for j in range(16)) == packed.tobytes()
+    np.testing.assert_array_equal(oracle.q4_0_dequantize(got_p, got_s)[0], _nibble_decode(packed, scale))
+
+
+def test_q4_0_largest_element_decodes_to_itself_and_codes_stay_in_range():
+    x = synth.normal(21, synth.stream_id("misc", extra=21), 4096 * 32).astype(np.float32).reshape(-1, 32)
+    p, sc = oracle.q4_0_quantize(x)
+    v = oracle.q4_0_dequantize(p, sc)
+    d16 = oracle.f16_to_f64(sc)[:, 0]
+    idx = np.argmax(np.abs(x), axis=1)  # numpy's argmax takes the first maximum, as the reading does
+    m = x[np.arange(len(x)), idx].astype(np.float64)
+    # code 0 decodes to -8 * fp16(m / -8)
+    np.testing.assert_array_equal(v[np.arange(len(x)), idx], -8.0 * d16)
+    # and -8 * fp16(m / -8) is m up to the scale's fp16 rounding
+    assert (np.abs(-8.0 * d16 - m) <= 8 * 2.0**-11 * np.abs(m) + 2.0**-21).all()
+    # every decoded value lies on the grid (c - 8) * fp16(d), c in 0..15
+    c = np.rint(v / np.where(d16 == 0, 1, d16)[:, None]) + 8
+    assert ((c >= 0) & (c <= 15)).all()
+
+
+def test_q4_0_error_bound():
+    # |x - x^| <= |d| / 2 + 8 |d - fp16(d)| away from the clamped top code, and at most
+    # |d| + 8 |d - fp16(d)| where x * id rounds past 15 (the asymmetric clamp of the format)
+    x = synth.normal(22, synth.stream_id("misc", extra=22), 2048 * 32).astype(np.float32).reshape(-1, 32)
+    p, sc = oracle.q4_0_quantize(x)
+    v = oracle.q4_0_dequantize(p, sc)
+    d16 = oracle.f16_to_f64(sc)[:, 0][:, None]
+    m = x[np.arange(len(x)), np.argmax(np.abs(x), axis=1)].astype(np.float64)[:, None]
+    d = m / -8.0
+    slack = 8 * np.abs(d - d16) + 1e-6 * np.abs(d)
+    t = x / d
+    err = np.abs(x - v)
+    inner = t < 7.5 - 1e-5  # below the clamped top code
+    assert (err <= np.abs(d) / 2 + slack + np.where(inner, 0.0, np.abs(d) / 2)).all()
+    assert (np.abs(x - v)[~inner] <= np.abs(d)[np.nonzero(~inner)[0]][:, 0] + 1e-6).all()
+
+
+def test_q4_0_attention_closed_forms():
+    # identical V rows: any softmax gives that row back; K q8_0 as in the asymmetric cache
+    H, Hk, D, n = 8, 2, 64, 40
+    (kc, ks), _ = _cache(n, Hk, D, 23)
+    vrow = synth.normal(23, synth.stream_id("v"), Hk * D).astype(np.float32).reshape(1, Hk, D)
+    vp, vs = oracle.q4_0_quantize(np.repeat(vrow, n, axis=0))
+    q = synth.normal(23, synth.stream_id("q"), H * D).reshape(H, D)
+    out = oracle.attn(q, L.Q8_0, kc, ks, L.Q4_0, vp, vs, 0.125)
+    V = oracle.q4_0_dequantize(vp, vs)
+    for h in range(H):
+        np.testing.assert_allclose(out[h], V[0, h // 4], rtol=0, atol=1e-14)
+    # random V: the two-pass oracle against the per-token long-double formulation and
+    # against numpy / scipy over the decoded values
+    v = synth.normal(24, synth.stream_id("v"), n * Hk * D).reshape(n, Hk, D)
+    vp, vs = oracle.q4_0_quantize(v)
+    a = oracle.attn(q, L.Q8_0, kc, ks, L.Q4_0, vp, vs, 0.125)
+    b = oracle.attn_bruteforce(q, L.Q8_0, kc, ks, L.Q4_0, vp, vs, 0.125)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-13)
+    K, V = oracle.q8_0_dequantize(kc, ks), oracle.q4_0_dequantize(vp, vs)
+    for h in range(H):
+        p_ = scipy.special.softmax(0.125 * (K[:, h // 4, :] @ q[h].astype(np.float64)))
+        np.testing.assert_allclose(a[h], p_ @ V[:, h // 4, :], rtol=1e-12, atol=1e-13)
+
+
+def test_q4_0_state_layout_and_roundtrip():
+    c = oracle.OracleCache(2, 4, 2, 64, L.Q8_0, L.Q4_0, 10000.0, 0)
+    for l in range(2):
+        k = synth.normal(25, synth.stream_id("k", l), 30 * 2 * 64).reshape(30, 2, 64)
+        v = synth.normal(25, synth.stream_id("v", l), 30 * 2 * 64).reshape(30, 2, 64)
+        c.append(l, 0, 0, k, v)
+    blob = c.state_get(0, 5, 25)
+    n = 20
+    pad = lambda x: (x + 15) // 16 * 16
+    ksec = pad(2 * n * 64) + pad(2 * n * 2 * 2)
+    vsec = pad(2 * n * 32) + pad(2 * n * 2 * 2)
+    assert len(blob) == 64 + pad(4 * n) + 2 * (ksec + vsec) == oracle.state_size(2, 2, 64, L.Q8_0, L.Q4_0, n)
+    # layer 1's V codes, head-major, equal the quantiser applied to the same rows
+    v1 = synth.normal(25, synth.stream_id("v", 1), 30 * 2 * 64).reshape(30, 2, 64)[5:25]
+    vp, vs = oracle.q4_0_quantize(v1)
+    off = 64 + pad(4 * n) + (ksec + vsec) + ksec
+    got = np.frombuffer(blob, np.uint8, 2 * n * 32, off).reshape(2, n, 32).transpose(1, 0, 2)
+    assert np.array_equal(got, vp)
+    c.state_set(3, blob)
+    assert c.state_get(3, -1, -1) == blob
+    c.seq_add(3, -1, -1, 7)  # rotates K only: the V bytes stay
+    after = c.state_get(3, -1, -1)
+    assert after[off:off + 2 * n * 32] == blob[off:off + 2 * n * 32]
 
 
 # ----------------------------------------------------------- attention ----
