@@ -75,6 +75,8 @@ H, HK, D = 40, 8, 128
 def kv_bytes_per_row(type_: str) -> int:
     if type_ == "q8_0":
         return 2 * HK * (D + (D // 32) * 2)  # 2176
+    if type_ == "q8_0/q4_0":  # q8_0 K, q4_0 V
+        return HK * (D + (D // 32) * 2) + HK * (D // 2 + (D // 32) * 2)  # 1088 + 576 = 1664
     return 2 * HK * D * 2  # 4096
 
 
@@ -415,8 +417,9 @@ def attn_only_gbs(kvc, torch, dev, type_: str, n: int, reps: int = 50):
 
     layers = max(8, -(-(512 << 20) // (n * kv_bytes_per_row(type_))))
 
-    t = kvc.KVC_Q8_0 if type_ == "q8_0" else kvc.KVC_F16
-    cache = kvc.KVCache(layers, H, HK, D, n + 64, 1, t, t, 1e6)
+    t = kvc.KVC_F16 if type_ == "f16" else kvc.KVC_Q8_0
+    tv = kvc.KVC_Q4_0 if type_ == "q8_0/q4_0" else t
+    cache = kvc.KVCache(layers, H, HK, D, n + 64, 1, t, tv, 1e6)
     try:
         for l in range(layers):
             for p0 in range(0, n, 8192):
@@ -664,8 +667,8 @@ def step_line(args, world: int, L: int, n: int, t_step: float, t_attn: float, t_
     }
 
 
-EXTRA_ROWS = ("q8_0_4k", "q8_0_64k", "q8_0_256k", "f16_16k", "f16_4k", "ragged_q8_0", "ragged_f16", "churn",
-              "keydiff", "split_32k_g4", "cold_store")
+EXTRA_ROWS = ("q8_0_4k", "q8_0_64k", "q8_0_256k", "f16_16k", "f16_4k", "q8_0_q4_0_16k", "q8_0_q4_0_64k",
+              "ragged_q8_0", "ragged_f16", "churn", "keydiff", "split_32k_g4", "cold_store")
 
 
 def run_child(args, name: str) -> dict:
@@ -714,6 +717,8 @@ def child_phase(args) -> dict:
         "q8_0_256k": lambda: attn_only_gbs(kvc, torch, dev, "q8_0", 262144),
         "f16_16k": lambda: attn_only_gbs(kvc, torch, dev, "f16", 16384),
         "f16_4k": lambda: attn_only_gbs(kvc, torch, dev, "f16", 4096),
+        "q8_0_q4_0_16k": lambda: attn_only_gbs(kvc, torch, dev, "q8_0/q4_0", 16384),
+        "q8_0_q4_0_64k": lambda: attn_only_gbs(kvc, torch, dev, "q8_0/q4_0", 65536),
         "ragged_q8_0": lambda: ragged(kvc, torch, dev, "q8_0"),
         "ragged_f16": lambda: ragged(kvc, torch, dev, "f16"),
         "churn": lambda: churn(kvc, torch, dev, args.churn_n, args.churn_cycles, args.layers),

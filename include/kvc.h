@@ -63,8 +63,17 @@ typedef enum kvc_status {
  * in fp32, scale stored as fp16(d) round-to-nearest-even.  The type is named
  * in [F5] section M6 ("-ctk q8_0") and [R4] section Measurements ("q8_0
  * K/V"); the pages give no bit layout, so this plainest reading is pinned.
+ * KVC_Q4_0 (V only, with q8_0 K and head_dim 128: the asymmetric cache of
+ * [F5] section M6 - PolyKV, "-ctk q8_0 -ctv q4_0"): blocks of 32 elements
+ * stored as 32 four-bit codes plus one fp16 scale d.  The pages name the type
+ * without defining it; the reading used: m = the element of largest
+ * magnitude, sign kept (the first one on ties), d = m / -8, code =
+ * min(15, trunc(x * (1/d) + 8.5)) with the product and the sum each rounded
+ * to fp32, scale stored as fp16(d); value = (code - 8) * d.  Byte j of a
+ * block (16 bytes) holds code j in its low four bits and code j + 16 in its
+ * high four bits.
  * KVC_F16: IEEE binary16, round to nearest even. */
-typedef enum kvc_type { KVC_F16 = 1, KVC_Q8_0 = 8 } kvc_type;
+typedef enum kvc_type { KVC_F16 = 1, KVC_Q4_0 = 2, KVC_Q8_0 = 8 } kvc_type;
 
 /* Where a context keeps its K/V.
  * KVC_DEVICE: device HBM, paged, any number of sequences.
@@ -96,8 +105,9 @@ typedef struct kvc_params {
     int32_t n_ctx;      /* device: cells per layer shared by all sequences;
                            host-resident: capacity of the one sequence */
     int32_t n_seq_max;  /* sequence ids are 0 .. n_seq_max-1 */
-    int32_t type_k;     /* kvc_type */
-    int32_t type_v;     /* kvc_type */
+    int32_t type_k;     /* kvc_type: KVC_Q8_0 or KVC_F16 */
+    int32_t type_v;     /* kvc_type: the same as type_k, or KVC_Q4_0 with
+                           type_k KVC_Q8_0 and head_dim 128 */
     float rope_base;    /* theta_i = rope_base^(-2i/D) */
     int32_t rope_mode;  /* kvc_rope */
     int32_t residency;  /* kvc_residency */
@@ -223,8 +233,9 @@ int kvc_seq_add(kvc_ctx *c, int seq, int p0, int p1, int delta);
  *   positions: int32 pos[n_tok];
  *   payload: for each layer, the K section then the V section, where a q8_0
  *     section is codes int8 [n_head_kv][n_tok][head_dim] followed by scales
- *     u16 (fp16 bits) [n_head_kv][n_tok][head_dim/32], and an f16 section is
- *     u16 [n_head_kv][n_tok][head_dim]. */
+ *     u16 (fp16 bits) [n_head_kv][n_tok][head_dim/32], a q4_0 section is
+ *     packed codes u8 [n_head_kv][n_tok][head_dim/2] followed by scales as
+ *     for q8_0, and an f16 section is u16 [n_head_kv][n_tok][head_dim]. */
 int kvc_state_get(kvc_ctx *c, int seq, int p0, int p1, void *dst, size_t cap,
                   size_t *n_written);
 

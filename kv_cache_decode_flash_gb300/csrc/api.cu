@@ -205,6 +205,7 @@ static inline int64_t pad16(int64_t x) { return (x + 15) / 16 * 16; }
 // State format sizes (see include/kvc.h).
 static int64_t section_bytes(const Ctx *c, int type, int64_t n) {
     if (type == KVC_Q8_0) return pad16((int64_t)c->Hk * n * c->D) + pad16((int64_t)c->Hk * n * (c->D / QK) * 2);
+    if (type == KVC_Q4_0) return pad16((int64_t)c->Hk * n * (c->D / 2)) + pad16((int64_t)c->Hk * n * (c->D / QK) * 2);
     return pad16((int64_t)c->Hk * n * c->D * 2);
 }
 static int64_t payload_bytes(const Ctx *c, int64_t n) {
@@ -260,7 +261,7 @@ static void zero_payload_pads(const Ctx *c, uint8_t *payload, int64_t n) {
             const int type = t == 0 ? c->tk : c->tv;
             const int64_t db = (int64_t)c->Hk * n * (t == 0 ? c->krow : c->vrow);
             std::memset(payload + off + db, 0, (size_t)(pad16(db) - db));
-            if (type == KVC_Q8_0) {
+            if (type != KVC_F16) {
                 const int64_t sb = (int64_t)c->Hk * n * (t == 0 ? c->ksb : c->vsb);
                 std::memset(payload + off + pad16(db) + sb, 0, (size_t)(pad16(sb) - sb));
             }
@@ -396,9 +397,15 @@ int kvc_create(const kvc_params *p, kvc_ctx **out) {
     if (p->head_dim != 64 && p->head_dim != 128) return bad("head_dim must be 64 or 128");
     if (p->n_head / p->n_head_kv > MAX_GROUP) return bad("more than 8 query heads per KV head");
     if (p->n_ctx < 1 || p->n_seq_max < 1) return bad("n_ctx and n_seq_max must be positive");
-    if ((p->type_k != KVC_Q8_0 && p->type_k != KVC_F16) || (p->type_v != KVC_Q8_0 && p->type_v != KVC_F16))
-        return bad("type must be KVC_Q8_0 or KVC_F16");
-    if (p->type_k != p->type_v) return bad("K and V must have the same type");
+    if ((p->type_k != KVC_Q8_0 && p->type_k != KVC_F16) ||
+        (p->type_v != KVC_Q8_0 && p->type_v != KVC_F16 && p->type_v != KVC_Q4_0))
+        return bad("type_k must be KVC_Q8_0 or KVC_F16, type_v KVC_Q8_0, KVC_F16 or KVC_Q4_0");
+    if (p->type_v == KVC_Q4_0) {
+        // the asymmetric cache: q8_0 K, q4_0 V
+        if (p->type_k != KVC_Q8_0 || p->head_dim != 128) return bad("q4_0 V needs q8_0 K and head_dim 128");
+    } else if (p->type_k != p->type_v) {
+        return bad("K and V must have the same type (or q8_0 K with q4_0 V)");
+    }
     if (p->rope_mode != KVC_ROPE_NEOX && p->rope_mode != KVC_ROPE_NORM) return bad("bad rope_mode");
     if (!(p->rope_base > 1.0f) || !std::isfinite(p->rope_base)) return bad("rope_base must be > 1");
     if (p->residency != KVC_DEVICE && p->residency != KVC_HOST_PINNED && p->residency != KVC_SPLIT_HEADS)
@@ -462,12 +469,13 @@ int kvc_create(const kvc_params *p, kvc_ctx **out) {
     c->tk = p->type_k;
     c->tv = p->type_v;
     c->krow = c->tk == KVC_Q8_0 ? c->D : 2 * c->D;
-    c->vrow = c->tv == KVC_Q8_0 ? c->D : 2 * c->D;
+    c->vrow = c->tv == KVC_Q8_0 ? c->D : (c->tv == KVC_Q4_0 ? c->D / 2 : 2 * c->D);
     c->ksb = c->tk == KVC_Q8_0 ? (c->D / QK) * 2 : 0;
-    c->vsb = c->tv == KVC_Q8_0 ? (c->D / QK) * 2 : 0;
+    c->vsb = c->tv != KVC_F16 ? (c->D / QK) * 2 : 0;
     c->host = p->residency == KVC_HOST_PINNED;
     c->occ = attn_ctas_per_sm(c->tk, c->D, c->r, 0);
-    c->occ2 = attn_ctas_per_sm(c->tk, c->D, c->r, 1);
+    // the two-CTA configuration exists for symmetric q8_0 only
+    c->occ2 = c->tv == c->tk ? attn_ctas_per_sm(c->tk, c->D, c->r, 1) : 0;
 
     auto fail = [&](int rc) {
         kvc_destroy(reinterpret_cast<kvc_ctx *>(c));

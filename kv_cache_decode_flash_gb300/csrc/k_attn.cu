@@ -168,6 +168,32 @@ __device__ __forceinline__ void vcodes_to_half2(uint32_t w, uint32_t &ev, uint32
     asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(od) : "r"(bias));
 }
 
+__device__ __forceinline__ void ldsm_x2_trans(const void *p, uint32_t &a, uint32_t &b) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+                 : "=r"(a), "=r"(b)
+                 : "r"(smem_u32(p)));
+}
+// A transposed word of packed q4_0 bytes holds bytes (row 2t: 2g, 2g+1) and
+// (row 2t+1: 2g, 2g+1) of a block, i.e. the codes of dims 2g, 2g+16 (byte 2g)
+// and 2g+1, 2g+17 (byte 2g+1) on both rows.  Return the exact half2 (rows 2t,
+// 2t+1) of code - 8 for each dim: a nibble or 16 x a nibble goes into the low
+// mantissa bits of 1024 (0x6400), then 1032 is subtracted, or the value is
+// scaled by 1/16 and 72 subtracted, both exactly.
+__device__ __forceinline__ void nibbles_to_half2(uint32_t w, uint32_t &d_lo_e, uint32_t &d_hi_e, uint32_t &d_lo_o,
+                                                 uint32_t &d_hi_o) {
+    const uint32_t w8 = w >> 8;
+    d_lo_e = (w & 0x000F000Fu) | 0x64006400u;  // dim 2g
+    d_hi_e = (w & 0x00F000F0u) | 0x64006400u;  // dim 2g + 16
+    d_lo_o = (w8 & 0x000F000Fu) | 0x64006400u; // dim 2g + 1
+    d_hi_o = (w8 & 0x00F000F0u) | 0x64006400u; // dim 2g + 17
+    const uint32_t b1032 = 0x64086408u;          // half2(1032, 1032)
+    const uint32_t s16 = 0x2C002C00u, m72 = 0xD480D480u; // half2(1/16), half2(-72)
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(d_lo_e) : "r"(b1032));
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(d_lo_o) : "r"(b1032));
+    asm("fma.rn.f16x2 %0, %0, %1, %2;" : "+r"(d_hi_e) : "r"(s16), "r"(m72));
+    asm("fma.rn.f16x2 %0, %0, %1, %2;" : "+r"(d_hi_o) : "r"(s16), "r"(m72));
+}
+
 // The NB fp16 scales of one row (NB = 2 or 4), one 4- or 8-byte load.
 template <int NB>
 __device__ __forceinline__ void load_scales(const uint8_t *p, uint32_t (&w)[NB / 2]) {
@@ -201,9 +227,10 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 // Static shape of one kernel instance.  W compute warps in groups of GW;
 // group j takes tiles j, j + G, j + 2G, ... and each of its warps owns 16
 // rows of a tile.  One more warp issues the tile loads.
-template <int TYPE, int D, int R, int CFG = 0>
+template <int TYPE, int D, int R, int CFG = 0, bool V4 = false>
 struct Shape {
     static constexpr bool Q8 = TYPE == KVC_Q8_0;
+    static_assert(!V4 || (Q8 && D == 128 && CFG == 0), "q4_0 V: with q8_0 K, head_dim 128, configuration 0");
     // CFG 0: one CTA per SM (16 compute warps for q8_0); CFG 1 (q8_0): two CTAs
     // per SM of 8 compute warps, each with half the SM's shared memory, for
     // launches whose work exceeds one wave of CFG 0 at the longest chunks
@@ -214,7 +241,7 @@ struct Shape {
     static constexpr int T = 16 * GW;                 // rows per tile
     static constexpr int NB = D / 32;                 // q8_0 blocks per row
     static constexpr int KROW = Q8 ? D : 2 * D;       // bytes per K row
-    static constexpr int VROW = KROW;                 // bytes per V row
+    static constexpr int VROW = V4 ? D / 2 : KROW;    // bytes per V row (q4_0: packed codes)
     static constexpr int SB = Q8 ? NB * 2 : 0;        // scale bytes per row
     static constexpr int KSUB = Q8 ? 1 : (D == 128 ? 2 : 1); // f16 K sub-tiles of 64 halves
     // scale copies start on the 16-byte boundary at or below a tile's first scale row: up to
@@ -271,12 +298,12 @@ struct TileInfo {
     int delta; // scale rows skipped by the 16-byte alignment of the scale copy
 };
 
-template <int TYPE, int D, int R, bool RAW = false, int CFG = 0>
-__global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, D, R, CFG>::MINB)
+template <int TYPE, int D, int R, bool RAW = false, int CFG = 0, bool V4 = false>
+__global__ void __launch_bounds__(Shape<TYPE, D, R, CFG, V4>::NTHREADS, Shape<TYPE, D, R, CFG, V4>::MINB)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmk,
                 const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmkb,
                 const __grid_constant__ CUtensorMap tmvb) {
-    using S = Shape<TYPE, D, R, CFG>;
+    using S = Shape<TYPE, D, R, CFG, V4>;
     constexpr int W = S::W, T = S::T, NT = S::NTHREADS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -509,7 +536,7 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
             load_row<D / 32>(p.app_k + in, lane, xk);
             load_row<D / 32>(p.app_v + in, lane, xv);
             store_row<D>(TYPE, p.app_lv.k, R, lane, xk);
-            store_row<D>(TYPE, p.app_lv.v, R, lane, xv);
+            store_row<D>(V4 ? KVC_Q4_0 : TYPE, p.app_lv.v, R, lane, xv);
             // order the stores before the bulk copies (async proxy) issued after the barrier
             asm volatile("fence.proxy.async.global;" ::: "memory");
         }
@@ -717,7 +744,20 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
                 uint32_t b0h, b1h, b0l, b1l;
                 split_pack(x[0], x[1], b0h, b0l);
                 split_pack(x[2], x[3], b1h, b1l);
-                if constexpr (S::Q8) {
+                if constexpr (V4) {
+                    // block b is one 16-byte chunk of each 64-byte row: ra = rows 0-7,
+                    // rb = rows 8-15; nibble pairs give the same even / odd dim
+                    // m-tiles as the int8 codes (dims 2g | 2g+16 and 2g+1 | 2g+17)
+                    uint32_t ra, rb;
+                    ldsm_x2_trans(vt + swz<S::VROW>(lm_row, b), ra, rb);
+                    uint32_t e0, e1, e2, e3, o0, o1, o2, o3;
+                    nibbles_to_half2(ra, e0, e1, o0, o1);
+                    nibbles_to_half2(rb, e2, e3, o2, o3);
+                    mma16816(acc[2 * b], e0, e1, e2, e3, b0h, b1h);
+                    mma16816(acc[2 * b], e0, e1, e2, e3, b0l, b1l);
+                    mma16816(acc[2 * b + 1], o0, o1, o2, o3, b0h, b1h);
+                    mma16816(acc[2 * b + 1], o0, o1, o2, o3, b0l, b1l);
+                } else if constexpr (S::Q8) {
                     uint32_t v0, v1, v2, v3;
                     ldsm_x4_trans(vt + swz<S::VROW>(lm_row, 2 * b + lm_hi), v0, v1, v2, v3);
                     // v0: rows 0-7 / bytes 0-15, v1: rows 8-15 / bytes 0-15,
@@ -948,10 +988,10 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG>::NTHREADS, Shape<TYPE, 
     }
 }
 
-template <int TYPE, int D, int R, bool RAW = false, int CFG = 0>
+template <int TYPE, int D, int R, bool RAW = false, int CFG = 0, bool V4 = false>
 cudaError_t launch_t(const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv, cudaStream_t st) {
     // tmk / tmv point at {16-row map, 128-row map} pairs
-    using S = Shape<TYPE, D, R, CFG>;
+    using S = Shape<TYPE, D, R, CFG, V4>;
     // the shared-memory attribute belongs to the current context: set it once per
     // context of each device (a reset device or another context gets it again)
     static uint64_t configured[MAX_DEVICES];
@@ -960,7 +1000,7 @@ cudaError_t launch_t(const AttnParams &p, const CUtensorMap *tmk, const CUtensor
     if (e != cudaSuccess) return e;
     const uint64_t ctx = current_context_id();
     if (dev < 0 || dev >= MAX_DEVICES || ctx == 0 || configured[dev] != ctx) {
-        e = cudaFuncSetAttribute(attn_kernel<TYPE, D, R, RAW, CFG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(attn_kernel<TYPE, D, R, RAW, CFG, V4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  S::SMEM);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < MAX_DEVICES) configured[dev] = ctx;
@@ -975,12 +1015,22 @@ cudaError_t launch_t(const AttnParams &p, const CUtensorMap *tmk, const CUtensor
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_kernel<TYPE, D, R, RAW, CFG>, p, tmk[0], tmv[0], tmk[1], tmv[1]);
+    return cudaLaunchKernelEx(&cfg, attn_kernel<TYPE, D, R, RAW, CFG, V4>, p, tmk[0], tmv[0], tmk[1], tmv[1]);
 }
 
 template <int TYPE, int D>
 cudaError_t launch_d(const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv, cudaStream_t st,
-                     bool raw, int cfg) {
+                     bool raw, int cfg, bool v4) {
+    if (v4) {
+        // q4_0 V: q8_0 K, head_dim 128, configuration 0 only
+        if constexpr (TYPE == KVC_Q8_0 && D == 128) {
+            if (raw || cfg != 0) return cudaErrorInvalidValue;
+            if (p.r <= 4) return launch_t<TYPE, D, 4, false, 0, true>(p, tmk, tmv, st);
+            if (p.r == 5) return launch_t<TYPE, D, 5, false, 0, true>(p, tmk, tmv, st);
+            if (p.r <= 8) return launch_t<TYPE, D, 8, false, 0, true>(p, tmk, tmv, st);
+        }
+        return cudaErrorInvalidValue;
+    }
     // plain int8 codes (caller buffers): one instance for every group size up to 8
     if constexpr (TYPE == KVC_Q8_0) {
         if (raw) return p.r <= 8 ? launch_t<TYPE, D, 8, true>(p, tmk, tmv, st) : cudaErrorInvalidValue;
@@ -1077,15 +1127,17 @@ int attn_merge_cap(int type, int D, int r, int cfg) {
     return D == 128 ? chunk_cap_d<KVC_F16, 128, 0>(r) : chunk_cap_d<KVC_F16, 64, 0>(r);
 }
 
-cudaError_t launch_attn(int type, const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv,
+cudaError_t launch_attn(int type, int type_v, const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv,
                         cudaStream_t st, bool raw_codes, int cfg) {
+    const bool v4 = type_v == KVC_Q4_0;
+    if (!v4 && type_v != type) return cudaErrorInvalidValue;
     if (type == KVC_Q8_0) {
-        if (p.D == 128) return launch_d<KVC_Q8_0, 128>(p, tmk, tmv, st, raw_codes, cfg);
-        if (p.D == 64) return launch_d<KVC_Q8_0, 64>(p, tmk, tmv, st, raw_codes, cfg);
-    } else {
+        if (p.D == 128) return launch_d<KVC_Q8_0, 128>(p, tmk, tmv, st, raw_codes, cfg, v4);
+        if (p.D == 64) return launch_d<KVC_Q8_0, 64>(p, tmk, tmv, st, raw_codes, cfg, v4);
+    } else if (!v4) {
         if (cfg != 0) return cudaErrorInvalidValue;
-        if (p.D == 128) return launch_d<KVC_F16, 128>(p, tmk, tmv, st, false, 0);
-        if (p.D == 64) return launch_d<KVC_F16, 64>(p, tmk, tmv, st, false, 0);
+        if (p.D == 128) return launch_d<KVC_F16, 128>(p, tmk, tmv, st, false, 0, false);
+        if (p.D == 64) return launch_d<KVC_F16, 64>(p, tmk, tmv, st, false, 0, false);
     }
     return cudaErrorInvalidValue;
 }
@@ -1107,7 +1159,7 @@ bool encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int row_byt
         }
         fn = reinterpret_cast<EncodeFn>(ptr);
     }
-    const bool q8 = type == KVC_Q8_0;
+    const bool q8 = type != KVC_F16; // q8_0 codes and packed q4_0 codes: bytes
     const int esize = q8 ? 1 : 2;
     const cuuint64_t elems = (cuuint64_t)(row_bytes / esize);
     cuuint64_t gdim[2] = {elems, (cuuint64_t)rows};

@@ -149,5 +149,5 @@ extern "C" int kvc_attn_decode_static(int type, int n_head, int n_head_kv, int h
     a.ticket = 0;
     a.stable_rows = 0; // caller buffers: nothing is read before the dependency wait
     a.pt_len = 1;
-    return launch_attn(type, p, tmk, tmv, st, /*raw_codes=*/true) == cudaSuccess ? KVC_OK : KVC_ECUDA;
+    return launch_attn(type, type, p, tmk, tmv, st, /*raw_codes=*/true) == cudaSuccess ? KVC_OK : KVC_ECUDA;
 }

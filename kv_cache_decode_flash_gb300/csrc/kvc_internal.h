@@ -94,7 +94,9 @@ struct AttnParams {
 // raw_codes: q8_0 codes are plain int8 (caller buffers) instead of offset binary.
 // cfg 0: one CTA per SM; cfg 1 (q8_0 only): two CTAs per SM, for launches whose
 // work exceeds one wave of cfg 0 at the longest chunks.
-cudaError_t launch_attn(int type, const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv,
+// type: the K type; type_v: the V type (the same, or KVC_Q4_0 with q8_0 K,
+// head_dim 128 and configuration 0).
+cudaError_t launch_attn(int type, int type_v, const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv,
                         cudaStream_t st, bool raw_codes = false, int cfg = 0);
 int attn_ctas_per_sm(int type, int D, int r, int cfg = 0); // 0: the configuration does not exist
 int attn_merge_cap(int type, int D, int r, int cfg = 0);   // most chunks per (sequence, kv head) a launch may use

@@ -182,7 +182,7 @@ int launch_attention(Ctx *c, const LayerView &lv, const CUtensorMap *tmk, const 
         p.part = c->part;
         p.part_cap = c->part_floats;
         for (int i = 0; i < cnt; ++i) p.seq[i].pt_len = c->host ? 1 : c->max_pages;
-        cudaError_t e = launch_attn(c->tk, p, tmk, tmv, st, false, pl.cfg);
+        cudaError_t e = launch_attn(c->tk, c->tv, p, tmk, tmv, st, false, pl.cfg);
         if (e != cudaSuccess) return cuda_fail(c, e, "attention kernel");
     }
     return KVC_OK;
@@ -547,7 +547,7 @@ static int rolling_attn(Ctx *c, int layer, const float *q, float *out, float kq_
         a.part_first = 0;
         a.pt_len = 1;
         p.total_chunks = (n + C - 1) / C;
-        cudaError_t e = launch_attn(c->tk, p, s->tmk, s->tmv, st, false, pl.cfg);
+        cudaError_t e = launch_attn(c->tk, c->tv, p, s->tmk, s->tmv, st, false, pl.cfg);
         if (e != cudaSuccess) return cuda_fail(c, e, "attention kernel");
         KVC_CU(c, cudaEventRecord(s->release, st));
         s->consumed_once = true;

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(HERE, "libkvc.so")
 
 KVC_OK, KVC_EINVAL, KVC_ENOMEM, KVC_ENOSPC, KVC_ERANGE = 0, -1, -2, -3, -4
 KVC_EFORMAT, KVC_ECUDA, KVC_ETIMEDOUT, KVC_EINTERNAL = -5, -6, -7, -8
-KVC_F16, KVC_Q8_0 = 1, 8
+KVC_F16, KVC_Q4_0, KVC_Q8_0 = 1, 2, 8
 KVC_DEVICE, KVC_HOST_PINNED, KVC_SPLIT_HEADS = 0, 1, 2
 KVC_ROPE_NEOX, KVC_ROPE_NORM = 0, 1
 

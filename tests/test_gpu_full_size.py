@@ -31,7 +31,7 @@ from twin import assert_attn_close
 
 pytestmark = pytest.mark.gpu
 
-Q8, F16 = oracle.Q8_0, oracle.F16
+Q8, F16, Q4 = oracle.Q8_0, oracle.F16, oracle.Q4_0
 H, HK, D, L = 40, 8, 128, 64
 SIGMA = 0.5
 BASE = 1e6
@@ -77,16 +77,19 @@ def _stored(type_, x):
     """The oracle's stored form of fp32 rows [n][Hk][D]."""
     if type_ == Q8:
         return oracle.q8_0_quantize(x)
+    if type_ == Q4:
+        return oracle.q4_0_quantize(x)
     return oracle.f32_to_f16(x), None
 
 
-def _oracle_attn(q, type_, k, v, kq_scale, heads):
+def _oracle_attn(q, type_, k, v, kq_scale, heads, type_v=None):
     """Oracle outputs fp64 [H][D] of the listed query heads (zero elsewhere),
     one host thread per head."""
+    tv = type_ if type_v is None else type_v
     kc, ks = _stored(type_, k)
-    vc, vs = _stored(type_, v)
+    vc, vs = _stored(tv, v)
     scale = float(np.float32(kq_scale))
-    one = lambda h: oracle.attn(q, type_, kc, ks, type_, vc, vs, scale, heads=(h, h + 1))
+    one = lambda h: oracle.attn(q, type_, kc, ks, tv, vc, vs, scale, heads=(h, h + 1))
     with ThreadPoolExecutor(max(1, min(len(heads), os.cpu_count() or 1))) as ex:
         return sum(ex.map(one, heads))
 
@@ -139,19 +142,20 @@ def test_full_device_resident_decode_step(type_, n):
         cache.close()
 
 
-@pytest.mark.parametrize("type_", [Q8, F16])
-def test_full_fused_decode_step_graph_replay(type_):
+@pytest.mark.parametrize("type_,type_v", [(Q8, Q8), (F16, F16), (Q8, Q4)])
+def test_full_fused_decode_step_graph_replay(type_, type_v):
     """The benchmark's step exactly as it times it: n_kv 16384, 64 layers,
     one fused kvc_decode_step launch per layer (row n-1 quantised inside the
     attention launch), run once eagerly, then captured as a CUDA graph and
     replayed three times (each replay rewrites row n-1).  The eager step and
     every replay give the same bits; layers 0, 31 and 63 of the last replay
-    against the oracle on all 40 query heads."""
+    against the oracle on all 40 query heads.  Also the asymmetric cache
+    (q8_0 K, q4_0 V)."""
     torch, kvc, dev = _env()
     n = 16384
     sampled = (0, 31, 63)
     scale = float(1.0 / np.sqrt(D))
-    cache = kvc.KVCache(L, H, HK, D, n + 256, 1, type_, type_, BASE, 0, kvc.KVC_DEVICE, 0)
+    cache = kvc.KVCache(L, H, HK, D, n + 256, 1, type_, type_v, BASE, 0, kvc.KVC_DEVICE, 0)
     try:
         host = _fill([cache], torch, dev, n - 1, 4096, keep=sampled)
         q = synth.normal_torch(0, synth.stream_id("q", 0, n + 7), L * H * D, 1.0, dev).view(L, 1, H, D)
@@ -184,7 +188,7 @@ def test_full_fused_decode_step_graph_replay(type_):
         for l in sampled:
             k = np.concatenate([host[l][0], knh[l]])
             v = np.concatenate([host[l][1], vnh[l]])
-            want = _oracle_attn(qh[l, 0], type_, k, v, scale, range(H))
+            want = _oracle_attn(qh[l, 0], type_, k, v, scale, range(H), type_v)
             _close_on_heads(got[l, 0], want, range(H), "fused step, graph replay, layer %d" % l)
         del gr
     finally:

@@ -28,7 +28,7 @@ def q_inputs(seed, layer, n_seq, H, D, extra=0):
 
 class Twin:
     def __init__(self, n_layer, H, Hk, D, n_ctx, n_seq_max=1, type_=8, rope_base=10000.0, rope_mode=0,
-                 page_rows=0, residency=0):
+                 page_rows=0, residency=0, type_v=None):
         import torch
 
         from kv_cache_decode_flash_gb300 import kvc
@@ -36,9 +36,10 @@ class Twin:
         self.torch, self.kvc = torch, kvc
         self.dev = torch.device("cuda:0")
         self.H, self.Hk, self.D, self.L = H, Hk, D, n_layer
-        self.gpu = kvc.KVCache(n_layer, H, Hk, D, n_ctx, n_seq_max, type_, type_, rope_base, rope_mode,
+        tv = type_ if type_v is None else type_v
+        self.gpu = kvc.KVCache(n_layer, H, Hk, D, n_ctx, n_seq_max, type_, tv, rope_base, rope_mode,
                                residency, 0, page_rows)
-        self.ref = oracle.OracleCache(n_layer, H, Hk, D, type_, type_, rope_base, rope_mode)
+        self.ref = oracle.OracleCache(n_layer, H, Hk, D, type_, tv, rope_base, rope_mode)
 
     def close(self):
         self.gpu.close()
