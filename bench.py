@@ -409,6 +409,119 @@ def host_pipeline(args, dev, torch, kvc, n=None, cells=HOST_CELLS, link=None, gp
     return res
 
 
+TIMELINE_CELLS = ((32768, (("ordered", 0, 128 << 20), ("N1_512MiB", 1, 512 << 20), ("N4_512MiB", 4, 512 << 20))),
+                  (65536, (("ordered", 0, 128 << 20), ("N1_512MiB", 1, 512 << 20))),
+                  (131072, (("ordered", 0, 128 << 20), ("rolling_N4_128MiB", 4, 128 << 20))))
+
+
+def _measure(iv, lo, hi):
+    """Length of the union of intervals [a, b) clipped to [lo, hi)."""
+    tot, end = 0.0, lo
+    for a, b in sorted(iv):
+        a, b = max(a, end), min(b, hi)
+        if b > a:
+            tot += b - a
+            end = b
+    return tot
+
+
+def _intersect(iv1, iv2):
+    out = []
+    for a1, b1 in iv1:
+        for a2, b2 in iv2:
+            a, b = max(a1, a2), min(b1, b2)
+            if b > a:
+                out.append((a, b))
+    return out
+
+
+def timeline_summary(recs, L):
+    """Summary of the middle one of three traced steps: recs are
+    (kind, layer, bytes, t0_us, t1_us), kind 0 delivery, 1 attention."""
+    att = [r for r in recs if r[0] == 1]
+    dlv = [r for r in recs if r[0] == 0]
+    per = len(att) // 3  # attention launches per step (several per layer with rolling tiles)
+    if per < L or len(att) != 3 * per:
+        return {"error": "%d attention records for 3 steps of %d layers" % (len(att), L)}
+    w0 = att[per - 1][4]  # end of the first step's last attention
+    w1 = att[2 * per - 1][4]
+    win = w1 - w0
+    D_iv = [(r[3], r[4]) for r in dlv]
+    A_iv = [(r[3], r[4]) for r in att]
+    copy = _measure(D_iv, w0, w1)
+    busy = _measure(A_iv, w0, w1)
+    hidden = _measure(_intersect([(max(a, w0), min(b, w1)) for a, b in D_iv if b > w0 and a < w1], A_iv), w0, w1)
+    inwin = [r for r in dlv if w0 <= r[3] < w1]
+    rates = sorted(r[2] / (r[4] - r[3]) / 1e3 for r in inwin if r[4] > r[3])  # GB/s (bytes / us / 1e3)
+    moved = sum(r[2] for r in inwin)
+    pct = lambda q: round(rates[min(len(rates) - 1, int(q * len(rates)))], 1) if rates else None
+    return {"step_ms": round(win / 1e3, 3), "steps_per_s": round(1e6 / win, 2),
+            "deliveries": len(inwin), "delivered_gb": round(moved / 1e9, 3),
+            "h2d_gbs_over_step": round(moved / win / 1e3, 1),
+            "per_delivery_gbs_p10_p50_p90": [pct(0.1), pct(0.5), pct(0.9)],
+            "copy_busy_frac": round(copy / win, 3), "attn_busy_frac": round(busy / win, 3),
+            "copy_hidden_frac": round(hidden / copy, 3) if copy > 0 else None,
+            "attn_hidden_frac": round(hidden / busy, 3) if busy > 0 else None,
+            "launches_per_step": per,
+            "compute_idle_ms": round((win - busy) / 1e3, 3)}
+
+
+def host_timeline(args, dev, torch, kvc) -> dict:
+    """Per-delivery timeline of the host transport (kvc_trace_*): for each
+    context length and (depth, budget) cell, one warm-up step, then three
+    traced steps; the middle one is summarised (timeline_summary)."""
+    from kv_cache_decode_flash_gb300 import synth
+
+    L = args.layers
+    out = {"link_gbs": round(measure_link(torch, dev), 2)}
+    scale = float(1.0 / np.sqrt(D))
+    for n, cells in TIMELINE_CELLS:
+        cache = kvc.KVCache(L, H, HK, D, n + 256, 1, kvc.KVC_Q8_0, kvc.KVC_Q8_0, 1e6, 0, kvc.KVC_HOST_PINNED)
+        try:
+            for l in range(L):
+                for p0 in range(0, n - 1, 8192):
+                    m = min(8192, n - 1 - p0)
+                    k = synth.normal_torch(0, synth.stream_id("k", l, p0), m * HK * D, 0.5, dev).view(m, HK, D)
+                    cache.append(l, 0, p0, k, k)
+            q = torch.randn(L, 1, H, D, device=dev)
+            kn = torch.randn(L, 1, HK, D, device=dev) * 0.5
+            o = torch.empty_like(q)
+            pos = n - 1
+
+            def step():
+                nonlocal pos
+                for l in range(L):
+                    cache.append(l, 0, pos, kn[l], kn[l])
+                    cache.attn_decode(l, [0], q[l], o[l], scale)
+                pos += 1
+
+            for name, depth, budget in cells:
+                kvc.kvc_pipeline_depth(cache.ctx, depth)
+                kvc.kvc_pipeline_budget(cache.ctx, budget)
+                step()
+                torch.cuda.synchronize()
+                kvc.kvc_trace_start(cache.ctx, 16 * L)
+                for _ in range(3):
+                    step()
+                torch.cuda.synchronize()
+                kvc.kvc_trace_stop(cache.ctx)
+                st = cache.stats()
+                summ = timeline_summary(kvc.kvc_trace_read(cache.ctx), L)
+                summ.update({"ring_engaged": st["ring_engaged"], "rolling": st["rolling"],
+                             "tile_rows": st["tile_rows"]})
+                if "h2d_gbs_over_step" in summ:
+                    summ["frac_of_link"] = round(summ["h2d_gbs_over_step"] / out["link_gbs"], 3)
+                out["%dk_%s" % (n // 1024, name)] = summ
+        finally:
+            cache.close()
+        torch.cuda.empty_cache()
+    out["note"] = ("CUDA-event trace of the middle of three decode steps: deliveries are the H2D copies of "
+                   "one layer (or rolling tile), attention the launches on the compute stream after their "
+                   "wait; copy_hidden_frac = share of copy time overlapped by attention, attn_hidden_frac = share "
+                   "of attention time overlapped by copies")
+    return out
+
+
 # ------------------------------------------------------- further rows --
 def attn_only_gbs(kvc, torch, dev, type_: str, n: int, reps: int = 50):
     """KV GB/s of back-to-back attention launches, one per layer, over enough
@@ -668,7 +781,7 @@ def step_line(args, world: int, L: int, n: int, t_step: float, t_attn: float, t_
 
 
 EXTRA_ROWS = ("q8_0_4k", "q8_0_64k", "q8_0_256k", "f16_16k", "f16_4k", "q8_0_q4_0_16k", "q8_0_q4_0_64k",
-              "ragged_q8_0", "ragged_f16", "churn", "keydiff", "split_32k_g4", "cold_store")
+              "ragged_q8_0", "ragged_f16", "churn", "keydiff", "split_32k_g4", "cold_store", "host_timeline")
 
 
 def run_child(args, name: str) -> dict:
@@ -725,6 +838,7 @@ def child_phase(args) -> dict:
         "keydiff": lambda: keydiff(kvc, torch, dev, args.churn_n, args.layers),
         "split_32k_g4": lambda: host_pipeline(args, dev, torch, kvc, 32768, SPLIT_CELLS, gpu_heads=4),
         "cold_store": lambda: cold_store(kvc, torch, dev, args.churn_n, args.layers),
+        "host_timeline": lambda: host_timeline(args, dev, torch, kvc),
     }
     return rows[name]()
 
@@ -849,10 +963,50 @@ def run_ours(args, rank: int, world: int):
             e2e_step()
     t_e2e = timed(e2e_step, args.steps)
 
-    t_step, t_attn, t_e2e, t_two = max_over_ranks([t_step, t_attn, t_e2e, t_two], dev, world)
+    # End to end without a graph: every step issues the 64 kvc_decode_step calls from the
+    # host through the C entry point (arguments built once, so the binding adds little),
+    # with the same pinned copies.  The sequence grows by one row per step, as in decode.
+    import ctypes as C
+
+    f_step = kvc.load().kvc_decode_step
+    ids = (C.c_int32 * 1)(0)
+    pos = (C.c_int32 * 1)(n)
+    largs = [(cache.ctx, l, 1, ids, pos, kbuf[l].data_ptr(), vbuf[l].data_ptr(), qbuf[l].data_ptr(),
+              obuf[l].data_ptr(), scale, s.cuda_stream) for l in range(L)]
+    eager_steps = min(args.steps, 100)
+    host_issue = [0.0]
+
+    def eager_step():
+        inbuf.copy_(hin, non_blocking=True)
+        h0 = time.perf_counter()
+        for a_ in largs:
+            rc_ = f_step(*a_)
+            if rc_ != 0:
+                raise RuntimeError("kvc_decode_step: %d" % rc_)
+        host_issue[0] += time.perf_counter() - h0
+        pos[0] += 1
+        ho.copy_(obuf, non_blocking=True)
+
+    for _ in range(3):
+        with torch.cuda.stream(s):
+            eager_step()
+    host_issue[0] = 0.0
+    n_eager0 = pos[0]
+    t_eager = timed(eager_step, eager_steps)
+    eager_rows = (n_eager0 + pos[0] - 1) / 2.0  # mean rows attended per step
+
+    t_step, t_attn, t_e2e, t_two, t_eager = max_over_ranks([t_step, t_attn, t_e2e, t_two, t_eager], dev, world)
 
     out = step_line(args, world, L, n, t_step, t_attn, t_e2e, t_two, int(hin.numel() * 4), int(ho.numel() * 4),
                     clk)
+    out["e2e_eager"] = {
+        "value": round(world * L * eager_rows * kv_bytes_per_row(args.type) * eager_steps / t_eager / GB, 2),
+        "unit": "GB/s", "ms_per_step": round(1000 * t_eager / eager_steps, 4), "steps": eager_steps,
+        "host_us_per_call": round(1e6 * host_issue[0] / (eager_steps * L), 2),
+        "h2d_bytes_per_step": int(hin.numel() * 4), "d2h_bytes_per_step": int(ho.numel() * 4),
+        "note": "no CUDA graph: 64 kvc_decode_step calls per step issued from the host through the C "
+                "entry point, each step appending the next position; host_us_per_call is the host time "
+                "of one call (argument checks, planning, launch)"}
     cache.close()
     del cache
     torch.cuda.empty_cache()
@@ -861,6 +1015,17 @@ def run_ours(args, rank: int, world: int):
         # that a failing phase is reported as that phase's error and the line above stands.
         if args.host_n > 0:
             out["host"] = run_child(args, "host")
+            h = out["host"]
+            if isinstance(h, dict) and "pipelined" in h and "ordered" in h:
+                # the metric's second half, near the front of the line
+                summary = {"n_kv": h.get("n_kv"), "link_gbs": h.get("link_gbs"),
+                           "pipelined_steps_per_s": h["pipelined"]["steps_per_s"],
+                           "pipelined_frac_of_link": h["pipelined"]["frac_of_link"],
+                           "ordered_steps_per_s": h["ordered"]["steps_per_s"],
+                           "ordered_frac_of_link": h["ordered"]["frac_of_link"]}
+                keys = list(out.keys())
+                at = keys.index("unit") + 1
+                out = {**{k: out[k] for k in keys[:at]}, "host_32k": summary, **{k: out[k] for k in keys[at:]}}
         if args.host_matrix:
             out["host_matrix"] = run_child(args, "host_matrix")
         if not args.no_extra:

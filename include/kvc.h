@@ -347,6 +347,31 @@ int kvc_set_timeout_ms(kvc_ctx *c, int ms);
  * succeed and the ones after fail with KVC_ENOMEM; n < 0 disables it. */
 int kvc_debug_fail_alloc_after(kvc_ctx *c, int n);
 
+/* Timeline of the host-resident transport, for measuring it (the pages show
+ * the pipeline's engagement by a scheduler dump; [R4] section Measurements).
+ * While tracing is on, a host-resident or split context records a timed CUDA
+ * event pair around every delivery (the copies of one layer or tile, on the
+ * stream that runs them: the transfer stream when pipelined, the caller's
+ * stream when ordered) and around every attention launch of the transport
+ * (on the caller's stream, after it has waited for the delivery).
+ * kvc_trace_start: clear the records and trace the next max_records
+ * (1 .. 65536) deliveries and launches; creates 2 * max_records events (kept
+ * until kvc_destroy).  kvc_trace_stop: stop recording.  kvc_trace_read: wait
+ * (bounded) for the recorded events, then write up to cap records into out
+ * (HOST), times in microseconds from the first record's start; *n receives
+ * the number recorded.  Errors: KVC_EINVAL (a device-resident context, bad
+ * arguments), KVC_ETIMEDOUT, KVC_ECUDA. */
+typedef struct kvc_trace_event {
+    int32_t kind;  /* 0 delivery (host -> device copies), 1 attention launch */
+    int32_t layer;
+    int64_t bytes; /* delivery: bytes copied; attention: K/V bytes of the rows attended */
+    double t0_us;  /* start (after the waits that precede it on its stream) */
+    double t1_us;  /* end */
+} kvc_trace_event;
+int kvc_trace_start(kvc_ctx *c, int max_records);
+int kvc_trace_stop(kvc_ctx *c);
+int kvc_trace_read(kvc_ctx *c, kvc_trace_event *out, int cap, int *n);
+
 /* Read and clear the device error word that kernels set instead of
  * trapping (a bounded wait that gave up, an index out of range).
  * *word receives it (0 = none).  Waits for the context's device work. */

@@ -379,6 +379,8 @@ void kvc_destroy(kvc_ctx *cc) {
     if (c->st_copy) cudaStreamDestroy(c->st_copy);
     for (auto ev : c->st_ev)
         if (ev) cudaEventDestroy(ev);
+    for (auto ev : c->trace.pool)
+        if (ev) cudaEventDestroy(ev);
     delete c;
 }
 

@@ -61,6 +61,21 @@ struct Transport {
     std::vector<int64_t> app_waited; // per layer: append generation the transfer stream has waited for
 };
 
+// Optional timeline of the host transport (kvc_trace_*): a timed event pair
+// around every delivery, on the stream that copies, and around every
+// attention launch, on the caller's stream, while tracing is on.
+struct TraceRec {
+    int32_t kind; // 0 delivery, 1 attention
+    int32_t layer;
+    int64_t bytes;
+};
+struct Trace {
+    bool on = false;
+    int cap = 0;                    // records the event pool holds
+    std::vector<cudaEvent_t> pool;  // 2 timed events per record
+    std::vector<TraceRec> recs;
+};
+
 struct Ctx {
     kvc_params prm;
     std::string err;
@@ -101,6 +116,7 @@ struct Ctx {
     uint8_t *hk_d = nullptr, *hv_d = nullptr, *hks_d = nullptr, *hvs_d = nullptr; // device aliases
     int64_t host_bytes = 0;
     Transport tr;
+    Trace trace;
     std::vector<cudaEvent_t> app_ev; // per layer: recorded after each append (orders early deliveries)
     std::vector<int64_t> app_gen;    // per layer: appends recorded into app_ev
     int32_t *zero_pt = nullptr;      // device page table {0} used for slots

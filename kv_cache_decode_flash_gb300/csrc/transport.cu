@@ -26,7 +26,9 @@
 #include "ctx.h"
 
 #include <algorithm>
+#include <chrono>
 #include <cstring>
+#include <thread>
 
 namespace kvc {
 
@@ -342,6 +344,33 @@ static int plan(Ctx *c, int64_t n, cudaStream_t st, bool *engaged) {
     return KVC_OK;
 }
 
+// ------------------------------------------------------------- tracing ----
+
+// Start a trace record on stream `st` (-1 when tracing is off or full).
+static int trace_begin(Ctx *c, int kind, int layer, cudaStream_t st) {
+    Trace &t = c->trace;
+    if (!t.on || (int)t.recs.size() >= t.cap) return -1;
+    const int i = (int)t.recs.size();
+    if (cudaEventRecord(t.pool[2 * (size_t)i], st) != cudaSuccess) {
+        cudaGetLastError();
+        t.on = false;
+        return -1;
+    }
+    t.recs.push_back(TraceRec{kind, layer, 0});
+    return i;
+}
+
+static void trace_end(Ctx *c, int i, int64_t bytes, cudaStream_t st) {
+    Trace &t = c->trace;
+    if (i < 0) return;
+    t.recs[(size_t)i].bytes = bytes;
+    if (cudaEventRecord(t.pool[2 * (size_t)i + 1], st) != cudaSuccess) {
+        cudaGetLastError();
+        t.recs.resize((size_t)i); // drop the unfinished record
+        t.on = false;
+    }
+}
+
 // Issue H2D copies of rows [r0, r0 + rows) of `layer` from the host store
 // into slot s (slot row 0 = layer row r0), after the slot's previous delivery
 // and its previous reader.
@@ -355,13 +384,17 @@ static int deliver_range(Ctx *c, Slot &s, int layer, int32_t r0, int32_t rows, i
         int rowb;
     } parts[4] = {{c->hk, s.kdata, c->krow}, {c->hv, s.vdata, c->vrow}, {c->hks, s.kscales, c->ksb},
                   {c->hvs, s.vscales, c->vsb}};
+    const int ti = trace_begin(c, 0, layer, x);
+    int64_t moved = 0;
     for (auto &pt : parts) {
         if (!pt.rowb || rows == 0) continue;
         const uint8_t *src = pt.host + ((int64_t)layer * c->Hk * hcap + r0) * pt.rowb;
         KVC_CU(c, cudaMemcpy2DAsync(pt.dev, (size_t)s.cap * pt.rowb, src, (size_t)hcap * pt.rowb,
                                     (size_t)rows * pt.rowb, (size_t)c->Hk, cudaMemcpyHostToDevice, x));
-        c->tr.bytes += (int64_t)rows * pt.rowb * c->Hk;
+        moved += (int64_t)rows * pt.rowb * c->Hk;
     }
+    c->tr.bytes += moved;
+    trace_end(c, ti, moved, x);
     s.layer = layer;
     s.r0 = r0;
     s.rows = rows;
@@ -547,8 +580,10 @@ static int rolling_attn(Ctx *c, int layer, const float *q, float *out, float kq_
         a.part_first = 0;
         a.pt_len = 1;
         p.total_chunks = (n + C - 1) / C;
+        const int ti = trace_begin(c, 1, layer, st);
         cudaError_t e = launch_attn(c->tk, c->tv, p, s->tmk, s->tmv, st, false, pl.cfg);
         if (e != cudaSuccess) return cuda_fail(c, e, "attention kernel");
+        trace_end(c, ti, (int64_t)n * row_bytes_all(c), st);
         KVC_CU(c, cudaEventRecord(s->release, st));
         s->consumed_once = true;
         // look-ahead: the next tile(s), on into the following layers
@@ -608,9 +643,11 @@ int transport_attn(Ctx *c, int layer, const float *q, float *out, float kq_scale
     a.n_rows = rows;
     a.out_row = 0;
     a.stable_rows = std::max(0, rows - c->recent[0][(size_t)layer]);
+    const int ti = trace_begin(c, 1, layer, st);
     rc = launch_attention(c, lv, s->tmk, s->tmv, s->cap, s->scale_bytes, 1, &a, q, out, kq_scale, st, nullptr,
                           nullptr);
     if (rc) return rc;
+    trace_end(c, ti, (int64_t)rows * row_bytes_all(c), st);
     c->clear_recent();
     if (engaged) {
         KVC_CU(c, cudaEventRecord(s->release, st));
@@ -624,3 +661,73 @@ int transport_attn(Ctx *c, int layer, const float *q, float *out, float kq_scale
 }
 
 } // namespace kvc
+
+// ------------------------------------------------------------- tracing API --
+using namespace kvc;
+
+static Ctx *trace_ctx(kvc_ctx *cc) {
+    Ctx *c = reinterpret_cast<Ctx *>(cc);
+    if (!c) return nullptr;
+    if (c->split) return c->part_host; // the transport belongs to the host half
+    return c->host ? c : nullptr;
+}
+
+extern "C" int kvc_trace_start(kvc_ctx *cc, int max_records) {
+    Ctx *c = trace_ctx(cc);
+    if (!c) return cc ? reinterpret_cast<Ctx *>(cc)->fail(KVC_EINVAL, "tracing needs a host-resident or split context")
+                      : KVC_EINVAL;
+    if (max_records < 1 || max_records > (1 << 16)) return c->fail(KVC_EINVAL, "max_records must be in [1, 65536]");
+    KVC_CU(c, cudaSetDevice(c->dev));
+    Trace &t = c->trace;
+    while ((int)t.pool.size() < 2 * max_records) {
+        cudaEvent_t e;
+        KVC_CU(c, cudaEventCreate(&e));
+        t.pool.push_back(e);
+    }
+    t.cap = max_records;
+    t.recs.clear();
+    t.on = true;
+    return KVC_OK;
+}
+
+extern "C" int kvc_trace_stop(kvc_ctx *cc) {
+    Ctx *c = trace_ctx(cc);
+    if (!c) return KVC_EINVAL;
+    c->trace.on = false;
+    return KVC_OK;
+}
+
+extern "C" int kvc_trace_read(kvc_ctx *cc, kvc_trace_event *out, int cap, int *n) {
+    Ctx *c = trace_ctx(cc);
+    if (!c) return KVC_EINVAL;
+    if (!n || cap < 0 || (cap > 0 && !out)) return c->fail(KVC_EINVAL, "bad output arguments");
+    Trace &t = c->trace;
+    *n = (int)t.recs.size();
+    if (t.recs.empty() || cap == 0) return KVC_OK;
+    KVC_CU(c, cudaSetDevice(c->dev));
+    // every recorded event must have completed (bounded host wait)
+    const size_t last = 2 * t.recs.size();
+    for (size_t i = 0; i < last; ++i) {
+        const auto t0 = std::chrono::steady_clock::now();
+        for (;;) {
+            const cudaError_t q = cudaEventQuery(t.pool[i]);
+            if (q == cudaSuccess) break;
+            if (q != cudaErrorNotReady) return cuda_fail(c, q, "trace event");
+            if (std::chrono::steady_clock::now() - t0 > std::chrono::milliseconds(c->timeout_ms))
+                return c->fail(KVC_ETIMEDOUT, "trace events did not complete");
+            std::this_thread::sleep_for(std::chrono::microseconds(50));
+        }
+    }
+    const int m = std::min(cap, (int)t.recs.size());
+    for (int i = 0; i < m; ++i) {
+        float a = 0.f, b = 0.f;
+        KVC_CU(c, cudaEventElapsedTime(&a, t.pool[0], t.pool[2 * (size_t)i]));
+        KVC_CU(c, cudaEventElapsedTime(&b, t.pool[0], t.pool[2 * (size_t)i + 1]));
+        out[i].kind = t.recs[(size_t)i].kind;
+        out[i].layer = t.recs[(size_t)i].layer;
+        out[i].bytes = t.recs[(size_t)i].bytes;
+        out[i].t0_us = 1000.0 * a;
+        out[i].t1_us = 1000.0 * b;
+    }
+    return KVC_OK;
+}

@@ -90,6 +90,9 @@ def load():
         "kvc_seq_positions": (i32, [p, i32, p, C.c_int32, C.POINTER(C.c_int32)]),
         "kvc_get_stats": (i32, [p, C.POINTER(kvc_stats)]),
         "kvc_set_chunk_rows": (i32, [p, i32]),
+        "kvc_trace_start": (i32, [p, i32]),
+        "kvc_trace_stop": (i32, [p]),
+        "kvc_trace_read": (i32, [p, p, i32, C.POINTER(C.c_int)]),
         "kvc_debug_chunk_plan": (i32, [i32, i32, i32, i32, i32, i32, i32, i32, p, C.POINTER(C.c_int32),
                                        C.POINTER(C.c_int32)]),
         "kvc_set_timeout_ms": (i32, [p, i32]),
@@ -183,6 +186,29 @@ def kvc_decode_step(ctx, layer, seq_ids, pos, k, v, q, out, kq_scale, stream=Non
     ps = (C.c_int32 * len(pos))(*[int(x) for x in pos])
     _check(ctx, load().kvc_decode_step(ctx, layer, len(seq_ids), ids, ps, _addr(k), _addr(v), _addr(q), _addr(out),
                                        float(kq_scale), _stream(stream, device)))
+
+
+class kvc_trace_event(C.Structure):
+    _fields_ = [("kind", C.c_int32), ("layer", C.c_int32), ("bytes", C.c_int64), ("t0_us", C.c_double),
+                ("t1_us", C.c_double)]
+
+
+def kvc_trace_start(ctx, max_records: int):
+    _check(ctx, load().kvc_trace_start(ctx, int(max_records)))
+
+
+def kvc_trace_stop(ctx):
+    _check(ctx, load().kvc_trace_stop(ctx))
+
+
+def kvc_trace_read(ctx) -> list:
+    """[(kind, layer, bytes, t0_us, t1_us)] of the host transport's recorded
+    deliveries (kind 0) and attention launches (kind 1)."""
+    n = C.c_int(0)
+    _check(ctx, load().kvc_trace_read(ctx, None, 0, C.byref(n)))
+    buf = (kvc_trace_event * max(1, n.value))()
+    _check(ctx, load().kvc_trace_read(ctx, buf, n.value, C.byref(n)))
+    return [(e.kind, e.layer, e.bytes, e.t0_us, e.t1_us) for e in buf[: n.value]]
 
 
 def kvc_seq_rm(ctx, seq, p0, p1):

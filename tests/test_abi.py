@@ -42,7 +42,9 @@ def test_params_init_and_status_strings():
 def test_create_rejects_bad_geometry_without_touching_a_gpu():
     from kv_cache_decode_flash_gb300 import kvc
 
-    for field, val in (("head_dim", 96), ("n_head", 7), ("page_rows", 20), ("type_k", 3)):
+    # q4_0 is a V type (with q8_0 K and head_dim 128; the default head_dim is 64)
+    for field, val in (("head_dim", 96), ("n_head", 7), ("page_rows", 20), ("type_k", 3), ("type_k", 2),
+                       ("type_v", 2)):
         p = kvc.kvc_params_init()
         setattr(p, field, val)
         with pytest.raises(kvc.KvcError) as e:

@@ -47,3 +47,32 @@ def test_value_is_whole_job_over_ranks():
     two = bench.step_line(a, 2, 64, 16384, 0.45, 0.448, 0.47, 0.52, 1, 1, {})
     assert abs(two["value"] - 2 * one["value"]) < 0.02 and two["n_gpus"] == 2
     assert abs(two["hbm_frac"] - one["hbm_frac"]) < 1e-4  # per-GPU fraction
+
+
+def test_timeline_summary_of_a_constructed_trace():
+    # two layers, three steps; each layer: a 1 MB delivery of 10 us, then a 5 us attention that
+    # overlaps the next layer's delivery by 2 us
+    recs, t = [], 0.0
+    for _ in range(3):
+        for l in range(2):
+            recs.append((0, l, 1_000_000, t, t + 10.0))
+            recs.append((1, l, 0, t + 10.0, t + 15.0))
+            t += 13.0
+    s = bench.timeline_summary(recs, 2)
+    assert s["step_ms"] == 0.026 and s["deliveries"] == 2
+    assert s["per_delivery_gbs_p10_p50_p90"] == [100.0, 100.0, 100.0]
+    # per step (26 us): copies busy 20 us, attention 10 us, 2 x 2 us of copy hidden
+    assert s["copy_busy_frac"] == round(20 / 26, 3) and s["attn_busy_frac"] == round(10 / 26, 3)
+    assert s["copy_hidden_frac"] == round(4 / 20, 3) and s["attn_hidden_frac"] == round(4 / 10, 3)
+    assert s["launches_per_step"] == 2
+    assert "error" in bench.timeline_summary(recs[:4], 2)
+    # rolling tiles: two attention launches per layer, the step found from the launch count
+    recs2, t = [], 0.0
+    for _ in range(3):
+        for l in range(2):
+            for _tile in range(2):
+                recs2.append((0, l, 500_000, t, t + 5.0))
+                recs2.append((1, l, 0, t + 5.0, t + 7.0))
+                t += 7.0
+    s2 = bench.timeline_summary(recs2, 2)
+    assert s2["launches_per_step"] == 4 and s2["step_ms"] == 0.028 and s2["deliveries"] == 4

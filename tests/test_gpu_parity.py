@@ -694,3 +694,36 @@ def test_evict_window_matches_oracle(type_):
         assert tw.gpu.n_tokens(0) == n - 64
     finally:
         tw.close()
+
+
+def test_host_transport_trace_records_deliveries_and_launches():
+    from kv_cache_decode_flash_gb300 import kvc
+
+    n, L = 2000, 3
+    tw = Twin(L, 8, 2, 128, n + 64, type_=Q8, residency=kvc.KVC_HOST_PINNED)
+    try:
+        tw.fill(0, n, seed=41)
+        with pytest.raises(kvc.KvcError):
+            dev_ctx = kvc.KVCache(1, 8, 2, 128, 64, 1, Q8, Q8)
+            try:
+                kvc.kvc_trace_start(dev_ctx.ctx, 8)  # device-resident: nothing to trace
+            finally:
+                dev_ctx.close()
+        q = q_inputs(41, 0, 1, 8, 128)
+        for depth in (0, 1):
+            kvc.kvc_pipeline_depth(tw.gpu.ctx, depth)
+            kvc.kvc_pipeline_budget(tw.gpu.ctx, 512 << 20)
+            kvc.kvc_trace_start(tw.gpu.ctx, 64)
+            for l in range(L):
+                got, want = tw.attn(l, [0], q, 0.088)
+                assert_attn_close(got, want, "traced layer %d" % l)
+            kvc.kvc_trace_stop(tw.gpu.ctx)
+            recs = kvc.kvc_trace_read(tw.gpu.ctx)
+            att = [r for r in recs if r[0] == 1]
+            dlv = [r for r in recs if r[0] == 0]
+            assert [r[1] for r in att] == list(range(L))
+            assert len(dlv) >= 1 and all(r[4] >= r[3] >= 0 for r in recs)
+            row_bytes = 2 * 2 * (128 + 8)  # K and V of 2 KV heads, codes and scales
+            assert all(r[2] == n * row_bytes for r in dlv)  # every delivery carries the layer's n rows
+    finally:
+        tw.close()
