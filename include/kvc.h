@@ -339,6 +339,14 @@ int kvc_set_chunk_rows(kvc_ctx *c, int rows);
 int kvc_debug_chunk_plan(int type, int head_dim, int n_head, int n_head_kv, int sms, int occ, int occ2,
                          int n_seq, const int32_t *rows, int32_t *chunk_rows, int32_t *cfg);
 
+/* Test hook, no context and no GPU needed: the same plan with each
+ * sequence's own rows per chunk.  A batch (n_seq > 1) of a cache whose K and
+ * V types are equal cuts every sequence into equal chunks, their length
+ * chosen over whole waves of chunks; a single sequence has the one length of
+ * kvc_debug_chunk_plan.  chunk_rows_seq: HOST int32[n_seq].  Errors: KVC_EINVAL. */
+int kvc_debug_chunk_plan_seq(int type, int head_dim, int n_head, int n_head_kv, int sms, int occ, int occ2,
+                             int n_seq, const int32_t *rows, int32_t *chunk_rows_seq, int32_t *cfg);
+
 /* Limit, in milliseconds, of every bounded host wait of the synchronous
  * operations (default 120000).  A wait that runs out returns KVC_ETIMEDOUT. */
 int kvc_set_timeout_ms(kvc_ctx *c, int ms);

@@ -298,7 +298,9 @@ struct TileInfo {
     int delta; // scale rows skipped by the 16-byte alignment of the scale copy
 };
 
-template <int TYPE, int D, int R, bool RAW = false, int CFG = 0, bool V4 = false>
+// BATCH: every sequence has its own chunk length (AttnSeq.chunk_rows); the
+// other instances read the launch's one (AttnParams.chunk_rows).
+template <int TYPE, int D, int R, bool RAW = false, int CFG = 0, bool V4 = false, bool BATCH = false>
 __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG, V4>::NTHREADS, Shape<TYPE, D, R, CFG, V4>::MINB)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmk,
                 const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmkb,
@@ -334,8 +336,9 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG, V4>::NTHREADS, Shape<TY
     const AttnSeq sq = p.seq[si];
     const int lc = chunk - sq.chunk0;
     const int r_act = p.r;
-    const int row_begin = lc * p.chunk_rows;
-    const int row_end = min(sq.n_rows, row_begin + p.chunk_rows);
+    const int crows = BATCH ? sq.chunk_rows : p.chunk_rows;
+    const int row_begin = lc * crows;
+    const int row_end = min(sq.n_rows, row_begin + crows);
     // fused quantise-on-append: this CTA's chunk holds the row it stores before reading it
     const bool app = p.app_k != nullptr && sq.app_row >= row_begin && sq.app_row < row_end;
 
@@ -988,7 +991,7 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG, V4>::NTHREADS, Shape<TY
     }
 }
 
-template <int TYPE, int D, int R, bool RAW = false, int CFG = 0, bool V4 = false>
+template <int TYPE, int D, int R, bool RAW = false, int CFG = 0, bool V4 = false, bool BATCH = false>
 cudaError_t launch_t(const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv, cudaStream_t st) {
     // tmk / tmv point at {16-row map, 128-row map} pairs
     using S = Shape<TYPE, D, R, CFG, V4>;
@@ -1000,7 +1003,7 @@ cudaError_t launch_t(const AttnParams &p, const CUtensorMap *tmk, const CUtensor
     if (e != cudaSuccess) return e;
     const uint64_t ctx = current_context_id();
     if (dev < 0 || dev >= MAX_DEVICES || ctx == 0 || configured[dev] != ctx) {
-        e = cudaFuncSetAttribute(attn_kernel<TYPE, D, R, RAW, CFG, V4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(attn_kernel<TYPE, D, R, RAW, CFG, V4, BATCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  S::SMEM);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < MAX_DEVICES) configured[dev] = ctx;
@@ -1015,7 +1018,7 @@ cudaError_t launch_t(const AttnParams &p, const CUtensorMap *tmk, const CUtensor
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_kernel<TYPE, D, R, RAW, CFG, V4>, p, tmk[0], tmv[0], tmk[1], tmv[1]);
+    return cudaLaunchKernelEx(&cfg, attn_kernel<TYPE, D, R, RAW, CFG, V4, BATCH>, p, tmk[0], tmv[0], tmk[1], tmv[1]);
 }
 
 template <int TYPE, int D>
@@ -1029,6 +1032,22 @@ cudaError_t launch_d(const AttnParams &p, const CUtensorMap *tmk, const CUtensor
             if (p.r == 5) return launch_t<TYPE, D, 5, false, 0, true>(p, tmk, tmv, st);
             if (p.r <= 8) return launch_t<TYPE, D, 8, false, 0, true>(p, tmk, tmv, st);
         }
+        return cudaErrorInvalidValue;
+    }
+    if (p.n_seq > 1) {
+        // a batch: per-sequence chunk lengths (symmetric types; plain launch configurations)
+        if (raw) return cudaErrorInvalidValue;
+        if constexpr (TYPE == KVC_Q8_0) {
+            if (cfg == 1) {
+                if (p.r <= 4) return launch_t<TYPE, D, 4, false, 1, false, true>(p, tmk, tmv, st);
+                if (p.r == 5) return launch_t<TYPE, D, 5, false, 1, false, true>(p, tmk, tmv, st);
+                if (p.r <= 8) return launch_t<TYPE, D, 8, false, 1, false, true>(p, tmk, tmv, st);
+                return cudaErrorInvalidValue;
+            }
+        }
+        if (p.r <= 4) return launch_t<TYPE, D, 4, false, 0, false, true>(p, tmk, tmv, st);
+        if (p.r == 5) return launch_t<TYPE, D, 5, false, 0, false, true>(p, tmk, tmv, st);
+        if (p.r <= 8) return launch_t<TYPE, D, 8, false, 0, false, true>(p, tmk, tmv, st);
         return cudaErrorInvalidValue;
     }
     // plain int8 codes (caller buffers): one instance for every group size up to 8

@@ -60,6 +60,7 @@ struct AttnSeq {
                                // ticket counting all of them
     int32_t pt_len;            // entries of page_table
     int32_t app_row;           // row this launch quantises and stores itself (fused append), or -1
+    int32_t chunk_rows;        // rows per chunk of this sequence (launches of more than one sequence)
 };
 
 struct AttnParams {

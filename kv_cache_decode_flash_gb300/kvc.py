@@ -95,6 +95,7 @@ def load():
         "kvc_trace_read": (i32, [p, p, i32, C.POINTER(C.c_int)]),
         "kvc_debug_chunk_plan": (i32, [i32, i32, i32, i32, i32, i32, i32, i32, p, C.POINTER(C.c_int32),
                                        C.POINTER(C.c_int32)]),
+        "kvc_debug_chunk_plan_seq": (i32, [i32, i32, i32, i32, i32, i32, i32, i32, p, p, C.POINTER(C.c_int32)]),
         "kvc_set_timeout_ms": (i32, [p, i32]),
         "kvc_debug_fail_alloc_after": (i32, [p, i32]),
         "kvc_check_device_error": (i32, [p, C.POINTER(C.c_uint32)]),
@@ -337,6 +338,19 @@ def kvc_debug_chunk_plan(type_, head_dim, n_head, n_head_kv, sms, occ, occ2, row
     if st != KVC_OK:
         raise KvcError(st, "bad chunk-plan arguments")
     return cr.value, cfg.value
+
+
+def kvc_debug_chunk_plan_seq(type_, head_dim, n_head, n_head_kv, sms, occ, occ2, rows):
+    """Each sequence's rows per chunk and the configuration of an attention
+    launch over sequences of `rows` rows, without a context or a GPU."""
+    arr = (C.c_int32 * len(rows))(*[int(r) for r in rows])
+    out = (C.c_int32 * len(rows))()
+    cfg = C.c_int32()
+    st = load().kvc_debug_chunk_plan_seq(type_, head_dim, n_head, n_head_kv, sms, occ, occ2, len(rows), arr, out,
+                                         C.byref(cfg))
+    if st != KVC_OK:
+        raise KvcError(st, "bad chunk-plan arguments")
+    return list(out), cfg.value
 
 
 def kvc_debug_fail_alloc_after(ctx, n):
