@@ -466,6 +466,22 @@ def timeline_summary(recs, L):
             "compute_idle_ms": round((win - busy) / 1e3, 3)}
 
 
+def link_series(torch, dev, n: int = 60, size: int = 64 << 20) -> list:
+    """min, p10 and p50 GB/s of n back-to-back pinned host -> device copies of
+    `size` bytes, each timed by its own CUDA events (the link on its own)."""
+    h = torch.empty(size, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(size, dtype=torch.uint8, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    d.copy_(h, non_blocking=True)
+    ev[0].record()
+    for i in range(n):
+        d.copy_(h, non_blocking=True)
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    r = sorted(size / (ev[i].elapsed_time(ev[i + 1]) * 1e-3) / GB for i in range(n))
+    return [round(r[0], 1), round(r[n // 10], 1), round(r[n // 2], 1)]
+
+
 def host_timeline(args, dev, torch, kvc) -> dict:
     """Per-delivery timeline of the host transport (kvc_trace_*): for each
     context length and (depth, budget) cell, one warm-up step, then three
@@ -500,7 +516,8 @@ def host_timeline(args, dev, torch, kvc) -> dict:
                 kvc.kvc_pipeline_budget(cache.ctx, budget)
                 step()
                 torch.cuda.synchronize()
-                kvc.kvc_trace_start(cache.ctx, 16 * L)
+                probe_before = link_series(torch, dev)
+                kvc.kvc_trace_start(cache.ctx, 64 * L)
                 for _ in range(3):
                     step()
                 torch.cuda.synchronize()
@@ -508,7 +525,9 @@ def host_timeline(args, dev, torch, kvc) -> dict:
                 st = cache.stats()
                 summ = timeline_summary(kvc.kvc_trace_read(cache.ctx), L)
                 summ.update({"ring_engaged": st["ring_engaged"], "rolling": st["rolling"],
-                             "tile_rows": st["tile_rows"]})
+                             "tile_rows": st["tile_rows"],
+                             "plain_copies_gbs_min_p10_p50": [probe_before[0], probe_before[1], probe_before[2],
+                                                              "before"] + link_series(torch, dev) + ["after"]})
                 if "h2d_gbs_over_step" in summ:
                     summ["frac_of_link"] = round(summ["h2d_gbs_over_step"] / out["link_gbs"], 3)
                 out["%dk_%s" % (n // 1024, name)] = summ
@@ -518,7 +537,8 @@ def host_timeline(args, dev, torch, kvc) -> dict:
     out["note"] = ("CUDA-event trace of the middle of three decode steps: deliveries are the H2D copies of "
                    "one layer (or rolling tile), attention the launches on the compute stream after their "
                    "wait; copy_hidden_frac = share of copy time overlapped by attention, attn_hidden_frac = share "
-                   "of attention time overlapped by copies")
+                   "of attention time overlapped by copies; plain_copies: 60 back-to-back 64 MiB pinned H2D "
+                   "copies just before and after the cell, each timed alone")
     return out
 
 

@@ -84,17 +84,28 @@ struct RopeArgs {
     float2 cs[64]; // (cos, sin) of delta * theta_i, i < D/2
 };
 
-__device__ __forceinline__ float code_at(const uint4 &w, int i) { // code i of 16 stored offset binary
+// Code i of 16 stored offset-binary bytes, as an exact float: the byte goes
+// into the low mantissa bits of 2^23 (0x4B0000uu = 2^23 + u), and 2^23 + 128
+// is subtracted.
+__device__ __forceinline__ float code_at(const uint4 &w, int i) {
     const uint32_t u = i < 4 ? w.x : i < 8 ? w.y : i < 12 ? w.z : w.w;
-    return (float)((int)((u >> (8 * (i & 3))) & 255u) - 128);
+    uint32_t f;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(f) : "r"(u), "r"(0x4B000000u), "r"(0x7440u | (uint32_t)(i & 3)));
+    return __fsub_rn(__uint_as_float(f), 8388736.0f);
 }
-__device__ __forceinline__ uint4 pack16(const int (&c)[16]) {
-    uint32_t u[4];
+// 16 rounded codes (integral floats in [-127, 127]) -> 16 offset-binary bytes:
+// c + 2^23 + 128 is exact and its low byte is c + 128; PRMTs gather the bytes.
+__device__ __forceinline__ uint4 pack16(const float (&c)[16]) {
+    uint32_t b[16], u[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        u[j] = ((uint32_t)(c[4 * j] & 255) | ((uint32_t)(c[4 * j + 1] & 255) << 8) |
-                ((uint32_t)(c[4 * j + 2] & 255) << 16) | ((uint32_t)(c[4 * j + 3] & 255) << 24)) ^
-               CODE_FLIP; // stored offset binary
+    for (int i = 0; i < 16; ++i) b[i] = __float_as_uint(__fadd_rn(c[i], 8388736.0f));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t lo, hi;
+        asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(lo) : "r"(b[4 * j]), "r"(b[4 * j + 1]));
+        asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(hi) : "r"(b[4 * j + 2]), "r"(b[4 * j + 3]));
+        asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(u[j]) : "r"(lo), "r"(hi));
+    }
     return make_uint4(u[0], u[1], u[2], u[3]);
 }
 
@@ -189,11 +200,11 @@ __global__ void __launch_bounds__(256, 4) rope_shift_kernel(const __grid_constan
             const float iA = (dA != 0.0f) ? __fdiv_rn(1.0f, dA) : 0.0f;
             const float iB = (dB != 0.0f) ? __fdiv_rn(1.0f, dB) : 0.0f;
             if (live) {
-                int qa[16], qb[16];
+                float qa[16], qb[16];
 #pragma unroll
                 for (int i = 0; i < V; ++i) {
-                    qa[i] = (int)roundf(__fmul_rn(ya[i], iA));
-                    qb[i] = (int)roundf(__fmul_rn(yb[i], iB));
+                    qa[i] = roundf(__fmul_rn(ya[i], iA));
+                    qb[i] = roundf(__fmul_rn(yb[i], iB));
                 }
                 uint8_t *row = reinterpret_cast<uint8_t *>(a.kdata) + R * D;
                 *reinterpret_cast<uint4 *>(row + da) = pack16(qa);
