@@ -754,7 +754,21 @@ def cold_store(kvc, torch, dev, n: int, layers: int, cycles: int = 8):
                 t_ad += t2 - t1
                 t_miss += t3 - t2
         ok = ok and bool((np.sort(cache.positions(0)) == np.arange(n)).all())
+        # restore versus recompute: admits of smaller blocks as well, so that the store's fitted
+        # model, restore_us = fixed + per_token * n, separates the fixed cost from the per-row one
+        for j, m in enumerate((512, 2048, 4096, 512, 2048, 4096)):
+            store.evict(cache, 0, 1, 0, m, 5000 + j, 0)
+            store.admit(cache, 0, 1, 5000 + j)
+        fixed_us, per_tok_us, samples = store.restore_model()
+        crossover = {}
+        for rec in (1.0, 10.0, 100.0):  # recompute cost per token (us) a caller might measure
+            crossover[str(rec)] = (round(fixed_us / (rec - per_tok_us)) if rec > per_tok_us else None)
         return {"n_kv": n, "block": blk, "layers": layers, "cycles": cycles, "block_state_bytes": size,
+                "restore_model": {"fixed_us": round(fixed_us, 1), "per_token_us": round(per_tok_us, 4),
+                                  "samples": samples,
+                                  "crossover_tokens_by_recompute_us_per_token": crossover,
+                                  "note": "least-squares fit over the store's timed admits (8192-row blocks and "
+                                          "512 / 2048 / 4096-row ones); restore wins above the crossover"},
                 "evict_ms": round(t_ev / cycles * 1e3, 3), "admit_ms": round(t_ad / cycles * 1e3, 3),
                 "miss_us": round(t_miss / cycles * 1e6, 1),
                 "evict_state_gbs": round(size / (t_ev / cycles) / GB, 1),

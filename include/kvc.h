@@ -484,6 +484,28 @@ int kvc_cold_evict(kvc_ctx *c, kvc_cold *s, int seq, int scratch, int p0, int p1
  * the store and the scratch is emptied. */
 int kvc_cold_admit(kvc_ctx *c, kvc_cold *s, int seq, int scratch, uint64_t key, int *hit, int32_t *n_tok);
 
+/* Restore versus recompute ([COLD] #3: bulk restore of KV bytes beats
+ * re-prefilling a large block, recompute wins for small ones; "restore-vs-
+ * recompute latency policy").  The store keeps a cost model of restoring,
+ *   restore_us(n) = fixed_us + per_token_us * n   (n rows of the block),
+ * fitted by least squares to the admits it has timed (the host wall clock of
+ * each kvc_cold_admit that hit: import, shift and copy, all synchronous;
+ * with one block size only, a line through 0), unless the caller set one.
+ * kvc_cold_restore_model: the model (zeros while there is none) and the
+ * number of timed admits.  kvc_cold_set_restore_model: use the caller's
+ * model (fixed_us >= 0, per_token_us >= 0); per_token_us < 0 returns to
+ * the fitted one.  kvc_cold_plan_admit: for the block under `key`, *n_tok
+ * its rows (0 when absent), *restore_us the model's estimate and *restore =
+ * 1 when that is below the caller's cost of recomputing the block,
+ * recompute_fixed_us + recompute_us_per_token * n_tok (the library runs no
+ * model, so the caller supplies it).  An absent block gives *restore = 0 (recompute);
+ * a present block without any model gives *restore = 1 and *restore_us = -1
+ * (lossless bytes first, the pages' default).  Errors: KVC_EINVAL. */
+int kvc_cold_restore_model(const kvc_cold *s, double *fixed_us, double *per_token_us, int64_t *samples);
+int kvc_cold_set_restore_model(kvc_cold *s, double fixed_us, double per_token_us);
+int kvc_cold_plan_admit(const kvc_cold *s, uint64_t key, double recompute_fixed_us, double recompute_us_per_token,
+                        int *restore, double *restore_us, int32_t *n_tok);
+
 /* The rows (*n_tok, 0 when absent) and class of the block under `key`. */
 int kvc_cold_find(const kvc_cold *s, uint64_t key, int32_t *n_tok, int32_t *cls);
 int kvc_cold_get_stats(const kvc_cold *s, kvc_cold_stats *out);

@@ -14,6 +14,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <chrono>
+#include <cmath>
 #include <cstring>
 #include <new>
 #include <string>
@@ -41,7 +43,34 @@ struct ColdStore {
     // freed pinned buffers kept for reuse (pinning host memory costs far more than filling it)
     std::vector<std::pair<uint8_t *, size_t>> spare;
     int64_t stored = 0, rejected = 0, dropped = 0, hits = 0, misses = 0;
+    // restore cost model: sums over the timed admits (rows, microseconds) for a
+    // least-squares line, or a model the caller set
+    int64_t samples = 0;
+    double sx = 0.0, sy = 0.0, sxx = 0.0, sxy = 0.0;
+    bool model_set = false;
+    double set_fixed = 0.0, set_per_tok = 0.0;
     std::string err;
+
+    // The restore model: set by the caller, else fitted to the timed admits
+    // (two or more distinct sizes: least squares; one size: proportional).
+    // False without either.
+    bool model(double *fixed, double *per_tok) const {
+        if (model_set) {
+            *fixed = set_fixed;
+            *per_tok = set_per_tok;
+            return true;
+        }
+        if (samples == 0) return false;
+        const double n = (double)samples, den = n * sxx - sx * sx;
+        if (samples >= 2 && den > 1e-9 * n * sxx) {
+            *per_tok = (n * sxy - sx * sy) / den;
+            *fixed = (sy - *per_tok * sx) / n;
+        } else {
+            *fixed = 0.0;
+            *per_tok = sy / sx;
+        }
+        return true;
+    }
     static constexpr size_t MAX_SPARE = 4;
 
     // A pinned buffer of at least `size` bytes (the smallest spare that fits, else a new one);
@@ -247,11 +276,20 @@ int kvc_cold_admit(kvc_ctx *cc, kvc_cold *cs, int seq, int scratch, uint64_t key
     int64_t tail = 0;
     for (int32_t p : c->seqs[(size_t)seq].pos) tail = std::max<int64_t>(tail, (int64_t)p + 1);
     size_t used = 0;
+    const auto t0 = std::chrono::steady_clock::now();
     int rc = kvc_state_set(cc, scratch, b.bytes, b.size, &used);
     if (!rc && tail != b.first_pos) rc = kvc_seq_add(cc, scratch, -1, -1, (int)(tail - b.first_pos));
     if (!rc) rc = kvc_seq_cp(cc, scratch, seq, -1, -1);
     const int rc2 = kvc_seq_rm(cc, scratch, -1, -1);
     if (rc || rc2) return s->fail(rc ? rc : rc2, "importing the block");
+    // the restore's cost (every call above is synchronous): one sample of the model
+    const double us = std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t0).count();
+    const double x = (double)b.n_tok;
+    ++s->samples;
+    s->sx += x;
+    s->sy += us;
+    s->sxx += x * x;
+    s->sxy += x * us;
     s->drop(i);
     ++s->hits;
     *hit = 1;
@@ -265,6 +303,55 @@ int kvc_cold_find(const kvc_cold *cs, uint64_t key, int32_t *n_tok, int32_t *cls
     const int i = s->find(key);
     *n_tok = i < 0 ? 0 : s->blocks[(size_t)i].n_tok;
     *cls = i < 0 ? -1 : s->blocks[(size_t)i].cls;
+    return KVC_OK;
+}
+
+int kvc_cold_restore_model(const kvc_cold *cs, double *fixed_us, double *per_token_us, int64_t *samples) {
+    if (!cs || !fixed_us || !per_token_us || !samples) return KVC_EINVAL;
+    const ColdStore *s = S(cs);
+    *samples = s->samples;
+    if (!s->model(fixed_us, per_token_us)) {
+        *fixed_us = 0.0;
+        *per_token_us = 0.0;
+    }
+    return KVC_OK;
+}
+
+int kvc_cold_set_restore_model(kvc_cold *cs, double fixed_us, double per_token_us) {
+    if (!cs) return KVC_EINVAL;
+    ColdStore *s = S(cs);
+    if (per_token_us < 0.0) { // back to the fitted model
+        s->model_set = false;
+        return KVC_OK;
+    }
+    if (!(fixed_us >= 0.0) || !std::isfinite(fixed_us) || !std::isfinite(per_token_us))
+        return s->fail(KVC_EINVAL, "the model needs finite fixed_us >= 0 and per_token_us >= 0");
+    s->model_set = true;
+    s->set_fixed = fixed_us;
+    s->set_per_tok = per_token_us;
+    return KVC_OK;
+}
+
+int kvc_cold_plan_admit(const kvc_cold *cs, uint64_t key, double recompute_fixed_us, double recompute_us_per_token,
+                        int *restore, double *restore_us, int32_t *n_tok) {
+    if (!cs || !restore || !restore_us || !n_tok) return KVC_EINVAL;
+    if (!std::isfinite(recompute_fixed_us) || !std::isfinite(recompute_us_per_token)) return KVC_EINVAL;
+    const ColdStore *s = S(cs);
+    const int i = s->find(key);
+    *restore = 0;
+    *restore_us = 0.0;
+    *n_tok = i < 0 ? 0 : s->blocks[(size_t)i].n_tok;
+    if (i < 0) return KVC_OK; // nothing stored: recompute
+    double fixed = 0.0, per_tok = 0.0;
+    if (!s->model(&fixed, &per_tok)) {
+        // no restore timed yet: the stored bytes are lossless and the pages' default
+        *restore = 1;
+        *restore_us = -1.0;
+        return KVC_OK;
+    }
+    const double n = (double)*n_tok;
+    *restore_us = fixed + per_tok * n;
+    *restore = *restore_us < recompute_fixed_us + recompute_us_per_token * n ? 1 : 0;
     return KVC_OK;
 }
 

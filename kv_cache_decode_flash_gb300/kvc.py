@@ -106,6 +106,10 @@ def load():
                                  C.POINTER(C.c_int32)]),
         "kvc_cold_admit": (i32, [p, p, i32, i32, C.c_uint64, C.POINTER(C.c_int), C.POINTER(C.c_int32)]),
         "kvc_cold_find": (i32, [p, C.c_uint64, C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
+        "kvc_cold_restore_model": (i32, [p, C.POINTER(C.c_double), C.POINTER(C.c_double), C.POINTER(C.c_int64)]),
+        "kvc_cold_set_restore_model": (i32, [p, C.c_double, C.c_double]),
+        "kvc_cold_plan_admit": (i32, [p, C.c_uint64, C.c_double, C.c_double, C.POINTER(C.c_int),
+                                      C.POINTER(C.c_double), C.POINTER(C.c_int32)]),
         "kvc_cold_get_stats": (i32, [p, C.POINTER(kvc_cold_stats)]),
     }
     for name, (res, args) in sig.items():
@@ -477,6 +481,27 @@ def kvc_cold_find(store, key):
     return n.value, cls.value
 
 
+def kvc_cold_restore_model(store):
+    """(fixed_us, per_token_us, samples) of the store's restore cost model."""
+    f, t, n = C.c_double(), C.c_double(), C.c_int64()
+    _check_cold(store, None, load().kvc_cold_restore_model(store, C.byref(f), C.byref(t), C.byref(n)))
+    return f.value, t.value, n.value
+
+
+def kvc_cold_set_restore_model(store, fixed_us, per_token_us):
+    _check_cold(store, None, load().kvc_cold_set_restore_model(store, float(fixed_us), float(per_token_us)))
+
+
+def kvc_cold_plan_admit(store, key, recompute_fixed_us, recompute_us_per_token):
+    """(restore, restore_us, n_tok) for the block under key: restore 1 when the
+    model's restore estimate is below the caller's recompute cost."""
+    r, us, n = C.c_int(), C.c_double(), C.c_int32()
+    _check_cold(store, None, load().kvc_cold_plan_admit(store, C.c_uint64(key), float(recompute_fixed_us),
+                                                         float(recompute_us_per_token), C.byref(r), C.byref(us),
+                                                         C.byref(n)))
+    return r.value, us.value, n.value
+
+
 def kvc_cold_get_stats(store) -> dict:
     st = kvc_cold_stats()
     _check_cold(store, None, load().kvc_cold_get_stats(store, C.byref(st)))
@@ -511,3 +536,12 @@ class ColdStore:
 
     def stats(self):
         return kvc_cold_get_stats(self.handle)
+
+    def restore_model(self):
+        return kvc_cold_restore_model(self.handle)
+
+    def set_restore_model(self, fixed_us, per_token_us):
+        kvc_cold_set_restore_model(self.handle, fixed_us, per_token_us)
+
+    def plan_admit(self, key, recompute_fixed_us, recompute_us_per_token):
+        return kvc_cold_plan_admit(self.handle, key, recompute_fixed_us, recompute_us_per_token)

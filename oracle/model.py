@@ -347,6 +347,40 @@ class ColdStore:
         self.blocks = []  # dicts: key, cls, n, first, stamp, blob
         self.clock = 0
         self.stats = {"stored": 0, "rejected": 0, "dropped": 0, "hits": 0, "misses": 0}
+        # restore cost samples (rows, microseconds) and an optional model set by the caller
+        self.samples = []
+        self.model_set = None
+
+    @staticmethod
+    def fit_restore_model(samples):
+        """Least-squares line through (rows, us) samples: (fixed_us, per_token_us);
+        one distinct size only: a line through 0; no samples: None
+        (Plan: lossless long context, #3: bulk restore beats re-prefill for large
+        blocks, recompute wins for small ones)."""
+        if not samples:
+            return None
+        x = np.array([s[0] for s in samples], np.float64)
+        y = np.array([s[1] for s in samples], np.float64)
+        n = float(len(x))
+        sx, sy, sxx, sxy = x.sum(), y.sum(), (x * x).sum(), (x * y).sum()
+        den = n * sxx - sx * sx
+        if len(x) >= 2 and den > 1e-9 * n * sxx:
+            b = (n * sxy - sx * sy) / den
+            return (sy - b * sx) / n, b
+        return 0.0, sy / sx
+
+    def plan_admit(self, key: int, recompute_fixed_us: float, recompute_us_per_token: float, model=None):
+        """(restore, restore_us, n_tok): restore when the model's estimate of
+        restoring the block is below recomputing it; absent block: (0, 0, 0);
+        no model: (1, -1, n), the stored bytes first."""
+        b = self.find(key)
+        if b is None:
+            return 0, 0.0, 0
+        m = model if model is not None else (self.model_set or self.fit_restore_model(self.samples))
+        if m is None:
+            return 1, -1.0, b["n"]
+        us = m[0] + m[1] * b["n"]
+        return int(us < recompute_fixed_us + recompute_us_per_token * b["n"]), us, b["n"]
 
     @property
     def tokens(self) -> int:

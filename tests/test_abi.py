@@ -57,3 +57,20 @@ def test_create_rejects_bad_geometry_without_touching_a_gpu():
         with pytest.raises(kvc.KvcError) as e:
             kvc.kvc_create(p)
         assert e.value.status == kvc.KVC_EINVAL, (gpu_heads, n_seq)
+
+
+def test_cold_store_restore_model_calls_without_a_gpu():
+    from kv_cache_decode_flash_gb300 import kvc
+
+    s = kvc.ColdStore(1000)
+    try:
+        assert s.restore_model() == (0.0, 0.0, 0)
+        assert s.plan_admit(123, 0.0, 10.0) == (0, 0.0, 0)  # nothing stored under the key: recompute
+        s.set_restore_model(1500.0, 0.9)
+        assert s.restore_model() == (1500.0, 0.9, 0)
+        with pytest.raises(kvc.KvcError):
+            s.set_restore_model(-1.0, 0.5)
+        s.set_restore_model(0.0, -1.0)  # back to the (empty) fitted model
+        assert s.restore_model() == (0.0, 0.0, 0)
+    finally:
+        s.close()

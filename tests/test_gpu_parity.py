@@ -727,3 +727,46 @@ def test_host_transport_trace_records_deliveries_and_launches():
             assert all(r[2] == n * row_bytes for r in dlv)  # every delivery carries the layer's n rows
     finally:
         tw.close()
+
+
+def test_cold_store_restore_vs_recompute_plan():
+    """Admits of three block sizes are timed into the store's restore model;
+    the planning call follows the oracle's rule with the fitted model and with
+    a model set by the caller, and answers recompute for an absent block."""
+    from kv_cache_decode_flash_gb300 import kvc
+
+    tw = Twin(2, 8, 2, 128, 8192, n_seq_max=2, type_=Q8, rope_base=1e6, page_rows=64)
+    store = kvc.ColdStore(1 << 20)
+    ref = oracle.ColdStore(1 << 20)
+    try:
+        tw.fill(0, 4096, seed=15, sigma=0.5)
+        sizes = (128, 512, 2048)
+        p0 = 0
+        for i, m in enumerate(sizes):  # evict the oldest rows as blocks of three sizes
+            stored, n = store.evict(tw.gpu, 0, 1, 0, m, key=100 + i, cls=0)
+            assert stored == 1 and n == m
+        assert store.restore_model() == (0.0, 0.0, 0)
+        # no model yet: the stored bytes first
+        assert store.plan_admit(100, 0.0, 1.0) == (1, -1.0, sizes[0])
+        for i in range(len(sizes)):
+            hit, n = store.admit(tw.gpu, 0, 1, 100 + i)
+            assert hit == 1 and n == sizes[i]
+        fixed, per, samples = store.restore_model()
+        assert samples == 3 and per > 0.0
+        # plans for blocks evicted again, against the oracle's rule with the same model
+        for i, m in enumerate(sizes):
+            store.evict(tw.gpu, 0, 1, 0, m, key=200 + i, cls=0)
+            ref.blocks.append({"key": 200 + i, "cls": 0, "n": m, "first": 0, "stamp": i, "blob": b""})
+        for model in ((fixed, per), (2000.0, 0.5)):
+            if model != (fixed, per):
+                store.set_restore_model(*model)
+            for rec in (0.1, 0.6, 1.0, 4.0, 20.0):
+                for i in range(len(sizes)):
+                    got = store.plan_admit(200 + i, 500.0, rec)
+                    want = ref.plan_admit(200 + i, 500.0, rec, model=model)
+                    assert got[0] == want[0] and got[2] == want[2], (model, rec, i, got, want)
+                    assert abs(got[1] - want[1]) <= 1e-9 * abs(want[1]) + 1e-9
+        assert store.plan_admit(999, 0.0, 1e9) == (0, 0.0, 0)
+    finally:
+        store.close()
+        tw.close()

@@ -679,3 +679,28 @@ def test_cold_store_invariants_random():
             assert stored == (key in after)
             if not stored:
                 assert gone == []
+
+
+def test_cold_store_restore_model_fit_and_decision():
+    # the fitted line against numpy's least-squares polynomial fit
+    cs = oracle.ColdStore(100)
+    rows = [512, 2048, 8192, 1024, 4096]
+    us = [900.0 + 0.85 * n + (13.0 if i % 2 else -9.0) for i, n in enumerate(rows)]
+    fixed, per = cs.fit_restore_model(list(zip(rows, us)))
+    slope, icpt = np.polyfit(np.array(rows, float), np.array(us, float), 1)
+    assert abs(per - slope) <= 1e-12 * abs(slope) + 1e-12 and abs(fixed - icpt) <= 1e-9 * abs(icpt) + 1e-9
+    # one block size only: a line through 0; no samples: no model
+    assert cs.fit_restore_model([(2048, 1000.0), (2048, 1200.0)]) == (0.0, 2200.0 / 4096.0)
+    assert cs.fit_restore_model([]) is None
+    # the decision: restore while fixed + per * n < recompute_fixed + recompute_per * n
+    cs.blocks.append({"key": 7, "cls": 0, "n": 1000, "first": 0, "stamp": 0, "blob": b""})
+    assert cs.plan_admit(7, 0.0, 1.0) == (1, -1.0, 1000)          # no model: the stored bytes first
+    assert cs.plan_admit(8, 0.0, 1.0) == (0, 0.0, 0)              # absent: recompute
+    m = (1500.0, 0.9)                                             # restore 2400 us for 1000 rows
+    assert cs.plan_admit(7, 0.0, 2.5, model=m) == (1, 2400.0, 1000)   # recompute 2500 us
+    assert cs.plan_admit(7, 0.0, 2.3, model=m)[0] == 0                # recompute 2300 us
+    assert cs.plan_admit(7, 2400.0 - 2300.0, 2.3, model=m)[0] == 0    # equal cost: recompute
+    # the crossover: restore wins above n* = fixed / (recompute_per - per)
+    for n, want in ((1000, 1), (900, 0)):
+        cs.blocks[0]["n"] = n
+        assert cs.plan_admit(7, 0.0, 2.5, model=m)[0] == want
