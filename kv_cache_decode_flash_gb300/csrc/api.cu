@@ -57,6 +57,7 @@ void dev_free(Ctx *c, void *p, int64_t bytes) {
 // Wait for the internal stream with a deadline (polling; never an unbounded
 // block).  Short waits spin; past 2 ms the poll sleeps between queries.
 int wait_internal(Ctx *c) {
+    KVC_CU(c, cudaMemcpyAsync(c->err_host, c->err_dev, 4, cudaMemcpyDeviceToHost, c->st));
     KVC_CU(c, cudaEventRecord(c->done, c->st));
     auto t0 = std::chrono::steady_clock::now();
     for (;;) {
@@ -67,9 +68,7 @@ int wait_internal(Ctx *c) {
         if (us > (int64_t)c->timeout_ms * 1000) return c->fail(KVC_ETIMEDOUT, "timed out waiting for device work");
         if (us > 2000) std::this_thread::sleep_for(std::chrono::microseconds(50));
     }
-    uint32_t word = 0;
-    KVC_CU(c, cudaMemcpyAsync(&word, c->err_dev, 4, cudaMemcpyDeviceToHost, c->st));
-    KVC_CU(c, cudaStreamSynchronize(c->st));
+    const uint32_t word = *(volatile uint32_t *)c->err_host;
     if (word) return c->fail(KVC_EINTERNAL, "a kernel reported device error word " + std::to_string(word));
     return KVC_OK;
 }
@@ -137,6 +136,17 @@ static inline void phys(const Ctx *c, const Seq &q, int64_t r, int32_t &page, in
     page = q.pages[(size_t)(lr / c->P)];
     cell = (int32_t)(lr % c->P);
 }
+
+// The rows of a sequence whose positions fall in [p0, p1), in row order.
+// The usual selection is one contiguous range of rows, which needs no index
+// list; the first pass (counts and extremes only) finds out.
+struct RowSel {
+    int64_t first = 0, count = 0;
+    int64_t pos_min = 0, pos_max = -1; // of the selected positions
+    bool contiguous = true;            // rows first .. first + count - 1
+    std::vector<int64_t> idx;          // the rows, when not contiguous
+    int64_t row(int64_t i) const { return contiguous ? first + i : idx[(size_t)i]; }
+};
 
 // Pages needed to hold rows [0, n) of a sequence with offset off.
 static inline int32_t pages_for(const Ctx *c, int32_t off, int64_t n) {
@@ -216,18 +226,29 @@ static int64_t state_bytes(const Ctx *c, int64_t n) { return 64 + pad16(4 * n) +
 // Runs between the pools and a packed payload laid out as in the state
 // format, for the rows idx[] of sequence q (row i of the selection is payload
 // row g * N + i of head g, N = idx.size()).
-static void add_payload_copies(const Ctx *c, const Seq &q, const std::vector<int64_t> &idx,
-                               std::vector<RowRun> &out) {
-    const int64_t n = (int64_t)idx.size();
+static void add_payload_copies(const Ctx *c, const Seq &q, const RowSel &sel, std::vector<RowRun> &out) {
+    const int64_t n = sel.count;
     for (int64_t i = 0; i < n;) {
         int32_t pg, cl;
-        phys(c, q, idx[(size_t)i], pg, cl);
-        int64_t j = i + 1;
-        while (j < n && idx[(size_t)j] == idx[(size_t)j - 1] + 1 && cl + (j - i) < c->P) ++j;
+        phys(c, q, sel.row(i), pg, cl);
+        int64_t j;
+        if (sel.contiguous) {
+            j = std::min<int64_t>(n, i + (c->P - cl));
+        } else {
+            j = i + 1;
+            while (j < n && sel.idx[(size_t)j] == sel.idx[(size_t)j - 1] + 1 && cl + (j - i) < c->P) ++j;
+        }
         for (int g = 0; g < c->Hk; ++g)
             out.push_back(RowRun{prow(c, pg, g, cl), (int64_t)g * n + i, (int32_t)(j - i), 0});
         i = j;
     }
+}
+// The contiguous selection of rows [first, first + count).
+static RowSel row_range(int64_t first, int64_t count) {
+    RowSel s;
+    s.first = first;
+    s.count = count;
+    return s;
 }
 
 // Copy arguments between the pools and a payload of n rows per head.
@@ -269,10 +290,52 @@ static void zero_payload_pads(const Ctx *c, uint8_t *payload, int64_t n) {
         }
 }
 
-static void select_rows(const Seq &q, int64_t p0, int64_t p1, std::vector<int64_t> &idx) {
-    idx.clear();
-    for (int64_t r = 0; r < q.n; ++r)
-        if (q.pos[(size_t)r] >= p0 && q.pos[(size_t)r] < p1) idx.push_back(r);
+// Whether p[0 .. n) are consecutive integers in order.
+static bool consecutive(const int32_t *p, int64_t n) {
+    if (n <= 1) return true;
+    const int64_t p0 = p[0];
+    int32_t bad = 0;
+    for (int64_t i = 1; i < n; ++i) bad |= p[i] ^ (int32_t)(p0 + i);
+    return bad == 0;
+}
+
+static void select_rows(const Seq &q, int64_t p0, int64_t p1, RowSel &s) {
+    s = RowSel();
+    const int64_t lo64 = std::max<int64_t>(p0, 0), hi64 = std::min<int64_t>(p1 - 1, INT32_MAX); // inclusive
+    if (q.n <= 0 || hi64 < lo64) return;
+    if (q.linear) { // row r holds position pos[0] + r
+        const int64_t b0 = q.pos[0];
+        const int64_t r0 = std::max<int64_t>(lo64 - b0, 0), r1 = std::min<int64_t>(hi64 - b0, (int64_t)q.n - 1);
+        if (r1 < r0) return;
+        s.first = r0;
+        s.count = r1 - r0 + 1;
+        s.pos_min = b0 + r0;
+        s.pos_max = b0 + r1;
+        return;
+    }
+    const int32_t lo = (int32_t)lo64, hi = (int32_t)hi64, n = q.n;
+    const int32_t *pos = q.pos.data();
+    int32_t cnt = 0, r_min = INT32_MAX, r_max = -1, p_min = INT32_MAX, p_max = INT32_MIN;
+    for (int32_t r = 0; r < n; ++r) {
+        const int32_t p = pos[r];
+        const bool in = p >= lo && p <= hi;
+        cnt += in ? 1 : 0;
+        r_min = std::min(r_min, in ? r : INT32_MAX);
+        r_max = std::max(r_max, in ? r : -1);
+        p_min = std::min(p_min, in ? p : INT32_MAX);
+        p_max = std::max(p_max, in ? p : INT32_MIN);
+    }
+    if (cnt == 0) return;
+    s.first = r_min;
+    s.count = cnt;
+    s.pos_min = p_min;
+    s.pos_max = p_max;
+    s.contiguous = (int64_t)r_max - r_min + 1 == cnt;
+    if (!s.contiguous) {
+        s.idx.reserve((size_t)cnt);
+        for (int32_t r = r_min; r <= r_max; ++r)
+            if (pos[r] >= lo && pos[r] <= hi) s.idx.push_back(r);
+    }
 }
 
 static void norm_range(int p0, int p1, int64_t &a, int64_t &b) {
@@ -364,6 +427,7 @@ void kvc_destroy(kvc_ctx *cc) {
     cudaFree(c->part);
     cudaFree(c->tickets);
     cudaFree(c->err_dev);
+    if (c->err_host) cudaFreeHost(c->err_host);
     cudaFree(c->staging);
     cudaFree(c->runs_dev);
     cudaFree(c->spans_dev);
@@ -491,6 +555,12 @@ int kvc_create(const kvc_params *p, kvc_ctx **out) {
     }
     if ((rc = dev_alloc(c, (void **)&c->err_dev, 4, "error word"))) return fail(rc);
     cudaMemsetAsync(c->err_dev, 0, 4, c->st);
+    if (cudaMallocHost((void **)&c->err_host, 4) != cudaSuccess) {
+        c->err_host = nullptr;
+        c->err = "cudaMallocHost failed for the error word";
+        return fail(KVC_ENOMEM);
+    }
+    *c->err_host = 0;
     if ((rc = dev_alloc(c, (void **)&c->tickets, (int64_t)MAX_SEQ_PER_LAUNCH * c->Hk * 4, "tickets")))
         return fail(rc);
     cudaMemsetAsync(c->tickets, 0, (size_t)MAX_SEQ_PER_LAUNCH * c->Hk * 4, c->st);
@@ -669,6 +739,7 @@ static int device_append_dst(Ctx *c, int layer, int seq, bool creates, int n_tok
 static void append_commit(Ctx *c, int layer, int seq, int pos0, int n_tok, bool creates) {
     Seq &q = c->seqs[seq];
     if (creates) {
+        q.linear = q.pos.empty() || (q.linear && (int64_t)q.pos.back() + 1 == pos0);
         for (int i = 0; i < n_tok; ++i) q.pos.push_back(pos0 + i);
         q.n += n_tok;
     }
@@ -845,17 +916,18 @@ int kvc_seq_rm(kvc_ctx *cc, int seq, int p0, int p1) {
     if (!q.synced()) return c->fail(KVC_EINVAL, "layers are not in sync (a step's appends are incomplete)");
     int64_t a, b;
     norm_range(p0, p1, a, b);
-    std::vector<int64_t> rm;
+    RowSel rm;
     select_rows(q, a, b, rm);
-    if (rm.empty()) return KVC_OK;
+    if (rm.count == 0) return KVC_OK;
     int rc = enter_sync(c);
     if (rc) return rc;
-    const int64_t k = (int64_t)rm.size();
-    const bool prefix = rm.front() == 0 && rm.back() == k - 1;
-    const bool suffix = rm.front() == q.n - k && rm.back() == q.n - 1;
+    const int64_t k = rm.count;
+    const bool prefix = rm.contiguous && rm.first == 0;
+    const bool suffix = rm.contiguous && rm.first + k == q.n;
     if (k == q.n) {
         q.n = 0;
         q.pos.clear();
+        q.linear = true;
         release_tail_pages(c, q);
     } else if (prefix) {
         q.off += (int32_t)k;
@@ -872,17 +944,23 @@ int kvc_seq_rm(kvc_ctx *cc, int seq, int p0, int p1) {
         release_tail_pages(c, q);
     } else {
         // compact: kept rows from the first removed row on go through staging
-        const int64_t i0 = rm.front();
-        std::vector<int64_t> keep;
-        size_t j = 0;
-        for (int64_t r = i0; r < q.n; ++r) {
-            if (j < rm.size() && rm[j] == r) {
-                ++j;
-                continue;
+        const int64_t i0 = rm.first;
+        RowSel keep;
+        if (rm.contiguous) {
+            keep = row_range(i0 + k, q.n - i0 - k);
+        } else {
+            keep.contiguous = false;
+            size_t j = 0;
+            for (int64_t r = i0; r < q.n; ++r) {
+                if (j < rm.idx.size() && rm.idx[j] == r) {
+                    ++j;
+                    continue;
+                }
+                keep.idx.push_back(r);
             }
-            keep.push_back(r);
+            keep.count = (int64_t)keep.idx.size();
         }
-        const int64_t nk = (int64_t)keep.size();
+        const int64_t nk = keep.count;
         if ((rc = ensure_staging(c, payload_bytes(c, nk)))) return rc;
         // pack the kept rows, then unpack them at logical rows i0 .. i0+nk-1
         std::vector<RowRun> runs;
@@ -891,20 +969,19 @@ int kvc_seq_rm(kvc_ctx *cc, int seq, int p0, int p1) {
         KVC_CU(c, launch_copy_runs(payload_args(c, nk, c->staging, true), c->runs_dev, (int64_t)runs.size(), c->L,
                                    c->st));
         if ((rc = wait_internal(c))) return rc;
-        std::vector<int64_t> dst((size_t)nk);
-        for (int64_t i = 0; i < nk; ++i) dst[(size_t)i] = i0 + i;
         runs.clear();
-        add_payload_copies(c, q, dst, runs);
+        add_payload_copies(c, q, row_range(i0, nk), runs);
         if ((rc = upload_runs(c, runs))) return rc;
         KVC_CU(c, launch_copy_runs(payload_args(c, nk, c->staging, false), c->runs_dev, (int64_t)runs.size(), c->L,
                                    c->st));
         if ((rc = wait_internal(c))) return rc;
         std::vector<int32_t> np;
         np.reserve((size_t)(q.n - k));
-        for (int64_t r = 0; r < i0; ++r) np.push_back(q.pos[(size_t)r]);
-        for (int64_t r : keep) np.push_back(q.pos[(size_t)r]);
+        np.insert(np.end(), q.pos.begin(), q.pos.begin() + i0);
+        for (int64_t i = 0; i < nk; ++i) np.push_back(q.pos[(size_t)keep.row(i)]);
         q.pos.swap(np);
         q.n -= (int32_t)k;
+        q.linear = consecutive(q.pos.data(), q.n);
         release_tail_pages(c, q);
     }
     for (auto &f : q.lfill) f = q.n;
@@ -924,24 +1001,32 @@ int kvc_seq_cp(kvc_ctx *cc, int src, int dst, int p0, int p1) {
     if (!a.synced() || !b.synced()) return c->fail(KVC_EINVAL, "layers are not in sync");
     int64_t lo, hi;
     norm_range(p0, p1, lo, hi);
-    std::vector<int64_t> sel;
+    RowSel sel;
     select_rows(a, lo, hi, sel);
-    if (sel.empty()) return KVC_OK;
+    if (sel.count == 0) return KVC_OK;
     int rc = enter_sync(c);
     if (rc) return rc;
     size_t first_new;
-    if ((rc = grow_pages(c, b, (int64_t)sel.size(), &first_new))) return rc;
+    if ((rc = grow_pages(c, b, sel.count, &first_new))) return rc;
     const int64_t base = b.n;
-    b.n += (int32_t)sel.size();
-    for (int64_t r : sel) b.pos.push_back(a.pos[(size_t)r]);
-    for (auto &f : b.lfill) f = b.n;
+    b.n += (int32_t)sel.count;
     std::vector<RowRun> runs;
-    for (size_t i = 0; i < sel.size();) {
-        size_t j = i + 1;
-        while (j < sel.size() && sel[j] == sel[j - 1] + 1) ++j;
-        add_row_copies(c, a, sel[i], b, base + (int64_t)i, (int64_t)(j - i), runs);
-        i = j;
+    if (sel.contiguous) {
+        b.pos.insert(b.pos.end(), a.pos.begin() + sel.first, a.pos.begin() + sel.first + sel.count);
+        add_row_copies(c, a, sel.first, b, base, sel.count, runs);
+    } else {
+        for (int64_t r : sel.idx) b.pos.push_back(a.pos[(size_t)r]);
+        for (size_t i = 0; i < sel.idx.size();) {
+            size_t j = i + 1;
+            while (j < sel.idx.size() && sel.idx[j] == sel.idx[j - 1] + 1) ++j;
+            add_row_copies(c, a, sel.idx[i], b, base + (int64_t)i, (int64_t)(j - i), runs);
+            i = j;
+        }
     }
+    const bool copied_linear = (a.linear && sel.contiguous) || consecutive(b.pos.data() + base, sel.count);
+    b.linear = (base == 0 || (b.linear && (int64_t)b.pos[(size_t)base - 1] + 1 == b.pos[(size_t)base])) &&
+               copied_linear;
+    for (auto &f : b.lfill) f = b.n;
     if ((rc = upload_pages(c, dst))) return rc;
     if ((rc = upload_runs(c, runs))) return rc;
     KVC_CU(c, launch_copy_runs(pool_args(c), c->runs_dev, (int64_t)runs.size(), c->L, c->st));
@@ -957,28 +1042,31 @@ int kvc_seq_add(kvc_ctx *cc, int seq, int p0, int p1, int delta) {
     if (!q.synced()) return c->fail(KVC_EINVAL, "layers are not in sync");
     int64_t a, b;
     norm_range(p0, p1, a, b);
-    std::vector<int64_t> sel;
+    if (delta == 0) return KVC_OK;
+    RowSel sel;
     select_rows(q, a, b, sel);
-    if (sel.empty() || delta == 0) return KVC_OK;
-    for (int64_t r : sel) {
-        const int64_t np = (int64_t)q.pos[(size_t)r] + delta;
-        if (np < 0 || np > INT32_MAX) return c->fail(KVC_ERANGE, "shifted position out of range");
-    }
-    int rc = enter_sync(c);
-    if (rc) return rc;
-    // runs of consecutive cells inside one page, one span per KV head (layer 0;
-    // the kernel repeats them for every layer), at most ROPE_SPAN_MAX rows each
-    std::vector<RopeSpan> spans;
-    for (size_t i = 0; i < sel.size();) {
+    if (sel.count == 0) return KVC_OK;
+    if (sel.pos_min + delta < 0 || sel.pos_max + delta > INT32_MAX)
+        return c->fail(KVC_ERANGE, "shifted position out of range");
+    // runs of consecutive cells inside one page, one span per KV head (layer
+    // 0; the kernel repeats them for every layer), at most ROPE_SPAN_MAX rows
+    std::vector<RopeSpan> &spans = c->spans_host;
+    spans.clear();
+    for (int64_t i = 0; i < sel.count;) {
         int32_t pg, cl;
-        phys(c, q, sel[i], pg, cl);
-        size_t j = i + 1;
-        while (j < sel.size() && sel[j] == sel[j - 1] + 1 && (int64_t)(j - i) < ROPE_SPAN_MAX &&
-               cl + (int64_t)(j - i) < c->P)
-            ++j;
+        phys(c, q, sel.row(i), pg, cl);
+        int64_t j = std::min<int64_t>({sel.count, i + ROPE_SPAN_MAX, i + (c->P - cl)});
+        if (!sel.contiguous)
+            for (int64_t m = i + 1; m < j; ++m)
+                if (sel.idx[(size_t)m] != sel.idx[(size_t)m - 1] + 1) {
+                    j = m;
+                    break;
+                }
         for (int g = 0; g < c->Hk; ++g) spans.push_back(RopeSpan{prow(c, pg, g, cl), (int32_t)(j - i), 0});
         i = j;
     }
+    int rc = enter_sync(c);
+    if (rc) return rc;
     const int64_t n_spans = (int64_t)spans.size();
     if (n_spans > c->spans_cap) {
         dev_free(c, c->spans_dev, c->spans_cap * (int64_t)sizeof(RopeSpan));
@@ -1002,7 +1090,12 @@ int kvc_seq_add(kvc_ctx *cc, int seq, int p0, int p1, int delta) {
                                       n_spans, cs, c->err_dev, c->st);
     if (e != cudaSuccess) return cuda_fail(c, e, "rope shift kernel");
     if ((rc = wait_internal(c))) return rc;
-    for (int64_t r : sel) q.pos[(size_t)r] += delta;
+    int32_t *pos = q.pos.data();
+    if (sel.contiguous)
+        for (int64_t r = sel.first; r < sel.first + sel.count; ++r) pos[r] += delta;
+    else
+        for (int64_t r : sel.idx) pos[r] += delta;
+    if (!(sel.contiguous && sel.first == 0 && sel.count == q.n)) q.linear = consecutive(pos, q.n);
     return KVC_OK;
 }
 
@@ -1122,9 +1215,9 @@ int kvc_state_get(kvc_ctx *cc, int seq, int p0, int p1, void *dst, size_t cap, s
     if (!q.synced()) return c->fail(KVC_EINVAL, "layers are not in sync");
     int64_t a, b;
     norm_range(p0, p1, a, b);
-    std::vector<int64_t> sel;
+    RowSel sel;
     select_rows(q, a, b, sel);
-    const int64_t n = (int64_t)sel.size();
+    const int64_t n = sel.count;
     const int64_t size = state_bytes(c, n);
     *n_written = (size_t)size;
     if (!dst) return KVC_OK;
@@ -1138,7 +1231,10 @@ int kvc_state_get(kvc_ctx *cc, int seq, int p0, int p1, void *dst, size_t cap, s
     std::memcpy(out, hdr, sizeof(hdr));
     const uint64_t pl = (uint64_t)payload_bytes(c, n);
     std::memcpy(out + 32, &pl, 8);
-    for (int64_t i = 0; i < n; ++i) std::memcpy(out + 64 + 4 * i, &q.pos[(size_t)sel[(size_t)i]], 4);
+    if (sel.contiguous)
+        std::memcpy(out + 64, q.pos.data() + sel.first, (size_t)(4 * n));
+    else
+        for (int64_t i = 0; i < n; ++i) std::memcpy(out + 64 + 4 * i, &q.pos[(size_t)sel.idx[(size_t)i]], 4);
     if (n > 0) {
         if ((rc = ensure_staging(c, (int64_t)pl))) return rc;
         if ((rc = ensure_copy_stream(c))) return rc;
@@ -1209,11 +1305,11 @@ int kvc_state_set(kvc_ctx *cc, int seq, const void *src, size_t nbytes, size_t *
     const int64_t base = q.n;
     q.n += (int32_t)n;
     q.pos.insert(q.pos.end(), pos.begin(), pos.end());
+    q.linear = (base == 0 || (q.linear && (int64_t)q.pos[(size_t)base - 1] + 1 == q.pos[(size_t)base])) &&
+               consecutive(pos.data(), n);
     for (auto &f : q.lfill) f = q.n;
-    std::vector<int64_t> idx((size_t)n);
-    for (int64_t i = 0; i < n; ++i) idx[(size_t)i] = base + i;
     std::vector<RowRun> runs;
-    add_payload_copies(c, q, idx, runs);
+    add_payload_copies(c, q, row_range(base, n), runs);
     if ((rc = upload_pages(c, seq))) return rc;
     if ((rc = upload_runs(c, runs))) return rc;
     const RunCopyArgs ca = payload_args(c, n, c->staging, false);

@@ -20,6 +20,10 @@ struct Seq {
     int32_t off = 0;
     int32_t n = 0;
     std::vector<int32_t> pos;
+    // pos[r] == pos[0] + r for every row (consecutive positions in row
+    // order), kept by every operation that changes pos; selections by
+    // position range are then arithmetic
+    bool linear = true;
     std::vector<int32_t> lfill;
     int32_t dev_pages = 0; // leading entries of `pages` known to match the device table
     bool synced() const {
@@ -126,6 +130,7 @@ struct Ctx {
     int64_t part_floats = 0;
     int32_t *tickets = nullptr;
     uint32_t *err_dev = nullptr;
+    uint32_t *err_host = nullptr; // pinned copy of the error word read by synchronous operations
     int chunk_override = 0;
 
     // staging for sequence / state operations
@@ -135,6 +140,7 @@ struct Ctx {
     int64_t runs_cap = 0;
     RopeSpan *spans_dev = nullptr;
     int64_t spans_cap = 0;
+    std::vector<RopeSpan> spans_host; // span list of the last shift (kept for its capacity)
     cudaStream_t st = nullptr; // internal stream of the synchronous operations
     cudaEvent_t done = nullptr;
     // state export/import: host copies of layer groups on their own stream,

@@ -80,152 +80,269 @@ struct RopeArgs {
     uint16_t *kscales;
     int64_t layer_rows;
     const RopeSpan *spans;
-    uint32_t *err; // a span outside the layer pool is reported and skipped
-    float2 cs[64]; // (cos, sin) of delta * theta_i, i < D/2
+    uint32_t *err;   // a span outside the layer pool is reported and skipped
+    float c[64];     // cos(delta * theta_i), i < D/2
+    float s[64];     // sin(delta * theta_i)
 };
 
-// Code i of 16 stored offset-binary bytes, as an exact float: the byte goes
-// into the low mantissa bits of 2^23 (0x4B0000uu = 2^23 + u), and 2^23 + 128
-// is subtracted.
-__device__ __forceinline__ float code_at(const uint4 &w, int i) {
+// Two-lane fp32 arithmetic (one instruction for both lanes, each lane rounded
+// as the scalar IEEE operation would be).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+// Code byte i of 16 stored offset-binary bytes, placed at bits 8..15 of the
+// float 2^23: the result is 2^23 + 256 u (u = code + 128), exact.
+__device__ __forceinline__ float code_hi(const uint4 &w, int i) {
     const uint32_t u = i < 4 ? w.x : i < 8 ? w.y : i < 12 ? w.z : w.w;
     uint32_t f;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(f) : "r"(u), "r"(0x4B000000u), "r"(0x7440u | (uint32_t)(i & 3)));
-    return __fsub_rn(__uint_as_float(f), 8388736.0f);
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(f) : "r"(u), "r"(0x4B000000u), "r"(0x7504u | ((uint32_t)(i & 3) << 4)));
+    return __uint_as_float(f);
 }
-// 16 rounded codes (integral floats in [-127, 127]) -> 16 offset-binary bytes:
-// c + 2^23 + 128 is exact and its low byte is c + 128; PRMTs gather the bytes.
-__device__ __forceinline__ uint4 pack16(const float (&c)[16]) {
-    uint32_t b[16], u[4];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) b[i] = __float_as_uint(__fadd_rn(c[i], 8388736.0f));
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        uint32_t lo, hi;
-        asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(lo) : "r"(b[4 * j]), "r"(b[4 * j + 1]));
-        asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(hi) : "r"(b[4 * j + 2]), "r"(b[4 * j + 3]));
-        asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(u[j]) : "r"(lo), "r"(hi));
-    }
-    return make_uint4(u[0], u[1], u[2], u[3]);
+// Rounding half away from zero of q (|q| < 2^22) is the truncation of
+// q + copysign(0.49999997, q) (the predecessor of 1/2): the sum is exact
+// except where q lies within half an ulp below a half-integer, and there it
+// rounds to a value that truncates the same way.  This gives the bias.
+__device__ __forceinline__ float2 half_away_bias(float2 q) {
+    return make_float2(__uint_as_float((__float_as_uint(q.x) & 0x80000000u) | 0x3EFFFFFFu),
+                       __uint_as_float((__float_as_uint(q.y) & 0x80000000u) | 0x3EFFFFFFu));
+}
+// Four signed codes (two's complement in the low bytes) -> one word of
+// offset-binary bytes.
+__device__ __forceinline__ uint32_t pack4(int c0, int c1, int c2, int c3) {
+    uint32_t lo, hi, w;
+    asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(lo) : "r"(c0), "r"(c1));
+    asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(hi) : "r"(c2), "r"(c3));
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(w) : "r"(lo), "r"(hi));
+    return w ^ 0x80808080u;
 }
 
 // One CTA per (span, layer); TPR threads per head-row, each holding two
 // 16-byte pieces A and B of the row:
 //   NEOX: A = dims [V k, V k + V), B = A + D/2 (the rotation partners);
 //   NORM: A, B = dims [2V k, 2V k + V), [2V k + V, 2V k + 2V) (pairs inside).
-// V = 16 values per piece for q8_0 codes, 8 for f16.  A q8_0 block of 32
-// dims is the A (or B) pieces of threads k and k ^ 1 (NEOX) or A and B of
-// one thread (NORM), so the requantisation max needs at most one shuffle.
+// V = 16 values per piece for q8_0 codes, 8 for f16.  Either way thread k
+// rotates by the V angles theta_{Vk} .. theta_{Vk+V-1}; their cos, sin and
+// -sin sit in shared memory.  A q8_0 block of 32 dims is the A (or B)
+// pieces of threads k and k ^ 1 (NEOX) or A and B of one thread (NORM), so
+// the requantisation max needs at most one shuffle; under NEOX each of the
+// two threads divides for one of the two blocks and they swap results.
 // Every thread runs the same number of passes (rows past the span end are
 // masked), so the shuffles always see the whole warp.
+//
+// Values are held as lane pairs for the two-lane arithmetic.  Pair t of a
+// piece holds elements (2t, 2t+1) under NEOX; under NORM pair 2j holds the
+// even elements (4j, 4j+2) and pair 2j+1 the odd ones (4j+1, 4j+3), so one
+// two-lane step rotates the adjacent pairs of angles 2j and 2j+1.
+template <int MODE>
+__device__ __forceinline__ constexpr int pair_elem(int t, int lane) {
+    return MODE == KVC_ROPE_NEOX ? 2 * t + lane : 4 * (t / 2) + (t & 1) + 2 * lane;
+}
+
 template <bool Q8, int D, int MODE>
 __global__ void __launch_bounds__(256, 4) rope_shift_kernel(const __grid_constant__ RopeArgs a) {
     constexpr int V = Q8 ? 16 : 8;
+    constexpr int NP = V / 2;      // lane pairs per piece
     constexpr int TPR = D / (2 * V);
     constexpr int RPP = 256 / TPR; // rows per pass of the CTA
     constexpr int NB = D / QK;
     constexpr int HALF = D / 2;
+    constexpr int TS = V + 4;      // padded stride of one thread's angles (no bank conflicts)
+    constexpr bool NEOX = MODE == KVC_ROPE_NEOX;
+    __shared__ __align__(16) float trig[3][TPR * TS];
     const RopeSpan sp = a.spans[blockIdx.x];
     if (sp.n < 0 || sp.row0 < 0 || sp.row0 + sp.n > a.layer_rows) { // the whole CTA leaves
         if (threadIdx.x == 0 && a.err) atomicOr(a.err, ERR_BAD_INDEX);
         return;
     }
+    for (int i = threadIdx.x; i < TPR * V; i += blockDim.x) {
+        const int o = (i / V) * TS + i % V;
+        trig[0][o] = a.c[i];
+        trig[1][o] = a.s[i];
+        trig[2][o] = -a.s[i];
+    }
+    __syncthreads();
     const int64_t base = sp.row0 + (int64_t)blockIdx.y * a.layer_rows;
     const int k = threadIdx.x % TPR;
-    const int da = MODE == KVC_ROPE_NEOX ? V * k : 2 * V * k; // first dim of A
-    const int db = MODE == KVC_ROPE_NEOX ? da + HALF : da + V; // first dim of B
-    for (int r0 = 0; r0 < sp.n; r0 += RPP) {
+    const int da = NEOX ? V * k : 2 * V * k; // first dim of A
+    const int db = NEOX ? da + HALF : da + V; // first dim of B
+    const float *tc = &trig[0][k * TS], *tsn = &trig[1][k * TS], *tns = &trig[2][k * TS];
+    // the next pass's row pieces are requested before this pass is computed
+    auto fetch = [&](int r0, uint4 &wa, uint4 &wb, uint16_t &ha, uint16_t &hb) {
         const int r = r0 + (int)threadIdx.x / TPR;
-        const bool live = r < sp.n;
-        const int64_t R = base + (live ? r : 0);
-        uint4 wa = make_uint4(0, 0, 0, 0), wb = wa;
-        float sa = 0.f, sb = 0.f;
-        if (live) {
+        if (r < sp.n) {
+            const int64_t R = base + r;
             if constexpr (Q8) {
                 const uint8_t *row = reinterpret_cast<const uint8_t *>(a.kdata) + R * D;
                 wa = *reinterpret_cast<const uint4 *>(row + da);
                 wb = *reinterpret_cast<const uint4 *>(row + db);
-                sa = __half2float(__ushort_as_half(a.kscales[R * NB + da / QK]));
-                sb = __half2float(__ushort_as_half(a.kscales[R * NB + db / QK]));
+                ha = a.kscales[R * NB + da / QK];
+                hb = a.kscales[R * NB + db / QK];
             } else {
                 const __half *row = reinterpret_cast<const __half *>(a.kdata) + R * D;
                 wa = *reinterpret_cast<const uint4 *>(row + da);
                 wb = *reinterpret_cast<const uint4 *>(row + db);
             }
         }
-        auto xa = [&](int i) {
-            if constexpr (Q8) return sa * code_at(wa, i); // exact
-            else return __half2float(reinterpret_cast<const __half *>(&wa)[i]);
-        };
-        auto xb = [&](int i) {
-            if constexpr (Q8) return sb * code_at(wb, i);
-            else return __half2float(reinterpret_cast<const __half *>(&wb)[i]);
-        };
-        float ya[V], yb[V];
-        if constexpr (MODE == KVC_ROPE_NEOX) {
-            // (a, b) = (x_i, x_{i + D/2}) -> (a cos - b sin, a sin + b cos)
+    };
+    uint4 wa = make_uint4(0, 0, 0, 0), wb = wa;
+    uint16_t ha = 0, hb = 0;
+    fetch(0, wa, wb, ha, hb);
+    for (int r0 = 0; r0 < sp.n; r0 += RPP) {
+        const int r = r0 + (int)threadIdx.x / TPR;
+        const bool live = r < sp.n;
+        const int64_t R = base + (live ? r : 0);
+        uint4 nwa = make_uint4(0, 0, 0, 0), nwb = nwa;
+        uint16_t nha = 0, nhb = 0;
+        if (r0 + RPP < sp.n) fetch(r0 + RPP, nwa, nwb, nha, nhb);
+        const float sa = __half2float(__ushort_as_half(ha)), sb = __half2float(__ushort_as_half(hb));
+        // dequantise into lane pairs.  q8_0: x = s (u - 128) as one FMA of
+        // 2^23 + 256 u by s/256 minus (2^23 + 2^15) s/256; the constant has
+        // 9 significant bits and s 11, so every term is exact.
+        float2 xa[NP], xb[NP];
+        if constexpr (Q8) {
+            const float sa8 = sa * (1.0f / 256.0f), sb8 = sb * (1.0f / 256.0f);
+            const float2 ma2 = make_float2(sa8, sa8), mb2 = make_float2(sb8, sb8);
+            const float oa = -8421376.0f * sa8, ob = -8421376.0f * sb8;
+            const float2 oa2 = make_float2(oa, oa), ob2 = make_float2(ob, ob);
 #pragma unroll
-            for (int i = 0; i < V; ++i) {
-                const float c = a.cs[da + i].x, s = a.cs[da + i].y, u = xa(i), v = xb(i);
-                ya[i] = __fmaf_rn(u, c, __fmul_rn(-v, s));
-                yb[i] = __fmaf_rn(u, s, __fmul_rn(v, c));
+            for (int t = 0; t < NP; ++t) {
+                const int e0 = pair_elem<MODE>(t, 0), e1 = pair_elem<MODE>(t, 1);
+                xa[t] = fma2(make_float2(code_hi(wa, e0), code_hi(wa, e1)), ma2, oa2);
+                xb[t] = fma2(make_float2(code_hi(wb, e0), code_hi(wb, e1)), mb2, ob2);
             }
         } else {
-            // (a, b) = (x_2i, x_2i+1), inside each piece
+            const __half *ha = reinterpret_cast<const __half *>(&wa), *hb = reinterpret_cast<const __half *>(&wb);
 #pragma unroll
-            for (int i = 0; i < V; i += 2) {
-                const float2 ta = a.cs[(da + i) / 2], tb = a.cs[(db + i) / 2];
-                const float u0 = xa(i), u1 = xa(i + 1), v0 = xb(i), v1 = xb(i + 1);
-                ya[i] = __fmaf_rn(u0, ta.x, __fmul_rn(-u1, ta.y));
-                ya[i + 1] = __fmaf_rn(u0, ta.y, __fmul_rn(u1, ta.x));
-                yb[i] = __fmaf_rn(v0, tb.x, __fmul_rn(-v1, tb.y));
-                yb[i + 1] = __fmaf_rn(v0, tb.y, __fmul_rn(v1, tb.x));
+            for (int t = 0; t < NP; ++t) {
+                const int e0 = pair_elem<MODE>(t, 0), e1 = pair_elem<MODE>(t, 1);
+                xa[t] = make_float2(__half2float(ha[e0]), __half2float(ha[e1]));
+                xb[t] = make_float2(__half2float(hb[e0]), __half2float(hb[e1]));
+            }
+        }
+        // rotate: (u, v) -> (u cos - v sin, u sin + v cos), the products v sin
+        // and v cos rounded before the fused multiply-add
+        float2 ya[NP], yb[NP];
+#pragma unroll
+        for (int m = 0; m < V / 4; ++m) { // angles 4m .. 4m+3 of this thread
+            const float4 c4 = *reinterpret_cast<const float4 *>(tc + 4 * m);
+            const float4 s4 = *reinterpret_cast<const float4 *>(tsn + 4 * m);
+            const float4 n4 = *reinterpret_cast<const float4 *>(tns + 4 * m);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) { // angle pair 2m + h
+                const float2 c2 = h ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y);
+                const float2 s2 = h ? make_float2(s4.z, s4.w) : make_float2(s4.x, s4.y);
+                const float2 n2 = h ? make_float2(n4.z, n4.w) : make_float2(n4.x, n4.y);
+                const int j = 2 * m + h;
+                if constexpr (NEOX) {
+                    ya[j] = fma2(xa[j], c2, mul2(xb[j], n2));
+                    yb[j] = fma2(xa[j], s2, mul2(xb[j], c2));
+                } else if (j < V / 4) { // piece A: even pair 2j, odd pair 2j+1
+                    ya[2 * j] = fma2(xa[2 * j], c2, mul2(xa[2 * j + 1], n2));
+                    ya[2 * j + 1] = fma2(xa[2 * j], s2, mul2(xa[2 * j + 1], c2));
+                } else { // piece B
+                    const int i = j - V / 4;
+                    yb[2 * i] = fma2(xb[2 * i], c2, mul2(xb[2 * i + 1], n2));
+                    yb[2 * i + 1] = fma2(xb[2 * i], s2, mul2(xb[2 * i + 1], c2));
+                }
             }
         }
         if constexpr (Q8) {
             float ma = 0.f, mb = 0.f;
 #pragma unroll
-            for (int i = 0; i < V; ++i) {
-                ma = fmaxf(ma, fabsf(ya[i]));
-                mb = fmaxf(mb, fabsf(yb[i]));
+            for (int t = 0; t < NP; ++t) {
+                ma = fmaxf(ma, fmaxf(fabsf(ya[t].x), fabsf(ya[t].y)));
+                mb = fmaxf(mb, fmaxf(fabsf(yb[t].x), fabsf(yb[t].y)));
             }
-            if constexpr (MODE == KVC_ROPE_NEOX) {
+            float iA, iB, d_own;
+            if constexpr (NEOX) {
                 // the other half of each block sits in thread k ^ 1 of this row
                 ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
                 mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+                const bool odd = k & 1; // even: A's block, odd: B's block (scale and reciprocal)
+                d_own = __fdiv_rn(odd ? mb : ma, 127.0f);
+                const float i_own = (d_own != 0.0f) ? __fdiv_rn(1.0f, d_own) : 0.0f;
+                const float i_oth = __shfl_xor_sync(0xffffffffu, i_own, 1);
+                iA = odd ? i_oth : i_own;
+                iB = odd ? i_own : i_oth;
             } else {
-                ma = mb = fmaxf(ma, mb); // A and B are one block
+                ma = fmaxf(ma, mb); // A and B are one block
+                d_own = __fdiv_rn(ma, 127.0f);
+                iA = iB = (d_own != 0.0f) ? __fdiv_rn(1.0f, d_own) : 0.0f;
             }
-            const float dA = __fdiv_rn(ma, 127.0f), dB = __fdiv_rn(mb, 127.0f);
-            const float iA = (dA != 0.0f) ? __fdiv_rn(1.0f, dA) : 0.0f;
-            const float iB = (dB != 0.0f) ? __fdiv_rn(1.0f, dB) : 0.0f;
             if (live) {
-                float qa[16], qb[16];
+                int ca[V], cb[V];
+                const float2 ia2 = make_float2(iA, iA), ib2 = make_float2(iB, iB);
 #pragma unroll
-                for (int i = 0; i < V; ++i) {
-                    qa[i] = roundf(__fmul_rn(ya[i], iA));
-                    qb[i] = roundf(__fmul_rn(yb[i], iB));
+                for (int t = 0; t < NP; ++t) {
+                    const float2 qa = mul2(ya[t], ia2), qb = mul2(yb[t], ib2);
+                    const float2 pa = add2(qa, half_away_bias(qa)), pb = add2(qb, half_away_bias(qb));
+                    const int e0 = pair_elem<MODE>(t, 0), e1 = pair_elem<MODE>(t, 1);
+                    ca[e0] = __float2int_rz(pa.x);
+                    ca[e1] = __float2int_rz(pa.y);
+                    cb[e0] = __float2int_rz(pb.x);
+                    cb[e1] = __float2int_rz(pb.y);
                 }
                 uint8_t *row = reinterpret_cast<uint8_t *>(a.kdata) + R * D;
-                *reinterpret_cast<uint4 *>(row + da) = pack16(qa);
-                *reinterpret_cast<uint4 *>(row + db) = pack16(qb);
-                if (MODE != KVC_ROPE_NEOX || (k & 1) == 0) {
-                    a.kscales[R * NB + da / QK] = __half_as_ushort(__float2half_rn(dA));
-                    if (MODE == KVC_ROPE_NEOX) a.kscales[R * NB + db / QK] = __half_as_ushort(__float2half_rn(dB));
+                *reinterpret_cast<uint4 *>(row + da) = make_uint4(pack4(ca[0], ca[1], ca[2], ca[3]),
+                                                                  pack4(ca[4], ca[5], ca[6], ca[7]),
+                                                                  pack4(ca[8], ca[9], ca[10], ca[11]),
+                                                                  pack4(ca[12], ca[13], ca[14], ca[15]));
+                *reinterpret_cast<uint4 *>(row + db) = make_uint4(pack4(cb[0], cb[1], cb[2], cb[3]),
+                                                                  pack4(cb[4], cb[5], cb[6], cb[7]),
+                                                                  pack4(cb[8], cb[9], cb[10], cb[11]),
+                                                                  pack4(cb[12], cb[13], cb[14], cb[15]));
+                if constexpr (NEOX) {
+                    a.kscales[R * NB + ((k & 1) ? db : da) / QK] = __half_as_ushort(__float2half_rn(d_own));
+                } else {
+                    a.kscales[R * NB + da / QK] = __half_as_ushort(__float2half_rn(d_own));
                 }
             }
         } else if (live) {
             __half *row = reinterpret_cast<__half *>(a.kdata) + R * D;
-            uint4 oa, ob;
-            __half *ha = reinterpret_cast<__half *>(&oa), *hb = reinterpret_cast<__half *>(&ob);
+            float fa[V], fb[V];
 #pragma unroll
-            for (int i = 0; i < V; ++i) {
-                ha[i] = __float2half_rn(ya[i]);
-                hb[i] = __float2half_rn(yb[i]);
+            for (int t = 0; t < NP; ++t) {
+                fa[pair_elem<MODE>(t, 0)] = ya[t].x;
+                fa[pair_elem<MODE>(t, 1)] = ya[t].y;
+                fb[pair_elem<MODE>(t, 0)] = yb[t].x;
+                fb[pair_elem<MODE>(t, 1)] = yb[t].y;
+            }
+            uint4 oa, ob;
+            __half2 *ha = reinterpret_cast<__half2 *>(&oa), *hb = reinterpret_cast<__half2 *>(&ob);
+#pragma unroll
+            for (int i = 0; i < V / 2; ++i) {
+                ha[i] = __floats2half2_rn(fa[2 * i], fa[2 * i + 1]);
+                hb[i] = __floats2half2_rn(fb[2 * i], fb[2 * i + 1]);
             }
             *reinterpret_cast<uint4 *>(row + da) = oa;
             *reinterpret_cast<uint4 *>(row + db) = ob;
         }
+        wa = nwa;
+        wb = nwb;
+        ha = nha;
+        hb = nhb;
     }
 }
 
@@ -253,7 +370,10 @@ cudaError_t launch_rope_shift(int type_k, int D, int mode, void *kdata, uint16_t
     a.layer_rows = layer_rows;
     a.spans = spans_dev;
     a.err = err;
-    for (int i = 0; i < 64; ++i) a.cs[i] = i < D / 2 ? cs[i] : make_float2(1.f, 0.f);
+    for (int i = 0; i < 64; ++i) {
+        a.c[i] = i < D / 2 ? cs[i].x : 1.f;
+        a.s[i] = i < D / 2 ? cs[i].y : 0.f;
+    }
     const dim3 grid((unsigned)n_spans, (unsigned)n_layer);
     const bool q8 = type_k == KVC_Q8_0, neox = mode == KVC_ROPE_NEOX;
 #define KVC_ROPE_LAUNCH(Q, DD, M) rope_shift_kernel<Q, DD, M><<<grid, 256, 0, st>>>(a)

@@ -178,6 +178,50 @@ def test_seq_ops_bit_exact(type_):
         tw.close()
 
 
+# Position-range selections over sequences whose positions are consecutive,
+# broken by a shift or a copy, and consecutive again: every step is checked
+# against the oracle (positions exact, V bytes exact, K within one code where
+# a row was shifted once).
+@pytest.mark.parametrize("page_rows", [32, 0])
+def test_position_ranges_across_shifts(page_rows):
+    tw = Twin(2, 8, 2, 64, 2048, n_seq_max=3, type_=Q8, rope_base=1e4, page_rows=page_rows)
+    try:
+        tw.fill(0, 600, seed=21, sigma=0.5)
+
+        def both(op, *args):
+            getattr(tw.gpu, op)(*args)
+            getattr(tw.ref, op)(*args)
+
+        steps = [("seq_add", 0, 300, 600, 1000),   # rows 300.. move to 1300..1599
+                 ("seq_cp", 0, 1, 200, 1400),      # contiguous rows, a gap in their positions
+                 ("seq_rm", 0, 1300, 1400),        # compaction in the middle
+                 ("seq_rm", 0, 1500, -1),          # suffix
+                 ("seq_cp", 1, 0, 1300, -1),       # rows appended out of position order
+                 ("seq_rm", 0, 1300, 1500)]        # back to positions 0..299
+        for st in steps:
+            both(*st)
+            for s_ in range(3):
+                if len(tw.ref.positions(s_)):
+                    _check_shifted_q8(tw, s_)
+                else:
+                    assert tw.gpu.n_tokens(s_) == 0, st
+            g = tw.ref.parse_state(tw.gpu.state_get(0, 250, 1350))
+            o = tw.ref.parse_state(tw.ref.state_get(0, 250, 1350))
+            assert np.array_equal(g[0], o[0]), st
+            for l in range(2):
+                assert np.array_equal(g[2][l].a, o[2][l].a), st
+        assert np.array_equal(tw.gpu.positions(0), np.arange(300))
+        tw.fill(0, 50, seed=22, pos0=300)           # appends continue the consecutive positions
+        assert tw.gpu.state_get(0, 280, 320) == tw.ref.state_get(0, 280, 320)
+        both("seq_cp", 0, 2, 290, 310)
+        _state_compare(tw, 2)
+        q = q_inputs(21, 1, 2, 8, 64)
+        got, want = tw.attn(1, [0, 2], q, 0.125)  # sequences without shifted rows
+        assert_attn_close(got, want, "after position-range operations")
+    finally:
+        tw.close()
+
+
 # 10 layers: the export/import copies run in 8 uneven layer groups
 @pytest.mark.parametrize("type_,n_layer", [(Q8, 3), (F16, 3), (Q8, 10), (F16, 10)])
 def test_state_roundtrip(type_, n_layer):
