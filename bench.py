@@ -47,7 +47,7 @@ GB = 1e9
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--n-kv", type=int, default=16384)
@@ -91,51 +91,72 @@ def peaks():
 
 # ----------------------------------------------------------------- clocks --
 class Clocks:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 50 ms from start() to stop(); the report keeps
+    the samples that fall inside the timed windows marked with window()."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.windows = []
         self.path = os.path.join("/tmp", "kvc_clocks_%d_%d.csv" % (os.getpid(), index))
 
     def start(self):
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                          "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        t_end = time.time() + 10.0  # the first sample shows the sampler is running
+        while time.time() < t_end and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
+
+    def window(self, t0: float, t1: float):
+        self.windows.append((t0, t1))
 
     def stop(self):
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.06)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
         self.f.close()
-        sm, smax, reasons = [], None, set()
-        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        import datetime
+
+        rows = []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax = float(parts[2])
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[2]), float(parts[3]),
+                                 [n for n, v in zip(names, parts[6:10]) if v.lower() in ("active", "1")]))
                 except ValueError:
                     continue
-                for name, val in zip(names[1:], parts[5:9]):
-                    if val.lower() in ("active", "1"):
-                        reasons.add(name)
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        inside = [r for r in rows if any(t0 - 0.025 <= r[0] <= t1 + 0.025 for t0, t1 in self.windows)]
+        note = "samples inside the timed windows"
+        if not inside and rows and self.windows:
+            mid = sum(t0 + t1 for t0, t1 in self.windows) / (2 * len(self.windows))
+            inside = [min(rows, key=lambda r: abs(r[0] - mid))]
+            note = "no sample fell inside the timed windows: the nearest one"
+        reasons = sorted({n for r in inside for n in r[3]})
+        return {"sm_mhz": statistics.median([r[1] for r in inside]) if inside else None,
+                "sm_max_mhz": inside[-1][2] if inside else None, "reasons": reasons, "samples": len(inside),
+                "timed_ms": round(1e3 * sum(t1 - t0 for t0, t1 in self.windows), 1), "note": note}
 
 
 def attn_traffic(type_: str, n_kv: int):
@@ -646,6 +667,21 @@ def churn(kvc, torch, dev, n: int, cycles: int, layers: int):
         again = torch.empty(size, dtype=torch.uint8, pin_memory=True)
         q = torch.randn(layers, 1, H, D, device=dev)
         o = torch.empty_like(q)
+        # the host link in each direction for a copy of the state's size between
+        # the same pinned buffers and device memory (best of 3)
+        devbuf = torch.empty(size, dtype=torch.uint8, device=dev)
+        link = {}
+        for name, dst, src in (("d2h", again, devbuf), ("h2d", devbuf, host)):
+            best = None
+            for _ in range(3):
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                dst.copy_(src)
+                torch.cuda.synchronize()
+                dt_ = time.perf_counter() - t0
+                best = dt_ if best is None else min(best, dt_)
+            link[name] = size / best / GB
+        del devbuf
         acc = {k: 0.0 for k in ("seq_cp", "state_get", "seq_rm", "slide", "state_set", "shift", "copy_in", "decode")}
 
         def timed(name, fn):
@@ -678,8 +714,13 @@ def churn(kvc, torch, dev, n: int, cycles: int, layers: int):
         for k2, v2 in acc.items():
             per = v2 / cycles
             ops[k2] = {"ms": round(per * 1e3, 3), "gbs": round(byts[k2] / per / GB, 1) if byts[k2] else None}
+        ops["state_get"]["frac_of_link"] = round(ops["state_get"]["gbs"] / link["d2h"], 3)
+        ops["state_set"]["frac_of_link"] = round(ops["state_set"]["gbs"] / link["h2d"], 3)
         return {"n_kv": n, "block": blk, "cycles": cycles, "layers": layers, "positions_ok": ok,
                 "state_round_trip_exact": exact,
+                "link_gbs": {"d2h": round(link["d2h"], 1), "h2d": round(link["h2d"], 1),
+                             "note": "one plain copy of the state's size between the same pinned buffers "
+                                     "and device memory, best of 3"},
                 "bytes": "seq_cp/copy_in/slide/shift: read+write; state_get/set: bytes exported; decode: KV read",
                 "ops": ops}
     finally:
@@ -955,26 +996,28 @@ def run_ours(args, rank: int, world: int):
 
             dist.barrier()
 
+    clocks = Clocks(local)
+
     def timed(fn, steps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
         torch.cuda.synchronize()
+        w0 = time.time()
         with torch.cuda.stream(s):
             e0.record(s)
             for _ in range(steps):
                 fn()
             e1.record(s)
         torch.cuda.synchronize()
+        clocks.window(w0, time.time())
         barrier()
         return e0.elapsed_time(e1) * 1e-3
 
     for _ in range(max(3, args.warmup)):
         step_graph.replay()
     torch.cuda.synchronize()
-    clocks = Clocks(local)
     clocks.start()
     t_step = timed(step_graph.replay, args.steps)
-    clk = clocks.stop()
     for _ in range(3):
         attn_graph.replay()
     t_attn = timed(attn_graph.replay, args.steps)
@@ -1027,6 +1070,7 @@ def run_ours(args, rank: int, world: int):
     host_issue[0] = 0.0
     n_eager0 = pos[0]
     t_eager = timed(eager_step, eager_steps)
+    clk = clocks.stop()  # over the timed windows of the step, attention-only, two-call and end-to-end legs
     eager_rows = (n_eager0 + pos[0] - 1) / 2.0  # mean rows attended per step
 
     t_step, t_attn, t_e2e, t_two, t_eager = max_over_ranks([t_step, t_attn, t_e2e, t_two, t_eager], dev, world)

@@ -78,6 +78,35 @@ int enter_sync(Ctx *c) {
     KVC_CU(c, cudaSetDevice(c->dev));
     KVC_CU(c, cudaDeviceSynchronize());
     c->clear_recent();
+    for (uint8_t *p : c->up_retired) cudaFreeHost(p);
+    c->up_retired.clear();
+    c->up_used = 0;
+    return KVC_OK;
+}
+
+// Host-to-device copy of a small host array on the internal stream, through
+// the pinned upload arena (an asynchronous copy; the caller's array may be
+// reused at once).  Falls back to a pageable copy if pinned memory is short.
+static int upload(Ctx *c, void *dst, const void *src, int64_t bytes) {
+    if (bytes <= 0) return KVC_OK;
+    const int64_t need = (bytes + 255) / 256 * 256;
+    if (c->up_used + need > c->up_cap) {
+        const int64_t cap = std::max<int64_t>({2 * c->up_cap, need, (int64_t)1 << 20});
+        uint8_t *p = nullptr;
+        if (cudaMallocHost((void **)&p, (size_t)cap) != cudaSuccess) {
+            cudaGetLastError();
+            KVC_CU(c, cudaMemcpyAsync(dst, src, (size_t)bytes, cudaMemcpyHostToDevice, c->st));
+            return KVC_OK;
+        }
+        if (c->up_host) c->up_retired.push_back(c->up_host);
+        c->up_host = p;
+        c->up_cap = cap;
+        c->up_used = 0;
+    }
+    uint8_t *h = c->up_host + c->up_used;
+    std::memcpy(h, src, (size_t)bytes);
+    c->up_used += need;
+    KVC_CU(c, cudaMemcpyAsync(dst, h, (size_t)bytes, cudaMemcpyHostToDevice, c->st));
     return KVC_OK;
 }
 
@@ -105,8 +134,7 @@ static int upload_runs(Ctx *c, const std::vector<RowRun> &runs) {
         if (rc) return rc;
         c->runs_cap = cap;
     }
-    KVC_CU(c, cudaMemcpyAsync(c->runs_dev, runs.data(), runs.size() * sizeof(RowRun), cudaMemcpyHostToDevice, c->st));
-    return KVC_OK;
+    return upload(c, c->runs_dev, runs.data(), (int64_t)(runs.size() * sizeof(RowRun)));
 }
 
 static int ensure_copy_stream(Ctx *c) {
@@ -119,9 +147,10 @@ static int ensure_copy_stream(Ctx *c) {
 // Re-upload the page tables of `s` (synchronous path).
 static int upload_pages(Ctx *c, int s) {
     Seq &q = c->seqs[s];
-    if (!q.pages.empty())
-        KVC_CU(c, cudaMemcpyAsync(c->pt_dev + (int64_t)s * c->max_pages, q.pages.data(), q.pages.size() * 4,
-                                  cudaMemcpyHostToDevice, c->st));
+    if (!q.pages.empty()) {
+        const int rc = upload(c, c->pt_dev + (int64_t)s * c->max_pages, q.pages.data(), (int64_t)q.pages.size() * 4);
+        if (rc) return rc;
+    }
     q.dev_pages = (int32_t)q.pages.size();
     return KVC_OK;
 }
@@ -428,6 +457,8 @@ void kvc_destroy(kvc_ctx *cc) {
     cudaFree(c->tickets);
     cudaFree(c->err_dev);
     if (c->err_host) cudaFreeHost(c->err_host);
+    if (c->up_host) cudaFreeHost(c->up_host);
+    for (uint8_t *p : c->up_retired) cudaFreeHost(p);
     cudaFree(c->staging);
     cudaFree(c->runs_dev);
     cudaFree(c->spans_dev);
@@ -1076,8 +1107,7 @@ int kvc_seq_add(kvc_ctx *cc, int seq, int p0, int p1, int delta) {
             return rc;
         c->spans_cap = n_spans;
     }
-    KVC_CU(c, cudaMemcpyAsync(c->spans_dev, spans.data(), spans.size() * sizeof(RopeSpan), cudaMemcpyHostToDevice,
-                              c->st));
+    if ((rc = upload(c, c->spans_dev, spans.data(), (int64_t)(spans.size() * sizeof(RopeSpan))))) return rc;
     // cos/sin of delta * theta_i in fp64, theta_i = base^(-2i/D)
     float2 cs[64];
     for (int i = 0; i < c->D / 2; ++i) {
@@ -1134,8 +1164,7 @@ int kvc_seq_key_scores(kvc_ctx *cc, int seq, int layer, float *scores, int32_t c
     const int64_t o_norm = o_mean + al((int64_t)c->Hk * c->D * 4), o_score = o_norm + al((int64_t)c->Hk * 4);
     if ((rc = ensure_staging(c, o_score + al(rows * 4)))) return rc;
     uint8_t *w = c->staging;
-    KVC_CU(c, cudaMemcpyAsync(w + o_blocks, blocks.data(), blocks.size() * sizeof(KeyDiffBlock),
-                              cudaMemcpyHostToDevice, c->st));
+    if ((rc = upload(c, w + o_blocks, blocks.data(), (int64_t)(blocks.size() * sizeof(KeyDiffBlock))))) return rc;
     KeyDiffArgs a;
     std::memset(&a, 0, sizeof(a));
     a.q8 = c->tk == KVC_Q8_0;
@@ -1157,7 +1186,7 @@ int kvc_seq_key_scores(kvc_ctx *cc, int seq, int layer, float *scores, int32_t c
     a.err = c->err_dev;
     cudaError_t e = launch_keydiff(a, c->sms, c->st);
     if (e != cudaSuccess) return cuda_fail(c, e, "KeyDiff kernels");
-    if (std::is_sorted(q.pos.begin(), q.pos.end())) {
+    if (q.linear || std::is_sorted(q.pos.begin(), q.pos.end())) {
         KVC_CU(c, cudaMemcpyAsync(scores, w + o_score, (size_t)rows * 4, cudaMemcpyDeviceToHost, c->st));
         return wait_internal(c);
     }

@@ -141,6 +141,12 @@ struct Ctx {
     RopeSpan *spans_dev = nullptr;
     int64_t spans_cap = 0;
     std::vector<RopeSpan> spans_host; // span list of the last shift (kept for its capacity)
+    // pinned bump arena for the small host-to-device uploads of synchronous
+    // operations (run and span lists, page tables); reset when the next
+    // synchronous operation starts, after the device is idle
+    uint8_t *up_host = nullptr;
+    int64_t up_cap = 0, up_used = 0;
+    std::vector<uint8_t *> up_retired; // smaller arenas that may still feed copies of this operation
     cudaStream_t st = nullptr; // internal stream of the synchronous operations
     cudaEvent_t done = nullptr;
     // state export/import: host copies of layer groups on their own stream,
