@@ -87,17 +87,25 @@ __device__ __forceinline__ bool mbar_wait_landed(uint64_t *bar, unsigned parity,
     return false;
 }
 
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            smem_u32(dst)),
-        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
+// Tile copies carry an L2 policy: the KV stream is read once per step, so its
+// lines go first when L2 needs room and the small data around it (queries,
+// partials, page tables, the new rows) stays resident.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
 }
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, unsigned bytes, uint64_t *bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
+                                            uint64_t pol) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+                 "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, unsigned bytes, uint64_t *bar, uint64_t pol) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
                  : "memory");
 }
 
@@ -389,6 +397,7 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG, V4>::NTHREADS, Shape<TY
     __syncthreads();
 
     // ---- tile loads, all issued by lane 0 of the load warp (warp W) -----------
+    const uint64_t pol = l2_evict_first_policy();
     auto issue = [&](int k) {
         const int s = k % S::STAGES;
         const int r0 = s_tstart[k];
@@ -423,14 +432,14 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG, V4>::NTHREADS, Shape<TY
             const int y = (int)(R0 + ro);
             if constexpr (S::KSUB == 1) {
                 // rows of at most 128 bytes: one swizzled box per tensor
-                tma_load_2d(st + ro * S::KROW, mk, 0, y, &full[s]);
-                tma_load_2d(st + S::KBYTES + ro * S::VROW, mv, 0, y, &full[s]);
+                tma_load_2d(st + ro * S::KROW, mk, 0, y, &full[s], pol);
+                tma_load_2d(st + S::KBYTES + ro * S::VROW, mv, 0, y, &full[s], pol);
             } else {
                 // 256-byte f16 rows: two 128-byte sub-tiles per tensor
-                tma_load_2d(st + ro * 128, mk, 0, y, &full[s]);
-                tma_load_2d(st + T * 128 + ro * 128, mk, 64, y, &full[s]);
-                tma_load_2d(st + S::KBYTES + ro * 128, mv, 0, y, &full[s]);
-                tma_load_2d(st + S::KBYTES + T * 128 + ro * 128, mv, 64, y, &full[s]);
+                tma_load_2d(st + ro * 128, mk, 0, y, &full[s], pol);
+                tma_load_2d(st + T * 128 + ro * 128, mk, 64, y, &full[s], pol);
+                tma_load_2d(st + S::KBYTES + ro * 128, mv, 0, y, &full[s], pol);
+                tma_load_2d(st + S::KBYTES + T * 128 + ro * 128, mv, 64, y, &full[s], pol);
             }
         };
         for (int b = 0; b < nbig; ++b) box(&tmkb, &tmvb, b * S::BIG);
@@ -438,8 +447,8 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG, V4>::NTHREADS, Shape<TY
         if constexpr (S::Q8) {
             if (sbytes) {
                 uint8_t *sc = scales + s * (2 * S::SCALE_BUF);
-                bulk_load(sc, reinterpret_cast<const uint8_t *>(p.ks) + saligned, sbytes, &full[s]);
-                bulk_load(sc + S::SCALE_BUF, reinterpret_cast<const uint8_t *>(p.vs) + saligned, sbytes, &full[s]);
+                bulk_load(sc, reinterpret_cast<const uint8_t *>(p.ks) + saligned, sbytes, &full[s], pol);
+                bulk_load(sc + S::SCALE_BUF, reinterpret_cast<const uint8_t *>(p.vs) + saligned, sbytes, &full[s], pol);
             }
         }
     };
