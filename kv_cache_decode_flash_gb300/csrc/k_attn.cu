@@ -163,6 +163,13 @@ __device__ __forceinline__ void split_pack(float x0, float x1, uint32_t &hi, uin
     hi = *reinterpret_cast<const uint32_t *>(&hh);
     lo = *reinterpret_cast<const uint32_t *>(&ll);
 }
+// Transpose of an 8x8 matrix of halves held as m16n8 accumulator rows (lane
+// i: row i/4, columns 2(i%4), 2(i%4)+1) into the same layout of the transpose.
+__device__ __forceinline__ uint32_t movt(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
 // A transposed V word holds codes (row 2t, dim 2g), (row 2t, dim 2g+1),
 // (row 2t+1, dim 2g), (row 2t+1, dim 2g+1); return the exact half2 of the
 // even dim (rows 2t, 2t+1) and of the odd dim.
@@ -233,20 +240,24 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Static shape of one kernel instance.  W compute warps in groups of GW;
-// group j takes tiles j, j + G, j + 2G, ... and each of its warps owns 16
-// rows of a tile.  One more warp issues the tile loads.
+// group j takes tiles j, j + G, j + 2G, ... and each of its warps owns SL
+// slabs of 16 rows of a tile, whose products it interleaves.  One more warp
+// issues the tile loads.
 template <int TYPE, int D, int R, int CFG = 0, bool V4 = false>
 struct Shape {
     static constexpr bool Q8 = TYPE == KVC_Q8_0;
     static_assert(!V4 || (Q8 && D == 128 && CFG == 0), "q4_0 V: with q8_0 K, head_dim 128, configuration 0");
-    // CFG 0: one CTA per SM (16 compute warps for q8_0); CFG 1 (q8_0): two CTAs
-    // per SM of 8 compute warps, each with half the SM's shared memory, for
-    // launches whose work exceeds one wave of CFG 0 at the longest chunks
-    static constexpr int W = (Q8 && CFG == 0) ? 16 : 8; // compute warps per CTA
-    static constexpr int GW = 8;                      // warps per group
+    // CFG 0: one CTA per SM (q8_0: 12 compute warps in 3 groups, two 16-row
+    // slabs each); CFG 1 (q8_0): two CTAs per SM of 8 compute warps, each with
+    // half the SM's shared memory, for launches whose work exceeds one wave of
+    // CFG 0 at the longest chunks
+    static constexpr bool FAT = Q8 && CFG == 0;
+    static constexpr int SL = FAT ? 2 : 1;            // 16-row slabs per warp and tile
+    static constexpr int W = FAT ? 12 : 8;            // compute warps per CTA
+    static constexpr int GW = FAT ? 4 : 8;            // warps per group
     static constexpr int G = W / GW;                  // groups
     static constexpr int NTHREADS = (W + 1) * 32;     // compute warps + the load warp
-    static constexpr int T = 16 * GW;                 // rows per tile
+    static constexpr int T = 16 * SL * GW;            // rows per tile
     static constexpr int NB = D / 32;                 // q8_0 blocks per row
     static constexpr int KROW = Q8 ? D : 2 * D;       // bytes per K row
     static constexpr int VROW = V4 ? D / 2 : KROW;    // bytes per V row (q4_0: packed codes)
@@ -262,22 +273,21 @@ struct Shape {
     static_assert(STAGE % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
     static constexpr int KSTEPS = D / 16;
     static constexpr int NBX = Q8 ? NB : 1;           // scale blocks per row (1 for f16)
-    static constexpr int PSTR = 24;                   // floats per head slot in the exchange (16 rows + pad)
-    static constexpr int PBUF = 8 * PSTR;             // floats per warp: p[8 head slots][rows]
     static constexpr int MAXT = 512;                  // tiles per chunk (host keeps chunks within it)
     static constexpr int QF_BYTES = KSTEPS * 32 * 16 + 64; // q fragments (one copy for all warps) + head scales
     static constexpr int SM_BUDGET = CFG == 1 ? 115712 : 232448; // shared memory one CTA may take
     static constexpr int MINB = CFG == 1 ? 2 : 1;                 // CTAs per SM the registers allow for
-    // shared memory besides the stages: base alignment, exchange buffers, tile tables, q
-    // fragments, and a margin for the kernel's static shared variables
-    static constexpr int FIXED = 1024 + W * PBUF * 4 + MAXT * 8 + 16 + QF_BYTES + 64;
+    // shared memory besides the stages: base alignment, tile tables, q fragments, and a
+    // margin for the kernel's static shared variables
+    static constexpr int FIXED = 1024 + MAXT * 8 + 16 + QF_BYTES + 64;
     static constexpr int PER_STAGE = STAGE + 2 * SCALE_BUF + 3 * 8; // tiles, scales, full/empty, tile info
     // as many stages (2..8) as fit, a whole number per group: group j takes tiles
     // j, j + G, ..., so with STAGES a multiple of G every phase of a stage belongs to
     // one group, whose warps consumed the stage's previous tile before waiting on it
     static constexpr int FIT = (SM_BUDGET - FIXED) / PER_STAGE;
-    static constexpr int FIT_G = FIT - FIT % G;
-    static constexpr int STAGES = FIT_G < 2 ? 2 : (FIT_G > 8 ? 8 : FIT_G);
+    static constexpr int FIT_C = FIT > 8 ? 8 : FIT;
+    static constexpr int FIT_G = FIT_C - FIT_C % G;
+    static constexpr int STAGES = FIT_G < 2 ? 2 : FIT_G;
     static_assert(STAGES % G == 0, "a stage's phases must all belong to one group");
     static constexpr int OOFF = ((2 * R + 3) / 4) * 4;  // partial: m[R], l[R], pad, then o[R][D] 16-byte aligned
     static constexpr int PF = OOFF + R * D;            // floats of one partial
@@ -319,8 +329,7 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG, V4>::NTHREADS, Shape<TY
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *stages = smem;                                  // [STAGES][K tile, V tile]
     uint8_t *scales = smem + S::STAGES * S::STAGE;           // [STAGES][K scales, V scales]
-    float *pbuf_all = reinterpret_cast<float *>(smem + S::RING);
-    uint64_t *full = reinterpret_cast<uint64_t *>(pbuf_all + W * S::PBUF);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::RING);
     uint64_t *empty = full + S::STAGES;
     TileInfo *tinfo = reinterpret_cast<TileInfo *>(empty + S::STAGES);
     int *s_tstart = reinterpret_cast<int *>(tinfo + S::STAGES); // first row of every tile
@@ -493,10 +502,10 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG, V4>::NTHREADS, Shape<TY
     const int gq = lane >> 2, tq = lane & 3;
     // ---- query fragments (B operand of QK), hi + lo fp16.  Warp 0 reads the
     // head group's rows (scaled by kq_scale log2 e) and their maxima, and leaves
-    // the values in the exchange buffers (not in use before the tile loop);
-    // after a barrier warp ks converts k-step ks.
+    // the values where the fragments go; after a barrier warp ks converts
+    // k-step ks in place (each lane its own 16 bytes).
     static_assert(S::KSTEPS <= W, "one converting warp per k-step");
-    float4 *qraw = reinterpret_cast<float4 *>(pbuf_all); // [KSTEPS][32 lanes]
+    float4 *qraw = reinterpret_cast<float4 *>(qfs); // [KSTEPS][32 lanes]
     int *s_eq = reinterpret_cast<int *>(shs + 8);        // e of each head slot
     if (warp == 0) {
         const bool hq = gq < r_act; // head slot this lane feeds into the MMA B operand
@@ -596,8 +605,8 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG, V4>::NTHREADS, Shape<TY
     // ---- per-warp state -------------------------------------------------------
     // softmax state of heads 2t, 2t+1; PV accumulators O^T[dims][heads] as
     // m16n8 fragments (rows = dims, columns = heads 2t, 2t+1)
-    float *pw = pbuf_all + warp * S::PBUF; // p[head slot][row], head stride PSTR
-    const int rbase = (warp % S::GW) * 16;  // this warp's rows in a tile of its group
+    constexpr int SL = S::SL;
+    const int rbase = (warp % S::GW) * (16 * SL); // this warp's first row in a tile of its group
 
     for (int k = warp / S::GW; k < n_tiles; k += S::G) {
         const int s = k % S::STAGES;
@@ -606,64 +615,85 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG, V4>::NTHREADS, Shape<TY
         const uint8_t *vt = st + S::KBYTES;
         const uint8_t *sct = scales + s * (2 * S::SCALE_BUF); // K scales, then V scales
         const int n = tinfo[s].n;
-        const int rows_w = min(max(n - rbase, 0), 16);
+        const int rows_w = min(max(n - rbase, 0), 16 * SL);
         if (rows_w > 0) {
-            // ---------------- QK on the tensor cores ----------------
-            float sc[4] = {0.f, 0.f, 0.f, 0.f}; // (row g, 2t) (row g, 2t+1) (row g+8, 2t) (row g+8, 2t+1)
-            const int ra = rbase + gq, rb = ra + 8;
-            // ldmatrix lane roles: rows 0-7 / 8-15 of the warp's slab, first / second 16-byte chunk
+            // ---------------- QK on the tensor cores, slab by slab interleaved ----------------
+            // sc[sl]: (row g, 2t) (row g, 2t+1) (row g+8, 2t) (row g+8, 2t+1) of slab sl
+            float sc[SL][4];
+#pragma unroll
+            for (int sl = 0; sl < SL; ++sl) sc[sl][0] = sc[sl][1] = sc[sl][2] = sc[sl][3] = 0.f;
+            // ldmatrix lane roles: rows 0-7 / 8-15 of a slab, first / second 16-byte chunk
             const int lm_row = rbase + (lane & 7) + ((lane >> 3) & 1) * 8;
             const int lm_hi = lane >> 4;
             if constexpr (S::Q8) {
-                // K scales of rows ra, rb: NB halves each, one 8- (or 4-) byte load per row
+                // K scales of rows g, g + 8 of every slab: NB halves each, one 8- (or 4-) byte load per row
                 const uint8_t *ksb = sct + (tinfo[s].delta + rbase) * S::SB;
-                uint32_t kw[2][S::NB / 2];
-                load_scales<S::NB>(ksb + gq * S::SB, kw[0]);
-                load_scales<S::NB>(ksb + (gq + 8) * S::SB, kw[1]);
+                uint32_t kw[SL][2][S::NB / 2];
+#pragma unroll
+                for (int sl = 0; sl < SL; ++sl) {
+                    load_scales<S::NB>(ksb + (16 * sl + gq) * S::SB, kw[sl][0]);
+                    load_scales<S::NB>(ksb + (16 * sl + gq + 8) * S::SB, kw[sl][1]);
+                }
 #pragma unroll
                 for (int b = 0; b < S::NB; ++b) {
-                    uint32_t r0, r1, r2, r3;
-                    ldsm_x4(st + swz<S::KROW>(lm_row, 2 * b + lm_hi), r0, r1, r2, r3);
-                    float c[4] = {0.f, 0.f, 0.f, 0.f};
-                    uint32_t a0, a1, a2, a3;
-                    codes_to_half2<RAW>(r0, a0, a2);
-                    codes_to_half2<RAW>(r1, a1, a3);
                     const uint4 qa = qfs[(2 * b) * 32 + lane], qb = qfs[(2 * b + 1) * 32 + lane];
-                    mma16816(c, a0, a1, a2, a3, qa.x, qa.y);
-                    mma16816(c, a0, a1, a2, a3, qa.z, qa.w);
-                    codes_to_half2<RAW>(r2, a0, a2);
-                    codes_to_half2<RAW>(r3, a1, a3);
-                    mma16816(c, a0, a1, a2, a3, qb.x, qb.y);
-                    mma16816(c, a0, a1, a2, a3, qb.z, qb.w);
-                    const float da = half_at(kw[0], b), db = half_at(kw[1], b);
-                    sc[0] = fmaf(da, c[0], sc[0]);
-                    sc[1] = fmaf(da, c[1], sc[1]);
-                    sc[2] = fmaf(db, c[2], sc[2]);
-                    sc[3] = fmaf(db, c[3], sc[3]);
+#pragma unroll
+                    for (int sl = 0; sl < SL; ++sl) {
+                        uint32_t r0, r1, r2, r3;
+                        ldsm_x4(st + swz<S::KROW>(lm_row + 16 * sl, 2 * b + lm_hi), r0, r1, r2, r3);
+                        float c[4] = {0.f, 0.f, 0.f, 0.f};
+                        uint32_t a0, a1, a2, a3;
+                        codes_to_half2<RAW>(r0, a0, a2);
+                        codes_to_half2<RAW>(r1, a1, a3);
+                        mma16816(c, a0, a1, a2, a3, qa.x, qa.y);
+                        mma16816(c, a0, a1, a2, a3, qa.z, qa.w);
+                        codes_to_half2<RAW>(r2, a0, a2);
+                        codes_to_half2<RAW>(r3, a1, a3);
+                        mma16816(c, a0, a1, a2, a3, qb.x, qb.y);
+                        mma16816(c, a0, a1, a2, a3, qb.z, qb.w);
+                        const float da = half_at(kw[sl][0], b), db = half_at(kw[sl][1], b);
+                        sc[sl][0] = fmaf(da, c[0], sc[sl][0]);
+                        sc[sl][1] = fmaf(da, c[1], sc[sl][1]);
+                        sc[sl][2] = fmaf(db, c[2], sc[sl][2]);
+                        sc[sl][3] = fmaf(db, c[3], sc[sl][3]);
+                    }
                 }
             } else {
                 const int lrow = rbase + (lane & 15);
 #pragma unroll
                 for (int ks = 0; ks < S::KSTEPS; ++ks) {
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4(st + (ks / 4) * T * 128 + swz<128>(lrow, 2 * (ks % 4) + (lane >> 4)), a0, a1, a2, a3);
                     const uint4 qk = qfs[ks * 32 + lane];
-                    mma16816(sc, a0, a1, a2, a3, qk.x, qk.y);
-                    mma16816(sc, a0, a1, a2, a3, qk.z, qk.w);
+#pragma unroll
+                    for (int sl = 0; sl < SL; ++sl) {
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4(st + (ks / 4) * T * 128 + swz<128>(lrow + 16 * sl, 2 * (ks % 4) + (lane >> 4)), a0, a1,
+                                a2, a3);
+                        mma16816(sc[sl], a0, a1, a2, a3, qk.x, qk.y);
+                        mma16816(sc[sl], a0, a1, a2, a3, qk.z, qk.w);
+                    }
                 }
             }
             // log2-domain scores; rows beyond the tile are -inf
-            float s2v[4];
-            s2v[0] = (gq < rows_w) ? sc[0] * hs0 : -INFINITY;
-            s2v[1] = (gq < rows_w) ? sc[1] * hs1 : -INFINITY;
-            s2v[2] = (gq + 8 < rows_w) ? sc[2] * hs0 : -INFINITY;
-            s2v[3] = (gq + 8 < rows_w) ? sc[3] * hs1 : -INFINITY;
+            float s2v[SL][4];
+#pragma unroll
+            for (int sl = 0; sl < SL; ++sl) {
+                const int r0 = 16 * sl + gq;
+                s2v[sl][0] = (r0 < rows_w) ? sc[sl][0] * hs0 : -INFINITY;
+                s2v[sl][1] = (r0 < rows_w) ? sc[sl][1] * hs1 : -INFINITY;
+                s2v[sl][2] = (r0 + 8 < rows_w) ? sc[sl][2] * hs0 : -INFINITY;
+                s2v[sl][3] = (r0 + 8 < rows_w) ? sc[sl][3] * hs1 : -INFINITY;
+            }
             // ---------------- online softmax (per warp) ----------------
             // The running maxima m0, m1 (warp-uniform) are only raised when a
             // score exceeds them by more than RESCALE_SLACK (log2 units), so
             // most tiles need no cross-lane reduction; probabilities are then
             // at most 2^RESCALE_SLACK, which the P' range exponent allows for.
-            float t0 = fmaxf(s2v[0], s2v[2]), t1 = fmaxf(s2v[1], s2v[3]);
+            float t0 = fmaxf(s2v[0][0], s2v[0][2]), t1 = fmaxf(s2v[0][1], s2v[0][3]);
+#pragma unroll
+            for (int sl = 1; sl < SL; ++sl) {
+                t0 = fmaxf(t0, fmaxf(s2v[sl][0], s2v[sl][2]));
+                t1 = fmaxf(t1, fmaxf(s2v[sl][1], s2v[sl][3]));
+            }
             const bool raise = __any_sync(0xffffffffu, t0 > m0 + RESCALE_SLACK || t1 > m1 + RESCALE_SLACK);
             float mn0 = m0, mn1 = m1;
             if (raise) {
@@ -672,37 +702,37 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG, V4>::NTHREADS, Shape<TY
                     t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, m));
                     t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, m));
                 }
-                mn0 = fmaxf(m0, t0); // finite: the slab has a live row
+                mn0 = fmaxf(m0, t0); // finite: the slabs have a live row
                 mn1 = fmaxf(m1, t1);
             }
-            float pr[4];
             // (head slots past the group have q = 0 and feed only columns that are never read)
-            pr[0] = ex2(s2v[0] - mn0);
-            pr[1] = ex2(s2v[1] - mn1);
-            pr[2] = ex2(s2v[2] - mn0);
-            pr[3] = ex2(s2v[3] - mn1);
-            // probabilities to [head][row] for the PV B operand
-            pw[(2 * tq) * S::PSTR + gq] = pr[0];
-            pw[(2 * tq + 1) * S::PSTR + gq] = pr[1];
-            pw[(2 * tq) * S::PSTR + gq + 8] = pr[2];
-            pw[(2 * tq + 1) * S::PSTR + gq + 8] = pr[3];
-            // ---------------- V scales of the rows this lane feeds (2t, 2t+1, 2t+8, 2t+9) -------
-            const int rr[4] = {2 * tq, 2 * tq + 1, 2 * tq + 8, 2 * tq + 9};
-            uint32_t vw[4][S::NBX / 2 > 0 ? S::NBX / 2 : 1];
+            float pr[SL][4];
+#pragma unroll
+            for (int sl = 0; sl < SL; ++sl) {
+                pr[sl][0] = ex2(s2v[sl][0] - mn0);
+                pr[sl][1] = ex2(s2v[sl][1] - mn1);
+                pr[sl][2] = ex2(s2v[sl][2] - mn0);
+                pr[sl][3] = ex2(s2v[sl][3] - mn1);
+            }
+            // ---------------- V scales of the rows this lane holds (g, g + 8 of each slab) -------
+            uint32_t vw[SL][2][S::NBX / 2 > 0 ? S::NBX / 2 : 1];
             int s_tile = 14 - RESCALE_SLACK; // f16: P' = p <= 2^RESCALE_SLACK
             if constexpr (S::Q8) {
                 const uint8_t *vsb = sct + S::SCALE_BUF + (tinfo[s].delta + rbase) * S::SB;
                 uint32_t wm = 0;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    // rows past the tile hold finite stale scales (or 0): their p is 0, and
-                    // the range exponent may only come out smaller than needed (safe)
-                    load_scales<S::NB>(vsb + rr[i] * S::SB, vw[i]);
+                for (int sl = 0; sl < SL; ++sl)
 #pragma unroll
-                    for (int h = 0; h < S::NB / 2; ++h) wm = __vmaxu2(wm, vw[i][h]); // fp16 >= 0: integer order
-                }
-                wm = __vmaxu2(wm, __shfl_xor_sync(0xffffffffu, wm, 1));
-                wm = __vmaxu2(wm, __shfl_xor_sync(0xffffffffu, wm, 2));
+                    for (int i = 0; i < 2; ++i) {
+                        // rows past the tile hold finite stale scales (or 0): their p is 0, and
+                        // the range exponent may only come out smaller than needed (safe)
+                        load_scales<S::NB>(vsb + (16 * sl + gq + 8 * i) * S::SB, vw[sl][i]);
+#pragma unroll
+                        for (int h = 0; h < S::NB / 2; ++h) wm = __vmaxu2(wm, vw[sl][i][h]); // fp16 >= 0: integer order
+                    }
+                wm = __vmaxu2(wm, __shfl_xor_sync(0xffffffffu, wm, 4));
+                wm = __vmaxu2(wm, __shfl_xor_sync(0xffffffffu, wm, 8));
+                wm = __vmaxu2(wm, __shfl_xor_sync(0xffffffffu, wm, 16));
                 const float dmax = __half2float(__ushort_as_half((uint16_t)max(wm & 0xffffu, wm >> 16)));
                 // 2^S * max(p * d) < 2^15 with p <= 2^RESCALE_SLACK: hi and lo of P' stay in fp16 range
                 // dmax is an fp16 value: a normal float in [2^-24, 2^16), so S stays in [-9, 30]
@@ -728,72 +758,82 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG, V4>::NTHREADS, Shape<TY
             }
             // per-lane partial row sums, in the same 2^S domain as the accumulators
             const float ps = pow2i(s_new);
-            l0 = fmaf(pr[0] + pr[2], ps, l0);
-            l1 = fmaf(pr[1] + pr[3], ps, l1);
+#pragma unroll
+            for (int sl = 0; sl < SL; ++sl) {
+                l0 = fmaf(pr[sl][0] + pr[sl][2], ps, l0);
+                l1 = fmaf(pr[sl][1] + pr[sl][3], ps, l1);
+                pr[sl][0] *= ps;
+                pr[sl][1] *= ps;
+                pr[sl][2] *= ps;
+                pr[sl][3] *= ps;
+            }
             sexp = s_new;
             have_s = true;
-            __syncwarp();
             // ---------------- PV on the tensor cores: O^T += V^T (P' hi + lo)^T --------------
-            float pv[4];
-            {
-                const float2 pa = *reinterpret_cast<const float2 *>(pw + gq * S::PSTR + 2 * tq);
-                const float2 pb = *reinterpret_cast<const float2 *>(pw + gq * S::PSTR + 2 * tq + 8);
-                pv[0] = pa.x * ps;
-                pv[1] = pa.y * ps;
-                pv[2] = pb.x * ps;
-                pv[3] = pb.y * ps;
-            }
+            // P' of a slab sits as accumulator rows (row g | g + 8, heads 2t, 2t+1); its hi and
+            // lo halves, transposed by movmatrix, are the B fragments (rows 2t, 2t+1 | 2t+8,
+            // 2t+9 of head g).
 #pragma unroll
             for (int b = 0; b < S::NBX; ++b) {
-                float x[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    if constexpr (S::Q8)
-                        x[i] = pv[i] * half_at(vw[i], b);
-                    else
-                        x[i] = pv[i]; // rows past the tile have p = 0
-                }
-                uint32_t b0h, b1h, b0l, b1l;
-                split_pack(x[0], x[1], b0h, b0l);
-                split_pack(x[2], x[3], b1h, b1l);
-                if constexpr (V4) {
-                    // block b is one 16-byte chunk of each 64-byte row: ra = rows 0-7,
-                    // rb = rows 8-15; nibble pairs give the same even / odd dim
-                    // m-tiles as the int8 codes (dims 2g | 2g+16 and 2g+1 | 2g+17)
-                    uint32_t ra, rb;
-                    ldsm_x2_trans(vt + swz<S::VROW>(lm_row, b), ra, rb);
-                    uint32_t e0, e1, e2, e3, o0, o1, o2, o3;
-                    nibbles_to_half2(ra, e0, e1, o0, o1);
-                    nibbles_to_half2(rb, e2, e3, o2, o3);
-                    mma16816(acc[2 * b], e0, e1, e2, e3, b0h, b1h);
-                    mma16816(acc[2 * b], e0, e1, e2, e3, b0l, b1l);
-                    mma16816(acc[2 * b + 1], o0, o1, o2, o3, b0h, b1h);
-                    mma16816(acc[2 * b + 1], o0, o1, o2, o3, b0l, b1l);
-                } else if constexpr (S::Q8) {
-                    uint32_t v0, v1, v2, v3;
-                    ldsm_x4_trans(vt + swz<S::VROW>(lm_row, 2 * b + lm_hi), v0, v1, v2, v3);
-                    // v0: rows 0-7 / bytes 0-15, v1: rows 8-15 / bytes 0-15,
-                    // v2: rows 0-7 / bytes 16-31, v3: rows 8-15 / bytes 16-31 of block b
-                    uint32_t e0, e1, e2, e3, o0, o1, o2, o3;
-                    vcodes_to_half2<RAW>(v0, e0, o0);
-                    vcodes_to_half2<RAW>(v2, e1, o1);
-                    vcodes_to_half2<RAW>(v1, e2, o2);
-                    vcodes_to_half2<RAW>(v3, e3, o3);
-                    mma16816(acc[2 * b], e0, e1, e2, e3, b0h, b1h);
-                    mma16816(acc[2 * b], e0, e1, e2, e3, b0l, b1l);
-                    mma16816(acc[2 * b + 1], o0, o1, o2, o3, b0h, b1h);
-                    mma16816(acc[2 * b + 1], o0, o1, o2, o3, b0l, b1l);
-                } else {
-                    // f16: the single "block" spans all D dims, NMT m-tiles of 16 dims
-                    const int lv_row = rbase + (lane & 7) + (lane >> 4) * 8;
-                    const int lv_c = (lane >> 3) & 1;
+                for (int sl = 0; sl < SL; ++sl) {
+                    float x[4];
+                    if constexpr (S::Q8) {
+                        const float dg = half_at(vw[sl][0], b), dg8 = half_at(vw[sl][1], b);
+                        x[0] = pr[sl][0] * dg;
+                        x[1] = pr[sl][1] * dg;
+                        x[2] = pr[sl][2] * dg8;
+                        x[3] = pr[sl][3] * dg8;
+                    } else {
+                        x[0] = pr[sl][0]; // rows past the tile have p = 0
+                        x[1] = pr[sl][1];
+                        x[2] = pr[sl][2];
+                        x[3] = pr[sl][3];
+                    }
+                    uint32_t hg, lg, hg8, lg8;
+                    split_pack(x[0], x[1], hg, lg);
+                    split_pack(x[2], x[3], hg8, lg8);
+                    const uint32_t b0h = movt(hg), b1h = movt(hg8), b0l = movt(lg), b1l = movt(lg8);
+                    const int vrow = lm_row + 16 * sl;
+                    if constexpr (V4) {
+                        // block b is one 16-byte chunk of each 64-byte row: ra = rows 0-7,
+                        // rb = rows 8-15; nibble pairs give the same even / odd dim
+                        // m-tiles as the int8 codes (dims 2g | 2g+16 and 2g+1 | 2g+17)
+                        uint32_t ra, rb;
+                        ldsm_x2_trans(vt + swz<S::VROW>(vrow, b), ra, rb);
+                        uint32_t e0, e1, e2, e3, o0, o1, o2, o3;
+                        nibbles_to_half2(ra, e0, e1, o0, o1);
+                        nibbles_to_half2(rb, e2, e3, o2, o3);
+                        mma16816(acc[2 * b], e0, e1, e2, e3, b0h, b1h);
+                        mma16816(acc[2 * b], e0, e1, e2, e3, b0l, b1l);
+                        mma16816(acc[2 * b + 1], o0, o1, o2, o3, b0h, b1h);
+                        mma16816(acc[2 * b + 1], o0, o1, o2, o3, b0l, b1l);
+                    } else if constexpr (S::Q8) {
+                        uint32_t v0, v1, v2, v3;
+                        ldsm_x4_trans(vt + swz<S::VROW>(vrow, 2 * b + lm_hi), v0, v1, v2, v3);
+                        // v0: rows 0-7 / bytes 0-15, v1: rows 8-15 / bytes 0-15,
+                        // v2: rows 0-7 / bytes 16-31, v3: rows 8-15 / bytes 16-31 of block b
+                        uint32_t e0, e1, e2, e3, o0, o1, o2, o3;
+                        vcodes_to_half2<RAW>(v0, e0, o0);
+                        vcodes_to_half2<RAW>(v2, e1, o1);
+                        vcodes_to_half2<RAW>(v1, e2, o2);
+                        vcodes_to_half2<RAW>(v3, e3, o3);
+                        mma16816(acc[2 * b], e0, e1, e2, e3, b0h, b1h);
+                        mma16816(acc[2 * b], e0, e1, e2, e3, b0l, b1l);
+                        mma16816(acc[2 * b + 1], o0, o1, o2, o3, b0h, b1h);
+                        mma16816(acc[2 * b + 1], o0, o1, o2, o3, b0l, b1l);
+                    } else {
+                        // f16: the single "block" spans all D dims, NMT m-tiles of 16 dims
+                        const int lv_row = rbase + 16 * sl + (lane & 7) + (lane >> 4) * 8;
+                        const int lv_c = (lane >> 3) & 1;
 #pragma unroll
-                    for (int mt = 0; mt < NMT; ++mt) {
-                        uint32_t a0, a1, a2, a3;
-                        ldsm_x4_trans(vt + (mt / 4) * T * 128 + swz<128>(lv_row, 2 * (mt % 4) + lv_c), a0, a1, a2,
-                                      a3);
-                        mma16816(acc[mt], a0, a1, a2, a3, b0h, b1h);
-                        mma16816(acc[mt], a0, a1, a2, a3, b0l, b1l);
+                        for (int mt = 0; mt < NMT; ++mt) {
+                            uint32_t a0, a1, a2, a3;
+                            ldsm_x4_trans(vt + (mt / 4) * T * 128 + swz<128>(lv_row, 2 * (mt % 4) + lv_c), a0, a1,
+                                          a2, a3);
+                            mma16816(acc[mt], a0, a1, a2, a3, b0h, b1h);
+                            mma16816(acc[mt], a0, a1, a2, a3, b0l, b1l);
+                        }
                     }
                 }
             }
