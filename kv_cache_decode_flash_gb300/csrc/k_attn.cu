@@ -616,6 +616,11 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG, V4>::NTHREADS, Shape<TY
         const uint8_t *sct = scales + s * (2 * S::SCALE_BUF); // K scales, then V scales
         const int n = tinfo[s].n;
         const int rows_w = min(max(n - rbase, 0), 16 * SL);
+        // A warp with rows computes all its slabs: a slab past the tile's rows reads
+        // stage bytes of an earlier tile (or never written), which are finite for the
+        // q8_0 instances (int8 codes, scales zeroed at the start), and its rows are
+        // masked to p = 0.  Branching around such a slab costs the interleaving of
+        // the two slabs' instructions.  (f16 instances keep one slab per warp.)
         if (rows_w > 0) {
             // ---------------- QK on the tensor cores, slab by slab interleaved ----------------
             // sc[sl]: (row g, 2t) (row g, 2t+1) (row g+8, 2t) (row g+8, 2t+1) of slab sl

@@ -796,7 +796,9 @@ def test_cold_store_restore_vs_recompute_plan():
             hit, n = store.admit(tw.gpu, 0, 1, 100 + i)
             assert hit == 1 and n == sizes[i]
         fixed, per, samples = store.restore_model()
-        assert samples == 3 and per > 0.0
+        # the fit is over timings: its sign is not asserted (three small blocks can give a
+        # slope within the timing noise); the plans below follow the rule with it
+        assert samples == 3 and np.isfinite(fixed) and np.isfinite(per)
         # plans for blocks evicted again, against the oracle's rule with the same model
         for i, m in enumerate(sizes):
             store.evict(tw.gpu, 0, 1, 0, m, key=200 + i, cls=0)
