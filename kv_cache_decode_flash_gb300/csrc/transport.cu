@@ -144,6 +144,15 @@ static ChunkPlan chunk_plan(const Ctx *c, int n_seq, const int32_t *rows) {
         const int64_t waves = std::max<int64_t>(1, (work + slots * cmax - 1) / (slots * cmax));
         C = (work + waves * slots - 1) / (waves * slots);
         C = std::min<int64_t>(cmax, std::max<int64_t>(64, (C + 15) / 16 * 16));
+        if (n_seq == 1 && rows[0] > 0) {
+            // One sequence: the same number of chunks (or fewer), each a whole number of
+            // 128-row tiles, so that a chunk's tiles start on tile boundaries of the pages
+            // instead of leaving a fragment tile at each end.  Measured on 64-layer graphs:
+            // 4k 8.43 -> 7.65 us, 16k 14.3 -> 13.3 us, 64k 33.6 -> 32.0 us.
+            const int64_t k = (rows[0] + C - 1) / C;
+            const int64_t c2 = ((rows[0] + k - 1) / k + 127) / 128 * 128;
+            if (c2 <= cmax) C = c2;
+        }
     }
     // at most `cap` chunks per (sequence, kv head)
     const int cap = attn_merge_cap(c->tk, c->D, c->r, pl.cfg);

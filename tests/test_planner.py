@@ -23,10 +23,23 @@ def ctas(rows, C, Hk=8):
 
 
 def test_decode_16k_leaves_the_merging_ctas_their_sms():
-    # 16384 rows x 8 KV heads: 144 CTAs of 912 rows, 8 SMs left to the previous launch's last CTAs
+    # 16384 rows x 8 KV heads: 144 slots (8 SMs left to the previous launch's last CTAs) give
+    # 18 chunks of 911 rows; whole 128-row tiles make that 16 chunks of 1024 rows, 128 CTAs
     C, cfg = plan([16384])
-    assert (C, cfg) == (912, 0)
-    assert ctas([16384], C) == 144
+    assert (C, cfg) == (1024, 0)
+    assert ctas([16384], C) == 128
+
+
+@pytest.mark.parametrize("n", [1000, 4096, 6144, 16384, 65536, 131072])
+def test_single_sequence_chunks_are_whole_tiles(n):
+    C, cfg = plan([n])
+    assert C % 128 == 0 or C == 8000
+    # no more chunks than rows-per-slot chunks (16-row multiples) would give
+    slots = SMS * OCC
+    if 8 * 8 <= slots and n * 8 <= (slots - 8) * 4096:
+        slots -= 8  # the SMs left to the previous launch's last CTAs
+    raw = -(-n * 8 // slots)
+    assert -(-n // C) <= -(-n // ((raw + 15) // 16 * 16))
 
 
 def test_long_single_sequence_fills_one_wave():
