@@ -16,22 +16,26 @@
 // bank-conflict free, and the q8_0 scales as 1-D bulk copies.  Tiles of rows
 // no in-flight kernel writes are requested before the programmatic-dependency
 // wait, so a launch prefetches under the end of the previous one.  The compute
-// warps form groups of 8 that take alternate tiles; a warp owns 16 rows of each
-// tile its group takes and runs its own online softmax:
+// warps form groups that take tiles in turn; a warp owns one or two 16-row
+// slabs of each tile its group takes (two: their products interleave) and runs
+// its own online softmax:
 //   QK  on the tensor cores (mma.sync m16n8k16, fp32 accumulate): int8 codes
 //       become exact fp16 values in registers, q is split into fp16 hi + lo
 //       parts (about 22 significant bits), and each 32-element block gets its
 //       own accumulator so the block scale is applied in fp32 afterwards;
 //   PV  on the tensor cores as O^T = V^T (P' hi + lo)^T, the q8_0 V scale
 //       folded into the probability (P' = p * d_v * 2^S per block, with a
-//       per-warp range exponent S that keeps hi and lo normal fp16).
+//       per-warp range exponent S that keeps hi and lo normal fp16); P' is
+//       formed in the accumulator layout of the scores and transposed into
+//       the B operand by movmatrix.
 // Warps merge inside the CTA; CTAs of one (sequence, kv head) merge through
 // global partials, the last CTA to arrive (an atomic ticket, no waiting)
 // combining them in fixed chunk order, so results are bitwise repeatable.
 // A decode step may also hand the kernel each sequence's new K/V row: the
 // CTA whose chunk holds it quantises and stores it before reading its tile.
-// Configuration 0 runs one CTA per SM (16 compute warps for q8_0, 8 for f16);
-// configuration 1 (q8_0) two CTAs of 8 compute warps per SM.
+// Configuration 0 runs one CTA per SM (q8_0: 12 compute warps in 3 groups of
+// 4, two slabs each; f16: 8 warps in one group, one slab each); configuration
+// 1 (q8_0) two CTAs of 8 compute warps (one slab each) per SM.
 #include "kvc_internal.h"
 #include "quant_row.cuh"
 
