@@ -334,8 +334,8 @@ int kvc_set_chunk_rows(kvc_ctx *c, int rows);
  * launch over n_seq sequences of rows[i] rows would use, for a KV type,
  * head_dim and head counts, on a device of `sms` SMs where configuration 0
  * fits occ CTAs per SM and configuration 1 (q8_0, two CTAs of half the
- * size) occ2 (0: not available).  *chunk_rows: rows per chunk (for one
- * sequence a whole number of 128-row tiles, at most 8000 rows); *cfg: the
+ * size) occ2 (0: not available).  *chunk_rows: rows per chunk, at most 8000
+ * (for one sequence, a whole number of 128-row tiles where that fits); *cfg: the
  * configuration.  rows: HOST int32[n_seq].  Errors: KVC_EINVAL. */
 int kvc_debug_chunk_plan(int type, int head_dim, int n_head, int n_head_kv, int sms, int occ, int occ2,
                          int n_seq, const int32_t *rows, int32_t *chunk_rows, int32_t *cfg);
