@@ -131,32 +131,40 @@ class Clocks:
         except Exception:
             self.proc.kill()
         self.f.close()
-        import datetime
-
-        rows = []
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 10:
-                    continue
-                try:
-                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                    rows.append((ts, float(parts[2]), float(parts[3]),
-                                 [n for n, v in zip(names, parts[6:10]) if v.lower() in ("active", "1")]))
-                except ValueError:
-                    continue
+            lines = f.readlines()
         os.unlink(self.path)
-        inside = [r for r in rows if any(t0 - 0.025 <= r[0] <= t1 + 0.025 for t0, t1 in self.windows)]
-        note = "samples inside the timed windows"
-        if not inside and rows and self.windows:
-            mid = sum(t0 + t1 for t0, t1 in self.windows) / (2 * len(self.windows))
-            inside = [min(rows, key=lambda r: abs(r[0] - mid))]
-            note = "no sample fell inside the timed windows: the nearest one"
-        reasons = sorted({n for r in inside for n in r[3]})
-        return {"sm_mhz": statistics.median([r[1] for r in inside]) if inside else None,
-                "sm_max_mhz": inside[-1][2] if inside else None, "reasons": reasons, "samples": len(inside),
-                "timed_ms": round(1e3 * sum(t1 - t0 for t0, t1 in self.windows), 1), "note": note}
+        return clock_summary(lines, self.windows)
+
+
+def clock_summary(lines, windows) -> dict:
+    """Median SM clock and throttle reasons of the nvidia-smi samples (CSV lines
+    of Clocks.FIELDS) that fall inside the timed windows [(t0, t1)] (epoch
+    seconds, 25 ms of slack); with none inside, the sample nearest to them."""
+    import datetime
+
+    rows = []
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            rows.append((ts, float(parts[2]), float(parts[3]),
+                         [n for n, v in zip(names, parts[6:10]) if v.lower() in ("active", "1")]))
+        except ValueError:
+            continue
+    inside = [r for r in rows if any(t0 - 0.025 <= r[0] <= t1 + 0.025 for t0, t1 in windows)]
+    note = "samples inside the timed windows"
+    if not inside and rows and windows:
+        mid = sum(t0 + t1 for t0, t1 in windows) / (2 * len(windows))
+        inside = [min(rows, key=lambda r: abs(r[0] - mid))]
+        note = "no sample fell inside the timed windows: the nearest one"
+    reasons = sorted({n for r in inside for n in r[3]})
+    return {"sm_mhz": statistics.median([r[1] for r in inside]) if inside else None,
+            "sm_max_mhz": inside[-1][2] if inside else None, "reasons": reasons, "samples": len(inside),
+            "timed_ms": round(1e3 * sum(t1 - t0 for t0, t1 in windows), 1), "note": note}
 
 
 def attn_traffic(type_: str, n_kv: int):

@@ -76,3 +76,23 @@ def test_timeline_summary_of_a_constructed_trace():
                 t += 7.0
     s2 = bench.timeline_summary(recs2, 2)
     assert s2["launches_per_step"] == 4 and s2["step_ms"] == 0.028 and s2["deliveries"] == 4
+
+
+def test_clock_summary_keeps_the_samples_inside_the_timed_windows():
+    import datetime
+
+    def line(ts, sm, reasons=("Not Active",) * 4):
+        stamp = datetime.datetime.fromtimestamp(ts).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return "%s, 0, %d, 2070, 900.5, 0x0, %s" % (stamp, sm, ", ".join(reasons))
+
+    t0 = 1_800_000_000.0
+    lines = [line(t0 - 1.0, 900), line(t0 + 0.1, 2070), line(t0 + 0.2, 2060),
+             line(t0 + 0.3, 2070, ("Not Active", "Not Active", "Not Active", "Active")),
+             line(t0 + 5.0, 1200), "garbage line"]
+    got = bench.clock_summary(lines, [(t0, t0 + 0.35)])
+    assert got["samples"] == 3 and got["sm_mhz"] == 2070.0 and got["sm_max_mhz"] == 2070.0
+    assert got["reasons"] == ["sw_power_cap"] and got["note"].startswith("samples inside")
+    # a window with no sample inside reports the nearest sample, and says so
+    got = bench.clock_summary(lines, [(t0 + 4.0, t0 + 4.01)])
+    assert got["samples"] == 1 and got["sm_mhz"] == 1200.0 and got["note"].startswith("no sample")
+    assert bench.clock_summary([], [(t0, t0 + 1)])["sm_mhz"] is None
