@@ -476,10 +476,11 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG, V4>::NTHREADS, Shape<TY
         asm volatile("prefetch.global.L2 [%0];" ::"l"(qb + lane * 128));
     }
     int prod_k = 0; // tiles issued so far (by the load lane)
-    // Before the wait: one tile per group (the first round); the other stages are
-    // requested once the query fragments are built, so that the query's load after
-    // the wait does not queue behind the whole prefetch.
-    constexpr int PRE = S::FAT ? S::G : S::STAGES;
+    // Before the wait: q8_0 one tile per group (the first round), f16 two tiles of its
+    // three; the other stages are requested once the query fragments are built, so that
+    // the query's load after the wait does not queue behind the whole prefetch.  (The
+    // two-CTA configuration keeps its two stages requested before the wait.)
+    constexpr int PRE = S::FAT ? S::G : (S::Q8 ? S::STAGES : 2);
     if (loader)
         while (prod_k < n_stable && prod_k < PRE) issue(prod_k++);
     pdl_wait();
@@ -488,7 +489,7 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG, V4>::NTHREADS, Shape<TY
         // pages of the tiles past the stable prefix, now that preceding kernels are complete
         for (int k = n_stable + lane; k < n_tiles; k += 32) s_tpage[k] = tile_page(k);
         __syncwarp();
-        if (lane == 0 && !S::FAT) {
+        if (lane == 0 && PRE >= S::STAGES) {
             // (the tile of a fused append's row waits until the row is stored)
             for (; prod_k < n_tiles && prod_k < S::STAGES; ++prod_k) {
                 if (app && s_tstart[prod_k] + tile_rows(s_tstart[prod_k]) > sq.app_row) break;
