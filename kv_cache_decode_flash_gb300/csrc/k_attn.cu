@@ -484,7 +484,6 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG, V4>::NTHREADS, Shape<TY
     if (loader)
         while (prod_k < n_stable && prod_k < PRE) issue(prod_k++);
     pdl_wait();
-    pdl_trigger();
     if (warp == W) {
         // pages of the tiles past the stable prefix, now that preceding kernels are complete
         for (int k = n_stable + lane; k < n_tiles; k += 32) s_tpage[k] = tile_page(k);
@@ -858,6 +857,9 @@ __global__ void __launch_bounds__(Shape<TYPE, D, R, CFG, V4>::NTHREADS, Shape<TY
     }
     } // compute warps
     __syncthreads();
+    // the next launch may be scheduled now (it waits for this grid's end before reading);
+    // its CTAs land on SMs as this launch's CTAs leave
+    pdl_trigger();
 
     // ---- CTA merge of the warps (stages are free now) -------------------------
     // Each warp stores its fragments as they sit in registers (lane-major,
