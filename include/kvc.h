@@ -348,6 +348,18 @@ int kvc_debug_chunk_plan(int type, int head_dim, int n_head, int n_head_kv, int 
 int kvc_debug_chunk_plan_seq(int type, int head_dim, int n_head, int n_head_kv, int sms, int occ, int occ2,
                              int n_seq, const int32_t *rows, int32_t *chunk_rows_seq, int32_t *cfg);
 
+/* Test hook, no context and no GPU needed: the rows of a sequence holding
+ * positions pos[0 .. n) that the sequence operations select for the range
+ * [p0, p1) (p0 < 0: from 0; p1 < 0: to the end).  linear != 0 states that the
+ * positions are consecutive (pos[r] == pos[0] + r), which a context records
+ * and then selects by arithmetic; a false statement is rejected.  The result
+ * does not depend on linear.  pos: HOST int32[n]; rows: HOST int64[n] or NULL
+ * (receives the selected rows in row order); *count: rows selected; *first:
+ * the first of them (0 when none); *contiguous: 1 when they are one run of
+ * consecutive rows.  Errors: KVC_EINVAL. */
+int kvc_debug_select_rows(const int32_t *pos, int32_t n, int linear, int p0, int p1, int64_t *rows,
+                          int64_t *count, int64_t *first, int32_t *contiguous);
+
 /* Limit, in milliseconds, of every bounded host wait of the synchronous
  * operations (default 120000).  A wait that runs out returns KVC_ETIMEDOUT. */
 int kvc_set_timeout_ms(kvc_ctx *c, int ms);

@@ -1480,6 +1480,28 @@ int kvc_set_timeout_ms(kvc_ctx *cc, int ms) {
     return KVC_OK;
 }
 
+int kvc_debug_select_rows(const int32_t *pos, int32_t n, int linear, int p0, int p1, int64_t *rows,
+                          int64_t *count, int64_t *first, int32_t *contiguous) {
+    if (n < 0 || (n > 0 && !pos) || !count || !first || !contiguous) return KVC_EINVAL;
+    Seq q;
+    q.n = n;
+    q.pos.assign(pos, pos + n);
+    for (int32_t r = 0; r < n; ++r)
+        if (q.pos[(size_t)r] < 0) return KVC_EINVAL;
+    q.linear = linear != 0;
+    if (q.linear && !consecutive(q.pos.data(), n)) return KVC_EINVAL;
+    int64_t a, b;
+    norm_range(p0, p1, a, b);
+    RowSel sel;
+    select_rows(q, a, b, sel);
+    *count = sel.count;
+    *first = sel.count ? sel.first : 0;
+    *contiguous = sel.contiguous ? 1 : 0;
+    if (rows)
+        for (int64_t i = 0; i < sel.count; ++i) rows[i] = sel.row(i);
+    return KVC_OK;
+}
+
 int kvc_debug_fail_alloc_after(kvc_ctx *cc, int n) {
     if (!cc) return KVC_EINVAL;
     Ctx *c = reinterpret_cast<Ctx *>(cc);

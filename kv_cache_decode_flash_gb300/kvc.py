@@ -96,6 +96,8 @@ def load():
         "kvc_debug_chunk_plan": (i32, [i32, i32, i32, i32, i32, i32, i32, i32, p, C.POINTER(C.c_int32),
                                        C.POINTER(C.c_int32)]),
         "kvc_debug_chunk_plan_seq": (i32, [i32, i32, i32, i32, i32, i32, i32, i32, p, p, C.POINTER(C.c_int32)]),
+        "kvc_debug_select_rows": (i32, [p, i32, i32, i32, i32, p, C.POINTER(C.c_int64), C.POINTER(C.c_int64),
+                                        C.POINTER(C.c_int32)]),
         "kvc_set_timeout_ms": (i32, [p, i32]),
         "kvc_debug_fail_alloc_after": (i32, [p, i32]),
         "kvc_check_device_error": (i32, [p, C.POINTER(C.c_uint32)]),
@@ -355,6 +357,21 @@ def kvc_debug_chunk_plan_seq(type_, head_dim, n_head, n_head_kv, sms, occ, occ2,
     if st != KVC_OK:
         raise KvcError(st, "bad chunk-plan arguments")
     return list(out), cfg.value
+
+
+def kvc_debug_select_rows(pos, p0, p1, linear=False):
+    """The rows a sequence operation selects for positions [p0, p1) of a
+    sequence holding `pos`, without a context or a GPU: (rows, first,
+    contiguous)."""
+    n = len(pos)
+    arr = (C.c_int32 * max(n, 1))(*[int(x) for x in pos])
+    out = (C.c_int64 * max(n, 1))()
+    cnt, first, contig = C.c_int64(), C.c_int64(), C.c_int32()
+    st = load().kvc_debug_select_rows(arr, n, 1 if linear else 0, int(p0), int(p1), out, C.byref(cnt),
+                                      C.byref(first), C.byref(contig))
+    if st != KVC_OK:
+        raise KvcError(st, "bad row-selection arguments")
+    return list(out[:cnt.value]), first.value, bool(contig.value)
 
 
 def kvc_debug_fail_alloc_after(ctx, n):

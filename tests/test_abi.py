@@ -74,3 +74,39 @@ def test_cold_store_restore_model_calls_without_a_gpu():
         assert s.restore_model() == (0.0, 0.0, 0)
     finally:
         s.close()
+
+
+def test_row_selection_matches_a_plain_filter():
+    """The sequence operations' row selection (by arithmetic when the positions
+    are consecutive, else by one counting pass and an index list) against a
+    plain filter over the positions, on consecutive, gapped, duplicated and
+    shuffled positions."""
+    import numpy as np
+
+    from kv_cache_decode_flash_gb300 import kvc
+
+    rng = np.random.default_rng(7)
+    cases = [np.arange(0, 300), np.arange(1000, 1513), np.arange(0)]
+    g = np.arange(0, 400)
+    g[150:] += 50  # a gap
+    cases.append(g)
+    d = np.concatenate([np.arange(0, 200), np.arange(50, 250)])  # duplicates after a shift
+    cases.append(d)
+    cases.append(rng.permutation(500))
+    cases.append(np.sort(rng.choice(5000, 700, replace=False)))
+    for pos in cases:
+        linear = len(pos) > 0 and bool(np.all(pos == pos[0] + np.arange(len(pos))))
+        top = int(pos.max()) + 3 if len(pos) else 10
+        ranges = [(-1, -1), (0, 1), (5, 5)] + [tuple(sorted(rng.integers(-1, top, 2))) for _ in range(40)]
+        for p0, p1 in ranges:
+            a = 0 if p0 < 0 else p0
+            b = 2**31 if p1 < 0 else p1
+            want = np.nonzero((pos >= a) & (pos < b))[0].tolist()
+            for lin in ([False, True] if linear else [False]):
+                rows, first, contig = kvc.kvc_debug_select_rows(pos.tolist(), p0, p1, linear=lin)
+                assert rows == want, (pos[:5], p0, p1, lin)
+                assert first == (want[0] if want else 0)
+                assert contig == (not want or want == list(range(want[0], want[0] + len(want))))
+    # a false "consecutive" statement is rejected
+    with pytest.raises(kvc.KvcError):
+        kvc.kvc_debug_select_rows([0, 1, 3], -1, -1, linear=True)
