@@ -10,6 +10,8 @@ here from its mathematics.
   placed at bits 8..15 of 2^23 is the float 2^23 + 256 u, and
   (2^23 + 256 u) * (s / 256) - (2^23 + 2^15) * (s / 256) = s (u - 128) with one
   rounding, exact for every fp16 scale s.
+- The attention turns stored int8 codes and q4_0 nibbles into exact fp16
+  operands through the mantissa of 1024.
 """
 import numpy as np
 
@@ -68,3 +70,30 @@ def test_dequantisation_by_one_fma_is_exact_for_every_scale_and_code():
     fma = (f[None, :] * s8.astype(np.float64)[:, None] + off.astype(np.float64)[:, None]).astype(np.float32)
     exact = s.astype(np.float64)[:, None] * (u[None, :] - 128.0)
     assert np.array_equal(fma.astype(np.float64), exact)
+
+
+def _half(bits):
+    return np.array(bits, np.uint16).view(np.float16)
+
+
+def test_int8_codes_to_fp16_by_the_mantissa_of_1024():
+    # the attention kernel's QK and PV operands: an offset-binary byte u = c + 128 placed in the
+    # low byte of 0x64uu is the half 1024 + u; subtracting half(1152) leaves c exactly
+    u = np.arange(256)
+    h = _half(0x6400 | u)
+    assert np.array_equal(h.astype(np.float64), 1024.0 + u)
+    c = (h - np.float16(1152)).astype(np.float64)  # float16 arithmetic, one rounding
+    assert np.array_equal(c, u - 128.0)
+
+
+def test_q4_0_nibbles_to_fp16_exactly():
+    # low nibble n in the mantissa of 1024: (1024 + n) - 1032 = n - 8; high nibble as 16 n:
+    # (1024 + 16 n) * (1/16) - 72 = n - 8, each with one rounding of an exact value
+    n = np.arange(16)
+    lo = (_half(0x6400 | n) - np.float16(1032)).astype(np.float64)
+    assert np.array_equal(lo, n - 8.0)
+    hi_in = _half(0x6400 | (n << 4))
+    hi = (hi_in.astype(np.float32) * np.float32(1 / 16) + np.float32(-72)).astype(np.float16).astype(np.float64)
+    assert np.array_equal(hi, n - 8.0)
+    assert np.float16(1 / 16) == _half(0x2C00) and np.float16(-72) == _half(0xD480)
+    assert np.float16(1032) == _half(0x6408) and np.float16(1152) == _half(0x6480)
